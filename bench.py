@@ -1,0 +1,556 @@
+#!/usr/bin/env python3
+"""Benchmark of the vocabulary-statistics hot path on one or more GPUs.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--rows N]
+
+One step is one pass of the whole path over one batch of synthetic input,
+N = 8192 rows x V = 151936 bf16 logits (the Qwen vocabulary), forward and
+backward of every statistic:
+
+  1. target logprob, k = 1        (logits N(0,3^2) + per-row offset U[-50,50];
+                                   5% ignored rows, 1% out-of-range targets)
+  2. entropy                      (policy a ~ N(0,3^2), 1% masked columns,
+  3. reverse KL(a||b)              reference b = a + N(0,0.5^2), mismatch rows,
+  4. forward KL(b||a)              one all -inf row)
+  5. softcap-fused logprob, cap 30 (logits N(0,15^2))
+  6. standalone softcap, cap 30, bf16 upstream gradient
+
+The metric is fwd+bwd achieved HBM bandwidth: the algorithmic bytes of the
+step (every logit read once per sweep that reads it, every gradient written
+once, plus ids, upstream gradients, outputs and per-row stats) divided by the
+device time of the step; per-op ms and TB/s are reported alongside.  Inputs
+(2.5 GB per tensor) are far larger than L2, so no flush is needed between
+steps.  Multi-GPU runs (torchrun) give each rank its own batch (weak scaling;
+rows are independent, no collective on the data path); the time is the
+maximum over ranks.
+
+``--impl reference`` times the CPU fp64 oracle on a bounded sample of the
+same workload (this is the baseline arm; no GPU is used).
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+N_ROWS = 8192
+VOCAB = 151936
+CAP = 30.0
+METRIC = "fwd+bwd achieved HBM TB/s, logp/entropy/KL/softcap, V=151936 bf16"
+WORKLOAD = ("fwd+bwd of logp k=1, entropy, reverse KL, forward KL, softcap-fused logp (cap 30) "
+            "and standalone softcap (cap 30), N=8192 x V=151936 bf16")
+OPS = ["logp", "entropy", "kl_reverse", "kl_forward", "cap_logp", "softcap"]
+KERNEL_NAMES = {  # op, pass -> CUDA kernel (for the ncu launch list)
+    ("logp", "fwd"): "row_fwd_kernel<bf16, logp, nocap>",
+    ("logp", "bwd"): "row_bwd_kernel<bf16, logp, nocap>",
+    ("entropy", "fwd"): "row_fwd_kernel<bf16, entropy, nocap>",
+    ("entropy", "bwd"): "row_bwd_kernel<bf16, entropy, nocap>",
+    ("kl_reverse", "fwd"): "row_fwd_kernel<bf16, kl, nocap>",
+    ("kl_reverse", "bwd"): "row_bwd_kernel<bf16, kl_reverse, nocap>",
+    ("kl_forward", "fwd"): "row_fwd_kernel<bf16, kl, nocap>",
+    ("kl_forward", "bwd"): "row_bwd_kernel<bf16, kl_forward, nocap>",
+    ("cap_logp", "fwd"): "row_fwd_kernel<bf16, logp, cap>",
+    ("cap_logp", "bwd"): "row_bwd_kernel<bf16, logp, cap>",
+    ("softcap", "fwd"): "softcap_fwd_kernel<bf16>",
+    ("softcap", "bwd"): "softcap_bwd_kernel<bf16, bf16>",
+}
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
+
+
+# ----------------------------------------------------------------------------
+# algorithmic bytes
+# ----------------------------------------------------------------------------
+
+def op_bytes(op: str, n: int, v: int, es: int = 2, k: int = 1) -> dict:
+    """Algorithmic bytes of one forward and one backward launch of `op`:
+    each logit read once per sweep, each gradient element written once, plus
+    the small per-row tensors (ids, upstream gradients, outputs, stats)."""
+    nv = n * v * es
+    stat = 8 * n
+    if op in ("logp", "cap_logp"):
+        small = n * k * (8 + 4)          # ids, logp (fwd) / ids, g (bwd)
+        return {"fwd": nv + small + stat, "bwd": 2 * nv + small + stat}
+    if op == "entropy":
+        return {"fwd": nv + 4 * n + stat, "bwd": 2 * nv + 8 * n + stat}
+    if op in ("kl_reverse", "kl_forward"):
+        return {"fwd": 2 * nv + 4 * n + 2 * stat, "bwd": 3 * nv + 8 * n + 2 * stat}
+    if op == "softcap":
+        return {"fwd": 2 * nv, "bwd": 3 * nv}
+    raise KeyError(op)
+
+
+def step_bytes(n: int, v: int) -> int:
+    return sum(sum(op_bytes(op, n, v).values()) for op in OPS)
+
+
+# ----------------------------------------------------------------------------
+# distributed helpers (host logic; covered by a gloo test)
+# ----------------------------------------------------------------------------
+
+def dist_env() -> tuple[int, int, int]:
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def max_over_ranks(value: float, device=None) -> float:
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return value
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier() -> None:
+    import torch.distributed as dist
+    if dist.is_available() and dist.is_initialized():
+        dist.barrier()
+
+
+def aggregate(bytes_per_rank: int, world: int, seconds: float) -> float:
+    """Whole-job throughput in TB/s: the bytes all ranks processed over the
+    slowest rank's time (each rank runs the same per-GPU workload)."""
+    return bytes_per_rank * world / seconds / 1e12
+
+
+# ----------------------------------------------------------------------------
+# clocks during the timed region
+# ----------------------------------------------------------------------------
+
+CLOCK_FIELDS = ["index", "clocks.sm", "clocks.max.sm", "power.draw", "clocks_event_reasons.active",
+                "clocks_event_reasons.hw_slowdown", "clocks_event_reasons.hw_thermal_slowdown",
+                "clocks_event_reasons.sw_thermal_slowdown", "clocks_event_reasons.sw_power_cap"]
+
+
+class ClockSampler:
+    """nvidia-smi sampling every 200 ms while the timed region runs."""
+
+    def __init__(self, gpu_id: str | None):
+        self.proc = None
+        self.path = None
+        if gpu_id is None:
+            return
+        fd, self.path = tempfile.mkstemp(prefix="clocks_", suffix=".csv")
+        os.close(fd)
+        try:
+            self.out = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={','.join(CLOCK_FIELDS)}", "--format=csv,noheader,nounits",
+                 "-lms", "200", "-i", gpu_id], stdout=self.out, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self) -> dict | None:
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.out.close()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) == len(CLOCK_FIELDS):
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        pw = [float(r[3]) for r in rows if r[3].replace(".", "").isdigit()]
+        reasons = []
+        for i, name in ((5, "hw_slowdown"), (6, "hw_thermal_slowdown"), (7, "sw_thermal_slowdown"),
+                        (8, "sw_power_cap")):
+            if any(r[i].lower().startswith("active") for r in rows):
+                reasons.append(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "power_w_max": max(pw) if pw else None, "reasons": reasons, "samples": len(rows)}
+
+
+def gpu_id_for(device) -> str | None:
+    import torch
+    try:
+        uuid = str(torch.cuda.get_device_properties(device).uuid)
+        return uuid if uuid.startswith("GPU-") else "GPU-" + uuid
+    except Exception:
+        return None
+
+
+# ----------------------------------------------------------------------------
+# peaks and ncu traffic
+# ----------------------------------------------------------------------------
+
+def hbm_peak() -> tuple[float, str]:
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return 6800.0, "fallback"
+
+
+def source_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "vocab_log_softmax_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        if name.endswith((".cu", ".cuh", ".h")):
+            with open(os.path.join(csrc, name), "rb") as f:
+                h.update(name.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+def traffic_for(kernel: str, n: int) -> float | None:
+    """DRAM bytes per launch from the committed ncu capture, scaled to n rows;
+    None when there is no capture or the kernels changed since it was taken."""
+    try:
+        with open(TRAFFIC_FILE) as f:
+            t = json.load(f)
+    except (OSError, ValueError):
+        return None
+    if t.get("source_hash") != source_hash():
+        return None
+    e = t.get("kernels", {}).get(kernel)
+    if not e:
+        return None
+    return e["dram_bytes_per_launch"] * n / e["rows"]
+
+
+# ----------------------------------------------------------------------------
+# the step
+# ----------------------------------------------------------------------------
+
+class Step:
+    """Device inputs, preallocated outputs, and the 12 launches of one step."""
+
+    def __init__(self, device, n: int, v: int, seed_offset: int = 0):
+        import torch
+
+        import workloads
+        self.n, self.v = n, v
+        c2 = workloads.logp_offset(device, n=n, v=v, seed=1 + seed_offset)
+        c3 = workloads.kl_masked(device, n=n, v=v, seed=2 + seed_offset)
+        c4 = workloads.softcap_wide(device, n=n, v=v, seed=3 + seed_offset)
+        self.inp = {
+            "x": c2["logits"], "ids": c2["ids"], "g": c2["g"],
+            "a": c3["a"], "b": c3["b"], "g_row": c3["g"],
+            "xc": c4["logits"], "ids_c": c4["ids"], "g_c": c4["g"], "gy": c4["gy_bf16"],
+        }
+        f32 = dict(dtype=torch.float32, device=device)
+        self.out = {
+            "lp": torch.empty((n, 1), **f32), "st": torch.empty((n, 2), **f32),
+            "st2": torch.empty((n, 2), **f32), "val": torch.empty((n,), **f32),
+            "H": torch.empty((n,), **f32), "klr": torch.empty((n,), **f32), "klf": torch.empty((n,), **f32),
+            "lpc": torch.empty((n, 1), **f32),
+            "d": torch.empty((n, v), dtype=torch.bfloat16, device=device),
+            "y": torch.empty((n, v), dtype=torch.bfloat16, device=device),
+        }
+
+    def launches(self):
+        """(op, pass, thunk) for the 12 launches of one step, in order."""
+        from vocab_log_softmax_gb300 import binding as B
+        i, o = self.inp, self.out
+        return [
+            ("logp", "fwd", lambda: B.vls_logp_fwd(i["x"], i["ids"], -100, 0.0, logp=o["lp"], stats=o["st"])),
+            ("logp", "bwd", lambda: B.vls_logp_bwd(i["x"], i["ids"], i["g"], o["st"], -100, 0.0, dlogits=o["d"])),
+            ("entropy", "fwd", lambda: B.vls_entropy_fwd(i["a"], 0.0, H=o["H"], stats=o["st"])),
+            ("entropy", "bwd", lambda: B.vls_entropy_bwd(i["a"], i["g_row"], o["H"], o["st"], 0.0, dlogits=o["d"])),
+            ("kl_reverse", "fwd", lambda: B.vls_kl_fwd(i["a"], i["b"], "reverse", 0.0, kl=o["klr"],
+                                                       stats_a=o["st"], stats_b=o["st2"])),
+            ("kl_reverse", "bwd", lambda: B.vls_kl_bwd(i["a"], i["b"], i["g_row"], o["klr"], o["st"], o["st2"],
+                                                       "reverse", 0.0, da=o["d"])),
+            ("kl_forward", "fwd", lambda: B.vls_kl_fwd(i["a"], i["b"], "forward", 0.0, kl=o["klf"],
+                                                       stats_a=o["st"], stats_b=o["st2"])),
+            ("kl_forward", "bwd", lambda: B.vls_kl_bwd(i["a"], i["b"], i["g_row"], o["klf"], o["st"], o["st2"],
+                                                       "forward", 0.0, da=o["d"])),
+            ("cap_logp", "fwd", lambda: B.vls_logp_fwd(i["xc"], i["ids_c"], -100, CAP, logp=o["lpc"], stats=o["st"])),
+            ("cap_logp", "bwd", lambda: B.vls_logp_bwd(i["xc"], i["ids_c"], i["g_c"], o["st"], -100, CAP,
+                                                       dlogits=o["d"])),
+            ("softcap", "fwd", lambda: B.vls_softcap_fwd(i["xc"], CAP, y=o["y"])),
+            ("softcap", "bwd", lambda: B.vls_softcap_bwd(i["xc"], i["gy"], CAP, gx=o["d"])),
+        ]
+
+    def results(self):
+        """The step's results a caller reads back: every forward output and
+        gradient (the gradient buffer is shared, so it is read after each op)."""
+        o = self.out
+        return [o["lp"], o["H"], o["klr"], o["klf"], o["lpc"], o["y"], o["d"]]
+
+
+def time_device(step: Step, steps: int, warmup: int, device):
+    import torch
+    launches = step.launches()
+    for _ in range(warmup):
+        for _, _, f in launches:
+            f()
+    torch.cuda.synchronize()
+    barrier()
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream(device)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(launches) + 1)] for _ in range(steps)]
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(gpu_id_for(device))
+    time.sleep(0.6)                      # let the sampler start before the timed region
+    start.record(stream)
+    for s in range(steps):
+        for j, (_, _, f) in enumerate(launches):
+            ev[s][j].record(stream)
+            f()
+        ev[s][-1].record(stream)
+    stop.record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    barrier()
+    total_ms = start.elapsed_time(stop)
+    per = {}
+    for j, (op, ps, _) in enumerate(launches):
+        per[(op, ps)] = statistics.mean(ev[s][j].elapsed_time(ev[s][j + 1]) for s in range(steps))
+    return total_ms, per, clk
+
+
+def time_e2e(step: Step, steps: int, device):
+    """Same step through the same calls, with every input copied in from
+    pinned host memory and every result copied back, inside the timed region."""
+    import torch
+    pinned_in = {k: t.detach().cpu().pin_memory() for k, t in step.inp.items()}
+    res = step.results()
+    pinned_out = [torch.empty(r.shape, dtype=r.dtype, pin_memory=True) for r in res[:-2]]
+    big = torch.empty(step.out["d"].shape, dtype=step.out["d"].dtype, pin_memory=True)
+    h2d = sum(t.numel() * t.element_size() for t in pinned_in.values())
+    launches = step.launches()
+    grad_ops = {"bwd"}
+
+    def one():
+        for k, t in pinned_in.items():
+            step.inp[k].copy_(t, non_blocking=True)
+        d2h = 0
+        for op, ps, f in launches:
+            f()
+            if ps in grad_ops:          # the shared gradient buffer is read back after each backward
+                big.copy_(step.out["d"], non_blocking=True)
+                d2h += big.numel() * big.element_size()
+        big.copy_(step.out["y"], non_blocking=True)
+        d2h += big.numel() * big.element_size()
+        for h, r in zip(pinned_out, res[:-2]):
+            h.copy_(r, non_blocking=True)
+            d2h += h.numel() * h.element_size()
+        return d2h
+
+    one()
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream(device)
+    s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s0.record(stream)
+    d2h = 0
+    for _ in range(steps):
+        d2h = one()
+    s1.record(stream)
+    torch.cuda.synchronize()
+    return s0.elapsed_time(s1) / steps, h2d, d2h
+
+
+# ----------------------------------------------------------------------------
+# CPU oracle (baseline arm)
+# ----------------------------------------------------------------------------
+
+def oracle_step(rows: dict) -> None:
+    """One pass of the whole path on the CPU fp64 oracle over the given rows."""
+    import oracle
+    x, ids, g = rows["x"], rows["ids"], rows["g"]
+    oracle.logp_fwd(x, ids)
+    oracle.logp_bwd(x, ids, g)
+    oracle.entropy_fwd(rows["a"])
+    oracle.entropy_bwd(rows["a"], rows["g_row"])
+    for d in ("reverse", "forward"):
+        oracle.kl_fwd(rows["a"], rows["b"], d)
+        oracle.kl_bwd(rows["a"], rows["b"], rows["g_row"], d)
+    oracle.logp_fwd(rows["xc"], rows["ids_c"], -100, CAP)
+    oracle.logp_bwd(rows["xc"], rows["ids_c"], rows["g_c"], -100, CAP)
+    oracle.softcap(rows["xc"], CAP)
+    oracle.softcap_grad(rows["xc"], rows["gy"], CAP)
+
+
+def host_rows(inp: dict, lo: int, hi: int) -> dict:
+    """Rows [lo, hi) of every input, decoded to float64 numpy on the host."""
+    import numpy as np
+    import torch
+
+    import oracle
+    out = {}
+    for k, t in inp.items():
+        s = t[lo:hi].detach().cpu()
+        if s.dtype == torch.bfloat16:
+            out[k] = oracle.decode_bf16_bits(s.view(torch.int16).numpy())
+        elif s.dtype.is_floating_point:
+            out[k] = s.to(torch.float64).numpy()
+        else:
+            out[k] = np.ascontiguousarray(s.numpy())
+    return out
+
+
+def cpu_baseline(inp: dict, n: int, v: int, budget_s: float = 15.0) -> dict:
+    """The oracle, as it stands, on a bounded sample of rows of the workload."""
+    probe = host_rows(inp, 0, 2)
+    t0 = time.perf_counter()
+    oracle_step(probe)
+    per_row = (time.perf_counter() - t0) / 2
+    s = int(max(2, min(n, budget_s / max(per_row, 1e-6))))
+    rows = host_rows(inp, 0, s)
+    t0 = time.perf_counter()
+    oracle_step(rows)
+    dt = time.perf_counter() - t0
+    return {"value": round(step_bytes(s, v) / dt / 1e12, 6), "unit": "TB/s", "cores": 1, "kind": "oracle",
+            "sample": f"first {s} of {n} rows of every input tensor, full V={v}; one numpy process",
+            "seconds": round(dt, 2)}
+
+
+def run_reference(args) -> None:
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    import workloads
+    n, v = args.rows, VOCAB
+    budget = 150.0
+    probe_inp = _cpu_inputs(workloads, 2, v)
+    rows = host_rows(probe_inp, 0, 2)
+    t0 = time.perf_counter()
+    oracle_step(rows)
+    per_row = (time.perf_counter() - t0) / 2
+    s = int(max(1, min(n, budget / (args.steps + args.warmup) / max(per_row, 1e-6))))
+    rows = host_rows(_cpu_inputs(workloads, s, v), 0, s)
+    for _ in range(args.warmup):
+        oracle_step(rows)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle_step(rows)
+    dt = (time.perf_counter() - t0) / args.steps
+    value = step_bytes(s, v) / dt / 1e12
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": "TB/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt * 1e3, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "rows_per_step": s, "rows_in_workload": n, "vocab": v,
+                   "sample": f"{s} rows per step (bounded sample of the {n}-row batch)"},
+        "cpu_baseline": {"value": round(value, 6), "unit": "TB/s", "cores": 1, "kind": "oracle",
+                         "sample": f"{s} of {n} rows per step, full V={v}"},
+        "e2e": {"value": round(value, 6), "unit": "TB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def _cpu_inputs(workloads, n: int, v: int) -> dict:
+    c2 = workloads.logp_offset("cpu", n=n, v=v)
+    c3 = workloads.kl_masked("cpu", n=max(n, 2), v=v)
+    c4 = workloads.softcap_wide("cpu", n=n, v=v)
+    return {"x": c2["logits"], "ids": c2["ids"], "g": c2["g"], "a": c3["a"][:n], "b": c3["b"][:n],
+            "g_row": c3["g"][:n], "xc": c4["logits"], "ids_c": c4["ids"], "g_c": c4["g"], "gy": c4["gy_bf16"]}
+
+
+# ----------------------------------------------------------------------------
+# main
+# ----------------------------------------------------------------------------
+
+def main() -> None:
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--rows", type=int, default=N_ROWS, help="rows per GPU (default 8192)")
+    ap.add_argument("--e2e-steps", type=int, default=3)
+    ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timing leg")
+    args = ap.parse_args()
+
+    if args.impl == "reference":
+        run_reference(args)
+        return
+
+    import torch
+    import torch.distributed as dist
+    rank, world, local_rank = dist_env()
+    if world > 1:
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    device = torch.device("cuda", local_rank if world > 1 else 0)
+    torch.cuda.set_device(device)
+
+    import vocab_log_softmax_gb300 as vls
+    vls.vls_version()                                     # fails loudly if libvls is missing
+    n, v = args.rows, VOCAB
+    step = Step(device, n, v, seed_offset=rank * 10)
+    torch.cuda.synchronize()
+
+    total_ms, per, clk = time_device(step, args.steps, args.warmup, device)
+    total_ms = max_over_ranks(total_ms, device)
+    ms = total_ms / args.steps
+    sb = step_bytes(n, v)
+    value = aggregate(sb, world, ms / 1e3)
+
+    per_op = {}
+    for op in OPS:
+        b = op_bytes(op, n, v)
+        f, bw = per[(op, "fwd")], per[(op, "bwd")]
+        per_op[op] = {"fwd_ms": round(f, 4), "bwd_ms": round(bw, 4), "fwd_bwd_ms": round(f + bw, 4),
+                      "fwd_tbs": round(b["fwd"] / f / 1e9, 3), "bwd_tbs": round(b["bwd"] / bw / 1e9, 3),
+                      "fwd_bwd_tbs": round((b["fwd"] + b["bwd"]) / (f + bw) / 1e9, 3)}
+    # dominant kernel: the launch with the largest share of the step's device time
+    kernel_time = {}
+    for (op, ps), t in per.items():
+        kernel_time.setdefault(KERNEL_NAMES[(op, ps)], []).append((op, ps, t))
+    dom_name, dom = max(kernel_time.items(), key=lambda kv: sum(t for _, _, t in kv[1]))
+    dom_bytes = sum(op_bytes(op, n, v)[ps] for op, ps, _ in dom)
+    dom_ms = sum(t for _, _, t in dom)
+    peak, peak_kind = hbm_peak()
+    achieved = dom_bytes / len(dom) / (dom_ms / len(dom)) / 1e6     # GB/s
+    tr = traffic_for(dom_name, n)
+    roofline = {"bound": "hbm", "kernel": dom_name, "achieved": round(achieved, 1), "peak": peak,
+                "peak_kind": peak_kind, "unit": "GB/s", "frac": round(achieved / peak, 4),
+                "traffic": None if tr is None else round(tr), "bytes_per_launch": dom_bytes // len(dom),
+                "share_of_step": round(dom_ms / ms, 4),
+                "step_frac": round(sb / (ms / 1e3) / 1e9 / peak, 4)}
+
+    e2e_ms, h2d, d2h = time_e2e(step, args.e2e_steps, device)
+    e2e_ms = max_over_ranks(e2e_ms, device)
+    e2e = {"value": round(aggregate(sb, world, e2e_ms / 1e3), 4), "unit": "TB/s", "h2d_bytes_per_step": h2d,
+           "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 3), "steps": args.e2e_steps}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(step.inp, n, v)
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": round(value, 4), "unit": "TB/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(ms, 4), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "rows_per_gpu": n, "vocab": v, "global_rows": n * world,
+                       "parallelism": f"dp{world} (row shards, no collective)",
+                       "l2": "inputs (2.5 GB per tensor) larger than L2; no flush",
+                       "bytes_per_step": sb, "per_op": per_op},
+            "roofline": roofline,
+            "cpu_baseline": cpu,
+            "e2e": e2e,
+            "gpu_launches": len(step.launches()) * args.steps,
+            "clocks": clk,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,176 @@
+/*
+ * vls.h -- C ABI of libvls, row-wise vocabulary log-softmax statistics on
+ * NVIDIA GB300 (sm_103a).
+ *
+ * A "row" is one token's logits over the vocabulary: N rows of V columns,
+ * row r starting at element r*ld of the base pointer, the V columns of a row
+ * contiguous (ld >= V; ld > V reads a slice such as logits[:, :V] in place).
+ * Every call computes in fp32 with one rounding at each store.  The softmax
+ * statistics are taken in one read of the logits (online max and sum of
+ * exponentials, "Add Triton kernels for vocab-parallel logprobs, entropy and
+ * KL", DeepSpeed PR #8838, section Changes and review "Suggested change");
+ * each forward saves per-row (max, log-sum-exp) so that its backward is one
+ * read of the logits plus one write of the gradient.
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ *  - Pointers: all data pointers are DEVICE pointers (cudaMalloc'd, or
+ *    managed memory) on one device.  The caller owns every buffer; the
+ *    library allocates, frees and synchronises nothing.
+ *  - Stream: `stream` is a cudaStream_t passed as void* (NULL = the legacy
+ *    default stream).  Every call only enqueues work on it and returns.
+ *  - Device guard: the launch goes to the device that holds the first input
+ *    pointer, whatever device is current; the current device is restored
+ *    before returning ("perf(logp): fused zero-workspace backward ...",
+ *    RL-Kernel PR #495, review "Hardening Proposals").  The stream must
+ *    belong to that device.
+ *  - Inputs are never written.  Outputs must not overlap inputs.
+ *  - N == 0 (or n == 0) returns VLS_OK without touching any pointer and
+ *    without a launch.
+ *  - Logits are finite or -inf (a mask).  A row whose logits are all -inf
+ *    has no distribution: its statistics and gradient row are NaN.
+ *  - cap: 0 means no softcap.  cap > 0 applies y = cap*tanh(x/cap) to every
+ *    logit before the softmax, in registers ("Final Logit Softcap",
+ *    section Summary); -inf logits then become -cap.
+ *  - Results are deterministic and batch invariant: a row's outputs depend
+ *    only on that row's data, V and the dtype, bit for bit, not on N, on the
+ *    row's position or on the alignment of the row in memory.
+ *  - Errors: each call returns VLS_OK (0) or one of the VLS_ERR_* codes
+ *    below; it never aborts, throws or prints.  Argument errors are found
+ *    before any CUDA call.  vls_status_string() names a code.
+ */
+#ifndef VLS_H_
+#define VLS_H_
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Element type of logits, gradients and softcap tensors. */
+typedef enum { VLS_F32 = 0, VLS_BF16 = 1 } vls_dtype;
+
+/* VLS_KL_REVERSE: KL(p_a || p_b); VLS_KL_FORWARD: KL(p_b || p_a).  In both the
+ * gradient flows to `a` (the policy) only; `b` (the reference) is detached
+ * (DeepSpeed PR #8838, review by @0z5a: "reverse KL with a detached
+ * teacher"). */
+typedef enum { VLS_KL_REVERSE = 0, VLS_KL_FORWARD = 1 } vls_kl_dir;
+
+/* Per-row statistics a forward saves for its backward: m = max_j z_j and
+ * log_s = log(sum_j exp(z_j - m)), so log p_j = (z_j - m) - log_s.  Kept as
+ * the pair rather than m + log_s so that the backward's (z - m) - log_s never
+ * adds a large common offset into an fp32 sum.  8 bytes per row. */
+typedef struct { float m; float log_s; } vls_rowstat;
+
+enum {
+  VLS_OK = 0,
+  VLS_ERR_NULL = 1,     /* a required pointer is NULL (with N > 0)               */
+  VLS_ERR_SHAPE = 2,    /* N < 0, V < 1, ld < V, k < 1 or k > VLS_MAX_TOPK, n < 0 */
+  VLS_ERR_DTYPE = 3,    /* dtype not a vls_dtype; gy dtype neither F32 nor dt     */
+  VLS_ERR_CAP = 4,      /* cap NaN, infinite or negative (softcap calls: cap <= 0) */
+  VLS_ERR_DEVICE = 5,   /* a pointer is not device memory, or pointers / stream
+                           sit on different devices                               */
+  VLS_ERR_LAUNCH = 6,   /* the CUDA launch failed (cudaGetLastError after launch) */
+  VLS_ERR_ARG = 7       /* another bad argument (e.g. an unknown KL direction)    */
+};
+
+/* Largest top-k the logprob calls accept. */
+#define VLS_MAX_TOPK 1024
+
+/* ------------------------------------------------------------------------ */
+/* Final-logit softcap, standalone ("Final Logit Softcap", Summary and       */
+/* Tensor and Precision Contract).                                           */
+/* ------------------------------------------------------------------------ */
+
+/* y[i] = cap * tanh(x[i] / cap) for i in [0, n); x and y are n contiguous
+ * elements of dtype dt (y may not alias x).  fp32 math, one cast at the
+ * store.  cap must be finite and > 0 (the page's constructor check). */
+int vls_softcap_fwd(const void* x, void* y, int64_t n, vls_dtype dt, float cap, void* stream);
+
+/* gx[i] = gy[i] * (1 - tanh^2(x[i] / cap)); the cap cancels in the derivative
+ * ("Final Logit Softcap", Summary).  x and gx have dtype dt; gy has dtype
+ * gy_dt, which is VLS_F32 or dt.  tanh is recomputed from the saved input. */
+int vls_softcap_bwd(const void* x, const void* gy, vls_dtype gy_dt, void* gx, int64_t n,
+                    vls_dtype dt, float cap, void* stream);
+
+/* ------------------------------------------------------------------------ */
+/* Target log-probabilities (DeepSpeed PR #8838, Changes; RL-Kernel PR #495, */
+/* Summary and Behavior changes).                                            */
+/* ------------------------------------------------------------------------ */
+
+/* logp[r*k + j] = log_softmax(z_r)[ids[r*k + j]] (fp32) for each of the k ids
+ * of row r, where z_r is row r of `logits` (after the softcap when cap > 0).
+ * An id is ignored when it equals ignore_index or lies outside [0, V); its
+ * logp is exactly 0.  ids: int64 [N, k] contiguous.  stats: [N], written for
+ * the backward.  1 <= k <= VLS_MAX_TOPK. */
+int vls_logp_fwd(const void* logits, int64_t ld, vls_dtype dt, int64_t N, int64_t V,
+                 const int64_t* ids, int32_t k, int64_t ignore_index, float cap,
+                 float* logp, vls_rowstat* stats, void* stream);
+
+/* Vector-Jacobian product of vls_logp_fwd for upstream g (fp32 [N, k]):
+ *   dlogits[r, c] = (sum over valid j with ids[r, j] == c of g[r, j]
+ *                    - G_r * p_r[c]) * dz/dx,
+ *   G_r = sum over valid j of g[r, j],  p_r = softmax(z_r),
+ * the one-hot terms of duplicate ids added in ascending j in fp32 before the
+ * single cast (DeepSpeed PR #8838, Changes).  A row without a valid id is
+ * written as exact zeros (RL-Kernel PR #495, Behavior changes).  dlogits:
+ * [N, V] contiguous, dtype dt.  stats: as written by vls_logp_fwd with the
+ * same logits, cap and dtype. */
+int vls_logp_bwd(const void* logits, int64_t ld, vls_dtype dt, int64_t N, int64_t V,
+                 const int64_t* ids, int32_t k, int64_t ignore_index, float cap,
+                 const float* g, const vls_rowstat* stats, void* dlogits, void* stream);
+
+/* ------------------------------------------------------------------------ */
+/* Entropy (DeepSpeed PR #8838, review "Suggested change": H = log S - W/S). */
+/* ------------------------------------------------------------------------ */
+
+/* H[r] = -sum_c p_r[c] log p_r[c] (fp32 [N]); stats [N] for the backward. */
+int vls_entropy_fwd(const void* logits, int64_t ld, vls_dtype dt, int64_t N, int64_t V,
+                    float cap, float* H, vls_rowstat* stats, void* stream);
+
+/* dlogits[r, c] = -g[r] * p_r[c] * (log p_r[c] + H[r]) * dz/dx, 0 on -inf
+ * columns.  g, H: fp32 [N]; dlogits: [N, V] contiguous, dtype dt. */
+int vls_entropy_bwd(const void* logits, int64_t ld, vls_dtype dt, int64_t N, int64_t V,
+                    float cap, const float* g, const float* H, const vls_rowstat* stats,
+                    void* dlogits, void* stream);
+
+/* ------------------------------------------------------------------------ */
+/* KL divergence (DeepSpeed PR #8838, review "Suggested change":             */
+/* KL = W/S_A - log S_A + log S_B).                                          */
+/* ------------------------------------------------------------------------ */
+
+/* kl[r] (fp32 [N]) between softmax(a_r) and softmax(b_r), in direction dir.
+ * +inf when the first distribution supports a column that the second masks
+ * (-inf logit), decided on the logits; NaN when a row of a or b is all -inf.
+ * a: rows of stride lda, b: rows of stride ldb, same dtype.  stats_a, stats_b:
+ * [N] for the backward. */
+int vls_kl_fwd(const void* a, int64_t lda, const void* b, int64_t ldb, vls_dtype dt,
+               int64_t N, int64_t V, vls_kl_dir dir, float cap, float* kl,
+               vls_rowstat* stats_a, vls_rowstat* stats_b, void* stream);
+
+/* Gradient of g[r] * kl[r] with respect to a:
+ *   reverse: da[r, c] = g p_a[c] ((log p_a[c] - log p_b[c]) - kl[r]) * dz/dx,
+ *            0 where a = -inf, a NaN row when kl[r] is +inf or NaN;
+ *   forward: da[r, c] = g (p_a[c] - p_b[c]) * dz/dx, a NaN row when kl[r] is NaN.
+ * g, kl: fp32 [N]; da: [N, V] contiguous, dtype dt. */
+int vls_kl_bwd(const void* a, int64_t lda, const void* b, int64_t ldb, vls_dtype dt,
+               int64_t N, int64_t V, vls_kl_dir dir, float cap, const float* g,
+               const float* kl, const vls_rowstat* stats_a, const vls_rowstat* stats_b,
+               void* da, void* stream);
+
+/* ------------------------------------------------------------------------ */
+/* Status                                                                    */
+/* ------------------------------------------------------------------------ */
+
+/* Static, NUL-terminated name of a status code ("VLS_OK", ...); never NULL. */
+const char* vls_status_string(int status);
+
+/* Library version, major*10000 + minor*100 + patch. */
+int vls_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* VLS_H_ */

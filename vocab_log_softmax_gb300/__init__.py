@@ -1,0 +1,156 @@
+"""vocab_log_softmax_gb300: row-wise vocabulary log-softmax statistics on
+GB300 (sm_103a).
+
+Two layers over the CUDA library libvls (C ABI in include/vls.h):
+
+* ``binding``: ``vls_*`` functions with the C ABI's names, argument
+  marshalling only (tensors in, raw pointers to the library);
+* the autograd functions below -- ``logprobs``, ``entropy``, ``kl`` and
+  ``softcap`` -- which save the forward's per-row statistics so that each
+  backward is one read of the logits and one write of the gradient.
+
+Every computation runs in the library's kernels; there is no CPU or eager
+fallback, and a missing library raises.
+"""
+
+from __future__ import annotations
+
+import torch
+
+from ._lib import VlsArgumentError, VlsError  # noqa: F401
+from .binding import (  # noqa: F401
+    vls_entropy_bwd,
+    vls_entropy_fwd,
+    vls_kl_bwd,
+    vls_kl_fwd,
+    vls_logp_bwd,
+    vls_logp_fwd,
+    vls_softcap_bwd,
+    vls_softcap_fwd,
+    vls_status_string,
+    vls_version,
+)
+
+__all__ = ["logprobs", "entropy", "kl", "softcap"]
+
+
+def _as_rows(x: torch.Tensor) -> torch.Tensor:
+    """[..., V] -> [N, V] with a contiguous vocabulary dimension (a view when possible)."""
+    if x.dim() == 0:
+        raise ValueError("expected at least one dimension (the vocabulary)")
+    v = x.shape[-1]
+    if x.dim() >= 2 and v > 1 and x.stride(-1) != 1:
+        x = x.contiguous()      # layouts the kernels cannot address are copied first
+    rows = x.reshape(-1, v)
+    if rows.shape[0] > 1 and v > 1 and rows.stride(1) != 1:
+        rows = rows.contiguous()
+    return rows
+
+
+def _cap(softcap) -> float:
+    if softcap is None:
+        return 0.0
+    c = float(softcap)
+    if not (c > 0.0 and c != float("inf")):
+        raise ValueError("softcap must be finite and positive")
+    return c
+
+
+class _Logprobs(torch.autograd.Function):
+    @staticmethod
+    def forward(ctx, logits, ids, ignore_index, cap):
+        rows = _as_rows(logits)
+        ids2 = ids.reshape(rows.shape[0], -1).to(torch.int64).contiguous()
+        logp, stats = vls_logp_fwd(rows, ids2, ignore_index, cap)
+        ctx.save_for_backward(rows, ids2, stats)
+        ctx.meta = (ignore_index, cap, logits.shape)
+        return logp.reshape(ids.shape)
+
+    @staticmethod
+    def backward(ctx, grad):
+        rows, ids2, stats = ctx.saved_tensors
+        ignore_index, cap, shape = ctx.meta
+        g = grad.reshape(ids2.shape).to(torch.float32).contiguous()
+        d = vls_logp_bwd(rows, ids2, g, stats, ignore_index, cap)
+        return d.reshape(shape), None, None, None
+
+
+class _Entropy(torch.autograd.Function):
+    @staticmethod
+    def forward(ctx, logits, cap):
+        rows = _as_rows(logits)
+        H, stats = vls_entropy_fwd(rows, cap)
+        ctx.save_for_backward(rows, H, stats)
+        ctx.meta = (cap, logits.shape)
+        return H.reshape(logits.shape[:-1])
+
+    @staticmethod
+    def backward(ctx, grad):
+        rows, H, stats = ctx.saved_tensors
+        cap, shape = ctx.meta
+        g = grad.reshape(-1).to(torch.float32).contiguous()
+        return vls_entropy_bwd(rows, g, H, stats, cap).reshape(shape), None
+
+
+class _KL(torch.autograd.Function):
+    @staticmethod
+    def forward(ctx, policy, reference, direction, cap):
+        a, b = _as_rows(policy), _as_rows(reference.detach())
+        kl, sa, sb = vls_kl_fwd(a, b, direction, cap)
+        ctx.save_for_backward(a, b, kl, sa, sb)
+        ctx.meta = (direction, cap, policy.shape)
+        return kl.reshape(policy.shape[:-1])
+
+    @staticmethod
+    def backward(ctx, grad):
+        a, b, kl, sa, sb = ctx.saved_tensors
+        direction, cap, shape = ctx.meta
+        g = grad.reshape(-1).to(torch.float32).contiguous()
+        return vls_kl_bwd(a, b, g, kl, sa, sb, direction, cap).reshape(shape), None, None, None
+
+
+class _Softcap(torch.autograd.Function):
+    @staticmethod
+    def forward(ctx, x, cap):
+        xc = x.contiguous()
+        ctx.save_for_backward(xc)
+        ctx.cap = cap
+        return vls_softcap_fwd(xc, cap)
+
+    @staticmethod
+    def backward(ctx, gy):
+        (xc,) = ctx.saved_tensors
+        if gy.dtype not in (torch.float32, xc.dtype):
+            gy = gy.to(torch.float32)
+        return vls_softcap_bwd(xc, gy.contiguous(), ctx.cap), None
+
+
+def logprobs(logits: torch.Tensor, ids: torch.Tensor, ignore_index: int = -100,
+             softcap: float | None = None) -> torch.Tensor:
+    """log_softmax(softcap(logits))[..., ids]: fp32, shaped like ``ids`` ([..., k] or [...]).
+
+    Ids equal to ``ignore_index`` or outside [0, V) give 0 and no gradient.
+    """
+    return _Logprobs.apply(logits, ids, int(ignore_index), _cap(softcap))
+
+
+def entropy(logits: torch.Tensor, softcap: float | None = None) -> torch.Tensor:
+    """Entropy of softmax(softcap(logits)) per row (fp32, shape logits.shape[:-1])."""
+    return _Entropy.apply(logits, _cap(softcap))
+
+
+def kl(policy: torch.Tensor, reference: torch.Tensor, direction: str = "reverse",
+       softcap: float | None = None) -> torch.Tensor:
+    """Per-row KL between softmax(policy) and softmax(reference).
+
+    ``direction="reverse"``: KL(p_policy || p_reference); ``"forward"``:
+    KL(p_reference || p_policy).  The gradient flows to ``policy`` only.
+    """
+    if direction not in ("reverse", "forward"):
+        raise ValueError("direction must be 'reverse' or 'forward'")
+    return _KL.apply(policy, reference, direction, _cap(softcap))
+
+
+def softcap(x: torch.Tensor, cap: float = 30.0) -> torch.Tensor:
+    """cap * tanh(x / cap), elementwise, in x's dtype."""
+    return _Softcap.apply(x, _cap(cap))

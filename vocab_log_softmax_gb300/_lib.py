@@ -1,0 +1,90 @@
+"""Loads libvls.so and declares its C ABI (include/vls.h) for ctypes.
+
+There is no fallback: if the library is missing or cannot be loaded, every
+entry point raises.  Build it with ``python -m vocab_log_softmax_gb300.build``
+(``__graft_entry__.build()`` does the same).
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+
+LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "lib", "libvls.so")
+
+VLS_F32 = 0
+VLS_BF16 = 1
+VLS_KL_REVERSE = 0
+VLS_KL_FORWARD = 1
+VLS_MAX_TOPK = 1024
+
+STATUS = {
+    0: "VLS_OK",
+    1: "VLS_ERR_NULL",
+    2: "VLS_ERR_SHAPE",
+    3: "VLS_ERR_DTYPE",
+    4: "VLS_ERR_CAP",
+    5: "VLS_ERR_DEVICE",
+    6: "VLS_ERR_LAUNCH",
+    7: "VLS_ERR_ARG",
+}
+
+_p = ctypes.c_void_p
+_i64 = ctypes.c_int64
+_i32 = ctypes.c_int32
+_int = ctypes.c_int
+_f = ctypes.c_float
+
+# name -> argument types, in the order of include/vls.h
+SIGNATURES = {
+    "vls_softcap_fwd": [_p, _p, _i64, _int, _f, _p],
+    "vls_softcap_bwd": [_p, _p, _int, _p, _i64, _int, _f, _p],
+    "vls_logp_fwd": [_p, _i64, _int, _i64, _i64, _p, _i32, _i64, _f, _p, _p, _p],
+    "vls_logp_bwd": [_p, _i64, _int, _i64, _i64, _p, _i32, _i64, _f, _p, _p, _p, _p],
+    "vls_entropy_fwd": [_p, _i64, _int, _i64, _i64, _f, _p, _p, _p],
+    "vls_entropy_bwd": [_p, _i64, _int, _i64, _i64, _f, _p, _p, _p, _p, _p],
+    "vls_kl_fwd": [_p, _i64, _p, _i64, _int, _i64, _i64, _int, _f, _p, _p, _p, _p],
+    "vls_kl_bwd": [_p, _i64, _p, _i64, _int, _i64, _i64, _int, _f, _p, _p, _p, _p, _p, _p],
+    "vls_status_string": [_int],
+    "vls_version": [],
+}
+
+_lib = None
+
+
+class VlsError(RuntimeError):
+    """A libvls call returned a status other than VLS_OK."""
+
+    def __init__(self, fn: str, status: int):
+        self.status = status
+        super().__init__(f"{fn} failed: {STATUS.get(status, status)}")
+
+
+class VlsArgumentError(VlsError, ValueError):
+    """A libvls call rejected its arguments (shape, dtype, cap, NULL pointer)."""
+
+
+def load() -> ctypes.CDLL:
+    """The loaded library (loaded once).  Raises if it has not been built."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise RuntimeError(
+            f"libvls.so not found at {LIB_PATH}; build it with "
+            "`python -m vocab_log_softmax_gb300.build` (no CPU fallback exists)")
+    lib = ctypes.CDLL(LIB_PATH)
+    for name, argtypes in SIGNATURES.items():
+        fn = getattr(lib, name)
+        fn.argtypes = argtypes
+        fn.restype = ctypes.c_char_p if name == "vls_status_string" else ctypes.c_int
+    _lib = lib
+    return lib
+
+
+def check(fn: str, status: int) -> None:
+    if status == 0:
+        return
+    if status in (1, 2, 3, 4, 7):
+        raise VlsArgumentError(fn, status)
+    raise VlsError(fn, status)

@@ -1,0 +1,185 @@
+"""Thin torch binding of the C ABI: one function per ``vls_*`` entry point,
+same names, argument marshalling only.
+
+Each function takes CUDA tensors, allocates its outputs with torch when they
+are not given, and passes raw pointers, sizes and the current CUDA stream of
+the inputs' device to libvls.  No arithmetic of the method happens here.
+
+Row layout: a logits tensor is [N, V] (or [V] for one row) whose last
+dimension is contiguous; its row stride may exceed V (a slice such as
+``logits[:, :-1]`` is read in place).  Gradients are returned contiguous.
+"""
+
+from __future__ import annotations
+
+import torch
+
+from . import _lib
+
+_DT = {torch.float32: _lib.VLS_F32, torch.bfloat16: _lib.VLS_BF16}
+_DIR = {"reverse": _lib.VLS_KL_REVERSE, "forward": _lib.VLS_KL_FORWARD}
+
+
+def _dtype(t: torch.Tensor) -> int:
+    try:
+        return _DT[t.dtype]
+    except KeyError:
+        raise TypeError(f"libvls supports float32 and bfloat16 tensors, not {t.dtype}") from None
+
+
+def _rows(t: torch.Tensor) -> tuple[int, int, int]:
+    """(N, V, row stride) of a 2-D tensor with a contiguous last dimension."""
+    if t.dim() != 2:
+        raise ValueError(f"expected a [N, V] tensor, got shape {tuple(t.shape)}")
+    n, v = t.shape
+    if v > 1 and t.stride(1) != 1:
+        raise ValueError("the vocabulary dimension must be contiguous (stride 1)")
+    if n > 1 and t.stride(0) < v:
+        raise ValueError("rows overlap (row stride smaller than V)")
+    return n, v, (t.stride(0) if n > 1 else v)
+
+
+def _stream(t: torch.Tensor, stream) -> int:
+    if stream is not None:
+        return int(stream.cuda_stream if hasattr(stream, "cuda_stream") else stream)
+    return int(torch.cuda.current_stream(t.device).cuda_stream)
+
+
+def _ptr(t) -> int | None:
+    return None if t is None else t.data_ptr()
+
+
+def _stats(n: int, device, out=None) -> torch.Tensor:
+    """vls_rowstat [N]: (m, log S) pairs as a float32 [N, 2] tensor."""
+    if out is not None:
+        return out
+    return torch.empty((n, 2), dtype=torch.float32, device=device)
+
+
+def vls_softcap_fwd(x: torch.Tensor, cap: float = 30.0, *, y=None, stream=None) -> torch.Tensor:
+    lib = _lib.load()
+    y = torch.empty_like(x, memory_format=torch.contiguous_format) if y is None else y
+    if not x.is_contiguous() or not y.is_contiguous():
+        raise ValueError("vls_softcap_fwd needs contiguous tensors")
+    st = lib.vls_softcap_fwd(_ptr(x), _ptr(y), x.numel(), _dtype(x), float(cap), _stream(x, stream))
+    _lib.check("vls_softcap_fwd", st)
+    return y
+
+
+def vls_softcap_bwd(x: torch.Tensor, gy: torch.Tensor, cap: float = 30.0, *, gx=None,
+                    stream=None) -> torch.Tensor:
+    lib = _lib.load()
+    gx = torch.empty_like(x, memory_format=torch.contiguous_format) if gx is None else gx
+    if not (x.is_contiguous() and gy.is_contiguous() and gx.is_contiguous()):
+        raise ValueError("vls_softcap_bwd needs contiguous tensors")
+    if gy.numel() != x.numel():
+        raise ValueError("gy must have as many elements as x")
+    st = lib.vls_softcap_bwd(_ptr(x), _ptr(gy), _dtype(gy), _ptr(gx), x.numel(), _dtype(x),
+                             float(cap), _stream(x, stream))
+    _lib.check("vls_softcap_bwd", st)
+    return gx
+
+
+def vls_logp_fwd(logits: torch.Tensor, ids: torch.Tensor, ignore_index: int = -100, cap: float = 0.0,
+                 *, logp=None, stats=None, stream=None) -> tuple[torch.Tensor, torch.Tensor]:
+    """Returns (logp [N, k] float32, stats [N, 2] float32)."""
+    lib = _lib.load()
+    n, v, ld = _rows(logits)
+    ids = ids.reshape(n, -1)
+    if ids.dtype != torch.int64 or not ids.is_contiguous():
+        raise ValueError("ids must be a contiguous int64 [N, k] tensor")
+    k = ids.shape[1]
+    logp = torch.empty((n, k), dtype=torch.float32, device=logits.device) if logp is None else logp
+    stats = _stats(n, logits.device, stats)
+    st = lib.vls_logp_fwd(_ptr(logits), ld, _dtype(logits), n, v, _ptr(ids), k, int(ignore_index),
+                          float(cap), _ptr(logp), _ptr(stats), _stream(logits, stream))
+    _lib.check("vls_logp_fwd", st)
+    return logp, stats
+
+
+def vls_logp_bwd(logits: torch.Tensor, ids: torch.Tensor, g: torch.Tensor, stats: torch.Tensor,
+                 ignore_index: int = -100, cap: float = 0.0, *, dlogits=None,
+                 stream=None) -> torch.Tensor:
+    lib = _lib.load()
+    n, v, ld = _rows(logits)
+    ids = ids.reshape(n, -1)
+    k = ids.shape[1]
+    g = g.reshape(n, k)
+    if g.dtype != torch.float32 or not g.is_contiguous():
+        raise ValueError("g must be a contiguous float32 [N, k] tensor")
+    if dlogits is None:
+        dlogits = torch.empty((n, v), dtype=logits.dtype, device=logits.device)
+    st = lib.vls_logp_bwd(_ptr(logits), ld, _dtype(logits), n, v, _ptr(ids), k, int(ignore_index),
+                          float(cap), _ptr(g), _ptr(stats), _ptr(dlogits), _stream(logits, stream))
+    _lib.check("vls_logp_bwd", st)
+    return dlogits
+
+
+def vls_entropy_fwd(logits: torch.Tensor, cap: float = 0.0, *, H=None, stats=None,
+                    stream=None) -> tuple[torch.Tensor, torch.Tensor]:
+    lib = _lib.load()
+    n, v, ld = _rows(logits)
+    H = torch.empty((n,), dtype=torch.float32, device=logits.device) if H is None else H
+    stats = _stats(n, logits.device, stats)
+    st = lib.vls_entropy_fwd(_ptr(logits), ld, _dtype(logits), n, v, float(cap), _ptr(H), _ptr(stats),
+                             _stream(logits, stream))
+    _lib.check("vls_entropy_fwd", st)
+    return H, stats
+
+
+def vls_entropy_bwd(logits: torch.Tensor, g: torch.Tensor, H: torch.Tensor, stats: torch.Tensor,
+                    cap: float = 0.0, *, dlogits=None, stream=None) -> torch.Tensor:
+    lib = _lib.load()
+    n, v, ld = _rows(logits)
+    if g.dtype != torch.float32 or not g.is_contiguous():
+        raise ValueError("g must be a contiguous float32 [N] tensor")
+    if dlogits is None:
+        dlogits = torch.empty((n, v), dtype=logits.dtype, device=logits.device)
+    st = lib.vls_entropy_bwd(_ptr(logits), ld, _dtype(logits), n, v, float(cap), _ptr(g), _ptr(H),
+                             _ptr(stats), _ptr(dlogits), _stream(logits, stream))
+    _lib.check("vls_entropy_bwd", st)
+    return dlogits
+
+
+def vls_kl_fwd(a: torch.Tensor, b: torch.Tensor, direction: str = "reverse", cap: float = 0.0, *,
+               kl=None, stats_a=None, stats_b=None,
+               stream=None) -> tuple[torch.Tensor, torch.Tensor, torch.Tensor]:
+    """Returns (kl [N], stats_a [N, 2], stats_b [N, 2])."""
+    lib = _lib.load()
+    n, v, lda = _rows(a)
+    nb, vb, ldb = _rows(b)
+    if (nb, vb) != (n, v):
+        raise ValueError("a and b must have the same shape")
+    if a.dtype != b.dtype:
+        raise TypeError("a and b must have the same dtype")
+    kl = torch.empty((n,), dtype=torch.float32, device=a.device) if kl is None else kl
+    stats_a = _stats(n, a.device, stats_a)
+    stats_b = _stats(n, a.device, stats_b)
+    st = lib.vls_kl_fwd(_ptr(a), lda, _ptr(b), ldb, _dtype(a), n, v, _DIR[direction], float(cap), _ptr(kl),
+                        _ptr(stats_a), _ptr(stats_b), _stream(a, stream))
+    _lib.check("vls_kl_fwd", st)
+    return kl, stats_a, stats_b
+
+
+def vls_kl_bwd(a: torch.Tensor, b: torch.Tensor, g: torch.Tensor, kl: torch.Tensor, stats_a: torch.Tensor,
+               stats_b: torch.Tensor, direction: str = "reverse", cap: float = 0.0, *, da=None,
+               stream=None) -> torch.Tensor:
+    lib = _lib.load()
+    n, v, lda = _rows(a)
+    _, _, ldb = _rows(b)
+    if g.dtype != torch.float32 or not g.is_contiguous():
+        raise ValueError("g must be a contiguous float32 [N] tensor")
+    if da is None:
+        da = torch.empty((n, v), dtype=a.dtype, device=a.device)
+    st = lib.vls_kl_bwd(_ptr(a), lda, _ptr(b), ldb, _dtype(a), n, v, _DIR[direction], float(cap), _ptr(g),
+                        _ptr(kl), _ptr(stats_a), _ptr(stats_b), _ptr(da), _stream(a, stream))
+    _lib.check("vls_kl_bwd", st)
+    return da
+
+
+def vls_status_string(status: int) -> str:
+    return _lib.load().vls_status_string(int(status)).decode()
+
+
+def vls_version() -> int:
+    return int(_lib.load().vls_version())

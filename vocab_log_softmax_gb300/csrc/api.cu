@@ -1,0 +1,371 @@
+// C ABI of libvls (declared in include/vls.h): argument validation, the
+// device guard, the launch-geometry policy and dispatch to the kernels.
+//
+// Validation order for every call: shapes, dtypes and cap first (no CUDA
+// call), then the empty-input fast return, then NULL pointers, then the
+// device of every pointer and of the stream, then the launch.
+#include <cmath>
+#include <cstdlib>
+#include <cstring>
+#include <initializer_list>
+
+#include "vls_internal.h"
+
+namespace vls {
+namespace {
+
+constexpr int64_t kMaxGrid = 0x7fffffff;
+
+bool dtype_ok(int dt) { return dt == VLS_F32 || dt == VLS_BF16; }
+
+// cap == 0 disables the softcap in the row calls; NaN, inf and negative
+// values are rejected ("Final Logit Softcap", Summary: the cap must be finite
+// and positive).
+int check_row_cap(float cap) { return (std::isfinite(cap) && cap >= 0.0f) ? VLS_OK : VLS_ERR_CAP; }
+int check_softcap_cap(float cap) { return (std::isfinite(cap) && cap > 0.0f) ? VLS_OK : VLS_ERR_CAP; }
+
+int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+// Optional tuning overrides (read once); they change the reduction tree, so
+// results are reproducible for a fixed setting only.
+int64_t env_int(const char* name, int64_t fallback) {
+  const char* s = std::getenv(name);
+  if (!s || !*s) return fallback;
+  const long long v = std::atoll(s);
+  return v > 0 ? v : fallback;
+}
+
+// Forward geometry: a function of V only.  Target ~2048 vectors (16384
+// columns) per CTA, at most 8 CTAs (one portable cluster) per row.
+void fwd_geometry(int64_t V, int* cluster, int64_t* vec_per_cta) {
+  static const int64_t target = env_int("VLS_FWD_VEC_PER_CTA", 2048);
+  const int64_t nvec = ceil_div(V, 8);
+  int64_t c = ceil_div(nvec, target);
+  if (c < 1) c = 1;
+  if (c > kMaxCluster) c = kMaxCluster;
+  *cluster = static_cast<int>(c);
+  *vec_per_cta = ceil_div(nvec, c);
+}
+
+// Backward geometry: results do not depend on it (pure map).  Top-k rows
+// prepare their id list once per CTA, so they take longer chunks.
+void bwd_geometry(int64_t V, int32_t k, int* chunks, int64_t* vec_per_cta) {
+  static const int64_t target = env_int("VLS_BWD_VEC_PER_CTA", 4096);
+  const int64_t nvec = ceil_div(V, 8);
+  const int64_t t = k > 1 ? 4 * target : target;
+  int64_t c = ceil_div(nvec, t);
+  if (c < 1) c = 1;
+  *chunks = static_cast<int>(c);
+  *vec_per_cta = ceil_div(nvec, c);
+}
+
+int sm_count(int dev) {
+  static int cache[64] = {0};
+  if (dev >= 0 && dev < 64 && cache[dev] > 0) return cache[dev];
+  int n = 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) {
+    cudaGetLastError();
+    n = 1;
+  }
+  if (dev >= 0 && dev < 64) cache[dev] = n;
+  return n;
+}
+
+// Finds the one device that holds every non-NULL pointer and owns the stream.
+int resolve_device(std::initializer_list<const void*> ptrs, void* stream, int* dev_out) {
+  int dev = -1;
+  for (const void* p : ptrs) {
+    if (!p) continue;
+    cudaPointerAttributes at;
+    if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+      cudaGetLastError();
+      return VLS_ERR_DEVICE;
+    }
+    if (at.type != cudaMemoryTypeDevice && at.type != cudaMemoryTypeManaged) return VLS_ERR_DEVICE;
+    if (dev < 0) dev = at.device;
+    if (at.device != dev) return VLS_ERR_DEVICE;
+  }
+  if (dev < 0) return VLS_ERR_DEVICE;
+  // NULL, cudaStreamLegacy (1) and cudaStreamPerThread (2) are per-device
+  // handles: they refer to the device made current by the guard.
+  if (reinterpret_cast<uintptr_t>(stream) > 2) {
+    int sdev = -1;
+    if (cudaStreamGetDevice(static_cast<cudaStream_t>(stream), &sdev) != cudaSuccess) {
+      cudaGetLastError();
+      return VLS_ERR_DEVICE;
+    }
+    if (sdev != dev) return VLS_ERR_DEVICE;
+  }
+  *dev_out = dev;
+  return VLS_OK;
+}
+
+// Makes `dev` current for the launch and restores the caller's device.
+class DeviceGuard {
+ public:
+  int enter(int dev) {
+    if (cudaGetDevice(&prev_) != cudaSuccess) {
+      cudaGetLastError();
+      return VLS_ERR_DEVICE;
+    }
+    if (prev_ != dev) {
+      if (cudaSetDevice(dev) != cudaSuccess) {
+        cudaGetLastError();
+        return VLS_ERR_DEVICE;
+      }
+      switched_ = true;
+    }
+    return VLS_OK;
+  }
+  ~DeviceGuard() {
+    if (switched_) cudaSetDevice(prev_);
+  }
+
+ private:
+  int prev_ = -1;
+  bool switched_ = false;
+};
+
+int launch_status(cudaError_t e) {
+  if (e == cudaSuccess) e = cudaGetLastError();
+  else cudaGetLastError();
+  return e == cudaSuccess ? VLS_OK : VLS_ERR_LAUNCH;
+}
+
+int check_rows(int64_t N, int64_t V, int64_t ld) {
+  if (N < 0 || V < 1 || ld < V) return VLS_ERR_SHAPE;
+  return VLS_OK;
+}
+
+FwdArgs fwd_args(int64_t N, int64_t V, float cap) {
+  FwdArgs a;
+  std::memset(&a, 0, sizeof(a));
+  a.rows = N;
+  a.vocab = V;
+  a.cap = cap;
+  a.rcap = cap > 0.0f ? 1.0f / cap : 0.0f;
+  fwd_geometry(V, &a.cluster, &a.vec_per_cta);
+  return a;
+}
+
+BwdArgs bwd_args(int64_t N, int64_t V, int32_t k, float cap) {
+  BwdArgs a;
+  std::memset(&a, 0, sizeof(a));
+  a.rows = N;
+  a.vocab = V;
+  a.cap = cap;
+  a.rcap = cap > 0.0f ? 1.0f / cap : 0.0f;
+  a.k = k;
+  bwd_geometry(V, k, &a.chunks, &a.vec_per_cta);
+  return a;
+}
+
+}  // namespace
+}  // namespace vls
+
+using namespace vls;
+
+extern "C" {
+
+int vls_version(void) { return 100; }
+
+const char* vls_status_string(int status) {
+  switch (status) {
+    case VLS_OK: return "VLS_OK";
+    case VLS_ERR_NULL: return "VLS_ERR_NULL: a required pointer is NULL";
+    case VLS_ERR_SHAPE: return "VLS_ERR_SHAPE: bad N, V, ld, k or n";
+    case VLS_ERR_DTYPE: return "VLS_ERR_DTYPE: unsupported dtype";
+    case VLS_ERR_CAP: return "VLS_ERR_CAP: cap must be finite and non-negative (softcap calls: positive)";
+    case VLS_ERR_DEVICE: return "VLS_ERR_DEVICE: pointer not device memory, or pointers/stream on different devices";
+    case VLS_ERR_LAUNCH: return "VLS_ERR_LAUNCH: CUDA launch failed";
+    case VLS_ERR_ARG: return "VLS_ERR_ARG: bad argument";
+    default: return "VLS_ERR_UNKNOWN";
+  }
+}
+
+int vls_softcap_fwd(const void* x, void* y, int64_t n, vls_dtype dt, float cap, void* stream) {
+  if (n < 0) return VLS_ERR_SHAPE;
+  if (!dtype_ok(dt)) return VLS_ERR_DTYPE;
+  if (int e = check_softcap_cap(cap)) return e;
+  if (n == 0) return VLS_OK;
+  if (!x || !y) return VLS_ERR_NULL;
+  int dev;
+  if (int e = resolve_device({x, y}, stream, &dev)) return e;
+  DeviceGuard guard;
+  if (int e = guard.enter(dev)) return e;
+  CapArgs a{x, nullptr, 0, y, n, cap, 1.0f / cap, 0};
+  const int64_t want = ceil_div(ceil_div(n, 8), 256);
+  const int64_t cap_grid = static_cast<int64_t>(sm_count(dev)) * 8;
+  a.grid = static_cast<int>(want < cap_grid ? (want < 1 ? 1 : want) : cap_grid);
+  return launch_status(launch_softcap_fwd(dt, a, static_cast<cudaStream_t>(stream)));
+}
+
+int vls_softcap_bwd(const void* x, const void* gy, vls_dtype gy_dt, void* gx, int64_t n, vls_dtype dt,
+                    float cap, void* stream) {
+  if (n < 0) return VLS_ERR_SHAPE;
+  if (!dtype_ok(dt) || !dtype_ok(gy_dt) || (gy_dt != VLS_F32 && gy_dt != dt)) return VLS_ERR_DTYPE;
+  if (int e = check_softcap_cap(cap)) return e;
+  if (n == 0) return VLS_OK;
+  if (!x || !gy || !gx) return VLS_ERR_NULL;
+  int dev;
+  if (int e = resolve_device({x, gy, gx}, stream, &dev)) return e;
+  DeviceGuard guard;
+  if (int e = guard.enter(dev)) return e;
+  CapArgs a{x, gy, gy_dt == VLS_F32 ? 1 : 0, gx, n, cap, 1.0f / cap, 0};
+  const int64_t want = ceil_div(ceil_div(n, 8), 256);
+  const int64_t cap_grid = static_cast<int64_t>(sm_count(dev)) * 8;
+  a.grid = static_cast<int>(want < cap_grid ? (want < 1 ? 1 : want) : cap_grid);
+  return launch_status(launch_softcap_bwd(dt, a, static_cast<cudaStream_t>(stream)));
+}
+
+int vls_logp_fwd(const void* logits, int64_t ld, vls_dtype dt, int64_t N, int64_t V, const int64_t* ids,
+                 int32_t k, int64_t ignore_index, float cap, float* logp, vls_rowstat* stats,
+                 void* stream) {
+  if (int e = check_rows(N, V, ld)) return e;
+  if (k < 1 || k > VLS_MAX_TOPK) return VLS_ERR_SHAPE;
+  if (!dtype_ok(dt)) return VLS_ERR_DTYPE;
+  if (int e = check_row_cap(cap)) return e;
+  if (N == 0) return VLS_OK;
+  if (!logits || !ids || !logp || !stats) return VLS_ERR_NULL;
+  FwdArgs a = fwd_args(N, V, cap);
+  if (N * a.cluster > kMaxGrid) return VLS_ERR_SHAPE;
+  int dev;
+  if (int e = resolve_device({logits, ids, logp, stats}, stream, &dev)) return e;
+  DeviceGuard guard;
+  if (int e = guard.enter(dev)) return e;
+  a.x = logits;
+  a.ldx = ld;
+  a.ids = ids;
+  a.k = k;
+  a.ignore_index = ignore_index;
+  a.logp = logp;
+  a.stats_x = stats;
+  return launch_status(launch_fwd_logp(dt, cap > 0.0f, a, static_cast<cudaStream_t>(stream)));
+}
+
+int vls_logp_bwd(const void* logits, int64_t ld, vls_dtype dt, int64_t N, int64_t V, const int64_t* ids,
+                 int32_t k, int64_t ignore_index, float cap, const float* g, const vls_rowstat* stats,
+                 void* dlogits, void* stream) {
+  if (int e = check_rows(N, V, ld)) return e;
+  if (k < 1 || k > VLS_MAX_TOPK) return VLS_ERR_SHAPE;
+  if (!dtype_ok(dt)) return VLS_ERR_DTYPE;
+  if (int e = check_row_cap(cap)) return e;
+  if (N == 0) return VLS_OK;
+  if (!logits || !ids || !g || !stats || !dlogits) return VLS_ERR_NULL;
+  BwdArgs a = bwd_args(N, V, k, cap);
+  if (N * a.chunks > kMaxGrid) return VLS_ERR_SHAPE;
+  int dev;
+  if (int e = resolve_device({logits, ids, g, stats, dlogits}, stream, &dev)) return e;
+  DeviceGuard guard;
+  if (int e = guard.enter(dev)) return e;
+  a.x = logits;
+  a.ldx = ld;
+  a.ids = ids;
+  a.ignore_index = ignore_index;
+  a.g = g;
+  a.stats_x = stats;
+  a.dx = dlogits;
+  return launch_status(launch_bwd_logp(dt, cap > 0.0f, a, static_cast<cudaStream_t>(stream)));
+}
+
+int vls_entropy_fwd(const void* logits, int64_t ld, vls_dtype dt, int64_t N, int64_t V, float cap,
+                    float* H, vls_rowstat* stats, void* stream) {
+  if (int e = check_rows(N, V, ld)) return e;
+  if (!dtype_ok(dt)) return VLS_ERR_DTYPE;
+  if (int e = check_row_cap(cap)) return e;
+  if (N == 0) return VLS_OK;
+  if (!logits || !H || !stats) return VLS_ERR_NULL;
+  FwdArgs a = fwd_args(N, V, cap);
+  if (N * a.cluster > kMaxGrid) return VLS_ERR_SHAPE;
+  int dev;
+  if (int e = resolve_device({logits, H, stats}, stream, &dev)) return e;
+  DeviceGuard guard;
+  if (int e = guard.enter(dev)) return e;
+  a.x = logits;
+  a.ldx = ld;
+  a.out = H;
+  a.stats_x = stats;
+  return launch_status(launch_fwd_entropy(dt, cap > 0.0f, a, static_cast<cudaStream_t>(stream)));
+}
+
+int vls_entropy_bwd(const void* logits, int64_t ld, vls_dtype dt, int64_t N, int64_t V, float cap,
+                    const float* g, const float* H, const vls_rowstat* stats, void* dlogits,
+                    void* stream) {
+  if (int e = check_rows(N, V, ld)) return e;
+  if (!dtype_ok(dt)) return VLS_ERR_DTYPE;
+  if (int e = check_row_cap(cap)) return e;
+  if (N == 0) return VLS_OK;
+  if (!logits || !g || !H || !stats || !dlogits) return VLS_ERR_NULL;
+  BwdArgs a = bwd_args(N, V, 1, cap);
+  if (N * a.chunks > kMaxGrid) return VLS_ERR_SHAPE;
+  int dev;
+  if (int e = resolve_device({logits, g, H, stats, dlogits}, stream, &dev)) return e;
+  DeviceGuard guard;
+  if (int e = guard.enter(dev)) return e;
+  a.x = logits;
+  a.ldx = ld;
+  a.g = g;
+  a.fout = H;
+  a.stats_x = stats;
+  a.dx = dlogits;
+  return launch_status(launch_bwd_entropy(dt, cap > 0.0f, a, static_cast<cudaStream_t>(stream)));
+}
+
+int vls_kl_fwd(const void* pa, int64_t lda, const void* pb, int64_t ldb, vls_dtype dt, int64_t N, int64_t V,
+               vls_kl_dir dir, float cap, float* kl, vls_rowstat* stats_a, vls_rowstat* stats_b,
+               void* stream) {
+  if (int e = check_rows(N, V, lda)) return e;
+  if (ldb < V) return VLS_ERR_SHAPE;
+  if (!dtype_ok(dt)) return VLS_ERR_DTYPE;
+  if (dir != VLS_KL_REVERSE && dir != VLS_KL_FORWARD) return VLS_ERR_ARG;
+  if (int e = check_row_cap(cap)) return e;
+  if (N == 0) return VLS_OK;
+  if (!pa || !pb || !kl || !stats_a || !stats_b) return VLS_ERR_NULL;
+  FwdArgs a = fwd_args(N, V, cap);
+  if (N * a.cluster > kMaxGrid) return VLS_ERR_SHAPE;
+  int dev;
+  if (int e = resolve_device({pa, pb, kl, stats_a, stats_b}, stream, &dev)) return e;
+  DeviceGuard guard;
+  if (int e = guard.enter(dev)) return e;
+  // the sweep's first argument is the distribution the expectation is over
+  const bool rev = dir == VLS_KL_REVERSE;
+  a.x = rev ? pa : pb;
+  a.ldx = rev ? lda : ldb;
+  a.y = rev ? pb : pa;
+  a.ldy = rev ? ldb : lda;
+  a.stats_x = rev ? stats_a : stats_b;
+  a.stats_y = rev ? stats_b : stats_a;
+  a.out = kl;
+  return launch_status(launch_fwd_kl(dt, cap > 0.0f, a, static_cast<cudaStream_t>(stream)));
+}
+
+int vls_kl_bwd(const void* pa, int64_t lda, const void* pb, int64_t ldb, vls_dtype dt, int64_t N, int64_t V,
+               vls_kl_dir dir, float cap, const float* g, const float* kl, const vls_rowstat* stats_a,
+               const vls_rowstat* stats_b, void* da, void* stream) {
+  if (int e = check_rows(N, V, lda)) return e;
+  if (ldb < V) return VLS_ERR_SHAPE;
+  if (!dtype_ok(dt)) return VLS_ERR_DTYPE;
+  if (dir != VLS_KL_REVERSE && dir != VLS_KL_FORWARD) return VLS_ERR_ARG;
+  if (int e = check_row_cap(cap)) return e;
+  if (N == 0) return VLS_OK;
+  if (!pa || !pb || !g || !kl || !stats_a || !stats_b || !da) return VLS_ERR_NULL;
+  BwdArgs a = bwd_args(N, V, 1, cap);
+  if (N * a.chunks > kMaxGrid) return VLS_ERR_SHAPE;
+  int dev;
+  if (int e = resolve_device({pa, pb, g, kl, stats_a, stats_b, da}, stream, &dev)) return e;
+  DeviceGuard guard;
+  if (int e = guard.enter(dev)) return e;
+  a.x = pa;
+  a.ldx = lda;
+  a.y = pb;
+  a.ldy = ldb;
+  a.g = g;
+  a.fout = kl;
+  a.stats_x = stats_a;
+  a.stats_y = stats_b;
+  a.dx = da;
+  return launch_status(
+      launch_bwd_kl(dir == VLS_KL_REVERSE, dt, cap > 0.0f, a, static_cast<cudaStream_t>(stream)));
+}
+
+}  // extern "C"

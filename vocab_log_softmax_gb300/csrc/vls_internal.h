@@ -1,0 +1,99 @@
+// Internal declarations shared by the C-ABI layer (api.cpp) and the kernel
+// translation units.  Nothing here is part of the public ABI.
+#pragma once
+
+#include <cstdint>
+
+#include <cuda_runtime.h>
+
+#include "vls.h"
+
+namespace vls {
+
+// Statistic computed by the one-read forward sweep.
+enum FwdOp { kFwdLogp = 0, kFwdEntropy = 1, kFwdKl = 2 };
+// Gradient map applied by the backward sweep.
+enum BwdOp { kBwdLogp = 0, kBwdEntropy = 1, kBwdKlReverse = 2, kBwdKlForward = 3 };
+
+// Threads per CTA of the row kernels.  Each thread owns whole 8-column
+// vectors; the reduction tree (lanes, then warps, then cluster ranks) is a
+// function of this constant and of the cluster size, never of N.
+constexpr int kRowThreads = 256;
+constexpr int kRowWarps = kRowThreads / 32;
+// Vectors each thread loads before using any of them (memory-level
+// parallelism).  Changing it does not change results: every thread still
+// visits its vectors in increasing order.
+constexpr int kUnroll = 4;
+constexpr int kMaxCluster = 8;
+
+struct FwdArgs {
+  // logits (logp / entropy), or the first KL argument: the distribution the
+  // expectation is taken over (a for reverse KL, b for forward KL)
+  const void* x;
+  int64_t ldx;
+  // second KL argument (KL only)
+  const void* y;
+  int64_t ldy;
+  int64_t rows;
+  int64_t vocab;
+  float cap;   // 0 = no softcap
+  float rcap;  // 1/cap rounded once (0 when cap == 0)
+  // logp
+  const int64_t* ids;
+  int32_t k;
+  int64_t ignore_index;
+  float* logp;
+  // entropy H or KL value per row
+  float* out;
+  // per-row stats of x and (KL) of y
+  vls_rowstat* stats_x;
+  vls_rowstat* stats_y;
+  // launch geometry: CTAs per row (= cluster size) and 8-column vectors per CTA
+  int cluster;
+  int64_t vec_per_cta;
+};
+
+struct BwdArgs {
+  const void* x;  // logits / policy a
+  int64_t ldx;
+  const void* y;  // reference b (KL only)
+  int64_t ldy;
+  int64_t rows;
+  int64_t vocab;
+  float cap;
+  float rcap;
+  const int64_t* ids;
+  int32_t k;
+  int64_t ignore_index;
+  const float* g;      // upstream gradient: [N, k] (logp) or [N]
+  const float* fout;   // forward value per row: H (entropy) or KL
+  const vls_rowstat* stats_x;
+  const vls_rowstat* stats_y;
+  void* dx;            // [N, V] contiguous gradient, dtype of x
+  int chunks;          // CTAs per row
+  int64_t vec_per_cta;
+};
+
+struct CapArgs {
+  const void* x;
+  const void* gy;   // backward only
+  int gy_f32;       // gy is fp32 (else the dtype of x)
+  void* out;        // y (forward) or gx (backward)
+  int64_t n;
+  float cap;
+  float rcap;
+  int grid;
+};
+
+// Launchers: one per kernel family, dispatching on dtype and softcap.  They
+// return a cudaError_t of the launch.
+cudaError_t launch_fwd_logp(vls_dtype dt, bool cap, const FwdArgs& a, cudaStream_t s);
+cudaError_t launch_fwd_entropy(vls_dtype dt, bool cap, const FwdArgs& a, cudaStream_t s);
+cudaError_t launch_fwd_kl(vls_dtype dt, bool cap, const FwdArgs& a, cudaStream_t s);
+cudaError_t launch_bwd_logp(vls_dtype dt, bool cap, const BwdArgs& a, cudaStream_t s);
+cudaError_t launch_bwd_entropy(vls_dtype dt, bool cap, const BwdArgs& a, cudaStream_t s);
+cudaError_t launch_bwd_kl(bool reverse, vls_dtype dt, bool cap, const BwdArgs& a, cudaStream_t s);
+cudaError_t launch_softcap_fwd(vls_dtype dt, const CapArgs& a, cudaStream_t s);
+cudaError_t launch_softcap_bwd(vls_dtype dt, const CapArgs& a, cudaStream_t s);
+
+}  // namespace vls
