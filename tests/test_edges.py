@@ -118,7 +118,7 @@ def test_topk(k):
     g = _gen(k + 1)
     ids = torch.randint(0, v, (3, k), generator=g, device=DEV)
     if k > 2:
-        ids[0, k // 2:] = ids[0, : k - k // 2]      # many duplicates
+        ids[0, k // 2:] = ids[0, : k - k // 2].clone()   # many duplicates
         ids[1, ::3] = -100
         ids[2, 1] = v + 1
     gk = torch.randn((3, k), generator=g, device=DEV)

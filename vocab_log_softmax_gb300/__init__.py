@@ -60,7 +60,7 @@ class _Logprobs(torch.autograd.Function):
     @staticmethod
     def forward(ctx, logits, ids, ignore_index, cap):
         rows = _as_rows(logits)
-        ids2 = ids.reshape(rows.shape[0], -1).to(torch.int64).contiguous()
+        ids2 = ids.reshape(rows.shape[0], ids.shape[-1] if ids.dim() > 1 else 1).to(torch.int64).contiguous()
         logp, stats = vls_logp_fwd(rows, ids2, ignore_index, cap)
         ctx.save_for_backward(rows, ids2, stats)
         ctx.meta = (ignore_index, cap, logits.shape)

@@ -39,6 +39,12 @@ def _rows(t: torch.Tensor) -> tuple[int, int, int]:
     return n, v, (t.stride(0) if n > 1 else v)
 
 
+def _ids2d(ids: torch.Tensor, n: int) -> torch.Tensor:
+    """ids as [N, k] (a 1-D tensor is [N] with k = 1)."""
+    k = ids.shape[-1] if ids.dim() >= 2 else 1
+    return ids.reshape(n, k)
+
+
 def _stream(t: torch.Tensor, stream) -> int:
     if stream is not None:
         return int(stream.cuda_stream if hasattr(stream, "cuda_stream") else stream)
@@ -85,7 +91,7 @@ def vls_logp_fwd(logits: torch.Tensor, ids: torch.Tensor, ignore_index: int = -1
     """Returns (logp [N, k] float32, stats [N, 2] float32)."""
     lib = _lib.load()
     n, v, ld = _rows(logits)
-    ids = ids.reshape(n, -1)
+    ids = _ids2d(ids, n)
     if ids.dtype != torch.int64 or not ids.is_contiguous():
         raise ValueError("ids must be a contiguous int64 [N, k] tensor")
     k = ids.shape[1]
@@ -102,7 +108,7 @@ def vls_logp_bwd(logits: torch.Tensor, ids: torch.Tensor, g: torch.Tensor, stats
                  stream=None) -> torch.Tensor:
     lib = _lib.load()
     n, v, ld = _rows(logits)
-    ids = ids.reshape(n, -1)
+    ids = _ids2d(ids, n)
     k = ids.shape[1]
     g = g.reshape(n, k)
     if g.dtype != torch.float32 or not g.is_contiguous():

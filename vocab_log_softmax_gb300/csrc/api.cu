@@ -35,10 +35,12 @@ int64_t env_int(const char* name, int64_t fallback) {
   return v > 0 ? v : fallback;
 }
 
-// Forward geometry: a function of V only.  Target ~2048 vectors (16384
-// columns) per CTA, at most 8 CTAs (one portable cluster) per row.
+// Forward geometry: a function of V only.  One CTA per row up to 24576
+// vectors (196608 columns), then a cluster of up to 8 CTAs.  Fewer, longer
+// CTAs win at the row counts this path serves (thousands of rows): every CTA
+// of a cluster waits at the cluster barrier for its slowest sibling.
 void fwd_geometry(int64_t V, int* cluster, int64_t* vec_per_cta) {
-  static const int64_t target = env_int("VLS_FWD_VEC_PER_CTA", 2048);
+  static const int64_t target = env_int("VLS_FWD_VEC_PER_CTA", 24576);
   const int64_t nvec = ceil_div(V, 8);
   int64_t c = ceil_div(nvec, target);
   if (c < 1) c = 1;

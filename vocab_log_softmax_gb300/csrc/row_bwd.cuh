@@ -14,12 +14,7 @@
 
 namespace vls {
 
-// p = exp((z - m) - log S), formed as 2^((z - m) log2 e - log S log2 e); z - m
-// is exact for bf16 logits and keeps a large common offset out of the
-// exponent.
-__device__ __forceinline__ float prob(float z, float m, float log_s_l2e) {
-  return dev::ex2(fmaf(z - m, dev::kLog2e, -log_s_l2e));
-}
+using namespace dev;
 
 // Per-CTA prepared form of a row's top-k ids: G = sum of the upstream
 // gradients of the valid ids (ascending j), and, for each distinct valid id
@@ -29,17 +24,20 @@ __device__ __forceinline__ float prob(float z, float m, float log_s_l2e) {
 struct TopkPrep {
   float G;
   int nfix;
+  bool any_valid;
 };
 
-__device__ __forceinline__ TopkPrep prep_topk(const BwdArgs& a, int64_t row, int64_t col_beg,
-                                              int64_t col_end, int64_t* s_id, float* s_g,
-                                              int64_t* fix_id, float* fix_g, float* s_G,
-                                              int* s_nfix) {
+__device__ __forceinline__ TopkPrep prep_topk(const BwdArgs& a, int64_t row, int64_t col_beg, int64_t col_end,
+                                              int64_t* s_id, float* s_g, int64_t* fix_id, float* fix_g,
+                                              float* s_G, int* s_nfix, int* s_any) {
   const int k = a.k;
   const int64_t V = a.vocab;
   const int64_t* ids = a.ids + row * k;
   const float* g = a.g + row * k;
-  if (threadIdx.x == 0) *s_nfix = 0;
+  if (threadIdx.x == 0) {
+    *s_nfix = 0;
+    *s_any = 0;
+  }
   for (int j = threadIdx.x; j < k; j += kRowThreads) {
     s_id[j] = ids[j];
     s_g[j] = g[j];
@@ -47,13 +45,18 @@ __device__ __forceinline__ TopkPrep prep_topk(const BwdArgs& a, int64_t row, int
   __syncthreads();
   if (threadIdx.x == 0) {
     float G = 0.0f;
+    int any = 0;
     for (int j = 0; j < k; ++j)
-      if (dev::valid_id(s_id[j], V, a.ignore_index)) G += s_g[j];
+      if (valid_id(s_id[j], V, a.ignore_index)) {
+        G += s_g[j];
+        any = 1;
+      }
     *s_G = G;
+    *s_any = any;
   }
   for (int j = threadIdx.x; j < k; j += kRowThreads) {
     const int64_t id = s_id[j];
-    if (!dev::valid_id(id, V, a.ignore_index) || id < col_beg || id >= col_end) continue;
+    if (!valid_id(id, V, a.ignore_index) || id < col_beg || id >= col_end) continue;
     bool first = true;
     for (int i = 0; i < j && first; ++i) first = s_id[i] != id;
     if (!first) continue;
@@ -65,12 +68,61 @@ __device__ __forceinline__ TopkPrep prep_topk(const BwdArgs& a, int64_t row, int
     fix_g[slot] = gs;
   }
   __syncthreads();
-  return TopkPrep{*s_G, *s_nfix};
+  return TopkPrep{*s_G, *s_nfix, *s_any != 0};
+}
+
+// Row constants of a backward map.
+struct BwdRow {
+  fp2 nm2;      // -m (of x)
+  fp2 nls2;     // -log S * log2 e (of x)
+  fp2 coef2;    // logp: -G (times 4 with a cap); entropy: -g; KL: g
+  fp2 k2;       // entropy: log S - H;  reverse KL: log S_a - log S_b + KL
+  fp2 nmq2;     // KL: -m_b
+  fp2 nlsq2;    // KL: -log S_b * log2 e
+};
+
+// Gradient of pair i of a vector: x holds the logits (the policy for KL), y
+// the reference (KL only).
+template <class T, int OP, bool CAP>
+__device__ __forceinline__ fp2 grad_pair(const Raw8<T>& x, const Raw8<T>& y, int i, const BwdRow& R,
+                                         const CapK& K) {
+  fp2 d, e2 = 0, r2 = 0;
+  if (CAP) {
+    d = fma2(cap_t2(x, i, K, e2, r2), splat(K.c), R.nm2);
+  } else {
+    d = add2(OP == kBwdLogp ? x.pair(i) : x.pair_clamped(i), R.nm2);
+  }
+  const fp2 p = ex2_2(fma2(d, splat(kLog2e), R.nls2));
+  fp2 r;
+  if constexpr (OP == kBwdLogp) {
+    r = mul2(p, R.coef2);
+  } else if constexpr (OP == kBwdEntropy) {
+    r = mul2(mul2(p, R.coef2), sub2(d, R.k2));
+  } else {
+    fp2 dq;
+    if (CAP) {
+      fp2 eq, rq;
+      dq = fma2(cap_t2(y, i, K, eq, rq), splat(K.c), R.nmq2);
+    } else {
+      dq = add2(y.pair_clamped(i), R.nmq2);
+    }
+    if constexpr (OP == kBwdKlReverse) {
+      r = mul2(mul2(p, R.coef2), sub2(sub2(d, dq), R.k2));
+    } else {
+      r = mul2(sub2(p, ex2_2(fma2(dq, splat(kLog2e), R.nlsq2))), R.coef2);
+    }
+  }
+  if (CAP) {
+    // dz/dx = 4 e r^2 (the 4 is folded into coef for logp)
+    r = mul2(mul2(r, e2), r2);
+    r = mul2(r, OP == kBwdLogp ? r2 : mul2(r2, splat(4.0f)));
+  }
+  return r;
 }
 
 template <class T, int OP, bool CAP>
 __global__ void __launch_bounds__(kRowThreads) row_bwd_kernel(const BwdArgs a) {
-  using namespace dev;
+  constexpr bool KL = OP >= kBwdKlReverse;
   const int64_t row = blockIdx.x / a.chunks;
   const int q = static_cast<int>(blockIdx.x - row * a.chunks);
   const int64_t V = a.vocab;
@@ -78,63 +130,75 @@ __global__ void __launch_bounds__(kRowThreads) row_bwd_kernel(const BwdArgs a) {
   const int64_t vb = static_cast<int64_t>(q) * a.vec_per_cta;
   const int64_t ve = min(vb + a.vec_per_cta, nvec);
   const T* xr = static_cast<const T*>(a.x) + row * a.ldx;
-  const T* yr = OP >= kBwdKlReverse ? static_cast<const T*>(a.y) + row * a.ldy : nullptr;
+  const T* yr = KL ? static_cast<const T*>(a.y) + row * a.ldy : xr;
   T* dr = static_cast<T*>(a.dx) + row * V;
-  const bool al = aligned16(xr) && aligned16(dr) && (OP < kBwdKlReverse || aligned16(yr));
+  const bool al = aligned16(xr) && aligned16(dr) && aligned16(yr);
+  const CapK K = cap_consts(CAP ? a.cap : 1.0f);
 
   const vls_rowstat sx = a.stats_x[row];
-  const float m = sx.m, log_s_l2e = sx.log_s * kLog2e;
+  BwdRow R;
+  R.nm2 = splat(-sx.m);
+  R.nls2 = splat(-sx.log_s * kLog2e);
+  R.k2 = 0;
+  R.nmq2 = 0;
+  R.nlsq2 = 0;
 
   // ---- per-row constants; rows whose gradient is a constant (zero / NaN) ----
-  float G = 0.0f, K = 0.0f, gr = 0.0f;
-  float mq = 0.0f, log_sq_l2e = 0.0f;
+  float G = 0.0f;
   int nfix = 0;
   bool nan_row = false, zero_row = false;
-  constexpr int kFix = OP == kBwdLogp ? VLS_MAX_TOPK : 1;
-  __shared__ int64_t fix_id[kFix];
-  __shared__ float fix_g[kFix];
+  int64_t* fix_id = nullptr;
+  float* fix_g = nullptr;
   if constexpr (OP == kBwdLogp) {
-    __shared__ int64_t s_id[VLS_MAX_TOPK];
-    __shared__ float s_g[VLS_MAX_TOPK];
+    // k = 1: one fixed slot; k > 1: ids, upstream grads and the fix-up list
+    // staged in dynamic shared memory (24 bytes per id)
+    __shared__ int64_t fix1_id;
+    __shared__ float fix1_g;
+    extern __shared__ __align__(16) unsigned char topk_smem[];
     __shared__ float s_G;
-    __shared__ int s_nfix;
+    __shared__ int s_nfix, s_any;
     const int64_t col_beg = vb * 8, col_end = min(ve * 8, V);
     if (a.k == 1) {
+      fix_id = &fix1_id;
+      fix_g = &fix1_g;
       const int64_t id = a.ids[row];
       if (valid_id(id, V, a.ignore_index)) {
         G = a.g[row];
         if (id >= col_beg && id < col_end) {
           nfix = 1;
           if (threadIdx.x == 0) {
-            fix_id[0] = id;
-            fix_g[0] = G;
+            fix1_id = id;
+            fix1_g = G;
           }
         }
       } else {
         zero_row = true;
       }
     } else {
-      const TopkPrep tp = prep_topk(a, row, col_beg, col_end, s_id, s_g, fix_id, fix_g, &s_G, &s_nfix);
+      int64_t* s_id = reinterpret_cast<int64_t*>(topk_smem);
+      fix_id = s_id + a.k;
+      float* s_g = reinterpret_cast<float*>(fix_id + a.k);
+      fix_g = s_g + a.k;
+      const TopkPrep tp =
+          prep_topk(a, row, col_beg, col_end, s_id, s_g, fix_id, fix_g, &s_G, &s_nfix, &s_any);
       G = tp.G;
       nfix = tp.nfix;
-      bool any_valid = false;
-      for (int j = 0; j < a.k && !any_valid; ++j) any_valid = valid_id(s_id[j], V, a.ignore_index);
-      zero_row = !any_valid;
+      zero_row = !tp.any_valid;
     }
-    G = -G;  // the streamed value is -G * p
+    R.coef2 = splat(CAP ? -4.0f * G : -G);  // the streamed value is -G p (dz/dx)
   } else if constexpr (OP == kBwdEntropy) {
     const float H = a.fout[row];
-    gr = -a.g[row];
-    K = sx.log_s - H;  // log p + H = (z - m) - K
-    nan_row = m == neg_inf() || isnan(H);
+    R.coef2 = splat(-a.g[row]);
+    R.k2 = splat(sx.log_s - H);  // log p + H = (z - m) - (log S - H)
+    nan_row = sx.m == neg_inf() || isnan(H);
   } else {
     const vls_rowstat sy = a.stats_y[row];
-    mq = sy.m;
-    log_sq_l2e = sy.log_s * kLog2e;
+    R.nmq2 = splat(-sy.m);
+    R.nlsq2 = splat(-sy.log_s * kLog2e);
     const float kl = a.fout[row];
-    gr = a.g[row];
+    R.coef2 = splat(a.g[row]);
     if constexpr (OP == kBwdKlReverse) {
-      K = (sx.log_s - sy.log_s) + kl;  // (log p_a - log p_b) - KL = (da - db) - K
+      R.k2 = splat((sx.log_s - sy.log_s) + kl);  // (log p_a - log p_b) - KL = (da - db) - k
       nan_row = !isfinite(kl);
     } else {
       nan_row = isnan(kl);
@@ -142,86 +206,61 @@ __global__ void __launch_bounds__(kRowThreads) row_bwd_kernel(const BwdArgs a) {
   }
 
   if (zero_row || nan_row) {
-    float c[8];
-#pragma unroll
-    for (int j = 0; j < 8; ++j) c[j] = nan_row ? qnan() : 0.0f;
-    for (int64_t v = vb + threadIdx.x; v < ve; v += kRowThreads) store_vec(dr, v, V, al, c);
+    const fp2 c = splat(nan_row ? qnan() : 0.0f);
+    const fp2 o[4] = {c, c, c, c};
+    for (int64_t v = vb + threadIdx.x; v < ve; v += kRowThreads) store_vec(dr, v, V, al, o);
     return;
   }
 
-  auto grad8 = [&](float (&x)[8], float (&y)[8], float (&out)[8]) {
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      float z = x[j], chain = 1.0f;
-      if (CAP) {
-        const float u = x[j] * a.rcap;
-        const float t = tanhf(u);
-        z = a.cap * t;
-        chain = softcap_dzdx(u, t);
-      }
-      float r;
-      if constexpr (OP == kBwdLogp) {
-        r = G * prob(z, m, log_s_l2e);
-      } else if constexpr (OP == kBwdEntropy) {
-        const float d = z - m;
-        r = gr * ex2(fmaf(d, kLog2e, -log_s_l2e)) * (fmaxf(d, -kFltMax) - K);
-      } else {
-        const float zb = CAP ? softcap_z(y[j], a.cap, a.rcap) : y[j];
-        const float da = z - m, db = zb - mq;
-        const float pa = ex2(fmaf(da, kLog2e, -log_s_l2e));
-        if constexpr (OP == kBwdKlReverse) {
-          r = gr * pa * ((fmaxf(da, -kFltMax) - fmaxf(db, -kFltMax)) - K);
-        } else {
-          r = gr * (pa - ex2(fmaf(db, kLog2e, -log_sq_l2e)));
-        }
-      }
-      out[j] = CAP ? r * chain : r;
-    }
-  };
-
+  constexpr int U = KL ? 2 : 4;
   int64_t v = vb + threadIdx.x;
   const int64_t vfull_end = min(ve, V >> 3);
   if (al) {
-    for (; v + (kUnroll - 1) * kRowThreads < vfull_end; v += kUnroll * kRowThreads) {
-      float x[kUnroll][8], y[kUnroll][8];
+    for (; v + (U - 1) * kRowThreads < vfull_end; v += U * kRowThreads) {
+      Raw8<T> x[U], y[U];
 #pragma unroll
-      for (int u = 0; u < kUnroll; ++u) {
-        Elem<T>::load8(xr + 8 * (v + u * kRowThreads), x[u]);
-        if constexpr (OP >= kBwdKlReverse) Elem<T>::load8(yr + 8 * (v + u * kRowThreads), y[u]);
+      for (int u = 0; u < U; ++u) {
+        x[u].load(xr + 8 * (v + u * kRowThreads));
+        if constexpr (KL) y[u].load(yr + 8 * (v + u * kRowThreads));
       }
 #pragma unroll
-      for (int u = 0; u < kUnroll; ++u) {
-        float out[8];
-        grad8(x[u], y[u], out);
-        Elem<T>::store8(dr + 8 * (v + u * kRowThreads), out);
+      for (int u = 0; u < U; ++u) {
+        fp2 o[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) o[i] = grad_pair<T, OP, CAP>(x[u], KL ? y[u] : x[u], i, R, K);
+        Out8<T>::store(dr + 8 * (v + u * kRowThreads), o);
       }
     }
   }
   for (; v < ve; v += kRowThreads) {
-    float x[8], y[8], out[8];
-    int nx = 8, ny = 8;
-    load_vec(xr, v, V, al, x, nx);
-    if constexpr (OP >= kBwdKlReverse) load_vec(yr, v, V, al, y, ny);
-    grad8(x, y, out);
-    store_vec(dr, v, V, al, out);
+    Raw8<T> x, y;
+    int valid;
+    load_raw(x, xr, v, V, al, valid);
+    if constexpr (KL) load_raw(y, yr, v, V, al, valid);
+    fp2 o[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) o[i] = grad_pair<T, OP, CAP>(x, KL ? y : x, i, R, K);
+    store_vec(dr, v, V, al, o);
   }
 
   if constexpr (OP == kBwdLogp) {
-    // one-hot columns: rewrite with (g_sum - G p) * dz/dx, one rounding
+    // one-hot columns: rewrite with (g_sum - G p) dz/dx, one rounding at the store
     if (nfix > 0) {
       __syncthreads();  // the streamed stores of this CTA precede the rewrites
       for (int f = threadIdx.x; f < nfix; f += kRowThreads) {
         const int64_t c = fix_id[f];
-        const float x = Elem<T>::load1(xr + c);
-        float z = x, chain = 1.0f;
+        const float x = load1(xr + c);
+        float d, chain = 1.0f;
         if (CAP) {
-          const float u = x * a.rcap;
-          const float t = tanhf(u);
-          z = a.cap * t;
-          chain = softcap_dzdx(u, t);
+          float e, r;
+          d = cap_d(cap_t(x, K, e, r), K.c, sx.m);
+          chain = 4.0f * e * r * r;
+        } else {
+          d = x - sx.m;
         }
-        const float r = fmaf(G, prob(z, m, log_s_l2e), fix_g[f]);
-        Elem<T>::store1(dr + c, CAP ? r * chain : r);
+        const float p = ex2(fmaf(d, kLog2e, -sx.log_s * kLog2e));
+        const float r = fmaf(-G, p, fix_g[f]);
+        Out8<T>::store1(dr + c, CAP ? r * chain : r);
       }
     }
   }
@@ -230,7 +269,8 @@ __global__ void __launch_bounds__(kRowThreads) row_bwd_kernel(const BwdArgs a) {
 template <class T, int OP, bool CAP>
 cudaError_t launch_bwd_t(const BwdArgs& a, cudaStream_t s) {
   const dim3 grid(static_cast<unsigned>(a.rows * a.chunks));
-  row_bwd_kernel<T, OP, CAP><<<grid, kRowThreads, 0, s>>>(a);
+  const size_t smem = (OP == kBwdLogp && a.k > 1) ? static_cast<size_t>(a.k) * 24 : 0;
+  row_bwd_kernel<T, OP, CAP><<<grid, kRowThreads, smem, s>>>(a);
   return cudaGetLastError();
 }
 

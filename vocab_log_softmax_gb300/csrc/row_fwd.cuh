@@ -9,43 +9,181 @@
 // warps), cluster ranks (xor 4..1 over up to 8 ranks, through distributed
 // shared memory into rank 0).  Nothing in that order depends on N, on the
 // row's position or on its alignment, so results are deterministic and batch
-// invariant (the reduction-tree rule of "TP4 GDN, convolution and D=256
-// attention mixers", RL-Kernel PR #507, and the one-block-per-row,
-// fixed-tree rule of RL-Kernel PR #495, Summary).
+// invariant (one block per row and a fixed reduction tree, "perf(logp): fused
+// zero-workspace backward ...", RL-Kernel PR #495, Summary; a tree fixed
+// regardless of the row count, "TP4 GDN, convolution and D=256 attention
+// mixers", RL-Kernel PR #507).
 #pragma once
 
 #include "vls_device.cuh"
 
 namespace vls {
 
-template <int OP>
-struct FwdState;
-template <>
-struct FwdState<kFwdLogp> { using type = dev::LogpState; };
-template <>
-struct FwdState<kFwdEntropy> { using type = dev::EntropyState; };
-template <>
-struct FwdState<kFwdKl> { using type = dev::KlState; };
+using namespace dev;
 
-template <class T, int OP, bool CAP>
-__device__ __forceinline__ void fold_vec(typename FwdState<OP>::type& st, float (&zx)[8],
-                                         float (&zy)[8], int nx, float cap, float rcap) {
-  using namespace dev;
-  apply_cap8<CAP>(zx, cap, rcap);
-  if (nx < 8) mask_tail(zx, nx);
-  if constexpr (OP == kFwdKl) {
-    apply_cap8<CAP>(zy, cap, rcap);
-    if (nx < 8) mask_tail(zy, nx);
-    st.update(zx, zy);
-  } else {
-    st.update(zx);
-  }
+// With a softcap the row max is the cap of the raw max (tanh is
+// increasing), so maxima are tracked on raw logits and only the new maximum
+// is transformed.  `fresh` forces the first transform with a cap, where a
+// vector of -inf still has a finite value (-c).
+template <bool CAP>
+__device__ __forceinline__ bool grows(float vmax_raw, float m_raw, float m) {
+  return vmax_raw > m_raw || (CAP && m == neg_inf());
 }
+
+template <bool PARTIAL>
+__device__ __forceinline__ fp2 keep(fp2 e, int i, int valid) {
+  if (!PARTIAL) return e;
+  float a, b;
+  upk(e, a, b);
+  return pk(2 * i < valid ? a : 0.0f, 2 * i + 1 < valid ? b : 0.0f);
+}
+
+template <class T, bool CAP>
+struct LogpAcc {
+  using State = LogpState;
+  float m_raw = neg_inf(), m = neg_inf();
+  fp2 nm2 = 0, s2 = 0;
+
+  template <bool PARTIAL>
+  __device__ __forceinline__ void update(const Raw8<T>& v, const Raw8<T>&, int valid, const CapK& K) {
+    const float vm = v.max();
+    if (grows<CAP>(vm, m_raw, m)) {
+      const float mn = CAP ? cap_z(vm, K) : vm;
+      s2 = mul2(s2, splat(rescale(m, mn)));
+      m_raw = vm;
+      m = mn;
+      nm2 = splat(-mn);
+    }
+    if (!CAP && m == neg_inf()) return;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      fp2 d;
+      if (CAP) {
+        fp2 e2, r2;
+        d = fma2(cap_t2(v, i, K, e2, r2), splat(K.c), nm2);
+      } else {
+        d = add2(v.pair(i), nm2);
+      }
+      s2 = add2(s2, keep<PARTIAL>(ex2_2(mul2(d, splat(kLog2e))), i, valid));
+    }
+  }
+  __device__ State state() const { return {m, sum2(s2)}; }
+};
+
+template <class T, bool CAP>
+struct EntropyAcc {
+  using State = EntropyState;
+  float m_raw = neg_inf(), m = neg_inf();
+  fp2 nm2 = 0, s2 = 0, w2 = 0;
+
+  template <bool PARTIAL>
+  __device__ __forceinline__ void update(const Raw8<T>& v, const Raw8<T>&, int valid, const CapK& K) {
+    const float vm = v.max();
+    if (grows<CAP>(vm, m_raw, m)) {
+      const float mn = CAP ? cap_z(vm, K) : vm;
+      const float f = rescale(m, mn);
+      w2 = m != neg_inf() ? mul2(fma2(s2, splat(m - mn), w2), splat(f)) : 0;
+      s2 = mul2(s2, splat(f));
+      m_raw = vm;
+      m = mn;
+      nm2 = splat(-mn);
+    }
+    if (!CAP && m == neg_inf()) return;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      fp2 d;
+      if (CAP) {
+        fp2 e2, r2;
+        d = fma2(cap_t2(v, i, K, e2, r2), splat(K.c), nm2);
+      } else {
+        d = add2(v.pair_clamped(i), nm2);  // -inf columns: e = 0 and 0 * d = 0
+      }
+      const fp2 e = keep<PARTIAL>(ex2_2(mul2(d, splat(kLog2e))), i, valid);
+      s2 = add2(s2, e);
+      w2 = fma2(e, d, w2);
+    }
+  }
+  __device__ State state() const { return {m, sum2(s2), sum2(w2)}; }
+};
+
+// KL(P||Q): `v` is a vector of P (first argument), `q` the same columns of Q.
+template <class T, bool CAP>
+struct KlAcc {
+  using State = KlState;
+  float mp_raw = neg_inf(), mp = neg_inf(), mq_raw = neg_inf(), mq = neg_inf();
+  fp2 nmp2 = 0, nmq2 = 0, sp2 = 0, sq2 = 0, w2 = 0;
+  uint32_t flag = 0;
+
+  template <bool PARTIAL>
+  __device__ __forceinline__ void update(const Raw8<T>& v, const Raw8<T>& q, int valid, const CapK& K) {
+    const float vmp = v.max(), vmq = q.max();
+    const bool up = grows<CAP>(vmp, mp_raw, mp), uq = grows<CAP>(vmq, mq_raw, mq);
+    if (up || uq) {
+      const float Mp = up ? (CAP ? cap_z(vmp, K) : vmp) : mp;
+      const float Mq = uq ? (CAP ? cap_z(vmq, K) : vmq) : mq;
+      const float fp = rescale(mp, Mp), fq = rescale(mq, Mq);
+      w2 = mp != neg_inf() ? mul2(fma2(sp2, splat((mp - Mp) - (mq - Mq)), w2), splat(fp)) : 0;
+      sp2 = mul2(sp2, splat(fp));
+      sq2 = mul2(sq2, splat(fq));
+      if (up) { mp_raw = vmp; mp = Mp; nmp2 = splat(-Mp); }
+      if (uq) { mq_raw = vmq; mq = Mq; nmq2 = splat(-Mq); }
+    }
+    if (!CAP) {
+#pragma unroll
+      for (int i = 0; i < 4; ++i) flag |= v.mismatch(i, q);
+    }
+    const bool p_ok = CAP || mp != neg_inf(), q_ok = CAP || mq != neg_inf();
+    if (p_ok && q_ok) {
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        fp2 dp, dq;
+        if (CAP) {
+          fp2 e2, r2;
+          dp = fma2(cap_t2(v, i, K, e2, r2), splat(K.c), nmp2);
+          dq = fma2(cap_t2(q, i, K, e2, r2), splat(K.c), nmq2);
+        } else {
+          dp = add2(v.pair_clamped(i), nmp2);
+          dq = add2(q.pair_clamped(i), nmq2);
+        }
+        const fp2 ep = keep<PARTIAL>(ex2_2(mul2(dp, splat(kLog2e))), i, valid);
+        const fp2 eq = keep<PARTIAL>(ex2_2(mul2(dq, splat(kLog2e))), i, valid);
+        sp2 = add2(sp2, ep);
+        sq2 = add2(sq2, eq);
+        w2 = fma2(ep, sub2(dp, dq), w2);
+      }
+    } else if (p_ok || q_ok) {
+      // one side has seen only -inf so far (no W term: a finite P column
+      // against an all -inf Q run is a mismatch, already flagged)
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        if (p_ok) sp2 = add2(sp2, keep<PARTIAL>(ex2_2(mul2(add2(v.pair_clamped(i), nmp2), splat(kLog2e))), i, valid));
+        if (q_ok) sq2 = add2(sq2, keep<PARTIAL>(ex2_2(mul2(add2(q.pair_clamped(i), nmq2), splat(kLog2e))), i, valid));
+      }
+    }
+  }
+  __device__ State state() const { return {mp, sum2(sp2), mq, sum2(sq2), sum2(w2), flag}; }
+};
+
+template <int OP, class T, bool CAP>
+struct FwdAccOf;
+template <class T, bool CAP>
+struct FwdAccOf<kFwdLogp, T, CAP> { using type = LogpAcc<T, CAP>; };
+template <class T, bool CAP>
+struct FwdAccOf<kFwdEntropy, T, CAP> { using type = EntropyAcc<T, CAP>; };
+template <class T, bool CAP>
+struct FwdAccOf<kFwdKl, T, CAP> { using type = KlAcc<T, CAP>; };
+
+// 16-byte loads in flight per thread before any is used: 4 vectors of one
+// tensor, or 2 vectors of each of the two KL tensors.
+template <int OP>
+constexpr int fwd_unroll() { return OP == kFwdKl ? 2 : 4; }
 
 template <class T, int OP, bool CAP>
 __global__ void __launch_bounds__(kRowThreads) row_fwd_kernel(const FwdArgs a) {
-  using namespace dev;
-  using S = typename FwdState<OP>::type;
+  using Acc = typename FwdAccOf<OP, T, CAP>::type;
+  using S = typename Acc::State;
+  constexpr int U = fwd_unroll<OP>();
+  constexpr bool KL = OP == kFwdKl;
   __shared__ S warp_part[kRowWarps];
   __shared__ S cta_part[kMaxCluster];
   __shared__ S row_state;
@@ -56,41 +194,44 @@ __global__ void __launch_bounds__(kRowThreads) row_fwd_kernel(const FwdArgs a) {
   if (C > 1) cluster_arrive_relaxed();
 
   const T* xr = static_cast<const T*>(a.x) + row * a.ldx;
-  const T* yr = OP == kFwdKl ? static_cast<const T*>(a.y) + row * a.ldy : nullptr;
+  const T* yr = KL ? static_cast<const T*>(a.y) + row * a.ldy : xr;
   const int64_t V = a.vocab;
   const int64_t nvec = (V + 7) >> 3;
   const int64_t vb = static_cast<int64_t>(q) * a.vec_per_cta;
   const int64_t ve = min(vb + a.vec_per_cta, nvec);
   const int64_t vfull_end = min(ve, V >> 3);
-  const bool al = aligned16(xr) && (OP != kFwdKl || aligned16(yr));
+  const bool al = aligned16(xr) && aligned16(yr);
+  const CapK K = cap_consts(CAP ? a.cap : 1.0f);
 
-  S st = S::identity();
+  Acc acc;
   int64_t v = vb + threadIdx.x;
   if (al) {
-    // unrolled body: kUnroll 16-byte loads in flight per tensor before any use
-    for (; v + (kUnroll - 1) * kRowThreads < vfull_end; v += kUnroll * kRowThreads) {
-      float zx[kUnroll][8], zy[kUnroll][8];
+    for (; v + (U - 1) * kRowThreads < vfull_end; v += U * kRowThreads) {
+      Raw8<T> rx[U], ry[U];
 #pragma unroll
-      for (int u = 0; u < kUnroll; ++u) {
-        Elem<T>::load8(xr + 8 * (v + u * kRowThreads), zx[u]);
-        if constexpr (OP == kFwdKl) Elem<T>::load8(yr + 8 * (v + u * kRowThreads), zy[u]);
+      for (int u = 0; u < U; ++u) {
+        rx[u].load(xr + 8 * (v + u * kRowThreads));
+        if constexpr (KL) ry[u].load(yr + 8 * (v + u * kRowThreads));
       }
 #pragma unroll
-      for (int u = 0; u < kUnroll; ++u) fold_vec<T, OP, CAP>(st, zx[u], zy[u], 8, a.cap, a.rcap);
+      for (int u = 0; u < U; ++u) acc.template update<false>(rx[u], KL ? ry[u] : rx[u], 8, K);
     }
   }
   // remaining vectors, the partial last vector and unaligned rows: same
   // vectors, same order, same arithmetic
   for (; v < ve; v += kRowThreads) {
-    float zx[8], zy[8];
-    int nx = 8, ny = 8;
-    load_vec(xr, v, V, al, zx, nx);
-    if constexpr (OP == kFwdKl) load_vec(yr, v, V, al, zy, ny);
-    fold_vec<T, OP, CAP>(st, zx, zy, nx, a.cap, a.rcap);
+    Raw8<T> rx, ry;
+    int valid;
+    load_raw(rx, xr, v, V, al, valid);
+    if constexpr (KL) load_raw(ry, yr, v, V, al, valid);
+    if (valid == 8)
+      acc.template update<false>(rx, KL ? ry : rx, 8, K);
+    else
+      acc.template update<true>(rx, KL ? ry : rx, valid, K);
   }
 
   // ---- fixed-tree reduction: lanes, warps, cluster ranks ----
-  st = warp_reduce(st);
+  S st = warp_reduce(acc.state());
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   if (lane == 0) warp_part[warp] = st;
   __syncthreads();
@@ -125,9 +266,9 @@ __global__ void __launch_bounds__(kRowThreads) row_fwd_kernel(const FwdArgs a) {
       const int64_t id = a.ids[row * a.k + j];
       float out = 0.0f;
       if (valid_id(id, V, a.ignore_index)) {
-        float z = Elem<T>::load1(xr + id);
-        if (CAP) z = softcap_z(z, a.cap, a.rcap);
-        out = m == neg_inf() ? qnan() : (z - m) - log_s;
+        const float x = load1(xr + id);
+        const float d = CAP ? cap_d(cap_t(x, K), K.c, m) : x - m;
+        out = m == neg_inf() ? qnan() : d - log_s;
       }
       a.logp[row * a.k + j] = out;
     }

@@ -1,6 +1,12 @@
 // Standalone final-logit softcap ("Final Logit Softcap", Summary and Tensor
-// and Precision Contract): y = c*tanh(x/c) and gx = gy*(1 - tanh^2(x/c)),
+// and Precision Contract): y = c tanh(x/c) and gx = gy (1 - tanh^2(x/c)),
 // fp32 math with one cast at the store, over a flat array of n elements.
+//
+// tanh and its slope come from one exponential and one reciprocal (see
+// cap_t in vls_device.cuh).  For the output itself relative accuracy matters
+// near 0, where (1 - e) loses digits, so |x/c| < 1/64 uses the odd cubic
+// u - u^3/3 of the Taylor series instead (relative error below 2 u^4/15 <
+// 1e-8 there).  The slope 4 e r^2 is accurate everywhere.
 //
 // Grid-stride kernels: the grid is a multiple of the SM count and each
 // thread handles 8-element vectors (16-byte accesses for bf16, two for
@@ -10,58 +16,125 @@
 
 namespace vls {
 
+using namespace dev;
+
 constexpr int kCapThreads = 256;
+constexpr float kCubicBelow = 1.0f / 64.0f;
+// 8-element vectors each thread loads before using any (memory-level parallelism)
+constexpr int kCapUnroll = 4;
+
+__device__ __forceinline__ float softcap_value(float x, const CapK& K, float rcap) {
+  const float u = x * rcap;
+  float t;
+  if (fabsf(u) < kCubicBelow) {
+    t = u * fmaf(u * u, -1.0f / 3.0f, 1.0f);
+  } else {
+    t = cap_t(x, K);
+  }
+  return K.c * t;
+}
+
+__device__ __forceinline__ float softcap_slope(float x, const CapK& K) {
+  float e, r;
+  cap_t(x, K, e, r);
+  return 4.0f * e * r * r;
+}
+
+template <class T>
+__device__ __forceinline__ fp2 softcap_pair(const Raw8<T>& v, int i, const CapK& K, float rcap) {
+  fp2 e2, r2;
+  const fp2 t2 = cap_t2(v, i, K, e2, r2);
+  const fp2 u2 = mul2(v.pair(i), splat(rcap));
+  const fp2 c2 = mul2(u2, fma2(mul2(u2, u2), splat(-1.0f / 3.0f), splat(1.0f)));
+  float t0, t1, u0, u1, c0, c1;
+  upk(t2, t0, t1);
+  upk(u2, u0, u1);
+  upk(c2, c0, c1);
+  return mul2(pk(fabsf(u0) < kCubicBelow ? c0 : t0, fabsf(u1) < kCubicBelow ? c1 : t1), splat(K.c));
+}
+
+template <class T, class G>
+__device__ __forceinline__ fp2 slope_pair(const Raw8<T>& v, const Raw8<G>& g, int i, const CapK& K) {
+  fp2 e2, r2;
+  cap_t2(v, i, K, e2, r2);
+  return mul2(mul2(mul2(g.pair(i), e2), r2), mul2(r2, splat(4.0f)));
+}
 
 template <class T>
 __global__ void __launch_bounds__(kCapThreads) softcap_fwd_kernel(const CapArgs a) {
-  using namespace dev;
   const T* x = static_cast<const T*>(a.x);
   T* y = static_cast<T*>(a.out);
+  const CapK K = cap_consts(a.cap);
   const int64_t nvec = a.n >> 3;
   const int64_t stride = static_cast<int64_t>(gridDim.x) * kCapThreads;
   const bool al = aligned16(x) && aligned16(y);
   int64_t v = static_cast<int64_t>(blockIdx.x) * kCapThreads + threadIdx.x;
   if (al) {
-    for (; v < nvec; v += stride) {
-      float z[8];
-      Elem<T>::load8(x + 8 * v, z);
+    for (; v + (kCapUnroll - 1) * stride < nvec; v += kCapUnroll * stride) {
+      Raw8<T> r[kCapUnroll];
 #pragma unroll
-      for (int j = 0; j < 8; ++j) z[j] = softcap_z(z[j], a.cap, a.rcap);
-      Elem<T>::store8(y + 8 * v, z);
+      for (int u = 0; u < kCapUnroll; ++u) r[u].load(x + 8 * (v + u * stride));
+#pragma unroll
+      for (int u = 0; u < kCapUnroll; ++u) {
+        fp2 o[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) o[i] = softcap_pair(r[u], i, K, a.rcap);
+        Out8<T>::store(y + 8 * (v + u * stride), o);
+      }
+    }
+    for (; v < nvec; v += stride) {
+      Raw8<T> r;
+      r.load(x + 8 * v);
+      fp2 o[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) o[i] = softcap_pair(r, i, K, a.rcap);
+      Out8<T>::store(y + 8 * v, o);
     }
     v = 8 * nvec + static_cast<int64_t>(blockIdx.x) * kCapThreads + threadIdx.x;
   }
-  for (; v < a.n; v += stride) Elem<T>::store1(y + v, softcap_z(Elem<T>::load1(x + v), a.cap, a.rcap));
+  for (; v < a.n; v += stride) Out8<T>::store1(y + v, softcap_value(load1(x + v), K, a.rcap));
 }
 
 template <class T, class G>
 __global__ void __launch_bounds__(kCapThreads) softcap_bwd_kernel(const CapArgs a) {
-  using namespace dev;
   const T* x = static_cast<const T*>(a.x);
   const G* gy = static_cast<const G*>(a.gy);
   T* gx = static_cast<T*>(a.out);
+  const CapK K = cap_consts(a.cap);
   const int64_t nvec = a.n >> 3;
   const int64_t stride = static_cast<int64_t>(gridDim.x) * kCapThreads;
   const bool al = aligned16(x) && aligned16(gy) && aligned16(gx);
   int64_t v = static_cast<int64_t>(blockIdx.x) * kCapThreads + threadIdx.x;
   if (al) {
-    for (; v < nvec; v += stride) {
-      float z[8], g[8];
-      Elem<T>::load8(x + 8 * v, z);
-      Elem<G>::load8(gy + 8 * v, g);
+    for (; v + (kCapUnroll - 1) * stride < nvec; v += kCapUnroll * stride) {
+      Raw8<T> r[kCapUnroll];
+      Raw8<G> g[kCapUnroll];
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const float u = z[j] * a.rcap;
-        z[j] = g[j] * softcap_dzdx(u, tanhf(u));
+      for (int u = 0; u < kCapUnroll; ++u) {
+        r[u].load(x + 8 * (v + u * stride));
+        g[u].load(gy + 8 * (v + u * stride));
       }
-      Elem<T>::store8(gx + 8 * v, z);
+#pragma unroll
+      for (int u = 0; u < kCapUnroll; ++u) {
+        fp2 o[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) o[i] = slope_pair(r[u], g[u], i, K);
+        Out8<T>::store(gx + 8 * (v + u * stride), o);
+      }
+    }
+    for (; v < nvec; v += stride) {
+      Raw8<T> r;
+      Raw8<G> g;
+      r.load(x + 8 * v);
+      g.load(gy + 8 * v);
+      fp2 o[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) o[i] = slope_pair(r, g, i, K);
+      Out8<T>::store(gx + 8 * v, o);
     }
     v = 8 * nvec + static_cast<int64_t>(blockIdx.x) * kCapThreads + threadIdx.x;
   }
-  for (; v < a.n; v += stride) {
-    const float u = Elem<T>::load1(x + v) * a.rcap;
-    Elem<T>::store1(gx + v, Elem<G>::load1(gy + v) * softcap_dzdx(u, tanhf(u)));
-  }
+  for (; v < a.n; v += stride) Out8<T>::store1(gx + v, load1(gy + v) * softcap_slope(load1(x + v), K));
 }
 
 cudaError_t launch_softcap_fwd(vls_dtype dt, const CapArgs& a, cudaStream_t s) {

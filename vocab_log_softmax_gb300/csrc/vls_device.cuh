@@ -1,6 +1,6 @@
-// Device building blocks shared by the row kernels: element loads/stores,
-// the fp32 softcap, the single-read online statistics and their fixed-order
-// reductions.
+// Device building blocks shared by the row kernels: raw 8-column vectors,
+// packed fp32-pair arithmetic, the fp32 softcap, the single-read online
+// statistics and their fixed-order reductions.
 #pragma once
 
 #include <cstdint>
@@ -17,7 +17,12 @@ namespace dev {
 namespace cg = cooperative_groups;
 
 constexpr float kLog2e = 1.4426950408889634f;
-constexpr float kFltMax = 3.402823466e38f;
+// Lowest finite bfloat16 (bits 0xff7f).  Clamping a logit up to it changes
+// nothing in any statistic -- its softmax weight is exactly 0 either way --
+// but keeps -inf out of products such as 0 * (z - m).
+constexpr float kLowest = -3.38953139e38f;
+constexpr uint32_t kLowestBf16x2 = 0xff7fff7fu;
+constexpr uint32_t kNegInfBf16x2 = 0xff80ff80u;
 
 __device__ __forceinline__ float neg_inf() { return __int_as_float(0xff800000u); }
 __device__ __forceinline__ float pos_inf() { return __int_as_float(0x7f800000u); }
@@ -29,6 +34,77 @@ __device__ __forceinline__ float ex2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
+}
+
+// 1/x on the special-function unit (PTX rcp.approx.ftz.f32).
+__device__ __forceinline__ float rcp(float x) {
+  float y;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// --------------------------------------------------------------------------
+// Packed fp32 pairs (PTX .f32x2 arithmetic, two IEEE round-to-nearest
+// operations per instruction: bit-identical to the scalar forms).
+// --------------------------------------------------------------------------
+using fp2 = unsigned long long;
+
+__device__ __forceinline__ fp2 pk(float lo, float hi) {
+  fp2 r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ void upk(fp2 v, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ fp2 add2(fp2 a, fp2 b) {
+  fp2 r;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ fp2 sub2(fp2 a, fp2 b) {
+  fp2 r;
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ fp2 mul2(fp2 a, fp2 b) {
+  fp2 r;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ fp2 fma2(fp2 a, fp2 b, fp2 c) {
+  fp2 r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+  return r;
+}
+__device__ __forceinline__ fp2 splat(float v) { return pk(v, v); }
+__device__ __forceinline__ fp2 ex2_2(fp2 y) {
+  float a, b;
+  upk(y, a, b);
+  return pk(ex2(a), ex2(b));
+}
+__device__ __forceinline__ fp2 rcp2(fp2 y) {
+  float a, b;
+  upk(y, a, b);
+  return pk(rcp(a), rcp(b));
+}
+__device__ __forceinline__ float sum2(fp2 v) {
+  float a, b;
+  upk(v, a, b);
+  return a + b;
+}
+
+// bfloat16x2 helpers on raw 32-bit words (two columns per word).
+__device__ __forceinline__ uint32_t bmax2(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("max.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  return r;
+}
+// 0xffff in each half where a == b, else 0
+__device__ __forceinline__ uint32_t beq2(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("set.eq.u32.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  return r;
 }
 
 // 16-byte read-only load that skips L1 (each logit is read once per sweep).
@@ -46,164 +122,175 @@ __device__ __forceinline__ void st16(void* p, uint4 v) {
                : "memory");
 }
 
+__device__ __forceinline__ bool aligned16(const void* p) {
+  return (reinterpret_cast<uintptr_t>(p) & 15u) == 0;
+}
+
+__device__ __forceinline__ bool valid_id(int64_t id, int64_t V, int64_t ignore_index) {
+  return id != ignore_index && id >= 0 && id < V;
+}
+
 // --------------------------------------------------------------------------
-// Element access.  A "vector" is 8 consecutive columns for every dtype, so
-// the column -> thread map (and with it every reduction order) does not
-// depend on the dtype: bf16 logits and their exact fp32 copies give the same
-// bits.
+// Raw 8-column vectors.  A vector is 8 consecutive columns for every dtype,
+// so the column -> thread map (and every reduction order built on it) does
+// not depend on the dtype: bf16 logits and their exact fp32 copies give the
+// same bits.  `pair(i)` is columns 2i, 2i+1 as an fp32 pair.
 // --------------------------------------------------------------------------
 template <class T>
-struct Elem;
+struct Raw8;
 
 template <>
-struct Elem<float> {
-  __device__ static float load1(const float* p) { return __ldg(p); }
-  __device__ static void load8(const float* p, float (&v)[8]) {
+struct Raw8<__nv_bfloat16> {
+  uint32_t w[4];
+  __device__ __forceinline__ void load(const __nv_bfloat16* p) {
+    const uint4 u = ld_stream16(p);
+    w[0] = u.x; w[1] = u.y; w[2] = u.z; w[3] = u.w;
+  }
+  // columns j >= valid read as -inf
+  __device__ __forceinline__ void load_scalar(const __nv_bfloat16* p, int valid) {
+    const unsigned short* q = reinterpret_cast<const unsigned short*>(p);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const uint32_t lo = 2 * i < valid ? __ldg(q + 2 * i) : 0xff80u;
+      const uint32_t hi = 2 * i + 1 < valid ? __ldg(q + 2 * i + 1) : 0xff80u;
+      w[i] = lo | (hi << 16);
+    }
+  }
+  __device__ __forceinline__ float max() const {
+    const uint32_t m = bmax2(bmax2(w[0], w[1]), bmax2(w[2], w[3]));
+    return fmaxf(__uint_as_float(m << 16), __uint_as_float(m & 0xffff0000u));
+  }
+  __device__ __forceinline__ fp2 pair(int i) const {
+    return pk(__uint_as_float(w[i] << 16), __uint_as_float(w[i] & 0xffff0000u));
+  }
+  __device__ __forceinline__ fp2 pair_clamped(int i) const {
+    const uint32_t c = bmax2(w[i], kLowestBf16x2);
+    return pk(__uint_as_float(c << 16), __uint_as_float(c & 0xffff0000u));
+  }
+  __device__ __forceinline__ fp2 pair_abs(int i) const {
+    const uint32_t a = w[i] & 0x7fff7fffu;
+    return pk(__uint_as_float(a << 16), __uint_as_float(a & 0xffff0000u));
+  }
+  // sign bits of columns 2i, 2i+1 in bit 31 of each word
+  __device__ __forceinline__ uint32_t sign_lo(int i) const { return w[i] << 16; }
+  __device__ __forceinline__ uint32_t sign_hi(int i) const { return w[i]; }
+  // nonzero iff some column of pair i has this = finite-or-+inf and q = -inf
+  __device__ __forceinline__ uint32_t mismatch(int i, const Raw8& q) const {
+    return beq2(q.w[i], kNegInfBf16x2) & ~beq2(w[i], kNegInfBf16x2);
+  }
+};
+
+template <>
+struct Raw8<float> {
+  float v[8];
+  __device__ __forceinline__ void load(const float* p) {
     const uint4 a = ld_stream16(p), b = ld_stream16(p + 4);
     v[0] = __uint_as_float(a.x); v[1] = __uint_as_float(a.y);
     v[2] = __uint_as_float(a.z); v[3] = __uint_as_float(a.w);
     v[4] = __uint_as_float(b.x); v[5] = __uint_as_float(b.y);
     v[6] = __uint_as_float(b.z); v[7] = __uint_as_float(b.w);
   }
-  __device__ static void store1(float* p, float v) { *p = v; }
-  __device__ static void store8(float* p, const float (&v)[8]) {
-    st16(p, make_uint4(__float_as_uint(v[0]), __float_as_uint(v[1]), __float_as_uint(v[2]),
-                       __float_as_uint(v[3])));
-    st16(p + 4, make_uint4(__float_as_uint(v[4]), __float_as_uint(v[5]), __float_as_uint(v[6]),
-                           __float_as_uint(v[7])));
+  __device__ __forceinline__ void load_scalar(const float* p, int valid) {
+#pragma unroll
+    for (int j = 0; j < 8; ++j) v[j] = j < valid ? __ldg(p + j) : neg_inf();
+  }
+  __device__ __forceinline__ float max() const {
+    return fmaxf(fmaxf(fmaxf(v[0], v[1]), fmaxf(v[2], v[3])), fmaxf(fmaxf(v[4], v[5]), fmaxf(v[6], v[7])));
+  }
+  __device__ __forceinline__ fp2 pair(int i) const { return pk(v[2 * i], v[2 * i + 1]); }
+  __device__ __forceinline__ fp2 pair_clamped(int i) const {
+    return pk(fmaxf(v[2 * i], kLowest), fmaxf(v[2 * i + 1], kLowest));
+  }
+  __device__ __forceinline__ fp2 pair_abs(int i) const { return pk(fabsf(v[2 * i]), fabsf(v[2 * i + 1])); }
+  __device__ __forceinline__ uint32_t sign_lo(int i) const { return __float_as_uint(v[2 * i]); }
+  __device__ __forceinline__ uint32_t sign_hi(int i) const { return __float_as_uint(v[2 * i + 1]); }
+  __device__ __forceinline__ uint32_t mismatch(int i, const Raw8& q) const {
+    return ((q.v[2 * i] == neg_inf()) & (v[2 * i] != neg_inf())) |
+           ((q.v[2 * i + 1] == neg_inf()) & (v[2 * i + 1] != neg_inf()));
   }
 };
 
-__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
-  // cvt.rn.bf16x2.f32: both halves rounded to nearest even
-  __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
-  return *reinterpret_cast<uint32_t*>(&h);
-}
-
-template <>
-struct Elem<__nv_bfloat16> {
-  __device__ static float load1(const __nv_bfloat16* p) {
-    const unsigned short u = __ldg(reinterpret_cast<const unsigned short*>(p));
-    return __uint_as_float(static_cast<uint32_t>(u) << 16);
-  }
-  __device__ static void load8(const __nv_bfloat16* p, float (&v)[8]) {
-    const uint4 w = ld_stream16(p);
-    v[0] = __uint_as_float(w.x << 16); v[1] = __uint_as_float(w.x & 0xffff0000u);
-    v[2] = __uint_as_float(w.y << 16); v[3] = __uint_as_float(w.y & 0xffff0000u);
-    v[4] = __uint_as_float(w.z << 16); v[5] = __uint_as_float(w.z & 0xffff0000u);
-    v[6] = __uint_as_float(w.w << 16); v[7] = __uint_as_float(w.w & 0xffff0000u);
-  }
-  __device__ static void store1(__nv_bfloat16* p, float v) { *p = __float2bfloat16_rn(v); }
-  __device__ static void store8(__nv_bfloat16* p, const float (&v)[8]) {
-    st16(p, make_uint4(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]), pack_bf16x2(v[4], v[5]),
-                       pack_bf16x2(v[6], v[7])));
-  }
-};
-
-// Loads the 8 columns [8*vec, 8*vec + 8) of a row.  `aligned` selects one
-// 16-byte load per 16 bytes; otherwise scalar loads give the same values.
-// Columns at or beyond V (only in the last, partial vector) are not read;
-// `valid` reports how many columns are real.
+// Loads vector `vec` of a row: one or two 16-byte loads when the row start is
+// 16-byte aligned and the vector is whole, else scalar loads (same values).
 template <class T>
-__device__ __forceinline__ void load_vec(const T* row, int64_t vec, int64_t V, bool aligned,
-                                         float (&v)[8], int& valid) {
+__device__ __forceinline__ void load_raw(Raw8<T>& r, const T* row, int64_t vec, int64_t V, bool aligned,
+                                         int& valid) {
   const int64_t c0 = vec * 8;
-  if (aligned && c0 + 8 <= V) {
-    Elem<T>::load8(row + c0, v);
-    valid = 8;
-    return;
-  }
   const int64_t rem = V - c0;
   valid = rem < 8 ? static_cast<int>(rem) : 8;
-#pragma unroll
-  for (int j = 0; j < 8; ++j) v[j] = j < valid ? Elem<T>::load1(row + c0 + j) : 0.0f;
+  if (aligned && valid == 8)
+    r.load(row + c0);
+  else
+    r.load_scalar(row + c0, valid);
 }
 
+// --------------------------------------------------------------------------
+// Final-logit softcap z = c tanh(x/c) in fp32 ("Final Logit Softcap",
+// Summary), written with one exponential and one reciprocal:
+//   a = |x|/c,  e = exp(-2a),  r = 1/(1+e),  tanh(a) = (1-e) r,
+//   d tanh/du = 1 - tanh^2 = 4 e r^2,
+// both with the sign of x.  1-e is exact for e in [1/2, 1] and the product
+// carries an absolute error of a few 1e-7 * c; 4 e r^2 keeps full relative
+// accuracy where tanh rounds to +-1.  x = -inf gives -c and slope 0.
+// --------------------------------------------------------------------------
+struct CapK {
+  float c;     // cap
+  float k;     // -2 log2(e) / c: exp(-2|x|/c) = 2^(|x| k)
+};
+
+__device__ __forceinline__ CapK cap_consts(float cap) { return {cap, -2.0f * kLog2e / cap}; }
+
+// tanh(x/c) and e = exp(-2|x|/c), r = 1/(1+e) for the slope.
+__device__ __forceinline__ float cap_t(float x, const CapK& K, float& e, float& r) {
+  e = ex2(fabsf(x) * K.k);
+  r = rcp(1.0f + e);
+  const float t = (1.0f - e) * r;
+  return __uint_as_float(__float_as_uint(t) | (__float_as_uint(x) & 0x80000000u));
+}
+__device__ __forceinline__ float cap_t(float x, const CapK& K) {
+  float e, r;
+  return cap_t(x, K, e, r);
+}
+
+// Packed form of cap_t for pair i of a raw vector (same operations).
 template <class T>
-__device__ __forceinline__ void store_vec(T* row, int64_t vec, int64_t V, bool aligned,
-                                          const float (&v)[8]) {
-  const int64_t c0 = vec * 8;
-  if (aligned && c0 + 8 <= V) {
-    Elem<T>::store8(row + c0, v);
-    return;
-  }
-#pragma unroll
-  for (int j = 0; j < 8; ++j)
-    if (c0 + j < V) Elem<T>::store1(row + c0 + j, v[j]);
+__device__ __forceinline__ fp2 cap_t2(const Raw8<T>& v, int i, const CapK& K, fp2& e2, fp2& r2) {
+  e2 = ex2_2(mul2(v.pair_abs(i), splat(K.k)));
+  r2 = rcp2(add2(e2, splat(1.0f)));
+  float t0, t1;
+  upk(mul2(sub2(splat(1.0f), e2), r2), t0, t1);
+  t0 = __uint_as_float(__float_as_uint(t0) | (v.sign_lo(i) & 0x80000000u));
+  t1 = __uint_as_float(__float_as_uint(t1) | (v.sign_hi(i) & 0x80000000u));
+  return pk(t0, t1);
 }
+
+// z - m for the softcapped logit: c t - m, one rounding.
+__device__ __forceinline__ float cap_d(float t, float c, float m) { return fmaf(t, c, -m); }
+
+// The softcapped value of the row max (tanh is increasing, so the max of z
+// is the cap of the max of x).
+__device__ __forceinline__ float cap_z(float x, const CapK& K) { return K.c * cap_t(x, K); }
 
 // --------------------------------------------------------------------------
-// Final-logit softcap z = c*tanh(x/c) in fp32 ("Final Logit Softcap",
-// Summary).  x/c is formed as x*(1/c): within one ulp of the correctly
-// rounded quotient.  tanh is CUDA's tanhf.
+// Online statistics (thread accumulators).  Each is centred on its running
+// max m:  S = sum e^{z-m};  entropy W = sum e^{z-m} (z-m);
+// KL(P||Q) W = sum e^{p-m_p} ((p-m_p) - (q-m_q)),
+// re-centred when a max grows ("Add Triton kernels for vocab-parallel
+// logprobs, entropy and KL", review "Suggested change"): when the max moves
+// from m to M the entropy W becomes e^{m-M} (W + S (m-M)) and the KL W becomes
+// e^{m_p-M_p} (W + S_p ((m_p-M_p) - (m_q-M_q))).  Even and odd columns of a
+// vector accumulate in the two halves of a packed pair.
 // --------------------------------------------------------------------------
-__device__ __forceinline__ float softcap_z(float x, float cap, float rcap) {
-  return cap * tanhf(x * rcap);
-}
 
-// dz/dx = 1 - tanh^2(x/c) = sech^2(x/c).  Near the origin 1 - t^2 has no
-// cancellation; elsewhere it is formed as 4e/(1+e)^2 with e = exp(-2|u|),
-// which keeps full relative accuracy where tanh rounds to +-1.
-__device__ __forceinline__ float softcap_dzdx(float u, float t) {
-  const float au = fabsf(u);
-  if (au < 0.5f) return fmaf(-t, t, 1.0f);
-  const float e = ex2(-2.0f * kLog2e * au);
-  const float r = __frcp_rn(1.0f + e);
-  return 4.0f * e * r * r;
-}
-
-template <bool CAP>
-__device__ __forceinline__ void apply_cap8(float (&z)[8], float cap, float rcap) {
-  if (CAP) {
-#pragma unroll
-    for (int j = 0; j < 8; ++j) z[j] = softcap_z(z[j], cap, rcap);
-  }
-}
-
-// Columns past the end of the row take part as masked (-inf) logits; the
-// mask goes after the softcap so that it stays -inf.
-__device__ __forceinline__ void mask_tail(float (&z)[8], int valid) {
-#pragma unroll
-  for (int j = 0; j < 8; ++j)
-    if (j >= valid) z[j] = neg_inf();
-}
-
-__device__ __forceinline__ float max8(const float (&z)[8]) {
-  return fmaxf(fmaxf(fmaxf(z[0], z[1]), fmaxf(z[2], z[3])),
-               fmaxf(fmaxf(z[4], z[5]), fmaxf(z[6], z[7])));
-}
-
-// 2^((m_old - m_new) * log2 e): the factor that re-centres a sum taken
-// around m_old onto m_new >= m_old; 0 when m_old = -inf.
+// 2^((m_old - m_new) log2 e): re-centres a sum from m_old onto m_new >= m_old;
+// 0 when m_old = -inf.
 __device__ __forceinline__ float rescale(float m_old, float m_new) {
   return ex2((m_old - m_new) * kLog2e);
 }
 
-// --------------------------------------------------------------------------
-// Online statistics.  Each state is centred on its running max m:
-//   S = sum e^{z-m};  entropy W = sum e^{z-m} (z-m);
-//   KL(P||Q) W = sum e^{p-m_p} ((p-m_p) - (q-m_q)),
-// re-centred when a max grows ("Add Triton kernels for vocab-parallel
-// logprobs, entropy and KL", review "Suggested change"); when the max moves
-// from m to M the entropy W becomes e^{m-M} (W + S (m-M)), and the KL W
-// becomes e^{m_p-M_p} (W + S_p ((m_p-M_p) - (m_q-M_q))).
-// --------------------------------------------------------------------------
 struct LogpState {
   float m, s;
   __device__ static LogpState identity() { return {neg_inf(), 0.0f}; }
-  __device__ __forceinline__ void update(const float (&z)[8]) {
-    const float vm = max8(z);
-    if (vm > m) {
-      s *= rescale(m, vm);
-      m = vm;
-    }
-    if (m != neg_inf()) {
-      float e[8];
-#pragma unroll
-      for (int j = 0; j < 8; ++j) e[j] = ex2((z[j] - m) * kLog2e);
-      s += ((e[0] + e[1]) + (e[2] + e[3])) + ((e[4] + e[5]) + (e[6] + e[7]));
-    }
-  }
   __device__ static LogpState combine(const LogpState& a, const LogpState& b) {
     const float M = fmaxf(a.m, b.m);
     if (M == neg_inf()) return identity();
@@ -217,33 +304,12 @@ struct LogpState {
 struct EntropyState {
   float m, s, w;
   __device__ static EntropyState identity() { return {neg_inf(), 0.0f, 0.0f}; }
-  __device__ __forceinline__ void update(const float (&z)[8]) {
-    const float vm = max8(z);
-    if (vm > m) {
-      const float f = rescale(m, vm);
-      w = s > 0.0f ? f * fmaf(s, m - vm, w) : 0.0f;
-      s *= f;
-      m = vm;
-    }
-    if (m != neg_inf()) {
-      float e[8], ed[8];
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const float d = z[j] - m;
-        e[j] = ex2(d * kLog2e);
-        // -inf columns: e = 0 and d is clamped so that 0 * d stays 0
-        ed[j] = e[j] * fmaxf(d, -kFltMax);
-      }
-      s += ((e[0] + e[1]) + (e[2] + e[3])) + ((e[4] + e[5]) + (e[6] + e[7]));
-      w += ((ed[0] + ed[1]) + (ed[2] + ed[3])) + ((ed[4] + ed[5]) + (ed[6] + ed[7]));
-    }
-  }
   __device__ static EntropyState combine(const EntropyState& a, const EntropyState& b) {
     const float M = fmaxf(a.m, b.m);
     if (M == neg_inf()) return identity();
     const float fa = rescale(a.m, M), fb = rescale(b.m, M);
-    const float wa = a.s > 0.0f ? fa * fmaf(a.s, a.m - M, a.w) : 0.0f;
-    const float wb = b.s > 0.0f ? fb * fmaf(b.s, b.m - M, b.w) : 0.0f;
+    const float wa = a.m != neg_inf() ? fa * fmaf(a.s, a.m - M, a.w) : 0.0f;
+    const float wb = b.m != neg_inf() ? fb * fmaf(b.s, b.m - M, b.w) : 0.0f;
     return {M, a.s * fa + b.s * fb, wa + wb};
   }
   __device__ EntropyState shfl_xor(int lane_mask) const {
@@ -253,51 +319,11 @@ struct EntropyState {
 };
 
 // KL(P||Q) with P the first argument.  `flag` records a column where P is
-// finite and Q is -inf (decided on the logits).
+// not -inf and Q is -inf (decided on the logits).
 struct KlState {
   float mp, sp, mq, sq, w;
-  int flag;
-  __device__ static KlState identity() { return {neg_inf(), 0.0f, neg_inf(), 0.0f, 0.0f, 0}; }
-  __device__ __forceinline__ void update(const float (&p)[8], const float (&q)[8]) {
-    const float vmp = max8(p), vmq = max8(q);
-    if (vmp > mp || vmq > mq) {
-      const float Mp = fmaxf(mp, vmp), Mq = fmaxf(mq, vmq);
-      const float fp = rescale(mp, Mp), fq = rescale(mq, Mq);
-      w = sp > 0.0f ? fp * fmaf(sp, (mp - Mp) - (mq - Mq), w) : 0.0f;
-      sp *= fp;
-      sq *= fq;
-      mp = Mp;
-      mq = Mq;
-    }
-#pragma unroll
-    for (int j = 0; j < 8; ++j) flag |= (q[j] == neg_inf()) & (p[j] != neg_inf());
-    if (mp != neg_inf()) {
-      float e[8], dp[8];
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        dp[j] = p[j] - mp;
-        e[j] = ex2(dp[j] * kLog2e);
-      }
-      sp += ((e[0] + e[1]) + (e[2] + e[3])) + ((e[4] + e[5]) + (e[6] + e[7]));
-      if (mq != neg_inf()) {
-        float ew[8];
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          // clamps keep 0 * (-inf) and inf - inf out of W; a column where
-          // only Q is -inf is caught by the flag
-          const float a = fmaxf(dp[j], -kFltMax), b = fmaxf(q[j] - mq, -kFltMax);
-          ew[j] = e[j] * (a - b);
-        }
-        w += ((ew[0] + ew[1]) + (ew[2] + ew[3])) + ((ew[4] + ew[5]) + (ew[6] + ew[7]));
-      }
-    }
-    if (mq != neg_inf()) {
-      float e[8];
-#pragma unroll
-      for (int j = 0; j < 8; ++j) e[j] = ex2((q[j] - mq) * kLog2e);
-      sq += ((e[0] + e[1]) + (e[2] + e[3])) + ((e[4] + e[5]) + (e[6] + e[7]));
-    }
-  }
+  uint32_t flag;
+  __device__ static KlState identity() { return {neg_inf(), 0.0f, neg_inf(), 0.0f, 0.0f, 0u}; }
   __device__ static KlState combine(const KlState& a, const KlState& b) {
     const float Mp = fmaxf(a.mp, b.mp), Mq = fmaxf(a.mq, b.mq);
     KlState r;
@@ -310,8 +336,8 @@ struct KlState {
     const float fqb = Mq == neg_inf() ? 0.0f : rescale(b.mq, Mq);
     r.sp = a.sp * fpa + b.sp * fpb;
     r.sq = a.sq * fqa + b.sq * fqb;
-    const float wa = a.sp > 0.0f ? fpa * fmaf(a.sp, (a.mp - Mp) - (a.mq - Mq), a.w) : 0.0f;
-    const float wb = b.sp > 0.0f ? fpb * fmaf(b.sp, (b.mp - Mp) - (b.mq - Mq), b.w) : 0.0f;
+    const float wa = a.mp != neg_inf() ? fpa * fmaf(a.sp, (a.mp - Mp) - (a.mq - Mq), a.w) : 0.0f;
+    const float wb = b.mp != neg_inf() ? fpb * fmaf(b.sp, (b.mp - Mp) - (b.mq - Mq), b.w) : 0.0f;
     r.w = wa + wb;
     return r;
   }
@@ -357,12 +383,73 @@ __device__ __forceinline__ void cluster_wait() {
   asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
-__device__ __forceinline__ bool aligned16(const void* p) {
-  return (reinterpret_cast<uintptr_t>(p) & 15u) == 0;
+// --------------------------------------------------------------------------
+// Stores of 8 fp32 values as one vector of the output dtype.
+// --------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  // cvt.rn.bf16x2.f32: both halves rounded to nearest even
+  __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&h);
 }
 
-__device__ __forceinline__ bool valid_id(int64_t id, int64_t V, int64_t ignore_index) {
-  return id != ignore_index && id >= 0 && id < V;
+template <class T>
+struct Out8;
+
+template <>
+struct Out8<float> {
+  __device__ static void store(float* p, const fp2 (&o)[4]) {
+    float v[8];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) upk(o[i], v[2 * i], v[2 * i + 1]);
+    st16(p, make_uint4(__float_as_uint(v[0]), __float_as_uint(v[1]), __float_as_uint(v[2]), __float_as_uint(v[3])));
+    st16(p + 4,
+         make_uint4(__float_as_uint(v[4]), __float_as_uint(v[5]), __float_as_uint(v[6]), __float_as_uint(v[7])));
+  }
+  __device__ static void store1(float* p, float v) { *p = v; }
+  __device__ static float nan_value() { return qnan(); }
+};
+
+template <>
+struct Out8<__nv_bfloat16> {
+  __device__ static void store(__nv_bfloat16* p, const fp2 (&o)[4]) {
+    uint32_t w[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      float a, b;
+      upk(o[i], a, b);
+      w[i] = pack_bf16x2(a, b);
+    }
+    st16(p, make_uint4(w[0], w[1], w[2], w[3]));
+  }
+  __device__ static void store1(__nv_bfloat16* p, float v) { *p = __float2bfloat16_rn(v); }
+};
+
+// Stores vector `vec` of an output row (whole and aligned: vector stores;
+// otherwise element by element, columns < V only).
+template <class T>
+__device__ __forceinline__ void store_vec(T* row, int64_t vec, int64_t V, bool aligned, const fp2 (&o)[4]) {
+  const int64_t c0 = vec * 8;
+  if (aligned && c0 + 8 <= V) {
+    Out8<T>::store(row + c0, o);
+    return;
+  }
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    float a, b;
+    upk(o[i], a, b);
+    if (c0 + 2 * i < V) Out8<T>::store1(row + c0 + 2 * i, a);
+    if (c0 + 2 * i + 1 < V) Out8<T>::store1(row + c0 + 2 * i + 1, b);
+  }
+}
+
+// Scalar element load (gathers, fix-ups).
+template <class T>
+__device__ __forceinline__ float load1(const T* p);
+template <>
+__device__ __forceinline__ float load1<float>(const float* p) { return __ldg(p); }
+template <>
+__device__ __forceinline__ float load1<__nv_bfloat16>(const __nv_bfloat16* p) {
+  return __uint_as_float(static_cast<uint32_t>(__ldg(reinterpret_cast<const unsigned short*>(p))) << 16);
 }
 
 }  // namespace dev
