@@ -322,6 +322,110 @@ def time_device(step: Step, steps: int, warmup: int, device):
     return total_ms, per, clk
 
 
+class ConfigRun:
+    """One of the five workloads, fwd+bwd of its ops, for per-config numbers
+    (``--workload``).  Not the headline step; the same kernels and geometry."""
+
+    def __init__(self, name: str, device):
+        import torch
+
+        import workloads
+        from vocab_log_softmax_gb300 import binding as B
+        self.name = name
+        f32 = dict(dtype=torch.float32, device=device)
+        L = []                                       # (label, bytes, thunk)
+        if name == "logp_small":
+            w = workloads.logp_small(device)
+            x, ids, g = w["logits"], w["ids"], w["g"]
+            n, v = x.shape
+            lp, st, d = torch.empty((n, 1), **f32), torch.empty((n, 2), **f32), torch.empty_like(x)
+            b = op_bytes("logp", n, v, es=4)
+            L += [("logp fwd", b["fwd"], lambda: B.vls_logp_fwd(x, ids, logp=lp, stats=st)),
+                  ("logp bwd", b["bwd"], lambda: B.vls_logp_bwd(x, ids, g, st, dlogits=d))]
+        elif name == "logp_offset":
+            w = workloads.logp_offset(device)
+            x, ids, g = w["logits"], w["ids"], w["g"]
+            n, v = x.shape
+            lp, st, d = torch.empty((n, 1), **f32), torch.empty((n, 2), **f32), torch.empty_like(x)
+            b = op_bytes("logp", n, v)
+            L += [("logp fwd", b["fwd"], lambda: B.vls_logp_fwd(x, ids, logp=lp, stats=st)),
+                  ("logp bwd", b["bwd"], lambda: B.vls_logp_bwd(x, ids, g, st, dlogits=d))]
+        elif name == "kl_masked":
+            w = workloads.kl_masked(device)
+            a_, b_, g = w["a"], w["b"], w["g"]
+            n, v = a_.shape
+            H, kl, sa, sb = (torch.empty((n,), **f32), torch.empty((n,), **f32), torch.empty((n, 2), **f32),
+                             torch.empty((n, 2), **f32))
+            d = torch.empty_like(a_)
+            be, bk = op_bytes("entropy", n, v), op_bytes("kl_reverse", n, v)
+            L += [("entropy fwd", be["fwd"], lambda: B.vls_entropy_fwd(a_, H=H, stats=sa)),
+                  ("entropy bwd", be["bwd"], lambda: B.vls_entropy_bwd(a_, g, H, sa, dlogits=d))]
+            for dr in ("forward", "reverse"):
+                L += [(f"{dr} KL fwd", bk["fwd"], lambda dr=dr: B.vls_kl_fwd(a_, b_, dr, kl=kl, stats_a=sa, stats_b=sb)),
+                      (f"{dr} KL bwd", bk["bwd"], lambda dr=dr: B.vls_kl_bwd(a_, b_, g, kl, sa, sb, dr, da=d))]
+        elif name == "softcap_wide":
+            w = workloads.softcap_wide(device)
+            x, ids, g, gy = w["logits"], w["ids"], w["g"], w["gy_bf16"]
+            n, v = x.shape
+            lp, st, d, y = torch.empty((n, 1), **f32), torch.empty((n, 2), **f32), torch.empty_like(x), torch.empty_like(x)
+            b, bs = op_bytes("cap_logp", n, v), op_bytes("softcap", n, v)
+            for c in w["caps"]:
+                L += [(f"cap{c:g} logp fwd", b["fwd"], lambda c=c: B.vls_logp_fwd(x, ids, -100, c, logp=lp, stats=st)),
+                      (f"cap{c:g} logp bwd", b["bwd"], lambda c=c: B.vls_logp_bwd(x, ids, g, st, -100, c, dlogits=d))]
+            L += [("softcap fwd", bs["fwd"], lambda: B.vls_softcap_fwd(x, 30.0, y=y)),
+                  ("softcap bwd", bs["bwd"], lambda: B.vls_softcap_bwd(x, gy, 30.0, gx=d))]
+        elif name == "long_seq":
+            w = workloads.long_seq(device)
+            x = w["logits"]
+            n, v = x.shape
+            k = w["idsk"].shape[1]
+            lp1, lpk = torch.empty((n, 1), **f32), torch.empty((n, k), **f32)
+            st, H, d = torch.empty((n, 2), **f32), torch.empty((n,), **f32), torch.empty_like(x)
+            b1, bk, be = op_bytes("logp", n, v), op_bytes("logp", n, v, k=k), op_bytes("entropy", n, v)
+            L += [("k=1 logp fwd", b1["fwd"], lambda: B.vls_logp_fwd(x, w["ids1"], logp=lp1, stats=st)),
+                  ("k=1 logp bwd", b1["bwd"], lambda: B.vls_logp_bwd(x, w["ids1"], w["g1"], st, dlogits=d)),
+                  ("k=256 logp fwd", bk["fwd"], lambda: B.vls_logp_fwd(x, w["idsk"], logp=lpk, stats=st)),
+                  ("k=256 logp bwd", bk["bwd"], lambda: B.vls_logp_bwd(x, w["idsk"], w["gk"], st, dlogits=d)),
+                  ("entropy fwd", be["fwd"], lambda: B.vls_entropy_fwd(x, H=H, stats=st)),
+                  ("entropy bwd", be["bwd"], lambda: B.vls_entropy_bwd(x, w["g_row"], H, st, dlogits=d))]
+        else:
+            raise SystemExit(f"unknown workload {name}")
+        self.launches = L
+        self.rows, self.vocab = n, v
+
+
+def run_config(args) -> None:
+    """Per-config fwd / bwd times (median over steps) and TB/s for every op."""
+    import torch
+    device = torch.device("cuda", 0)
+    run = ConfigRun(args.workload, device)
+    for _ in range(args.warmup):
+        for _, _, f in run.launches:
+            f()
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream(device)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(run.launches) + 1)] for _ in range(args.steps)]
+    for s in range(args.steps):
+        for j, (_, _, f) in enumerate(run.launches):
+            ev[s][j].record(stream)
+            f()
+        ev[s][-1].record(stream)
+    torch.cuda.synchronize()
+    peak, kind = hbm_peak()
+    ops = {}
+    for j, (label, nbytes, _) in enumerate(run.launches):
+        ts = sorted(ev[s][j].elapsed_time(ev[s][j + 1]) for s in range(args.steps))
+        med = ts[len(ts) // 2]
+        ops[label] = {"ms_median": round(med, 4), "ms_p10": round(ts[len(ts) // 10], 4),
+                      "ms_p90": round(ts[(9 * len(ts)) // 10], 4), "tbs": round(nbytes / med / 1e9, 3),
+                      "frac_of_measured": round(nbytes / med / 1e6 / peak, 4), "bytes": nbytes}
+    total_b = sum(b for _, b, _ in run.launches)
+    total_ms = sum(o["ms_median"] for o in ops.values())
+    print(json.dumps({"workload": run.name, "rows": run.rows, "vocab": run.vocab, "steps": args.steps,
+                      "fwd_bwd_ms": round(total_ms, 4), "tbs": round(total_b / total_ms / 1e9, 3),
+                      "peak_gbs": peak, "peak_kind": kind, "ops": ops}), flush=True)
+
+
 def time_e2e(step: Step, steps: int, device):
     """Same step through the same calls, with every input copied in from
     pinned host memory and every result copied back, inside the timed region."""
@@ -473,7 +577,13 @@ def main() -> None:
     ap.add_argument("--rows", type=int, default=N_ROWS, help="rows per GPU (default 8192)")
     ap.add_argument("--e2e-steps", type=int, default=3)
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timing leg")
+    ap.add_argument("--workload", default="step",
+                    choices=["step", "logp_small", "logp_offset", "kl_masked", "softcap_wide", "long_seq"],
+                    help="step (default): the benchmark step; otherwise per-op times of one workload")
     args = ap.parse_args()
+    if args.workload != "step" and args.impl == "ours":
+        run_config(args)
+        return
 
     if args.impl == "reference":
         run_reference(args)

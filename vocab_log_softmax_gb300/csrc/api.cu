@@ -196,9 +196,7 @@ int vls_softcap_fwd(const void* x, void* y, int64_t n, vls_dtype dt, float cap, 
   DeviceGuard guard;
   if (int e = guard.enter(dev)) return e;
   CapArgs a{x, nullptr, 0, y, n, cap, 1.0f / cap, 0};
-  const int64_t want = ceil_div(ceil_div(n, 8), 256);
-  const int64_t cap_grid = static_cast<int64_t>(sm_count(dev)) * 8;
-  a.grid = static_cast<int>(want < cap_grid ? (want < 1 ? 1 : want) : cap_grid);
+  a.grid = sm_count(dev);
   return launch_status(launch_softcap_fwd(dt, a, static_cast<cudaStream_t>(stream)));
 }
 
@@ -214,9 +212,7 @@ int vls_softcap_bwd(const void* x, const void* gy, vls_dtype gy_dt, void* gx, in
   DeviceGuard guard;
   if (int e = guard.enter(dev)) return e;
   CapArgs a{x, gy, gy_dt == VLS_F32 ? 1 : 0, gx, n, cap, 1.0f / cap, 0};
-  const int64_t want = ceil_div(ceil_div(n, 8), 256);
-  const int64_t cap_grid = static_cast<int64_t>(sm_count(dev)) * 8;
-  a.grid = static_cast<int>(want < cap_grid ? (want < 1 ? 1 : want) : cap_grid);
+  a.grid = sm_count(dev);
   return launch_status(launch_softcap_bwd(dt, a, static_cast<cudaStream_t>(stream)));
 }
 

@@ -120,8 +120,11 @@ __device__ __forceinline__ fp2 grad_pair(const Raw8<T>& x, const Raw8<T>& y, int
   return r;
 }
 
+// Six resident CTAs per SM (at most 40 registers a thread) keep enough
+// loads in flight; with a larger register budget occupancy halves and the
+// sweep slows down.
 template <class T, int OP, bool CAP>
-__global__ void __launch_bounds__(kRowThreads) row_bwd_kernel(const BwdArgs a) {
+__global__ void __launch_bounds__(kRowThreads, 6) row_bwd_kernel(const BwdArgs a) {
   constexpr bool KL = OP >= kBwdKlReverse;
   const int64_t row = blockIdx.x / a.chunks;
   const int q = static_cast<int>(blockIdx.x - row * a.chunks);

@@ -61,7 +61,7 @@ __device__ __forceinline__ fp2 slope_pair(const Raw8<T>& v, const Raw8<G>& g, in
 }
 
 template <class T>
-__global__ void __launch_bounds__(kCapThreads) softcap_fwd_kernel(const CapArgs a) {
+__global__ void __launch_bounds__(kCapThreads, 6) softcap_fwd_kernel(const CapArgs a) {
   const T* x = static_cast<const T*>(a.x);
   T* y = static_cast<T*>(a.out);
   const CapK K = cap_consts(a.cap);
@@ -96,7 +96,7 @@ __global__ void __launch_bounds__(kCapThreads) softcap_fwd_kernel(const CapArgs 
 }
 
 template <class T, class G>
-__global__ void __launch_bounds__(kCapThreads) softcap_bwd_kernel(const CapArgs a) {
+__global__ void __launch_bounds__(kCapThreads, 6) softcap_bwd_kernel(const CapArgs a) {
   const T* x = static_cast<const T*>(a.x);
   const G* gy = static_cast<const G*>(a.gy);
   T* gx = static_cast<T*>(a.out);
@@ -137,24 +137,32 @@ __global__ void __launch_bounds__(kCapThreads) softcap_bwd_kernel(const CapArgs 
   for (; v < a.n; v += stride) Out8<T>::store1(gx + v, load1(gy + v) * softcap_slope(load1(x + v), K));
 }
 
-cudaError_t launch_softcap_fwd(vls_dtype dt, const CapArgs& a, cudaStream_t s) {
-  if (dt == VLS_BF16)
-    softcap_fwd_kernel<__nv_bfloat16><<<a.grid, kCapThreads, 0, s>>>(a);
-  else
-    softcap_fwd_kernel<float><<<a.grid, kCapThreads, 0, s>>>(a);
+// Grid-stride launch with exactly one wave: (resident CTAs per SM) x SMs,
+// fewer when n is small.  `a.grid` holds the SM count on entry.
+template <class K>
+cudaError_t launch_one_wave(K kernel, CapArgs a, cudaStream_t s) {
+  int per_sm = 0;
+  cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kCapThreads, 0);
+  if (e != cudaSuccess) return e;
+  if (per_sm < 1) per_sm = 1;
+  const int64_t want = ((a.n >> 3) + kCapThreads - 1) / kCapThreads;
+  const int64_t full = static_cast<int64_t>(a.grid) * per_sm;
+  a.grid = static_cast<int>(want < 1 ? 1 : (want < full ? want : full));
+  kernel<<<a.grid, kCapThreads, 0, s>>>(a);
   return cudaGetLastError();
+}
+
+cudaError_t launch_softcap_fwd(vls_dtype dt, const CapArgs& a, cudaStream_t s) {
+  if (dt == VLS_BF16) return launch_one_wave(softcap_fwd_kernel<__nv_bfloat16>, a, s);
+  return launch_one_wave(softcap_fwd_kernel<float>, a, s);
 }
 
 cudaError_t launch_softcap_bwd(vls_dtype dt, const CapArgs& a, cudaStream_t s) {
   if (dt == VLS_BF16) {
-    if (a.gy_f32)
-      softcap_bwd_kernel<__nv_bfloat16, float><<<a.grid, kCapThreads, 0, s>>>(a);
-    else
-      softcap_bwd_kernel<__nv_bfloat16, __nv_bfloat16><<<a.grid, kCapThreads, 0, s>>>(a);
-  } else {
-    softcap_bwd_kernel<float, float><<<a.grid, kCapThreads, 0, s>>>(a);
+    if (a.gy_f32) return launch_one_wave(softcap_bwd_kernel<__nv_bfloat16, float>, a, s);
+    return launch_one_wave(softcap_bwd_kernel<__nv_bfloat16, __nv_bfloat16>, a, s);
   }
-  return cudaGetLastError();
+  return launch_one_wave(softcap_bwd_kernel<float, float>, a, s);
 }
 
 }  // namespace vls

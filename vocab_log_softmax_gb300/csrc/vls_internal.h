@@ -82,7 +82,7 @@ struct CapArgs {
   int64_t n;
   float cap;
   float rcap;
-  int grid;
+  int grid;         // the SM count on entry to the launcher, the grid size after
 };
 
 // Launchers: one per kernel family, dispatching on dtype and softcap.  They
