@@ -50,11 +50,12 @@ void fwd_geometry(int64_t V, int* cluster, int64_t* vec_per_cta) {
 }
 
 // Backward geometry: results do not depend on it (pure map).  Top-k rows
-// prepare their id list once per CTA, so they take longer chunks.
+// prepare their id list once per CTA, so they take whole rows up to 262144
+// columns.
 void bwd_geometry(int64_t V, int32_t k, int* chunks, int64_t* vec_per_cta) {
   static const int64_t target = env_int("VLS_BWD_VEC_PER_CTA", 4096);
   const int64_t nvec = ceil_div(V, 8);
-  const int64_t t = k > 1 ? 4 * target : target;
+  const int64_t t = k > 1 ? 8 * target : target;
   int64_t c = ceil_div(nvec, t);
   if (c < 1) c = 1;
   *chunks = static_cast<int>(c);

@@ -16,59 +16,108 @@ namespace vls {
 
 using namespace dev;
 
-// Per-CTA prepared form of a row's top-k ids: G = sum of the upstream
-// gradients of the valid ids (ascending j), and, for each distinct valid id
-// that falls in this CTA's columns, the sum of its upstream gradients
-// (ascending j).  DeepSpeed PR #8838, Changes: the top-k one-hot terms are
-// added in fp32 before the single cast.
+// Per-CTA prepared form of a row's top-k ids (DeepSpeed PR #8838, Changes:
+// the top-k one-hot terms are added in fp32 before the single cast):
+//  - G, the sum of the upstream gradients of the valid ids, by a fixed tree
+//    (each thread sums j = t, t+256, ... in order, then lanes xor 16..1,
+//    then the 8 warp partials in order) -- the same bits in every CTA;
+//  - the valid ids sorted as keys (id << 11 | j) by a shared-memory bitonic
+//    sort, so duplicates sit together in ascending j; for each distinct id
+//    in this CTA's columns, the sum of its upstream gradients in ascending j.
+// Shared memory: keys[P] (P = next power of two >= k), fix_id[k], g[k],
+// fix_g[k]: 8 P + 16 k bytes.
 struct TopkPrep {
   float G;
   int nfix;
   bool any_valid;
 };
 
+constexpr int kTopkJBits = 11;  // j < 2048 > VLS_MAX_TOPK
+
+__host__ __device__ __forceinline__ int topk_pow2(int k) {
+  int p = 1;
+  while (p < k) p <<= 1;
+  return p;
+}
+
+// keys[P] + fix_id[k] (8 bytes each) + g[k] + fix_g[k] (4 bytes each)
+__host__ __device__ __forceinline__ size_t topk_smem_bytes(int k) {
+  return 8 * static_cast<size_t>(topk_pow2(k)) + 16 * static_cast<size_t>(k);
+}
+
 __device__ __forceinline__ TopkPrep prep_topk(const BwdArgs& a, int64_t row, int64_t col_beg, int64_t col_end,
-                                              int64_t* s_id, float* s_g, int64_t* fix_id, float* fix_g,
-                                              float* s_G, int* s_nfix, int* s_any) {
+                                              unsigned char* smem, int64_t*& fix_id, float*& fix_g,
+                                              float* s_warp, int* s_nfix) {
   const int k = a.k;
+  const int P = topk_pow2(k);
   const int64_t V = a.vocab;
   const int64_t* ids = a.ids + row * k;
   const float* g = a.g + row * k;
-  if (threadIdx.x == 0) {
-    *s_nfix = 0;
-    *s_any = 0;
-  }
-  for (int j = threadIdx.x; j < k; j += kRowThreads) {
-    s_id[j] = ids[j];
-    s_g[j] = g[j];
-  }
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    float G = 0.0f;
-    int any = 0;
-    for (int j = 0; j < k; ++j)
-      if (valid_id(s_id[j], V, a.ignore_index)) {
-        G += s_g[j];
+  unsigned long long* key = reinterpret_cast<unsigned long long*>(smem);
+  fix_id = reinterpret_cast<int64_t*>(key + P);
+  float* s_g = reinterpret_cast<float*>(fix_id + k);
+  fix_g = s_g + k;
+  constexpr unsigned long long kNone = ~0ull;
+
+  if (threadIdx.x == 0) *s_nfix = 0;
+  float gpart = 0.0f;
+  int any = 0;
+  for (int j = threadIdx.x; j < P; j += kRowThreads) {
+    unsigned long long kj = kNone;
+    if (j < k) {
+      const int64_t id = ids[j];
+      const float gj = g[j];
+      s_g[j] = gj;
+      if (valid_id(id, V, a.ignore_index)) {
+        kj = (static_cast<unsigned long long>(id) << kTopkJBits) | static_cast<unsigned long long>(j);
+        gpart += gj;
         any = 1;
       }
-    *s_G = G;
-    *s_any = any;
+    }
+    key[j] = kj;
   }
-  for (int j = threadIdx.x; j < k; j += kRowThreads) {
-    const int64_t id = s_id[j];
-    if (!valid_id(id, V, a.ignore_index) || id < col_beg || id >= col_end) continue;
-    bool first = true;
-    for (int i = 0; i < j && first; ++i) first = s_id[i] != id;
-    if (!first) continue;
+  // G by a fixed tree
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) gpart += __shfl_xor_sync(0xffffffffu, gpart, off);
+  if ((threadIdx.x & 31) == 0) s_warp[threadIdx.x >> 5] = gpart;
+  const bool any_valid = __syncthreads_or(any) != 0;
+  float G = 0.0f;
+#pragma unroll
+  for (int w = 0; w < kRowWarps; ++w) G += s_warp[w];
+
+  // bitonic sort of the P keys, ascending
+  for (int size = 2; size <= P; size <<= 1) {
+    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+      for (int t = threadIdx.x; t < (P >> 1); t += kRowThreads) {
+        const int lo = 2 * t - (t & (stride - 1));
+        const int hi = lo + stride;
+        const bool up = (lo & size) == 0;
+        const unsigned long long x = key[lo], y = key[hi];
+        if ((x > y) == up) {
+          key[lo] = y;
+          key[hi] = x;
+        }
+      }
+      __syncthreads();
+    }
+  }
+
+  // one fix-up entry per distinct id of this CTA's columns
+  for (int s = threadIdx.x; s < k; s += kRowThreads) {
+    const unsigned long long ks = key[s];
+    if (ks == kNone) continue;
+    const int64_t id = static_cast<int64_t>(ks >> kTopkJBits);
+    if (s > 0 && (key[s - 1] >> kTopkJBits) == (ks >> kTopkJBits)) continue;
+    if (id < col_beg || id >= col_end) continue;
     float gs = 0.0f;
-    for (int i = j; i < k; ++i)
-      if (s_id[i] == id) gs += s_g[i];
+    for (int t = s; t < k && (key[t] >> kTopkJBits) == (ks >> kTopkJBits); ++t)
+      gs += s_g[key[t] & ((1ull << kTopkJBits) - 1)];
     const int slot = atomicAdd(s_nfix, 1);
     fix_id[slot] = id;
     fix_g[slot] = gs;
   }
   __syncthreads();
-  return TopkPrep{*s_G, *s_nfix, *s_any != 0};
+  return TopkPrep{G, *s_nfix, any_valid};
 }
 
 // Row constants of a backward map.
@@ -153,13 +202,13 @@ __global__ void __launch_bounds__(kRowThreads, 6) row_bwd_kernel(const BwdArgs a
   int64_t* fix_id = nullptr;
   float* fix_g = nullptr;
   if constexpr (OP == kBwdLogp) {
-    // k = 1: one fixed slot; k > 1: ids, upstream grads and the fix-up list
-    // staged in dynamic shared memory (24 bytes per id)
+    // k = 1: one fixed slot; k > 1: sorted keys, upstream grads and the
+    // fix-up list in dynamic shared memory
     __shared__ int64_t fix1_id;
     __shared__ float fix1_g;
     extern __shared__ __align__(16) unsigned char topk_smem[];
-    __shared__ float s_G;
-    __shared__ int s_nfix, s_any;
+    __shared__ float s_warp[kRowWarps];
+    __shared__ int s_nfix;
     const int64_t col_beg = vb * 8, col_end = min(ve * 8, V);
     if (a.k == 1) {
       fix_id = &fix1_id;
@@ -178,12 +227,16 @@ __global__ void __launch_bounds__(kRowThreads, 6) row_bwd_kernel(const BwdArgs a
         zero_row = true;
       }
     } else {
-      int64_t* s_id = reinterpret_cast<int64_t*>(topk_smem);
-      fix_id = s_id + a.k;
-      float* s_g = reinterpret_cast<float*>(fix_id + a.k);
-      fix_g = s_g + a.k;
-      const TopkPrep tp =
-          prep_topk(a, row, col_beg, col_end, s_id, s_g, fix_id, fix_g, &s_G, &s_nfix, &s_any);
+      // the id preparation takes a few microseconds: start this thread's
+      // first vectors on their way to L2 so that DRAM latency overlaps it
+      if (al) {
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int64_t pv = vb + threadIdx.x + u * kRowThreads;
+          if (pv < (V >> 3) && pv < ve) prefetch_l2(xr + 8 * pv);
+        }
+      }
+      const TopkPrep tp = prep_topk(a, row, col_beg, col_end, topk_smem, fix_id, fix_g, s_warp, &s_nfix);
       G = tp.G;
       nfix = tp.nfix;
       zero_row = !tp.any_valid;
@@ -272,7 +325,7 @@ __global__ void __launch_bounds__(kRowThreads, 6) row_bwd_kernel(const BwdArgs a
 template <class T, int OP, bool CAP>
 cudaError_t launch_bwd_t(const BwdArgs& a, cudaStream_t s) {
   const dim3 grid(static_cast<unsigned>(a.rows * a.chunks));
-  const size_t smem = (OP == kBwdLogp && a.k > 1) ? static_cast<size_t>(a.k) * 24 : 0;
+  const size_t smem = (OP == kBwdLogp && a.k > 1) ? topk_smem_bytes(a.k) : 0;
   row_bwd_kernel<T, OP, CAP><<<grid, kRowThreads, smem, s>>>(a);
   return cudaGetLastError();
 }

@@ -3,13 +3,13 @@
 //
 // Launch shape: a cluster of `cluster` CTAs per row (cluster size a function
 // of V only), each CTA owning a contiguous run of 8-column vectors.  Inside a
-// CTA, thread t owns vectors t, t + 256, t + 512, ... of that run and folds
-// them in increasing order into its online state; the states are then
-// combined by a fixed tree: lanes (xor 16..1), warps (xor 4..1 over 8
-// warps), cluster ranks (xor 4..1 over up to 8 ranks, through distributed
-// shared memory into rank 0).  Nothing in that order depends on N, on the
-// row's position or on its alignment, so results are deterministic and batch
-// invariant (one block per row and a fixed reduction tree, "perf(logp): fused
+// CTA of T = kFwdThreads threads, thread t owns vectors t, t + T, t + 2T, ...
+// of that run and folds them in increasing order into its online state; the
+// states are then combined by a fixed tree: lanes (xor 16..1), warps (xor
+// T/64..1 over the T/32 warps), cluster ranks (xor 4..1 over up to 8 ranks,
+// through distributed shared memory into rank 0).  Nothing in that order
+// depends on N, on the row's position or on its alignment, so results are
+// deterministic and batch invariant (one block per row and a fixed reduction tree, "perf(logp): fused
 // zero-workspace backward ...", RL-Kernel PR #495, Summary; a tree fixed
 // regardless of the row count, "TP4 GDN, convolution and D=256 attention
 // mixers", RL-Kernel PR #507).
@@ -179,12 +179,12 @@ template <int OP>
 constexpr int fwd_unroll() { return OP == kFwdKl ? 2 : 4; }
 
 template <class T, int OP, bool CAP>
-__global__ void __launch_bounds__(kRowThreads) row_fwd_kernel(const FwdArgs a) {
+__global__ void __launch_bounds__(kFwdThreads) row_fwd_kernel(const FwdArgs a) {
   using Acc = typename FwdAccOf<OP, T, CAP>::type;
   using S = typename Acc::State;
   constexpr int U = fwd_unroll<OP>();
   constexpr bool KL = OP == kFwdKl;
-  __shared__ S warp_part[kRowWarps];
+  __shared__ S warp_part[kFwdWarps];
   __shared__ S cta_part[kMaxCluster];
   __shared__ S row_state;
 
@@ -206,12 +206,12 @@ __global__ void __launch_bounds__(kRowThreads) row_fwd_kernel(const FwdArgs a) {
   Acc acc;
   int64_t v = vb + threadIdx.x;
   if (al) {
-    for (; v + (U - 1) * kRowThreads < vfull_end; v += U * kRowThreads) {
+    for (; v + (U - 1) * kFwdThreads < vfull_end; v += U * kFwdThreads) {
       Raw8<T> rx[U], ry[U];
 #pragma unroll
       for (int u = 0; u < U; ++u) {
-        rx[u].load(xr + 8 * (v + u * kRowThreads));
-        if constexpr (KL) ry[u].load(yr + 8 * (v + u * kRowThreads));
+        rx[u].load(xr + 8 * (v + u * kFwdThreads));
+        if constexpr (KL) ry[u].load(yr + 8 * (v + u * kFwdThreads));
       }
 #pragma unroll
       for (int u = 0; u < U; ++u) acc.template update<false>(rx[u], KL ? ry[u] : rx[u], 8, K);
@@ -219,7 +219,7 @@ __global__ void __launch_bounds__(kRowThreads) row_fwd_kernel(const FwdArgs a) {
   }
   // remaining vectors, the partial last vector and unaligned rows: same
   // vectors, same order, same arithmetic
-  for (; v < ve; v += kRowThreads) {
+  for (; v < ve; v += kFwdThreads) {
     Raw8<T> rx, ry;
     int valid;
     load_raw(rx, xr, v, V, al, valid);
@@ -237,7 +237,7 @@ __global__ void __launch_bounds__(kRowThreads) row_fwd_kernel(const FwdArgs a) {
   __syncthreads();
   S blk = S::identity();
   if (warp == 0) {
-    blk = reduce8(lane < kRowWarps ? warp_part[lane] : S::identity());
+    blk = reduce_lanes<kFwdWarps>(lane < kFwdWarps ? warp_part[lane] : S::identity());
     if (lane == 0 && C == 1) row_state = blk;
   }
   if (C > 1) {
@@ -250,7 +250,7 @@ __global__ void __launch_bounds__(kRowThreads) row_fwd_kernel(const FwdArgs a) {
     cluster_wait();  // all partials have landed in rank 0
     if (q != 0) return;
     if (warp == 0) {
-      const S r = reduce8(lane < C ? cta_part[lane] : S::identity());
+      const S r = reduce_lanes<kMaxCluster>(lane < C ? cta_part[lane] : S::identity());
       if (lane == 0) row_state = r;
     }
   }
@@ -262,7 +262,7 @@ __global__ void __launch_bounds__(kRowThreads) row_fwd_kernel(const FwdArgs a) {
     const float m = fin.m;
     const float log_s = logf(fin.s);
     if (threadIdx.x == 0) a.stats_x[row] = vls_rowstat{m, log_s};
-    for (int j = threadIdx.x; j < a.k; j += kRowThreads) {
+    for (int j = threadIdx.x; j < a.k; j += kFwdThreads) {
       const int64_t id = a.ids[row * a.k + j];
       float out = 0.0f;
       if (valid_id(id, V, a.ignore_index)) {
@@ -299,7 +299,7 @@ template <class T, int OP, bool CAP>
 cudaError_t launch_fwd_t(const FwdArgs& a, cudaStream_t s) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(a.rows * a.cluster));
-  cfg.blockDim = dim3(kRowThreads);
+  cfg.blockDim = dim3(kFwdThreads);
   cfg.dynamicSmemBytes = 0;
   cfg.stream = s;
   cudaLaunchAttribute attr[1];

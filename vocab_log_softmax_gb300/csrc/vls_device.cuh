@@ -116,6 +116,11 @@ __device__ __forceinline__ uint4 ld_stream16(const void* p) {
   return r;
 }
 
+// Starts pulling the 128-byte line at p into L2 (no register, no wait).
+__device__ __forceinline__ void prefetch_l2(const void* p) {
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+}
+
 __device__ __forceinline__ void st16(void* p, uint4 v) {
   asm volatile("st.global.v4.u32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z),
                "r"(v.w)
@@ -361,12 +366,12 @@ __device__ __forceinline__ S warp_reduce(S s) {
   return s;
 }
 
-// Butterfly over the first 8 lanes (xor 4, 2, 1); lanes 8..31 hold identities
-// that never reach lanes 0..7.
-template <class S>
-__device__ __forceinline__ S reduce8(S s) {
+// Butterfly over the first W lanes (xor W/2, ..., 1); lanes W..31 hold
+// identities that never reach lanes 0..W-1.
+template <int W, class S>
+__device__ __forceinline__ S reduce_lanes(S s) {
 #pragma unroll
-  for (int off = 4; off > 0; off >>= 1) s = S::combine(s, s.shfl_xor(off));
+  for (int off = W / 2; off > 0; off >>= 1) s = S::combine(s, s.shfl_xor(off));
   return s;
 }
 

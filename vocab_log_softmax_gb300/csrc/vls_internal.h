@@ -20,6 +20,14 @@ enum BwdOp { kBwdLogp = 0, kBwdEntropy = 1, kBwdKlReverse = 2, kBwdKlForward = 3
 // function of this constant and of the cluster size, never of N.
 constexpr int kRowThreads = 256;
 constexpr int kRowWarps = kRowThreads / 32;
+// Threads per CTA of the forward sweep (its reduction tree: lanes, then the
+// kFwdWarps warps, then cluster ranks).
+#ifndef VLS_FWD_THREADS
+#define VLS_FWD_THREADS 256
+#endif
+constexpr int kFwdThreads = VLS_FWD_THREADS;
+constexpr int kFwdWarps = kFwdThreads / 32;
+static_assert(kFwdThreads == 256 || kFwdThreads == 512 || kFwdThreads == 1024, "forward CTA width");
 // Vectors each thread loads before using any of them (memory-level
 // parallelism).  Changing it does not change results: every thread still
 // visits its vectors in increasing order.
