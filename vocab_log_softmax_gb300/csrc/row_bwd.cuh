@@ -171,9 +171,10 @@ __device__ __forceinline__ fp2 grad_pair(const Raw8<T>& x, const Raw8<T>& y, int
 
 // Six resident CTAs per SM (at most 40 registers a thread) keep enough
 // loads in flight; with a larger register budget occupancy halves and the
-// sweep slows down.
+// sweep slows down.  The softcapped map runs a software pipeline and gets
+// kCapMinBlocks CTAs per SM.
 template <class T, int OP, bool CAP>
-__global__ void __launch_bounds__(kRowThreads, 6) row_bwd_kernel(const BwdArgs a) {
+__global__ void __launch_bounds__(kRowThreads, CAP ? kCapMinBlocks : 6) row_bwd_kernel(const BwdArgs a) {
   constexpr bool KL = OP >= kBwdKlReverse;
   const int64_t row = blockIdx.x / a.chunks;
   const int q = static_cast<int>(blockIdx.x - row * a.chunks);
@@ -268,23 +269,64 @@ __global__ void __launch_bounds__(kRowThreads, 6) row_bwd_kernel(const BwdArgs a
     return;
   }
 
-  constexpr int U = KL ? 2 : 4;
   int64_t v = vb + threadIdx.x;
   const int64_t vfull_end = min(ve, V >> 3);
-  if (al) {
-    for (; v + (U - 1) * kRowThreads < vfull_end; v += U * kRowThreads) {
-      Raw8<T> x[U], y[U];
+  if constexpr (CAP) {
+    // Heavy per-element arithmetic (two exponentials and a reciprocal):
+    // software-pipelined, the next batch's loads issued before the current
+    // batch is computed, alternating between two register buffers.
+    constexpr int U = (KL || sizeof(T) == 4) ? 1 : 2;
+    constexpr int64_t kStep = U * kRowThreads;
+    if (al && v + (U - 1) * kRowThreads < vfull_end) {
+      Raw8<T> xa[U], ya[U], xb[U], yb[U];
+      auto load = [&](Raw8<T>(&x)[U], Raw8<T>(&y)[U], int64_t at) {
 #pragma unroll
-      for (int u = 0; u < U; ++u) {
-        x[u].load(xr + 8 * (v + u * kRowThreads));
-        if constexpr (KL) y[u].load(yr + 8 * (v + u * kRowThreads));
+        for (int u = 0; u < U; ++u) {
+          x[u].load(xr + 8 * (at + u * kRowThreads));
+          if constexpr (KL) y[u].load(yr + 8 * (at + u * kRowThreads));
+        }
+      };
+      auto work = [&](const Raw8<T>(&x)[U], const Raw8<T>(&y)[U], int64_t at) {
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+          fp2 o[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) o[i] = grad_pair<T, OP, CAP>(x[u], KL ? y[u] : x[u], i, R, K);
+          Out8<T>::store(dr + 8 * (at + u * kRowThreads), o);
+        }
+      };
+      load(xa, ya, v);
+      for (;;) {
+        bool more = v + kStep + (U - 1) * kRowThreads < vfull_end;
+        if (more) load(xb, yb, v + kStep);
+        work(xa, ya, v);
+        v += kStep;
+        if (!more) break;
+        more = v + kStep + (U - 1) * kRowThreads < vfull_end;
+        if (more) load(xa, ya, v + kStep);
+        work(xb, yb, v);
+        v += kStep;
+        if (!more) break;
       }
+    }
+  } else {
+    // light arithmetic: plain batches of U loads in flight per thread
+    constexpr int U = KL ? 2 : 4;
+    if (al) {
+      for (; v + (U - 1) * kRowThreads < vfull_end; v += U * kRowThreads) {
+        Raw8<T> x[U], y[U];
 #pragma unroll
-      for (int u = 0; u < U; ++u) {
-        fp2 o[4];
+        for (int u = 0; u < U; ++u) {
+          x[u].load(xr + 8 * (v + u * kRowThreads));
+          if constexpr (KL) y[u].load(yr + 8 * (v + u * kRowThreads));
+        }
 #pragma unroll
-        for (int i = 0; i < 4; ++i) o[i] = grad_pair<T, OP, CAP>(x[u], KL ? y[u] : x[u], i, R, K);
-        Out8<T>::store(dr + 8 * (v + u * kRowThreads), o);
+        for (int u = 0; u < U; ++u) {
+          fp2 o[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) o[i] = grad_pair<T, OP, CAP>(x[u], KL ? y[u] : x[u], i, R, K);
+          Out8<T>::store(dr + 8 * (v + u * kRowThreads), o);
+        }
       }
     }
   }

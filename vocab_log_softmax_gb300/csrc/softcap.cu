@@ -8,10 +8,11 @@
 // u - u^3/3 of the Taylor series instead (relative error below 2 u^4/15 <
 // 1e-8 there).  The slope 4 e r^2 is accurate everywhere.
 //
-// Grid-stride kernels: the grid is a multiple of the SM count and each
-// thread handles 8-element vectors (16-byte accesses for bf16, two for
-// fp32); a misaligned pointer or the last n % 8 elements take scalar
-// accesses with the same arithmetic.
+// Grid-stride kernels: the grid is one wave of resident CTAs (a multiple of
+// the SM count) and each thread handles 8-element vectors (16-byte accesses
+// for bf16, two for fp32); a misaligned pointer or the last n % 8 elements
+// take scalar accesses with the same arithmetic.  The forward runs a
+// software pipeline over two register buffers.
 #include "vls_device.cuh"
 
 namespace vls {
@@ -20,8 +21,10 @@ using namespace dev;
 
 constexpr int kCapThreads = 256;
 constexpr float kCubicBelow = 1.0f / 64.0f;
-// 8-element vectors each thread loads before using any (memory-level parallelism)
-constexpr int kCapUnroll = 4;
+// 8-element vectors per register buffer; with two buffers in a software
+// pipeline, up to 2 x kCapUnroll vectors per thread are in flight
+template <class T>
+constexpr int cap_unroll() { return sizeof(T) == 2 ? 2 : 1; }
 
 __device__ __forceinline__ float softcap_value(float x, const CapK& K, float rcap) {
   const float u = x * rcap;
@@ -61,7 +64,8 @@ __device__ __forceinline__ fp2 slope_pair(const Raw8<T>& v, const Raw8<G>& g, in
 }
 
 template <class T>
-__global__ void __launch_bounds__(kCapThreads, 6) softcap_fwd_kernel(const CapArgs a) {
+__global__ void __launch_bounds__(kCapThreads, kCapMinBlocks) softcap_fwd_kernel(const CapArgs a) {
+  constexpr int kCapUnroll = cap_unroll<T>();
   const T* x = static_cast<const T*>(a.x);
   T* y = static_cast<T*>(a.out);
   const CapK K = cap_consts(a.cap);
@@ -70,16 +74,35 @@ __global__ void __launch_bounds__(kCapThreads, 6) softcap_fwd_kernel(const CapAr
   const bool al = aligned16(x) && aligned16(y);
   int64_t v = static_cast<int64_t>(blockIdx.x) * kCapThreads + threadIdx.x;
   if (al) {
-    for (; v + (kCapUnroll - 1) * stride < nvec; v += kCapUnroll * stride) {
-      Raw8<T> r[kCapUnroll];
+    if (v + (kCapUnroll - 1) * stride < nvec) {
+      // software-pipelined over two register buffers (see the backward map)
+      Raw8<T> ra[kCapUnroll], rb[kCapUnroll];
+      auto load = [&](Raw8<T>(&r)[kCapUnroll], int64_t at) {
 #pragma unroll
-      for (int u = 0; u < kCapUnroll; ++u) r[u].load(x + 8 * (v + u * stride));
+        for (int u = 0; u < kCapUnroll; ++u) r[u].load(x + 8 * (at + u * stride));
+      };
+      auto work = [&](const Raw8<T>(&r)[kCapUnroll], int64_t at) {
 #pragma unroll
-      for (int u = 0; u < kCapUnroll; ++u) {
-        fp2 o[4];
+        for (int u = 0; u < kCapUnroll; ++u) {
+          fp2 o[4];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) o[i] = softcap_pair(r[u], i, K, a.rcap);
-        Out8<T>::store(y + 8 * (v + u * stride), o);
+          for (int i = 0; i < 4; ++i) o[i] = softcap_pair(r[u], i, K, a.rcap);
+          Out8<T>::store(y + 8 * (at + u * stride), o);
+        }
+      };
+      const int64_t step = kCapUnroll * stride;
+      load(ra, v);
+      for (;;) {
+        bool more = v + step + (kCapUnroll - 1) * stride < nvec;
+        if (more) load(rb, v + step);
+        work(ra, v);
+        v += step;
+        if (!more) break;
+        more = v + step + (kCapUnroll - 1) * stride < nvec;
+        if (more) load(ra, v + step);
+        work(rb, v);
+        v += step;
+        if (!more) break;
       }
     }
     for (; v < nvec; v += stride) {
@@ -95,8 +118,12 @@ __global__ void __launch_bounds__(kCapThreads, 6) softcap_fwd_kernel(const CapAr
   for (; v < a.n; v += stride) Out8<T>::store1(y + v, softcap_value(load1(x + v), K, a.rcap));
 }
 
+// The slope needs one exponential and one reciprocal per element; plain
+// batches of 4 vectors per thread (two input streams) keep it at the copy
+// bandwidth, where a software pipeline measured slower.
 template <class T, class G>
 __global__ void __launch_bounds__(kCapThreads, 6) softcap_bwd_kernel(const CapArgs a) {
+  constexpr int U = 4;
   const T* x = static_cast<const T*>(a.x);
   const G* gy = static_cast<const G*>(a.gy);
   T* gx = static_cast<T*>(a.out);
@@ -106,16 +133,16 @@ __global__ void __launch_bounds__(kCapThreads, 6) softcap_bwd_kernel(const CapAr
   const bool al = aligned16(x) && aligned16(gy) && aligned16(gx);
   int64_t v = static_cast<int64_t>(blockIdx.x) * kCapThreads + threadIdx.x;
   if (al) {
-    for (; v + (kCapUnroll - 1) * stride < nvec; v += kCapUnroll * stride) {
-      Raw8<T> r[kCapUnroll];
-      Raw8<G> g[kCapUnroll];
+    for (; v + (U - 1) * stride < nvec; v += U * stride) {
+      Raw8<T> r[U];
+      Raw8<G> g[U];
 #pragma unroll
-      for (int u = 0; u < kCapUnroll; ++u) {
+      for (int u = 0; u < U; ++u) {
         r[u].load(x + 8 * (v + u * stride));
         g[u].load(gy + 8 * (v + u * stride));
       }
 #pragma unroll
-      for (int u = 0; u < kCapUnroll; ++u) {
+      for (int u = 0; u < U; ++u) {
         fp2 o[4];
 #pragma unroll
         for (int i = 0; i < 4; ++i) o[i] = slope_pair(r[u], g[u], i, K);

@@ -28,6 +28,13 @@ constexpr int kRowWarps = kRowThreads / 32;
 constexpr int kFwdThreads = VLS_FWD_THREADS;
 constexpr int kFwdWarps = kFwdThreads / 32;
 static_assert(kFwdThreads == 256 || kFwdThreads == 512 || kFwdThreads == 1024, "forward CTA width");
+// Resident CTAs per SM the softcapped maps (capped backward, standalone
+// softcap) are compiled for; their software-pipelined loops need more
+// registers than the plain maps (6 CTAs, 40 registers).
+#ifndef VLS_CAP_MIN_BLOCKS
+#define VLS_CAP_MIN_BLOCKS 5
+#endif
+constexpr int kCapMinBlocks = VLS_CAP_MIN_BLOCKS;
 // Vectors each thread loads before using any of them (memory-level
 // parallelism).  Changing it does not change results: every thread still
 // visits its vectors in increasing order.
