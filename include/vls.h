@@ -66,7 +66,8 @@ typedef struct { float m; float log_s; } vls_rowstat;
 enum {
   VLS_OK = 0,
   VLS_ERR_NULL = 1,     /* a required pointer is NULL (with N > 0)               */
-  VLS_ERR_SHAPE = 2,    /* N < 0, V < 1, ld < V, k < 1 or k > VLS_MAX_TOPK, n < 0 */
+  VLS_ERR_SHAPE = 2,    /* N < 0, V < 1, ld < V, k < 1 or k > VLS_MAX_TOPK, n < 0,
+                           R < 1, a shard outside [0, V_total)                   */
   VLS_ERR_DTYPE = 3,    /* dtype not a vls_dtype; gy dtype neither F32 nor dt     */
   VLS_ERR_CAP = 4,      /* cap NaN, infinite or negative (softcap calls: cap <= 0) */
   VLS_ERR_DEVICE = 5,   /* a pointer is not device memory, or pointers / stream
@@ -158,6 +159,71 @@ int vls_kl_bwd(const void* a, int64_t lda, const void* b, int64_t ldb, vls_dtype
                int64_t N, int64_t V, vls_kl_dir dir, float cap, const float* g,
                const float* kl, const vls_rowstat* stats_a, const vls_rowstat* stats_b,
                void* da, void* stream);
+
+/* ------------------------------------------------------------------------ */
+/* Vocabulary-parallel statistics, split phase (DeepSpeed PR #8838, Changes: */
+/* local max and sum-exp from one read, rescaled to the global max, so that  */
+/* tensor parallelism needs one MAX and one SUM all-reduce; review           */
+/* "Suggested change": entropy / KL sums re-centred on the global max, the   */
+/* support-mismatch flag sharing the MAX all-reduce).                        */
+/*                                                                           */
+/* Each rank holds the columns [vocab_offset, vocab_offset + V_shard) of a   */
+/* V_total-column vocabulary.  vls_*_partial sweeps its shard once and       */
+/* writes one vls_partial per row; the caller gathers the R ranks' partial   */
+/* arrays in rank order into one [R, N] array (an all-gather of 24 bytes per */
+/* row per rank) and vls_*_combine folds them in rank order 0..R-1 and       */
+/* writes the same outputs and per-row statistics as the unsharded forward.  */
+/* The backward then runs per shard: vls_entropy_bwd / vls_kl_bwd unchanged  */
+/* on the shard with the combined statistics, vls_logp_bwd_shard for logp.   */
+/* V_shard = 0 (an empty shard) is allowed and gives the identity partial.   */
+/* Results are deterministic for a fixed sharding; they match the unsharded  */
+/* call up to rounding (the reduction tree differs).                         */
+/* ------------------------------------------------------------------------ */
+
+/* Per-row partial state of one shard, centred on the shard's maxima.
+ * logp: m, s.  entropy: m, s, w = sum e^{z-m}(z-m).  KL(P||Q) (P the first
+ * argument of the direction): m, s of P, w = sum e^{p-m}((p-m)-(q-mq)),
+ * mq, sq of Q, flag = a column with P finite and Q = -inf. */
+typedef struct {
+  float m, s, w, mq, sq;
+  uint32_t flag;
+} vls_partial;
+
+/* Partial of vls_logp_fwd over a shard.  part: [N].  zt: fp32 [N, k]; for an
+ * id that is valid against V_total and lies in this shard, the raw (uncapped)
+ * logit of that column, else 0 -- summed over the ranks it is the target's
+ * logit (exactly one rank owns a valid id). */
+int vls_logp_partial(const void* logits, int64_t ld, vls_dtype dt, int64_t N, int64_t V_shard,
+                     int64_t vocab_offset, int64_t V_total, const int64_t* ids, int32_t k,
+                     int64_t ignore_index, float cap, vls_partial* part, float* zt, void* stream);
+
+/* Folds parts [R, N] (rank-major) and zt [R, N, k] into logp [N, k] and stats [N]. */
+int vls_logp_combine(const vls_partial* parts, const float* zt, int32_t R, int64_t N, const int64_t* ids,
+                     int32_t k, int64_t V_total, int64_t ignore_index, float cap, float* logp,
+                     vls_rowstat* stats, void* stream);
+
+/* vls_logp_bwd for a shard: ids are global column indices (valid against
+ * V_total); the one-hot terms land in this shard's columns only, while G
+ * sums the upstream gradients of every valid id.  dlogits: [N, V_shard]
+ * contiguous.  stats: from vls_logp_combine. */
+int vls_logp_bwd_shard(const void* logits, int64_t ld, vls_dtype dt, int64_t N, int64_t V_shard,
+                       int64_t vocab_offset, int64_t V_total, const int64_t* ids, int32_t k,
+                       int64_t ignore_index, float cap, const float* g, const vls_rowstat* stats,
+                       void* dlogits, void* stream);
+
+int vls_entropy_partial(const void* logits, int64_t ld, vls_dtype dt, int64_t N, int64_t V_shard, float cap,
+                        vls_partial* part, void* stream);
+
+/* Folds parts [R, N] into H [N] and stats [N]. */
+int vls_entropy_combine(const vls_partial* parts, int32_t R, int64_t N, float* H, vls_rowstat* stats,
+                        void* stream);
+
+int vls_kl_partial(const void* a, int64_t lda, const void* b, int64_t ldb, vls_dtype dt, int64_t N,
+                   int64_t V_shard, vls_kl_dir dir, float cap, vls_partial* part, void* stream);
+
+/* Folds parts [R, N] into kl [N], stats_a [N], stats_b [N] (dir as in the partials). */
+int vls_kl_combine(const vls_partial* parts, int32_t R, int64_t N, vls_kl_dir dir, float* kl,
+                   vls_rowstat* stats_a, vls_rowstat* stats_b, void* stream);
 
 /* ------------------------------------------------------------------------ */
 /* Status                                                                    */

@@ -45,6 +45,13 @@ SIGNATURES = {
     "vls_entropy_bwd": [_p, _i64, _int, _i64, _i64, _f, _p, _p, _p, _p, _p],
     "vls_kl_fwd": [_p, _i64, _p, _i64, _int, _i64, _i64, _int, _f, _p, _p, _p, _p],
     "vls_kl_bwd": [_p, _i64, _p, _i64, _int, _i64, _i64, _int, _f, _p, _p, _p, _p, _p, _p],
+    "vls_logp_partial": [_p, _i64, _int, _i64, _i64, _i64, _i64, _p, _i32, _i64, _f, _p, _p, _p],
+    "vls_logp_combine": [_p, _p, _i32, _i64, _p, _i32, _i64, _i64, _f, _p, _p, _p],
+    "vls_logp_bwd_shard": [_p, _i64, _int, _i64, _i64, _i64, _i64, _p, _i32, _i64, _f, _p, _p, _p, _p],
+    "vls_entropy_partial": [_p, _i64, _int, _i64, _i64, _f, _p, _p],
+    "vls_entropy_combine": [_p, _i32, _i64, _p, _p, _p],
+    "vls_kl_partial": [_p, _i64, _p, _i64, _int, _i64, _i64, _int, _f, _p, _p],
+    "vls_kl_combine": [_p, _i32, _i64, _int, _p, _p, _p, _p],
     "vls_status_string": [_int],
     "vls_version": [],
 }

@@ -183,6 +183,137 @@ def vls_kl_bwd(a: torch.Tensor, b: torch.Tensor, g: torch.Tensor, kl: torch.Tens
     return da
 
 
+# ---------------------------------------------------------------------------
+# vocabulary-parallel split phase
+# ---------------------------------------------------------------------------
+
+PARTIAL_FIELDS = 6  # vls_partial: m, s, w, mq, sq, flag (4 bytes each)
+
+
+def _partials(shape, device, out=None) -> torch.Tensor:
+    """vls_partial arrays as float32 [..., 6] tensors (the flag word keeps its bits)."""
+    if out is not None:
+        return out
+    return torch.empty((*shape, PARTIAL_FIELDS), dtype=torch.float32, device=device)
+
+
+def _shard_rows(t: torch.Tensor) -> tuple[int, int, int]:
+    """Like _rows, but a shard may have 0 columns."""
+    if t.dim() != 2:
+        raise ValueError(f"expected a [N, V_shard] tensor, got shape {tuple(t.shape)}")
+    n, v = t.shape
+    if v == 0:
+        return n, 0, 0
+    return _rows(t)
+
+
+def _ptr_or_none(t: torch.Tensor):
+    return t.data_ptr() if t.numel() > 0 else None
+
+
+def vls_logp_partial(logits: torch.Tensor, ids: torch.Tensor, vocab_offset: int, vocab_total: int,
+                     ignore_index: int = -100, cap: float = 0.0, *, part=None, zt=None,
+                     stream=None) -> tuple[torch.Tensor, torch.Tensor]:
+    """Returns (part [N, 6], zt [N, k]) for the shard [vocab_offset, vocab_offset + V_shard)."""
+    lib = _lib.load()
+    n, v, ld = _shard_rows(logits)
+    ids = _ids2d(ids, n)
+    if ids.dtype != torch.int64 or not ids.is_contiguous():
+        raise ValueError("ids must be a contiguous int64 [N, k] tensor")
+    k = ids.shape[1]
+    part = _partials((n,), ids.device, part)
+    zt = torch.empty((n, k), dtype=torch.float32, device=ids.device) if zt is None else zt
+    st = lib.vls_logp_partial(_ptr_or_none(logits), ld, _dtype(logits), n, v, int(vocab_offset), int(vocab_total),
+                              _ptr(ids), k, int(ignore_index), float(cap), _ptr(part), _ptr(zt),
+                              _stream(ids, stream))
+    _lib.check("vls_logp_partial", st)
+    return part, zt
+
+
+def vls_logp_combine(parts: torch.Tensor, zt: torch.Tensor, ids: torch.Tensor, vocab_total: int,
+                     ignore_index: int = -100, cap: float = 0.0, *, logp=None, stats=None,
+                     stream=None) -> tuple[torch.Tensor, torch.Tensor]:
+    """parts [R, N, 6] and zt [R, N, k] in rank order -> (logp [N, k], stats [N, 2])."""
+    lib = _lib.load()
+    r, n = parts.shape[0], parts.shape[1]
+    ids = _ids2d(ids, n)
+    k = ids.shape[1]
+    if not (parts.is_contiguous() and zt.is_contiguous() and tuple(zt.shape) == (r, n, k)):
+        raise ValueError("parts must be contiguous [R, N, 6] and zt contiguous [R, N, k]")
+    logp = torch.empty((n, k), dtype=torch.float32, device=parts.device) if logp is None else logp
+    stats = _stats(n, parts.device, stats)
+    st = lib.vls_logp_combine(_ptr(parts), _ptr(zt), r, n, _ptr(ids), k, int(vocab_total), int(ignore_index),
+                              float(cap), _ptr(logp), _ptr(stats), _stream(parts, stream))
+    _lib.check("vls_logp_combine", st)
+    return logp, stats
+
+
+def vls_logp_bwd_shard(logits: torch.Tensor, ids: torch.Tensor, g: torch.Tensor, stats: torch.Tensor,
+                       vocab_offset: int, vocab_total: int, ignore_index: int = -100, cap: float = 0.0, *,
+                       dlogits=None, stream=None) -> torch.Tensor:
+    lib = _lib.load()
+    n, v, ld = _shard_rows(logits)
+    ids = _ids2d(ids, n)
+    k = ids.shape[1]
+    g = g.reshape(n, k)
+    if g.dtype != torch.float32 or not g.is_contiguous():
+        raise ValueError("g must be a contiguous float32 [N, k] tensor")
+    if dlogits is None:
+        dlogits = torch.empty((n, v), dtype=logits.dtype, device=ids.device)
+    st = lib.vls_logp_bwd_shard(_ptr_or_none(logits), ld, _dtype(logits), n, v, int(vocab_offset),
+                                int(vocab_total), _ptr(ids), k, int(ignore_index), float(cap), _ptr(g),
+                                _ptr(stats), _ptr_or_none(dlogits), _stream(ids, stream))
+    _lib.check("vls_logp_bwd_shard", st)
+    return dlogits
+
+
+def vls_entropy_partial(logits: torch.Tensor, cap: float = 0.0, *, part=None, stream=None) -> torch.Tensor:
+    lib = _lib.load()
+    n, v, ld = _shard_rows(logits)
+    part = _partials((n,), logits.device, part)
+    st = lib.vls_entropy_partial(_ptr_or_none(logits), ld, _dtype(logits), n, v, float(cap), _ptr(part),
+                                 _stream(part, stream))
+    _lib.check("vls_entropy_partial", st)
+    return part
+
+
+def vls_entropy_combine(parts: torch.Tensor, *, H=None, stats=None, stream=None) -> tuple[torch.Tensor, torch.Tensor]:
+    lib = _lib.load()
+    r, n = parts.shape[0], parts.shape[1]
+    H = torch.empty((n,), dtype=torch.float32, device=parts.device) if H is None else H
+    stats = _stats(n, parts.device, stats)
+    st = lib.vls_entropy_combine(_ptr(parts), r, n, _ptr(H), _ptr(stats), _stream(parts, stream))
+    _lib.check("vls_entropy_combine", st)
+    return H, stats
+
+
+def vls_kl_partial(a: torch.Tensor, b: torch.Tensor, direction: str = "reverse", cap: float = 0.0, *, part=None,
+                   stream=None) -> torch.Tensor:
+    lib = _lib.load()
+    n, v, lda = _shard_rows(a)
+    _, vb, ldb = _shard_rows(b)
+    if vb != v or a.dtype != b.dtype:
+        raise ValueError("a and b shards must have the same shape and dtype")
+    part = _partials((n,), a.device, part)
+    st = lib.vls_kl_partial(_ptr_or_none(a), lda, _ptr_or_none(b), ldb, _dtype(a), n, v, _DIR[direction],
+                            float(cap), _ptr(part), _stream(part, stream))
+    _lib.check("vls_kl_partial", st)
+    return part
+
+
+def vls_kl_combine(parts: torch.Tensor, direction: str = "reverse", *, kl=None, stats_a=None, stats_b=None,
+                   stream=None) -> tuple[torch.Tensor, torch.Tensor, torch.Tensor]:
+    lib = _lib.load()
+    r, n = parts.shape[0], parts.shape[1]
+    kl = torch.empty((n,), dtype=torch.float32, device=parts.device) if kl is None else kl
+    stats_a = _stats(n, parts.device, stats_a)
+    stats_b = _stats(n, parts.device, stats_b)
+    st = lib.vls_kl_combine(_ptr(parts), r, n, _DIR[direction], _ptr(kl), _ptr(stats_a), _ptr(stats_b),
+                            _stream(parts, stream))
+    _lib.check("vls_kl_combine", st)
+    return kl, stats_a, stats_b
+
+
 def vls_status_string(status: int) -> str:
     return _lib.load().vls_status_string(int(status)).decode()
 

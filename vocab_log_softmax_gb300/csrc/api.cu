@@ -147,6 +147,8 @@ FwdArgs fwd_args(int64_t N, int64_t V, float cap) {
   a.vocab = V;
   a.cap = cap;
   a.rcap = cap > 0.0f ? 1.0f / cap : 0.0f;
+  a.vocab_offset = 0;
+  a.vocab_total = V;
   fwd_geometry(V, &a.cluster, &a.vec_per_cta);
   return a;
 }
@@ -159,8 +161,17 @@ BwdArgs bwd_args(int64_t N, int64_t V, int32_t k, float cap) {
   a.cap = cap;
   a.rcap = cap > 0.0f ? 1.0f / cap : 0.0f;
   a.k = k;
+  a.vocab_offset = 0;
+  a.vocab_total = V;
   bwd_geometry(V, k, &a.chunks, &a.vec_per_cta);
   return a;
+}
+
+// A shard [offset, offset + V_shard) of a V_total-column vocabulary.
+int check_shard(int64_t N, int64_t V_shard, int64_t ld, int64_t offset, int64_t V_total) {
+  if (N < 0 || V_shard < 0 || ld < V_shard || V_total < 1 || offset < 0 || offset + V_shard > V_total)
+    return VLS_ERR_SHAPE;
+  return VLS_OK;
 }
 
 }  // namespace
@@ -365,6 +376,177 @@ int vls_kl_bwd(const void* pa, int64_t lda, const void* pb, int64_t ldb, vls_dty
   a.dx = da;
   return launch_status(
       launch_bwd_kl(dir == VLS_KL_REVERSE, dt, cap > 0.0f, a, static_cast<cudaStream_t>(stream)));
+}
+
+
+// ---------------------------------------------------------------------------
+// vocabulary-parallel split phase
+// ---------------------------------------------------------------------------
+
+int vls_logp_partial(const void* logits, int64_t ld, vls_dtype dt, int64_t N, int64_t V_shard,
+                     int64_t vocab_offset, int64_t V_total, const int64_t* ids, int32_t k,
+                     int64_t ignore_index, float cap, vls_partial* part, float* zt, void* stream) {
+  if (int e = check_shard(N, V_shard, ld, vocab_offset, V_total)) return e;
+  if (k < 1 || k > VLS_MAX_TOPK) return VLS_ERR_SHAPE;
+  if (!dtype_ok(dt)) return VLS_ERR_DTYPE;
+  if (int e = check_row_cap(cap)) return e;
+  if (N == 0) return VLS_OK;
+  if ((!logits && V_shard > 0) || !ids || !part || !zt) return VLS_ERR_NULL;
+  FwdArgs a = fwd_args(N, V_shard, cap);
+  if (N * a.cluster > kMaxGrid) return VLS_ERR_SHAPE;
+  int dev;
+  if (int e = resolve_device({V_shard > 0 ? logits : nullptr, ids, part, zt}, stream, &dev)) return e;
+  DeviceGuard guard;
+  if (int e = guard.enter(dev)) return e;
+  a.x = logits;
+  a.ldx = ld;
+  a.ids = ids;
+  a.k = k;
+  a.ignore_index = ignore_index;
+  a.vocab_offset = vocab_offset;
+  a.vocab_total = V_total;
+  a.part = part;
+  a.zt = zt;
+  return launch_status(launch_fwd_logp(dt, cap > 0.0f, a, static_cast<cudaStream_t>(stream)));
+}
+
+int vls_logp_combine(const vls_partial* parts, const float* zt, int32_t R, int64_t N, const int64_t* ids,
+                     int32_t k, int64_t V_total, int64_t ignore_index, float cap, float* logp,
+                     vls_rowstat* stats, void* stream) {
+  if (N < 0 || R < 1 || V_total < 1 || k < 1 || k > VLS_MAX_TOPK) return VLS_ERR_SHAPE;
+  if (int e = check_row_cap(cap)) return e;
+  if (N == 0) return VLS_OK;
+  if (!parts || !zt || !ids || !logp || !stats) return VLS_ERR_NULL;
+  int dev;
+  if (int e = resolve_device({parts, zt, ids, logp, stats}, stream, &dev)) return e;
+  DeviceGuard guard;
+  if (int e = guard.enter(dev)) return e;
+  CombineArgs a;
+  std::memset(&a, 0, sizeof(a));
+  a.parts = parts;
+  a.zt = zt;
+  a.R = R;
+  a.rows = N;
+  a.ids = ids;
+  a.k = k;
+  a.vocab_total = V_total;
+  a.ignore_index = ignore_index;
+  a.cap = cap;
+  a.logp = logp;
+  a.stats_x = stats;
+  return launch_status(launch_combine(kFwdLogp, a, static_cast<cudaStream_t>(stream)));
+}
+
+int vls_logp_bwd_shard(const void* logits, int64_t ld, vls_dtype dt, int64_t N, int64_t V_shard,
+                       int64_t vocab_offset, int64_t V_total, const int64_t* ids, int32_t k,
+                       int64_t ignore_index, float cap, const float* g, const vls_rowstat* stats,
+                       void* dlogits, void* stream) {
+  if (int e = check_shard(N, V_shard, ld, vocab_offset, V_total)) return e;
+  if (k < 1 || k > VLS_MAX_TOPK) return VLS_ERR_SHAPE;
+  if (!dtype_ok(dt)) return VLS_ERR_DTYPE;
+  if (int e = check_row_cap(cap)) return e;
+  if (N == 0 || V_shard == 0) return VLS_OK;
+  if (!logits || !ids || !g || !stats || !dlogits) return VLS_ERR_NULL;
+  BwdArgs a = bwd_args(N, V_shard, k, cap);
+  if (N * a.chunks > kMaxGrid) return VLS_ERR_SHAPE;
+  int dev;
+  if (int e = resolve_device({logits, ids, g, stats, dlogits}, stream, &dev)) return e;
+  DeviceGuard guard;
+  if (int e = guard.enter(dev)) return e;
+  a.x = logits;
+  a.ldx = ld;
+  a.ids = ids;
+  a.ignore_index = ignore_index;
+  a.g = g;
+  a.stats_x = stats;
+  a.dx = dlogits;
+  a.vocab_offset = vocab_offset;
+  a.vocab_total = V_total;
+  return launch_status(launch_bwd_logp(dt, cap > 0.0f, a, static_cast<cudaStream_t>(stream)));
+}
+
+int vls_entropy_partial(const void* logits, int64_t ld, vls_dtype dt, int64_t N, int64_t V_shard, float cap,
+                        vls_partial* part, void* stream) {
+  if (N < 0 || V_shard < 0 || ld < V_shard) return VLS_ERR_SHAPE;
+  if (!dtype_ok(dt)) return VLS_ERR_DTYPE;
+  if (int e = check_row_cap(cap)) return e;
+  if (N == 0) return VLS_OK;
+  if ((!logits && V_shard > 0) || !part) return VLS_ERR_NULL;
+  FwdArgs a = fwd_args(N, V_shard, cap);
+  if (N * a.cluster > kMaxGrid) return VLS_ERR_SHAPE;
+  int dev;
+  if (int e = resolve_device({V_shard > 0 ? logits : nullptr, part}, stream, &dev)) return e;
+  DeviceGuard guard;
+  if (int e = guard.enter(dev)) return e;
+  a.x = logits;
+  a.ldx = ld;
+  a.part = part;
+  return launch_status(launch_fwd_entropy(dt, cap > 0.0f, a, static_cast<cudaStream_t>(stream)));
+}
+
+int vls_entropy_combine(const vls_partial* parts, int32_t R, int64_t N, float* H, vls_rowstat* stats,
+                        void* stream) {
+  if (N < 0 || R < 1) return VLS_ERR_SHAPE;
+  if (N == 0) return VLS_OK;
+  if (!parts || !H || !stats) return VLS_ERR_NULL;
+  int dev;
+  if (int e = resolve_device({parts, H, stats}, stream, &dev)) return e;
+  DeviceGuard guard;
+  if (int e = guard.enter(dev)) return e;
+  CombineArgs a;
+  std::memset(&a, 0, sizeof(a));
+  a.parts = parts;
+  a.R = R;
+  a.rows = N;
+  a.out = H;
+  a.stats_x = stats;
+  return launch_status(launch_combine(kFwdEntropy, a, static_cast<cudaStream_t>(stream)));
+}
+
+int vls_kl_partial(const void* pa, int64_t lda, const void* pb, int64_t ldb, vls_dtype dt, int64_t N,
+                   int64_t V_shard, vls_kl_dir dir, float cap, vls_partial* part, void* stream) {
+  if (N < 0 || V_shard < 0 || lda < V_shard || ldb < V_shard) return VLS_ERR_SHAPE;
+  if (!dtype_ok(dt)) return VLS_ERR_DTYPE;
+  if (dir != VLS_KL_REVERSE && dir != VLS_KL_FORWARD) return VLS_ERR_ARG;
+  if (int e = check_row_cap(cap)) return e;
+  if (N == 0) return VLS_OK;
+  if (((!pa || !pb) && V_shard > 0) || !part) return VLS_ERR_NULL;
+  FwdArgs a = fwd_args(N, V_shard, cap);
+  if (N * a.cluster > kMaxGrid) return VLS_ERR_SHAPE;
+  int dev;
+  if (int e = resolve_device({V_shard > 0 ? pa : nullptr, V_shard > 0 ? pb : nullptr, part}, stream, &dev))
+    return e;
+  DeviceGuard guard;
+  if (int e = guard.enter(dev)) return e;
+  const bool rev = dir == VLS_KL_REVERSE;
+  a.x = rev ? pa : pb;
+  a.ldx = rev ? lda : ldb;
+  a.y = rev ? pb : pa;
+  a.ldy = rev ? ldb : lda;
+  a.part = part;
+  return launch_status(launch_fwd_kl(dt, cap > 0.0f, a, static_cast<cudaStream_t>(stream)));
+}
+
+int vls_kl_combine(const vls_partial* parts, int32_t R, int64_t N, vls_kl_dir dir, float* kl,
+                   vls_rowstat* stats_a, vls_rowstat* stats_b, void* stream) {
+  if (N < 0 || R < 1) return VLS_ERR_SHAPE;
+  if (dir != VLS_KL_REVERSE && dir != VLS_KL_FORWARD) return VLS_ERR_ARG;
+  if (N == 0) return VLS_OK;
+  if (!parts || !kl || !stats_a || !stats_b) return VLS_ERR_NULL;
+  int dev;
+  if (int e = resolve_device({parts, kl, stats_a, stats_b}, stream, &dev)) return e;
+  DeviceGuard guard;
+  if (int e = guard.enter(dev)) return e;
+  CombineArgs a;
+  std::memset(&a, 0, sizeof(a));
+  a.parts = parts;
+  a.R = R;
+  a.rows = N;
+  a.out = kl;
+  const bool rev = dir == VLS_KL_REVERSE;
+  a.stats_x = rev ? stats_a : stats_b;
+  a.stats_y = rev ? stats_b : stats_a;
+  return launch_status(launch_combine(kFwdKl, a, static_cast<cudaStream_t>(stream)));
 }
 
 }  // extern "C"

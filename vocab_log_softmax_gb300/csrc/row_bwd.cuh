@@ -16,6 +16,10 @@ namespace vls {
 
 using namespace dev;
 
+// Ids are global vocabulary columns, valid against vocab_total; the CTA
+// holds local columns [col_beg, col_end) of a shard that starts at global
+// column vocab_offset (0 and V for an unsharded row).
+//
 // Per-CTA prepared form of a row's top-k ids (DeepSpeed PR #8838, Changes:
 // the top-k one-hot terms are added in fp32 before the single cast):
 //  - G, the sum of the upstream gradients of the valid ids, by a fixed tree
@@ -50,7 +54,6 @@ __device__ __forceinline__ TopkPrep prep_topk(const BwdArgs& a, int64_t row, int
                                               float* s_warp, int* s_nfix) {
   const int k = a.k;
   const int P = topk_pow2(k);
-  const int64_t V = a.vocab;
   const int64_t* ids = a.ids + row * k;
   const float* g = a.g + row * k;
   unsigned long long* key = reinterpret_cast<unsigned long long*>(smem);
@@ -68,7 +71,7 @@ __device__ __forceinline__ TopkPrep prep_topk(const BwdArgs& a, int64_t row, int
       const int64_t id = ids[j];
       const float gj = g[j];
       s_g[j] = gj;
-      if (valid_id(id, V, a.ignore_index)) {
+      if (valid_id(id, a.vocab_total, a.ignore_index)) {
         kj = (static_cast<unsigned long long>(id) << kTopkJBits) | static_cast<unsigned long long>(j);
         gpart += gj;
         any = 1;
@@ -106,14 +109,14 @@ __device__ __forceinline__ TopkPrep prep_topk(const BwdArgs& a, int64_t row, int
   for (int s = threadIdx.x; s < k; s += kRowThreads) {
     const unsigned long long ks = key[s];
     if (ks == kNone) continue;
-    const int64_t id = static_cast<int64_t>(ks >> kTopkJBits);
+    const int64_t local = static_cast<int64_t>(ks >> kTopkJBits) - a.vocab_offset;
     if (s > 0 && (key[s - 1] >> kTopkJBits) == (ks >> kTopkJBits)) continue;
-    if (id < col_beg || id >= col_end) continue;
+    if (local < col_beg || local >= col_end) continue;
     float gs = 0.0f;
     for (int t = s; t < k && (key[t] >> kTopkJBits) == (ks >> kTopkJBits); ++t)
       gs += s_g[key[t] & ((1ull << kTopkJBits) - 1)];
     const int slot = atomicAdd(s_nfix, 1);
-    fix_id[slot] = id;
+    fix_id[slot] = local;
     fix_g[slot] = gs;
   }
   __syncthreads();
@@ -215,12 +218,13 @@ __global__ void __launch_bounds__(kRowThreads, CAP ? kCapMinBlocks : 6) row_bwd_
       fix_id = &fix1_id;
       fix_g = &fix1_g;
       const int64_t id = a.ids[row];
-      if (valid_id(id, V, a.ignore_index)) {
+      if (valid_id(id, a.vocab_total, a.ignore_index)) {
         G = a.g[row];
-        if (id >= col_beg && id < col_end) {
+        const int64_t local = id - a.vocab_offset;
+        if (local >= col_beg && local < col_end) {
           nfix = 1;
           if (threadIdx.x == 0) {
-            fix1_id = id;
+            fix1_id = local;
             fix1_g = G;
           }
         }

@@ -178,6 +178,36 @@ struct FwdAccOf<kFwdKl, T, CAP> { using type = KlAcc<T, CAP>; };
 template <int OP>
 constexpr int fwd_unroll() { return OP == kFwdKl ? 2 : 4; }
 
+// ---- finalisation, shared with the vocabulary-parallel combine ----
+
+// log p of a target from its raw logit x and the row's (m, log S); NaN for
+// a row without a distribution.
+template <bool CAP>
+__device__ __forceinline__ float logp_of(float x, float m, float log_s, const CapK& K) {
+  const float d = CAP ? cap_d(cap_t(x, K), K.c, m) : x - m;
+  return m == neg_inf() ? qnan() : d - log_s;
+}
+// H = log S - W/S
+__device__ __forceinline__ float entropy_of(const EntropyState& f, float log_s) {
+  return f.m == neg_inf() ? qnan() : log_s - f.w / f.s;
+}
+// KL = W/S_p - log S_p + log S_q; +inf on a support mismatch; NaN when a row
+// of either tensor has no distribution
+__device__ __forceinline__ float kl_of(const KlState& f, float log_sp, float log_sq) {
+  if (f.mp == neg_inf() || f.mq == neg_inf()) return qnan();
+  if (f.flag) return pos_inf();
+  return f.w / f.sp + (log_sq - log_sp);
+}
+
+__device__ __forceinline__ vls_partial to_partial(const LogpState& s) { return {s.m, s.s, 0.0f, 0.0f, 0.0f, 0u}; }
+__device__ __forceinline__ vls_partial to_partial(const EntropyState& s) { return {s.m, s.s, s.w, 0.0f, 0.0f, 0u}; }
+__device__ __forceinline__ vls_partial to_partial(const KlState& s) { return {s.mp, s.sp, s.w, s.mq, s.sq, s.flag}; }
+__device__ __forceinline__ void from_partial(const vls_partial& p, LogpState& s) { s = {p.m, p.s}; }
+__device__ __forceinline__ void from_partial(const vls_partial& p, EntropyState& s) { s = {p.m, p.s, p.w}; }
+__device__ __forceinline__ void from_partial(const vls_partial& p, KlState& s) {
+  s = {p.m, p.s, p.mq, p.sq, p.w, p.flag};
+}
+
 template <class T, int OP, bool CAP>
 __global__ void __launch_bounds__(kFwdThreads) row_fwd_kernel(const FwdArgs a) {
   using Acc = typename FwdAccOf<OP, T, CAP>::type;
@@ -258,39 +288,40 @@ __global__ void __launch_bounds__(kFwdThreads) row_fwd_kernel(const FwdArgs a) {
 
   // ---- finalise (rank 0 of the row) ----
   const S fin = row_state;
+  if (a.part != nullptr) {
+    // vocabulary-parallel partial: the state itself, and for logp the raw
+    // logits of the target ids this shard owns (0 for the others)
+    if (threadIdx.x == 0) a.part[row] = to_partial(fin);
+    if constexpr (OP == kFwdLogp) {
+      for (int j = threadIdx.x; j < a.k; j += kFwdThreads) {
+        const int64_t id = a.ids[row * a.k + j];
+        const int64_t local = id - a.vocab_offset;
+        const bool own = valid_id(id, a.vocab_total, a.ignore_index) && local >= 0 && local < V;
+        a.zt[row * a.k + j] = own ? load1(xr + local) : 0.0f;
+      }
+    }
+    return;
+  }
   if constexpr (OP == kFwdLogp) {
     const float m = fin.m;
     const float log_s = logf(fin.s);
     if (threadIdx.x == 0) a.stats_x[row] = vls_rowstat{m, log_s};
     for (int j = threadIdx.x; j < a.k; j += kFwdThreads) {
       const int64_t id = a.ids[row * a.k + j];
-      float out = 0.0f;
-      if (valid_id(id, V, a.ignore_index)) {
-        const float x = load1(xr + id);
-        const float d = CAP ? cap_d(cap_t(x, K), K.c, m) : x - m;
-        out = m == neg_inf() ? qnan() : d - log_s;
-      }
-      a.logp[row * a.k + j] = out;
+      a.logp[row * a.k + j] = valid_id(id, V, a.ignore_index) ? logp_of<CAP>(load1(xr + id), m, log_s, K) : 0.0f;
     }
   } else if constexpr (OP == kFwdEntropy) {
     if (threadIdx.x == 0) {
       const float log_s = logf(fin.s);
       a.stats_x[row] = vls_rowstat{fin.m, log_s};
-      a.out[row] = fin.m == neg_inf() ? qnan() : log_s - fin.w / fin.s;
+      a.out[row] = entropy_of(fin, log_s);
     }
   } else {
     if (threadIdx.x == 0) {
       const float log_sp = logf(fin.sp), log_sq = logf(fin.sq);
       a.stats_x[row] = vls_rowstat{fin.mp, log_sp};
       a.stats_y[row] = vls_rowstat{fin.mq, log_sq};
-      float kl;
-      if (fin.mp == neg_inf() || fin.mq == neg_inf())
-        kl = qnan();
-      else if (fin.flag)
-        kl = pos_inf();
-      else
-        kl = fin.w / fin.sp + (log_sq - log_sp);
-      a.out[row] = kl;
+      a.out[row] = kl_of(fin, log_sp, log_sq);
     }
   }
 }

@@ -66,6 +66,14 @@ struct FwdArgs {
   // launch geometry: CTAs per row (= cluster size) and 8-column vectors per CTA
   int cluster;
   int64_t vec_per_cta;
+  // vocabulary-parallel partial mode (part != nullptr): the rows hold the
+  // columns [vocab_offset, vocab_offset + vocab) of a vocab_total-column
+  // vocabulary; the kernel writes its per-row state to part and (logp) the
+  // raw logits of the owned target ids to zt instead of finalising
+  int64_t vocab_offset;
+  int64_t vocab_total;
+  vls_partial* part;
+  float* zt;
 };
 
 struct BwdArgs {
@@ -87,6 +95,26 @@ struct BwdArgs {
   void* dx;            // [N, V] contiguous gradient, dtype of x
   int chunks;          // CTAs per row
   int64_t vec_per_cta;
+  // logp over a vocabulary shard: ids are global columns, valid against
+  // vocab_total; this shard holds [vocab_offset, vocab_offset + vocab)
+  int64_t vocab_offset;
+  int64_t vocab_total;
+};
+
+struct CombineArgs {
+  const vls_partial* parts;  // [R, N]
+  const float* zt;           // logp: [R, N, k]
+  int32_t R;
+  int64_t rows;
+  const int64_t* ids;
+  int32_t k;
+  int64_t vocab_total;
+  int64_t ignore_index;
+  float cap;
+  float* logp;
+  float* out;                // H or KL
+  vls_rowstat* stats_x;
+  vls_rowstat* stats_y;      // KL: stats of the second argument
 };
 
 struct CapArgs {
@@ -108,6 +136,7 @@ cudaError_t launch_fwd_kl(vls_dtype dt, bool cap, const FwdArgs& a, cudaStream_t
 cudaError_t launch_bwd_logp(vls_dtype dt, bool cap, const BwdArgs& a, cudaStream_t s);
 cudaError_t launch_bwd_entropy(vls_dtype dt, bool cap, const BwdArgs& a, cudaStream_t s);
 cudaError_t launch_bwd_kl(bool reverse, vls_dtype dt, bool cap, const BwdArgs& a, cudaStream_t s);
+cudaError_t launch_combine(FwdOp op, const CombineArgs& a, cudaStream_t s);
 cudaError_t launch_softcap_fwd(vls_dtype dt, const CapArgs& a, cudaStream_t s);
 cudaError_t launch_softcap_bwd(vls_dtype dt, const CapArgs& a, cudaStream_t s);
 
