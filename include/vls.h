@@ -161,6 +161,33 @@ int vls_kl_bwd(const void* a, int64_t lda, const void* b, int64_t ldb, vls_dtype
                void* da, void* stream);
 
 /* ------------------------------------------------------------------------ */
+/* Fused statistics: target logprobs, entropy and KL of the same policy      */
+/* logits from one read of the policy (and one of the reference), and one    */
+/* backward pass for any weighted sum of them.  The quantities are the ones  */
+/* above; RL and distillation losses take them together (DeepSpeed PR #8838, */
+/* Changes: logprobs, entropy and KL over the same shard).                   */
+/* ------------------------------------------------------------------------ */
+
+/* Forward.  a: policy logits; b: reference logits (NULL when kl is NULL).
+ * logp [N, k] (NULL to skip; needs ids), H [N] (NULL to skip), kl [N] in
+ * direction dir (NULL to skip).  stats_a [N] always; stats_b [N] with kl.
+ * Each output equals the corresponding single call's. */
+int vls_fused_fwd(const void* a, int64_t lda, const void* b, int64_t ldb, vls_dtype dt, int64_t N, int64_t V,
+                  const int64_t* ids, int32_t k, int64_t ignore_index, vls_kl_dir dir, float cap,
+                  float* logp, float* H, float* kl, vls_rowstat* stats_a, vls_rowstat* stats_b,
+                  void* stream);
+
+/* Backward: da = d/da of sum_r [ sum_j g_logp[r,j] logp[r,j] + g_H[r] H[r]
+ * + g_kl[r] KL[r] ], the sum of the single calls' gradients computed in fp32
+ * and cast once.  A term is left out when its upstream pointer is NULL
+ * (g_logp needs ids; g_H needs H; g_kl needs b, kl and stats_b).  da: [N, V]
+ * contiguous, dtype dt. */
+int vls_fused_bwd(const void* a, int64_t lda, const void* b, int64_t ldb, vls_dtype dt, int64_t N, int64_t V,
+                  const int64_t* ids, int32_t k, int64_t ignore_index, vls_kl_dir dir, float cap,
+                  const float* g_logp, const float* g_H, const float* g_kl, const float* H, const float* kl,
+                  const vls_rowstat* stats_a, const vls_rowstat* stats_b, void* da, void* stream);
+
+/* ------------------------------------------------------------------------ */
 /* Vocabulary-parallel statistics, split phase (DeepSpeed PR #8838, Changes: */
 /* local max and sum-exp from one read, rescaled to the global max, so that  */
 /* tensor parallelism needs one MAX and one SUM all-reduce; review           */

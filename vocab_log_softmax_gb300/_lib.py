@@ -45,6 +45,9 @@ SIGNATURES = {
     "vls_entropy_bwd": [_p, _i64, _int, _i64, _i64, _f, _p, _p, _p, _p, _p],
     "vls_kl_fwd": [_p, _i64, _p, _i64, _int, _i64, _i64, _int, _f, _p, _p, _p, _p],
     "vls_kl_bwd": [_p, _i64, _p, _i64, _int, _i64, _i64, _int, _f, _p, _p, _p, _p, _p, _p],
+    "vls_fused_fwd": [_p, _i64, _p, _i64, _int, _i64, _i64, _p, _i32, _i64, _int, _f, _p, _p, _p, _p, _p, _p],
+    "vls_fused_bwd": [_p, _i64, _p, _i64, _int, _i64, _i64, _p, _i32, _i64, _int, _f, _p, _p, _p, _p, _p, _p, _p,
+                      _p, _p],
     "vls_logp_partial": [_p, _i64, _int, _i64, _i64, _i64, _i64, _p, _i32, _i64, _f, _p, _p, _p],
     "vls_logp_combine": [_p, _p, _i32, _i64, _p, _i32, _i64, _i64, _f, _p, _p, _p],
     "vls_logp_bwd_shard": [_p, _i64, _int, _i64, _i64, _i64, _i64, _p, _i32, _i64, _f, _p, _p, _p, _p],

@@ -184,6 +184,75 @@ def vls_kl_bwd(a: torch.Tensor, b: torch.Tensor, g: torch.Tensor, kl: torch.Tens
 
 
 # ---------------------------------------------------------------------------
+# fused statistics
+# ---------------------------------------------------------------------------
+
+def vls_fused_fwd(a: torch.Tensor, b: torch.Tensor | None = None, ids: torch.Tensor | None = None, *,
+                  logp: bool = True, entropy: bool = True, kl: bool | None = None, direction: str = "reverse",
+                  ignore_index: int = -100, cap: float = 0.0, stream=None) -> dict:
+    """One read of the policy a (and of the reference b for KL).  Returns a
+    dict with 'logp' [N, k] (when ids are given and logp), 'H' [N] (entropy),
+    'kl' [N] (when b is given), 'stats_a' and 'stats_b' [N, 2]."""
+    lib = _lib.load()
+    n, v, lda = _rows(a)
+    want_kl = (b is not None) if kl is None else bool(kl)
+    ldb = 0
+    if want_kl:
+        nb, vb, ldb = _rows(b)
+        if (nb, vb) != (n, v) or b.dtype != a.dtype:
+            raise ValueError("a and b must have the same shape and dtype")
+    f32 = dict(dtype=torch.float32, device=a.device)
+    out = {"stats_a": torch.empty((n, 2), **f32)}
+    k = 0
+    if logp and ids is not None:
+        ids = _ids2d(ids, n)
+        if ids.dtype != torch.int64 or not ids.is_contiguous():
+            raise ValueError("ids must be a contiguous int64 [N, k] tensor")
+        k = ids.shape[1]
+        out["logp"] = torch.empty((n, k), **f32)
+    if entropy:
+        out["H"] = torch.empty((n,), **f32)
+    if want_kl:
+        out["kl"] = torch.empty((n,), **f32)
+        out["stats_b"] = torch.empty((n, 2), **f32)
+    st = lib.vls_fused_fwd(_ptr(a), lda, _ptr(b) if want_kl else None, ldb, _dtype(a), n, v,
+                           _ptr(ids) if k else None, k, int(ignore_index), _DIR[direction], float(cap),
+                           _ptr(out.get("logp")), _ptr(out.get("H")), _ptr(out.get("kl")), _ptr(out["stats_a"]),
+                           _ptr(out.get("stats_b")), _stream(a, stream))
+    _lib.check("vls_fused_fwd", st)
+    return out
+
+
+def vls_fused_bwd(a: torch.Tensor, fwd: dict, b: torch.Tensor | None = None, ids: torch.Tensor | None = None, *,
+                  g_logp: torch.Tensor | None = None, g_H: torch.Tensor | None = None,
+                  g_kl: torch.Tensor | None = None, direction: str = "reverse", ignore_index: int = -100,
+                  cap: float = 0.0, da=None, stream=None) -> torch.Tensor:
+    """Gradient w.r.t. a of sum(g_logp * logp) + sum(g_H * H) + sum(g_kl * KL);
+    `fwd` is vls_fused_fwd's result; absent gradients leave their term out."""
+    lib = _lib.load()
+    n, v, lda = _rows(a)
+    ldb = _rows(b)[2] if g_kl is not None else 0
+    k = 1
+    if g_logp is not None:
+        ids = _ids2d(ids, n)
+        k = ids.shape[1]
+        g_logp = g_logp.reshape(n, k)
+    for t in (g_logp, g_H, g_kl):
+        if t is not None and (t.dtype != torch.float32 or not t.is_contiguous()):
+            raise ValueError("upstream gradients must be contiguous float32")
+    if da is None:
+        da = torch.empty((n, v), dtype=a.dtype, device=a.device)
+    st = lib.vls_fused_bwd(_ptr(a), lda, _ptr(b) if g_kl is not None else None, ldb, _dtype(a), n, v,
+                           _ptr(ids) if g_logp is not None else None, k, int(ignore_index), _DIR[direction],
+                           float(cap), _ptr(g_logp), _ptr(g_H), _ptr(g_kl),
+                           _ptr(fwd.get("H")) if g_H is not None else None,
+                           _ptr(fwd.get("kl")) if g_kl is not None else None, _ptr(fwd["stats_a"]),
+                           _ptr(fwd.get("stats_b")) if g_kl is not None else None, _ptr(da), _stream(a, stream))
+    _lib.check("vls_fused_bwd", st)
+    return da
+
+
+# ---------------------------------------------------------------------------
 # vocabulary-parallel split phase
 # ---------------------------------------------------------------------------
 

@@ -380,6 +380,90 @@ int vls_kl_bwd(const void* pa, int64_t lda, const void* pb, int64_t ldb, vls_dty
 
 
 // ---------------------------------------------------------------------------
+// fused statistics
+// ---------------------------------------------------------------------------
+
+int vls_fused_fwd(const void* pa, int64_t lda, const void* pb, int64_t ldb, vls_dtype dt, int64_t N, int64_t V,
+                  const int64_t* ids, int32_t k, int64_t ignore_index, vls_kl_dir dir, float cap, float* logp,
+                  float* H, float* kl, vls_rowstat* stats_a, vls_rowstat* stats_b, void* stream) {
+  if (int e = check_rows(N, V, lda)) return e;
+  const bool want_kl = kl != nullptr;
+  if (want_kl && ldb < V) return VLS_ERR_SHAPE;
+  if (logp && (k < 1 || k > VLS_MAX_TOPK)) return VLS_ERR_SHAPE;
+  if (!dtype_ok(dt)) return VLS_ERR_DTYPE;
+  if (want_kl && dir != VLS_KL_REVERSE && dir != VLS_KL_FORWARD) return VLS_ERR_ARG;
+  if (int e = check_row_cap(cap)) return e;
+  if (N == 0) return VLS_OK;
+  if (!pa || !stats_a || (logp && !ids) || (want_kl && (!pb || !stats_b))) return VLS_ERR_NULL;
+  FwdArgs a = fwd_args(N, V, cap);
+  if (N * a.cluster > kMaxGrid) return VLS_ERR_SHAPE;
+  int dev;
+  if (int e = resolve_device({pa, want_kl ? pb : nullptr, logp ? ids : nullptr, logp, H, kl, stats_a,
+                              want_kl ? stats_b : nullptr},
+                             stream, &dev))
+    return e;
+  DeviceGuard guard;
+  if (int e = guard.enter(dev)) return e;
+  a.x = pa;
+  a.ldx = lda;
+  a.y = want_kl ? pb : nullptr;
+  a.ldy = want_kl ? ldb : 0;
+  a.ids = ids;
+  a.k = logp ? k : 0;
+  a.ignore_index = ignore_index;
+  a.logp = logp;
+  a.h = H;
+  a.kl = kl;
+  a.stats_x = stats_a;
+  a.stats_y = stats_b;
+  const FusedKl fk = !want_kl ? kFusedNoKl : (dir == VLS_KL_REVERSE ? kFusedKlReverse : kFusedKlForward);
+  return launch_status(launch_fwd_fused(fk, dt, cap > 0.0f, a, static_cast<cudaStream_t>(stream)));
+}
+
+int vls_fused_bwd(const void* pa, int64_t lda, const void* pb, int64_t ldb, vls_dtype dt, int64_t N, int64_t V,
+                  const int64_t* ids, int32_t k, int64_t ignore_index, vls_kl_dir dir, float cap,
+                  const float* g_logp, const float* g_H, const float* g_kl, const float* H, const float* kl,
+                  const vls_rowstat* stats_a, const vls_rowstat* stats_b, void* da, void* stream) {
+  if (int e = check_rows(N, V, lda)) return e;
+  const bool want_kl = g_kl != nullptr;
+  if (want_kl && ldb < V) return VLS_ERR_SHAPE;
+  if (g_logp && (k < 1 || k > VLS_MAX_TOPK)) return VLS_ERR_SHAPE;
+  if (!dtype_ok(dt)) return VLS_ERR_DTYPE;
+  if (!g_logp && !g_H && !g_kl) return VLS_ERR_ARG;
+  if (want_kl && dir != VLS_KL_REVERSE && dir != VLS_KL_FORWARD) return VLS_ERR_ARG;
+  if (int e = check_row_cap(cap)) return e;
+  if (N == 0) return VLS_OK;
+  if (!pa || !stats_a || !da || (g_logp && !ids) || (g_H && !H) || (want_kl && (!pb || !kl || !stats_b)))
+    return VLS_ERR_NULL;
+  BwdArgs a = bwd_args(N, V, g_logp ? k : 1, cap);
+  if (N * a.chunks > kMaxGrid) return VLS_ERR_SHAPE;
+  int dev;
+  if (int e = resolve_device({pa, want_kl ? pb : nullptr, g_logp ? ids : nullptr, g_logp, g_H, g_kl, H, kl,
+                              stats_a, want_kl ? stats_b : nullptr, da},
+                             stream, &dev))
+    return e;
+  DeviceGuard guard;
+  if (int e = guard.enter(dev)) return e;
+  a.x = pa;
+  a.ldx = lda;
+  a.y = want_kl ? pb : nullptr;
+  a.ldy = want_kl ? ldb : 0;
+  a.ids = ids;
+  a.k = g_logp ? k : 1;
+  a.ignore_index = ignore_index;
+  a.g = g_logp;
+  a.g_h = g_H;
+  a.g_kl = g_kl;
+  a.h = H;
+  a.kl = kl;
+  a.stats_x = stats_a;
+  a.stats_y = stats_b;
+  a.dx = da;
+  const FusedKl fk = !want_kl ? kFusedNoKl : (dir == VLS_KL_REVERSE ? kFusedKlReverse : kFusedKlForward);
+  return launch_status(launch_bwd_fused(fk, dt, cap > 0.0f, a, static_cast<cudaStream_t>(stream)));
+}
+
+// ---------------------------------------------------------------------------
 // vocabulary-parallel split phase
 // ---------------------------------------------------------------------------
 

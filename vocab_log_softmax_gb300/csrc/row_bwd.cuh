@@ -131,11 +131,16 @@ struct BwdRow {
   fp2 k2;       // entropy: log S - H;  reverse KL: log S_a - log S_b + KL
   fp2 nmq2;     // KL: -m_b
   fp2 nlsq2;    // KL: -log S_b * log2 e
+  // fused: gradient = p_a c0 + (p_a d_a) c1 + (p_a d_b) c2 + ngk p_b
+  fp2 c1, c2, ngk;
 };
+
+template <int OP, int DIR>
+constexpr bool bwd_reads_two() { return OP == kBwdKlReverse || OP == kBwdKlForward || (OP == kBwdFused && DIR != kFusedNoKl); }
 
 // Gradient of pair i of a vector: x holds the logits (the policy for KL), y
 // the reference (KL only).
-template <class T, int OP, bool CAP>
+template <class T, int OP, bool CAP, int DIR = kFusedNoKl>
 __device__ __forceinline__ fp2 grad_pair(const Raw8<T>& x, const Raw8<T>& y, int i, const BwdRow& R,
                                          const CapK& K) {
   fp2 d, e2 = 0, r2 = 0;
@@ -150,6 +155,23 @@ __device__ __forceinline__ fp2 grad_pair(const Raw8<T>& x, const Raw8<T>& y, int
     r = mul2(p, R.coef2);
   } else if constexpr (OP == kBwdEntropy) {
     r = mul2(mul2(p, R.coef2), sub2(d, R.k2));
+  } else if constexpr (OP == kBwdFused) {
+    // p c0 + (p d_a) c1 + (p d_b) c2 (+ ngk p_b); coef2 holds c0.  p is
+    // multiplied in first, so masked columns (p = 0, d = -3.4e38) give 0.
+    r = fma2(mul2(p, d), R.c1, mul2(p, R.coef2));
+    if constexpr (DIR != kFusedNoKl) {
+      fp2 db;
+      if (CAP) {
+        fp2 eq, rq;
+        db = fma2(cap_t2(y, i, K, eq, rq), splat(K.c), R.nmq2);
+      } else {
+        db = add2(y.pair_clamped(i), R.nmq2);
+      }
+      if constexpr (DIR == kFusedKlReverse)
+        r = fma2(mul2(p, db), R.c2, r);
+      else
+        r = fma2(ex2_2(fma2(db, splat(kLog2e), R.nlsq2)), R.ngk, r);
+    }
   } else {
     fp2 dq;
     if (CAP) {
@@ -172,13 +194,39 @@ __device__ __forceinline__ fp2 grad_pair(const Raw8<T>& x, const Raw8<T>& y, int
   return r;
 }
 
+// Scalar form of the fused gradient at one column (the one-hot fix-up).
+template <class T, bool CAP, int DIR>
+__device__ __forceinline__ float fused_at(const T* xr, const T* yr, int64_t c, const vls_rowstat& sx, float mq,
+                                          float log_sq, float c0, float c1, float c2, float ngk, float gsum,
+                                          const CapK& K, float& chain) {
+  const float x = load1(xr + c);
+  float d;
+  chain = 1.0f;
+  if (CAP) {
+    float e, r;
+    d = cap_d(cap_t(x, K, e, r), K.c, sx.m);
+    chain = 4.0f * e * r * r;
+  } else {
+    d = fmaxf(x, kLowest) - sx.m;
+  }
+  const float p = ex2(fmaf(d, kLog2e, -sx.log_s * kLog2e));
+  float r = fmaf(p * d, c1, fmaf(p, c0, gsum));
+  if constexpr (DIR != kFusedNoKl) {
+    const float y = load1(yr + c);
+    const float db = CAP ? cap_d(cap_t(y, K), K.c, mq) : fmaxf(y, kLowest) - mq;
+    if constexpr (DIR == kFusedKlReverse) r = fmaf(p * db, c2, r);
+    else r = fmaf(ex2(fmaf(db, kLog2e, -log_sq * kLog2e)), ngk, r);
+  }
+  return r;
+}
+
 // Six resident CTAs per SM (at most 40 registers a thread) keep enough
 // loads in flight; with a larger register budget occupancy halves and the
 // sweep slows down.  The softcapped map runs a software pipeline and gets
 // kCapMinBlocks CTAs per SM.
-template <class T, int OP, bool CAP>
+template <class T, int OP, bool CAP, int DIR = kFusedNoKl>
 __global__ void __launch_bounds__(kRowThreads, CAP ? kCapMinBlocks : 6) row_bwd_kernel(const BwdArgs a) {
-  constexpr bool KL = OP >= kBwdKlReverse;
+  constexpr bool KL = bwd_reads_two<OP, DIR>();
   const int64_t row = blockIdx.x / a.chunks;
   const int q = static_cast<int>(blockIdx.x - row * a.chunks);
   const int64_t V = a.vocab;
@@ -198,6 +246,10 @@ __global__ void __launch_bounds__(kRowThreads, CAP ? kCapMinBlocks : 6) row_bwd_
   R.k2 = 0;
   R.nmq2 = 0;
   R.nlsq2 = 0;
+  R.c1 = 0;
+  R.c2 = 0;
+  R.ngk = 0;
+  float c0 = 0.0f, c1 = 0.0f, c2 = 0.0f, ngk = 0.0f, mq = 0.0f, log_sq = 0.0f;
 
   // ---- per-row constants; rows whose gradient is a constant (zero / NaN) ----
   float G = 0.0f;
@@ -205,7 +257,8 @@ __global__ void __launch_bounds__(kRowThreads, CAP ? kCapMinBlocks : 6) row_bwd_
   bool nan_row = false, zero_row = false;
   int64_t* fix_id = nullptr;
   float* fix_g = nullptr;
-  if constexpr (OP == kBwdLogp) {
+  const bool has_logp = OP == kBwdLogp || (OP == kBwdFused && a.g != nullptr);
+  if (OP == kBwdLogp || OP == kBwdFused) {
     // k = 1: one fixed slot; k > 1: sorted keys, upstream grads and the
     // fix-up list in dynamic shared memory
     __shared__ int64_t fix1_id;
@@ -214,7 +267,9 @@ __global__ void __launch_bounds__(kRowThreads, CAP ? kCapMinBlocks : 6) row_bwd_
     __shared__ float s_warp[kRowWarps];
     __shared__ int s_nfix;
     const int64_t col_beg = vb * 8, col_end = min(ve * 8, V);
-    if (a.k == 1) {
+    if (!has_logp) {
+      // fused backward without a logprob term
+    } else if (a.k == 1) {
       fix_id = &fix1_id;
       fix_g = &fix1_g;
       const int64_t id = a.ids[row];
@@ -246,7 +301,45 @@ __global__ void __launch_bounds__(kRowThreads, CAP ? kCapMinBlocks : 6) row_bwd_
       nfix = tp.nfix;
       zero_row = !tp.any_valid;
     }
-    R.coef2 = splat(CAP ? -4.0f * G : -G);  // the streamed value is -G p (dz/dx)
+    if constexpr (OP == kBwdLogp) {
+      R.coef2 = splat(CAP ? -4.0f * G : -G);  // the streamed value is -G p (dz/dx)
+    } else {
+      // fused: p_a (c0 + c1 d_a + c2 d_b) + ngk p_b, one term per present gradient
+      const bool has_h = a.g_h != nullptr, has_k = DIR != kFusedNoKl && a.g_kl != nullptr;
+      if (has_logp) c0 = -G;
+      if (has_h) {
+        const float gh = a.g_h[row], H = a.h[row];
+        c0 = fmaf(gh, sx.log_s - H, c0);  // -g_H p (d - (log S - H))
+        c1 -= gh;
+        nan_row |= isnan(H);
+      }
+      if constexpr (DIR != kFusedNoKl) {
+        const vls_rowstat sy = a.stats_y[row];
+        mq = sy.m;
+        log_sq = sy.log_s;
+        R.nmq2 = splat(-sy.m);
+        R.nlsq2 = splat(-sy.log_s * kLog2e);
+        if (has_k) {
+          const float gk = a.g_kl[row], kl = a.kl[row];
+          if constexpr (DIR == kFusedKlReverse) {
+            c0 = fmaf(-gk, (sx.log_s - sy.log_s) + kl, c0);  // g_K p ((d_a - d_b) - (lS_a - lS_b + KL))
+            c1 += gk;
+            c2 = -gk;
+            nan_row |= !isfinite(kl);
+          } else {
+            c0 += gk;  // g_K (p_a - p_b)
+            ngk = -gk;
+            nan_row |= isnan(kl);
+          }
+        }
+      }
+      nan_row |= sx.m == neg_inf() && (has_h || has_k);
+      zero_row = zero_row && !has_h && !has_k;
+      R.coef2 = splat(c0);
+      R.c1 = splat(c1);
+      R.c2 = splat(c2);
+      R.ngk = splat(ngk);
+    }
   } else if constexpr (OP == kBwdEntropy) {
     const float H = a.fout[row];
     R.coef2 = splat(-a.g[row]);
@@ -295,7 +388,7 @@ __global__ void __launch_bounds__(kRowThreads, CAP ? kCapMinBlocks : 6) row_bwd_
         for (int u = 0; u < U; ++u) {
           fp2 o[4];
 #pragma unroll
-          for (int i = 0; i < 4; ++i) o[i] = grad_pair<T, OP, CAP>(x[u], KL ? y[u] : x[u], i, R, K);
+          for (int i = 0; i < 4; ++i) o[i] = grad_pair<T, OP, CAP, DIR>(x[u], KL ? y[u] : x[u], i, R, K);
           Out8<T>::store(dr + 8 * (at + u * kRowThreads), o);
         }
       };
@@ -328,7 +421,7 @@ __global__ void __launch_bounds__(kRowThreads, CAP ? kCapMinBlocks : 6) row_bwd_
         for (int u = 0; u < U; ++u) {
           fp2 o[4];
 #pragma unroll
-          for (int i = 0; i < 4; ++i) o[i] = grad_pair<T, OP, CAP>(x[u], KL ? y[u] : x[u], i, R, K);
+          for (int i = 0; i < 4; ++i) o[i] = grad_pair<T, OP, CAP, DIR>(x[u], KL ? y[u] : x[u], i, R, K);
           Out8<T>::store(dr + 8 * (v + u * kRowThreads), o);
         }
       }
@@ -341,10 +434,21 @@ __global__ void __launch_bounds__(kRowThreads, CAP ? kCapMinBlocks : 6) row_bwd_
     if constexpr (KL) load_raw(y, yr, v, V, al, valid);
     fp2 o[4];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) o[i] = grad_pair<T, OP, CAP>(x, KL ? y : x, i, R, K);
+    for (int i = 0; i < 4; ++i) o[i] = grad_pair<T, OP, CAP, DIR>(x, KL ? y : x, i, R, K);
     store_vec(dr, v, V, al, o);
   }
 
+  if constexpr (OP == kBwdFused) {
+    // one-hot columns: rewrite with g_sum + (the streamed value), one rounding
+    if (nfix > 0) {
+      __syncthreads();  // the streamed stores of this CTA precede the rewrites
+      for (int f = threadIdx.x; f < nfix; f += kRowThreads) {
+        float chain;
+        const float r = fused_at<T, CAP, DIR>(xr, yr, fix_id[f], sx, mq, log_sq, c0, c1, c2, ngk, fix_g[f], K, chain);
+        Out8<T>::store1(dr + fix_id[f], CAP ? r * chain : r);
+      }
+    }
+  }
   if constexpr (OP == kBwdLogp) {
     // one-hot columns: rewrite with (g_sum - G p) dz/dx, one rounding at the store
     if (nfix > 0) {
@@ -368,11 +472,12 @@ __global__ void __launch_bounds__(kRowThreads, CAP ? kCapMinBlocks : 6) row_bwd_
   }
 }
 
-template <class T, int OP, bool CAP>
+template <class T, int OP, bool CAP, int DIR = kFusedNoKl>
 cudaError_t launch_bwd_t(const BwdArgs& a, cudaStream_t s) {
   const dim3 grid(static_cast<unsigned>(a.rows * a.chunks));
-  const size_t smem = (OP == kBwdLogp && a.k > 1) ? topk_smem_bytes(a.k) : 0;
-  row_bwd_kernel<T, OP, CAP><<<grid, kRowThreads, smem, s>>>(a);
+  const bool topk = (OP == kBwdLogp || (OP == kBwdFused && a.g != nullptr)) && a.k > 1;
+  const size_t smem = topk ? topk_smem_bytes(a.k) : 0;
+  row_bwd_kernel<T, OP, CAP, DIR><<<grid, kRowThreads, smem, s>>>(a);
   return cudaGetLastError();
 }
 

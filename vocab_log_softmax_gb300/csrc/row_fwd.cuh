@@ -164,19 +164,105 @@ struct KlAcc {
   __device__ State state() const { return {mp, sum2(sp2), mq, sum2(sq2), sum2(w2), flag}; }
 };
 
-template <int OP, class T, bool CAP>
+// Fused sweep over the policy a (`v`) and, with a KL term, the reference b
+// (`q`): a's statistics and entropy W as EntropyAcc, b's as LogpAcc, and the
+// KL W of direction DIR as KlAcc with P = a (reverse) or P = b (forward).
+template <class T, bool CAP, int DIR>
+struct FusedAcc {
+  using State = FusedState<DIR>;
+  static constexpr bool kHasB = DIR != kFusedNoKl;
+  float ma_raw = neg_inf(), ma = neg_inf(), mb_raw = neg_inf(), mb = neg_inf();
+  fp2 nma2 = 0, nmb2 = 0, sa2 = 0, wh2 = 0, sb2 = 0, wk2 = 0;
+  uint32_t flag = 0;
+
+  template <bool PARTIAL>
+  __device__ __forceinline__ void update(const Raw8<T>& v, const Raw8<T>& q, int valid, const CapK& K) {
+    const float vma = v.max();
+    const bool ua = grows<CAP>(vma, ma_raw, ma);
+    float vmb = neg_inf();
+    bool ub = false;
+    if constexpr (kHasB) {
+      vmb = q.max();
+      ub = grows<CAP>(vmb, mb_raw, mb);
+    }
+    if (ua || ub) {
+      const float Ma = ua ? (CAP ? cap_z(vma, K) : vma) : ma;
+      const float Mb = ub ? (CAP ? cap_z(vmb, K) : vmb) : mb;
+      const float fa = rescale(ma, Ma), fb = rescale(mb, Mb);
+      wh2 = ma != neg_inf() ? mul2(fma2(sa2, splat(ma - Ma), wh2), splat(fa)) : 0;
+      if constexpr (DIR == kFusedKlReverse)
+        wk2 = ma != neg_inf() ? mul2(fma2(sa2, splat((ma - Ma) - (mb - Mb)), wk2), splat(fa)) : 0;
+      if constexpr (DIR == kFusedKlForward)
+        wk2 = mb != neg_inf() ? mul2(fma2(sb2, splat((mb - Mb) - (ma - Ma)), wk2), splat(fb)) : 0;
+      sa2 = mul2(sa2, splat(fa));
+      sb2 = mul2(sb2, splat(fb));
+      if (ua) { ma_raw = vma; ma = Ma; nma2 = splat(-Ma); }
+      if (ub) { mb_raw = vmb; mb = Mb; nmb2 = splat(-Mb); }
+    }
+    if constexpr (kHasB && !CAP) {
+#pragma unroll
+      for (int i = 0; i < 4; ++i) flag |= DIR == kFusedKlReverse ? v.mismatch(i, q) : q.mismatch(i, v);
+    }
+    const bool a_ok = CAP || ma != neg_inf(), b_ok = CAP || mb != neg_inf();
+    if (a_ok && (!kHasB || b_ok)) {
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        fp2 da, db = 0;
+        if (CAP) {
+          fp2 e2, r2;
+          da = fma2(cap_t2(v, i, K, e2, r2), splat(K.c), nma2);
+          if constexpr (kHasB) db = fma2(cap_t2(q, i, K, e2, r2), splat(K.c), nmb2);
+        } else {
+          da = add2(v.pair_clamped(i), nma2);
+          if constexpr (kHasB) db = add2(q.pair_clamped(i), nmb2);
+        }
+        const fp2 ea = keep<PARTIAL>(ex2_2(mul2(da, splat(kLog2e))), i, valid);
+        sa2 = add2(sa2, ea);
+        wh2 = fma2(ea, da, wh2);
+        if constexpr (kHasB) {
+          const fp2 eb = keep<PARTIAL>(ex2_2(mul2(db, splat(kLog2e))), i, valid);
+          sb2 = add2(sb2, eb);
+          if constexpr (DIR == kFusedKlReverse) wk2 = fma2(ea, sub2(da, db), wk2);
+          else wk2 = fma2(eb, sub2(db, da), wk2);
+        }
+      }
+    } else if (a_ok || b_ok) {
+      // one side has seen only -inf so far: no cross term (a finite column
+      // of the KL's first argument against an all -inf run is flagged)
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        if (a_ok) {
+          const fp2 da = add2(v.pair_clamped(i), nma2);
+          const fp2 ea = keep<PARTIAL>(ex2_2(mul2(da, splat(kLog2e))), i, valid);
+          sa2 = add2(sa2, ea);
+          wh2 = fma2(ea, da, wh2);
+        }
+        if (b_ok) sb2 = add2(sb2, keep<PARTIAL>(ex2_2(mul2(add2(q.pair_clamped(i), nmb2), splat(kLog2e))), i, valid));
+      }
+    }
+  }
+  __device__ State state() const { return {ma, sum2(sa2), sum2(wh2), mb, sum2(sb2), sum2(wk2), flag}; }
+};
+
+template <int OP, class T, bool CAP, int DIR>
 struct FwdAccOf;
-template <class T, bool CAP>
-struct FwdAccOf<kFwdLogp, T, CAP> { using type = LogpAcc<T, CAP>; };
-template <class T, bool CAP>
-struct FwdAccOf<kFwdEntropy, T, CAP> { using type = EntropyAcc<T, CAP>; };
-template <class T, bool CAP>
-struct FwdAccOf<kFwdKl, T, CAP> { using type = KlAcc<T, CAP>; };
+template <class T, bool CAP, int DIR>
+struct FwdAccOf<kFwdLogp, T, CAP, DIR> { using type = LogpAcc<T, CAP>; };
+template <class T, bool CAP, int DIR>
+struct FwdAccOf<kFwdEntropy, T, CAP, DIR> { using type = EntropyAcc<T, CAP>; };
+template <class T, bool CAP, int DIR>
+struct FwdAccOf<kFwdKl, T, CAP, DIR> { using type = KlAcc<T, CAP>; };
+template <class T, bool CAP, int DIR>
+struct FwdAccOf<kFwdFused, T, CAP, DIR> { using type = FusedAcc<T, CAP, DIR>; };
+
+// the sweep reads a second tensor
+template <int OP, int DIR>
+constexpr bool reads_two() { return OP == kFwdKl || (OP == kFwdFused && DIR != kFusedNoKl); }
 
 // 16-byte loads in flight per thread before any is used: 4 vectors of one
 // tensor, or 2 vectors of each of the two KL tensors.
-template <int OP>
-constexpr int fwd_unroll() { return OP == kFwdKl ? 2 : 4; }
+template <int OP, int DIR>
+constexpr int fwd_unroll() { return reads_two<OP, DIR>() ? 2 : 4; }
 
 // ---- finalisation, shared with the vocabulary-parallel combine ----
 
@@ -208,12 +294,12 @@ __device__ __forceinline__ void from_partial(const vls_partial& p, KlState& s) {
   s = {p.m, p.s, p.mq, p.sq, p.w, p.flag};
 }
 
-template <class T, int OP, bool CAP>
+template <class T, int OP, bool CAP, int DIR = kFusedNoKl>
 __global__ void __launch_bounds__(kFwdThreads) row_fwd_kernel(const FwdArgs a) {
-  using Acc = typename FwdAccOf<OP, T, CAP>::type;
+  using Acc = typename FwdAccOf<OP, T, CAP, DIR>::type;
   using S = typename Acc::State;
-  constexpr int U = fwd_unroll<OP>();
-  constexpr bool KL = OP == kFwdKl;
+  constexpr int U = fwd_unroll<OP, DIR>();
+  constexpr bool KL = reads_two<OP, DIR>();
   __shared__ S warp_part[kFwdWarps];
   __shared__ S cta_part[kMaxCluster];
   __shared__ S row_state;
@@ -288,10 +374,12 @@ __global__ void __launch_bounds__(kFwdThreads) row_fwd_kernel(const FwdArgs a) {
 
   // ---- finalise (rank 0 of the row) ----
   const S fin = row_state;
-  if (a.part != nullptr) {
+  if (OP != kFwdFused && a.part != nullptr) {
     // vocabulary-parallel partial: the state itself, and for logp the raw
     // logits of the target ids this shard owns (0 for the others)
-    if (threadIdx.x == 0) a.part[row] = to_partial(fin);
+    if constexpr (OP != kFwdFused) {
+      if (threadIdx.x == 0) a.part[row] = to_partial(fin);
+    }
     if constexpr (OP == kFwdLogp) {
       for (int j = threadIdx.x; j < a.k; j += kFwdThreads) {
         const int64_t id = a.ids[row * a.k + j];
@@ -316,17 +404,39 @@ __global__ void __launch_bounds__(kFwdThreads) row_fwd_kernel(const FwdArgs a) {
       a.stats_x[row] = vls_rowstat{fin.m, log_s};
       a.out[row] = entropy_of(fin, log_s);
     }
-  } else {
+  } else if constexpr (OP == kFwdKl) {
     if (threadIdx.x == 0) {
       const float log_sp = logf(fin.sp), log_sq = logf(fin.sq);
       a.stats_x[row] = vls_rowstat{fin.mp, log_sp};
       a.stats_y[row] = vls_rowstat{fin.mq, log_sq};
       a.out[row] = kl_of(fin, log_sp, log_sq);
     }
+  } else {
+    // fused: stats_x / stats_y are a's and b's, whatever the direction
+    const float log_sa = logf(fin.sa);
+    if (a.logp != nullptr) {
+      for (int j = threadIdx.x; j < a.k; j += kFwdThreads) {
+        const int64_t id = a.ids[row * a.k + j];
+        a.logp[row * a.k + j] = valid_id(id, V, a.ignore_index) ? logp_of<CAP>(load1(xr + id), fin.ma, log_sa, K) : 0.0f;
+      }
+    }
+    if (threadIdx.x == 0) {
+      a.stats_x[row] = vls_rowstat{fin.ma, log_sa};
+      if (a.h != nullptr) a.h[row] = entropy_of(EntropyState{fin.ma, fin.sa, fin.wh}, log_sa);
+      if constexpr (DIR != kFusedNoKl) {
+        const float log_sb = logf(fin.sb);
+        a.stats_y[row] = vls_rowstat{fin.mb, log_sb};
+        if (a.kl != nullptr) {
+          a.kl[row] = DIR == kFusedKlReverse
+                          ? kl_of(KlState{fin.ma, fin.sa, fin.mb, fin.sb, fin.wk, fin.flag}, log_sa, log_sb)
+                          : kl_of(KlState{fin.mb, fin.sb, fin.ma, fin.sa, fin.wk, fin.flag}, log_sb, log_sa);
+        }
+      }
+    }
   }
 }
 
-template <class T, int OP, bool CAP>
+template <class T, int OP, bool CAP, int DIR = kFusedNoKl>
 cudaError_t launch_fwd_t(const FwdArgs& a, cudaStream_t s) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(a.rows * a.cluster));
@@ -340,7 +450,7 @@ cudaError_t launch_fwd_t(const FwdArgs& a, cudaStream_t s) {
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = a.cluster > 1 ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, row_fwd_kernel<T, OP, CAP>, a);
+  return cudaLaunchKernelEx(&cfg, row_fwd_kernel<T, OP, CAP, DIR>, a);
 }
 
 template <int OP>

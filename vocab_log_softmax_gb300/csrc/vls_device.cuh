@@ -358,6 +358,50 @@ struct KlState {
   }
 };
 
+// Fused sweep (logprobs + entropy + KL of the same policy a): a's max and
+// sum-exp, the entropy W of a, and (DIR != kFusedNoKl) b's max and sum-exp
+// and the KL W in direction DIR (P = a for reverse, P = b for forward).
+template <int DIR>
+struct FusedState {
+  float ma, sa, wh, mb, sb, wk;
+  uint32_t flag;
+  __device__ static FusedState identity() { return {neg_inf(), 0.0f, 0.0f, neg_inf(), 0.0f, 0.0f, 0u}; }
+  __device__ static FusedState combine(const FusedState& x, const FusedState& y) {
+    FusedState r;
+    const float Ma = fmaxf(x.ma, y.ma), Mb = fmaxf(x.mb, y.mb);
+    const float fax = Ma == neg_inf() ? 0.0f : rescale(x.ma, Ma);
+    const float fay = Ma == neg_inf() ? 0.0f : rescale(y.ma, Ma);
+    const float fbx = Mb == neg_inf() ? 0.0f : rescale(x.mb, Mb);
+    const float fby = Mb == neg_inf() ? 0.0f : rescale(y.mb, Mb);
+    r.ma = Ma;
+    r.mb = Mb;
+    r.sa = x.sa * fax + y.sa * fay;
+    r.sb = x.sb * fbx + y.sb * fby;
+    r.wh = (x.ma != neg_inf() ? fax * fmaf(x.sa, x.ma - Ma, x.wh) : 0.0f) +
+           (y.ma != neg_inf() ? fay * fmaf(y.sa, y.ma - Ma, y.wh) : 0.0f);
+    if (DIR == kFusedKlForward) {
+      r.wk = (x.mb != neg_inf() ? fbx * fmaf(x.sb, (x.mb - Mb) - (x.ma - Ma), x.wk) : 0.0f) +
+             (y.mb != neg_inf() ? fby * fmaf(y.sb, (y.mb - Mb) - (y.ma - Ma), y.wk) : 0.0f);
+    } else {
+      r.wk = (x.ma != neg_inf() ? fax * fmaf(x.sa, (x.ma - Ma) - (x.mb - Mb), x.wk) : 0.0f) +
+             (y.ma != neg_inf() ? fay * fmaf(y.sa, (y.ma - Ma) - (y.mb - Mb), y.wk) : 0.0f);
+    }
+    r.flag = x.flag | y.flag;
+    return r;
+  }
+  __device__ FusedState shfl_xor(int lane_mask) const {
+    FusedState r;
+    r.ma = __shfl_xor_sync(0xffffffffu, ma, lane_mask);
+    r.sa = __shfl_xor_sync(0xffffffffu, sa, lane_mask);
+    r.wh = __shfl_xor_sync(0xffffffffu, wh, lane_mask);
+    r.mb = __shfl_xor_sync(0xffffffffu, mb, lane_mask);
+    r.sb = __shfl_xor_sync(0xffffffffu, sb, lane_mask);
+    r.wk = __shfl_xor_sync(0xffffffffu, wk, lane_mask);
+    r.flag = __shfl_xor_sync(0xffffffffu, flag, lane_mask);
+    return r;
+  }
+};
+
 // Butterfly over the 32 lanes of a warp, always xor 16, 8, 4, 2, 1.
 template <class S>
 __device__ __forceinline__ S warp_reduce(S s) {

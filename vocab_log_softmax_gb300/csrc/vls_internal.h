@@ -11,9 +11,11 @@
 namespace vls {
 
 // Statistic computed by the one-read forward sweep.
-enum FwdOp { kFwdLogp = 0, kFwdEntropy = 1, kFwdKl = 2 };
+enum FwdOp { kFwdLogp = 0, kFwdEntropy = 1, kFwdKl = 2, kFwdFused = 3 };
 // Gradient map applied by the backward sweep.
-enum BwdOp { kBwdLogp = 0, kBwdEntropy = 1, kBwdKlReverse = 2, kBwdKlForward = 3 };
+enum BwdOp { kBwdLogp = 0, kBwdEntropy = 1, kBwdKlReverse = 2, kBwdKlForward = 3, kBwdFused = 4 };
+// KL term of the fused sweeps
+enum FusedKl { kFusedNoKl = 0, kFusedKlReverse = 1, kFusedKlForward = 2 };
 
 // Threads per CTA of the row kernels.  Each thread owns whole 8-column
 // vectors; the reduction tree (lanes, then warps, then cluster ranks) is a
@@ -74,6 +76,9 @@ struct FwdArgs {
   int64_t vocab_total;
   vls_partial* part;
   float* zt;
+  // fused sweep: entropy and KL outputs (either may be null)
+  float* h;
+  float* kl;
 };
 
 struct BwdArgs {
@@ -99,6 +104,12 @@ struct BwdArgs {
   // vocab_total; this shard holds [vocab_offset, vocab_offset + vocab)
   int64_t vocab_offset;
   int64_t vocab_total;
+  // fused backward: upstream gradients (null = term left out) and the
+  // forward's H and KL
+  const float* g_h;
+  const float* g_kl;
+  const float* h;
+  const float* kl;
 };
 
 struct CombineArgs {
@@ -137,6 +148,8 @@ cudaError_t launch_bwd_logp(vls_dtype dt, bool cap, const BwdArgs& a, cudaStream
 cudaError_t launch_bwd_entropy(vls_dtype dt, bool cap, const BwdArgs& a, cudaStream_t s);
 cudaError_t launch_bwd_kl(bool reverse, vls_dtype dt, bool cap, const BwdArgs& a, cudaStream_t s);
 cudaError_t launch_combine(FwdOp op, const CombineArgs& a, cudaStream_t s);
+cudaError_t launch_fwd_fused(FusedKl kl, vls_dtype dt, bool cap, const FwdArgs& a, cudaStream_t s);
+cudaError_t launch_bwd_fused(FusedKl kl, vls_dtype dt, bool cap, const BwdArgs& a, cudaStream_t s);
 cudaError_t launch_softcap_fwd(vls_dtype dt, const CapArgs& a, cudaStream_t s);
 cudaError_t launch_softcap_bwd(vls_dtype dt, const CapArgs& a, cudaStream_t s);
 
