@@ -388,6 +388,33 @@ class ConfigRun:
                   ("k=256 logp bwd", bk["bwd"], lambda: B.vls_logp_bwd(x, w["idsk"], w["gk"], st, dlogits=d)),
                   ("entropy fwd", be["fwd"], lambda: B.vls_entropy_fwd(x, H=H, stats=st)),
                   ("entropy bwd", be["bwd"], lambda: B.vls_entropy_bwd(x, w["g_row"], H, st, dlogits=d))]
+        elif name == "fused":
+            # logprobs + entropy + reverse KL of one policy: fused calls vs the six separate calls
+            w = workloads.kl_masked(device, n=N_ROWS, v=VOCAB)
+            wl = workloads.logp_offset(device, n=N_ROWS, v=VOCAB)
+            a_, b_, g = w["a"], w["b"], w["g"]
+            ids, gl = wl["ids"], wl["g"]
+            n, v = a_.shape
+            out = {}
+            d = torch.empty_like(a_)
+            nv = n * v * 2
+            small = n * (8 + 4 + 4 + 4 + 16)
+
+            def ffwd():
+                out.update(B.vls_fused_fwd(a_, b_, ids))
+
+            L += [("fused fwd (logp+H+KL)", 2 * nv + small, ffwd),
+                  ("fused bwd (logp+H+KL)", 3 * nv + small,
+                   lambda: B.vls_fused_bwd(a_, out, b_, ids, g_logp=gl, g_H=g, g_kl=g, da=d))]
+            lp, H, kl = torch.empty((n, 1), **f32), torch.empty((n,), **f32), torch.empty((n,), **f32)
+            st1, st2, st3 = (torch.empty((n, 2), **f32) for _ in range(3))
+            bl, be, bk = op_bytes("logp", n, v), op_bytes("entropy", n, v), op_bytes("kl_reverse", n, v)
+            L += [("separate logp fwd", bl["fwd"], lambda: B.vls_logp_fwd(a_, ids, logp=lp, stats=st1)),
+                  ("separate entropy fwd", be["fwd"], lambda: B.vls_entropy_fwd(a_, H=H, stats=st1)),
+                  ("separate KL fwd", bk["fwd"], lambda: B.vls_kl_fwd(a_, b_, kl=kl, stats_a=st2, stats_b=st3)),
+                  ("separate logp bwd", bl["bwd"], lambda: B.vls_logp_bwd(a_, ids, gl, st1, dlogits=d)),
+                  ("separate entropy bwd", be["bwd"], lambda: B.vls_entropy_bwd(a_, g, H, st1, dlogits=d)),
+                  ("separate KL bwd", bk["bwd"], lambda: B.vls_kl_bwd(a_, b_, g, kl, st2, st3, da=d))]
         else:
             raise SystemExit(f"unknown workload {name}")
         self.launches = L
@@ -578,7 +605,7 @@ def main() -> None:
     ap.add_argument("--e2e-steps", type=int, default=3)
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timing leg")
     ap.add_argument("--workload", default="step",
-                    choices=["step", "logp_small", "logp_offset", "kl_masked", "softcap_wide", "long_seq"],
+                    choices=["step", "logp_small", "logp_offset", "kl_masked", "softcap_wide", "long_seq", "fused"],
                     help="step (default): the benchmark step; otherwise per-op times of one workload")
     args = ap.parse_args()
     if args.workload != "step" and args.impl == "ours":

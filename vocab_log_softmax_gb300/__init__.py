@@ -21,6 +21,8 @@ from ._lib import VlsArgumentError, VlsError  # noqa: F401
 from .binding import (  # noqa: F401
     vls_entropy_bwd,
     vls_entropy_fwd,
+    vls_fused_bwd,
+    vls_fused_fwd,
     vls_kl_bwd,
     vls_kl_fwd,
     vls_logp_bwd,
@@ -31,7 +33,7 @@ from .binding import (  # noqa: F401
     vls_version,
 )
 
-__all__ = ["logprobs", "entropy", "kl", "softcap"]
+__all__ = ["logprobs", "entropy", "kl", "softcap", "stats"]
 
 
 def _as_rows(x: torch.Tensor) -> torch.Tensor:
@@ -47,6 +49,15 @@ def _as_rows(x: torch.Tensor) -> torch.Tensor:
     return rows
 
 
+def _ids_rows(ids: torch.Tensor, n: int) -> torch.Tensor:
+    """ids shaped like the logits' leading dims (k = 1) or with a trailing k -> [N, k] int64."""
+    if n == 0 or ids.numel() % n != 0:
+        if n == 0:
+            return ids.reshape(0, ids.shape[-1] if ids.dim() > 0 else 1).to(torch.int64)
+        raise ValueError(f"ids with {ids.numel()} elements do not divide into {n} rows")
+    return ids.reshape(n, ids.numel() // n).to(torch.int64).contiguous()
+
+
 def _cap(softcap) -> float:
     if softcap is None:
         return 0.0
@@ -60,7 +71,7 @@ class _Logprobs(torch.autograd.Function):
     @staticmethod
     def forward(ctx, logits, ids, ignore_index, cap):
         rows = _as_rows(logits)
-        ids2 = ids.reshape(rows.shape[0], ids.shape[-1] if ids.dim() > 1 else 1).to(torch.int64).contiguous()
+        ids2 = _ids_rows(ids, rows.shape[0])
         logp, stats = vls_logp_fwd(rows, ids2, ignore_index, cap)
         ctx.save_for_backward(rows, ids2, stats)
         ctx.meta = (ignore_index, cap, logits.shape)
@@ -123,6 +134,51 @@ class _Softcap(torch.autograd.Function):
         if gy.dtype not in (torch.float32, xc.dtype):
             gy = gy.to(torch.float32)
         return vls_softcap_bwd(xc, gy.contiguous(), ctx.cap), None
+
+
+class _Stats(torch.autograd.Function):
+    @staticmethod
+    def forward(ctx, policy, reference, ids, direction, ignore_index, cap):
+        a = _as_rows(policy)
+        b = _as_rows(reference.detach()) if reference is not None else None
+        ids2 = None
+        if ids is not None:
+            ids2 = _ids_rows(ids, a.shape[0])
+        out = vls_fused_fwd(a, b, ids2, logp=ids is not None, entropy=True, direction=direction,
+                            ignore_index=ignore_index, cap=cap)
+        ctx.save_for_backward(a, b, ids2, out["stats_a"], out.get("stats_b"), out["H"], out.get("kl"))
+        ctx.meta = (direction, ignore_index, cap, policy.shape, ids.shape if ids is not None else None)
+        lead = policy.shape[:-1]
+        empty = a.new_empty(0, dtype=torch.float32)
+        logp = out["logp"].reshape(ids.shape) if ids is not None else empty
+        klv = out["kl"].reshape(lead) if b is not None else empty
+        return logp, out["H"].reshape(lead), klv
+
+    @staticmethod
+    def backward(ctx, g_logp, g_H, g_kl):
+        a, b, ids2, sa, sb, H, kl = ctx.saved_tensors
+        direction, ignore_index, cap, shape, ids_shape = ctx.meta
+        f32 = lambda g, shp: None if g is None else g.reshape(shp).to(torch.float32).contiguous()  # noqa: E731
+        gl = f32(g_logp, ids2.shape) if ids2 is not None else None
+        gh = f32(g_H, (-1,))
+        gk = f32(g_kl, (-1,)) if b is not None else None
+        if gl is None and gh is None and gk is None:
+            return None, None, None, None, None, None
+        fwd = {"stats_a": sa, "stats_b": sb, "H": H, "kl": kl}
+        da = vls_fused_bwd(a, fwd, b, ids2, g_logp=gl, g_H=gh, g_kl=gk, direction=direction,
+                           ignore_index=ignore_index, cap=cap)
+        return da.reshape(shape), None, None, None, None, None
+
+
+def stats(policy: torch.Tensor, ids: torch.Tensor | None = None, reference: torch.Tensor | None = None,
+          direction: str = "reverse", ignore_index: int = -100, softcap: float | None = None):
+    """(logp, entropy, kl) of softmax(softcap(policy)) from one read of the
+    policy (and one of the reference): logp like ``logprobs`` (empty without
+    ids), entropy per row, KL against the detached reference (empty without
+    one).  The backward of any weighted sum of the three is one pass."""
+    if direction not in ("reverse", "forward"):
+        raise ValueError("direction must be 'reverse' or 'forward'")
+    return _Stats.apply(policy, reference, ids, direction, int(ignore_index), _cap(softcap))
 
 
 def logprobs(logits: torch.Tensor, ids: torch.Tensor, ignore_index: int = -100,
