@@ -49,7 +49,7 @@ extern "C" {
 #endif
 
 /* Element type of logits, gradients and softcap tensors. */
-typedef enum { VLS_F32 = 0, VLS_BF16 = 1 } vls_dtype;
+typedef enum { VLS_F32 = 0, VLS_BF16 = 1, VLS_F16 = 2 } vls_dtype;
 
 /* VLS_KL_REVERSE: KL(p_a || p_b); VLS_KL_FORWARD: KL(p_b || p_a).  In both the
  * gradient flows to `a` (the policy) only; `b` (the reference) is detached

@@ -97,7 +97,7 @@ def test_binding_rejects_bad_layouts():
     import torch
 
     from vocab_log_softmax_gb300 import binding as B
-    x = torch.zeros((4, 6), dtype=torch.float16)
+    x = torch.zeros((4, 6), dtype=torch.float64)
     with pytest.raises(TypeError):
         B.vls_entropy_fwd(x)
     with pytest.raises(ValueError):

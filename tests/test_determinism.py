@@ -88,6 +88,19 @@ def test_bf16_equals_exact_fp32_copy(batch):
         assert bitwise_equal(ob[k], of[k].to(torch.bfloat16)), k
 
 
+def test_f16_equals_exact_fp32_copy(batch):
+    """The same for float16 logits (values rescaled into float16's range)."""
+    a, b, ids, gk, gr = batch
+    a16 = (a.float() * 0.25).to(torch.float16)
+    b16 = (b.float() * 0.25).to(torch.float16)
+    oh = _all_outputs(a16, b16, ids, gk, gr)
+    of = _all_outputs(a16.float(), b16.float(), ids, gk, gr)
+    for k in ("logp", "stats", "H", "kl_reverse", "kl_forward"):
+        assert bitwise_equal(oh[k], of[k]), k
+    for k in ("dlogp", "dH", "dkl_reverse", "dkl_forward"):
+        assert bitwise_equal(oh[k], of[k].to(torch.float16)), k
+
+
 def test_k1_equals_same_id_in_topk(batch):
     a = batch[0]
     w = workloads.long_seq(DEV, n=8, v=a.shape[1])

@@ -15,7 +15,7 @@ from vocab_log_softmax_gb300 import _lib
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
-DTYPES = [torch.float32, torch.bfloat16]
+DTYPES = [torch.float32, torch.bfloat16, torch.float16]
 
 
 def _gen(seed):
@@ -194,3 +194,26 @@ def test_uniform_rows_closed_form():
     h, _ = B.vls_entropy_fwd(x)
     assert_fp32_close(lp, np.full((3, 1), -np.log(v)), "uniform logp")
     assert_fp32_close(h, np.full(3, np.log(v)), "uniform entropy")
+
+
+def test_float16_range_limits():
+    """float16 logits at the ends of its range, next to -inf masks: the
+    lowest finite float16 (-65504) is a real logit, not a mask."""
+    v = 4001
+    g = _gen(65504)
+    a = (3.0 * torch.randn((6, v), generator=g, device=DEV)).to(torch.float16)
+    b = (a.float() + 0.5 * torch.randn((6, v), generator=g, device=DEV)).to(torch.float16)
+    a[0, :] = -65504.0                          # a whole row at the lowest finite value: uniform
+    a[0, 17] = float("-inf")
+    b[0, :] = -65504.0
+    b[0, 17] = float("-inf")
+    a[1, 5] = 65504.0                           # the largest finite value dominates the row
+    a[2, 100:110] = -65504.0
+    b[2, 100:110] = float("-inf")               # mismatch against finite (if tiny) policy weight
+    ids = torch.randint(0, v, (6, 2), generator=g, device=DEV)
+    gk = torch.randn((6, 2), generator=g, device=DEV)
+    gr = torch.randn((6,), generator=g, device=DEV)
+    check_logp(a, ids, gk, what="f16 limits logp")
+    check_entropy(a, gr, what="f16 limits entropy")
+    for d in ("reverse", "forward"):
+        check_kl(a, b, gr, d, what="f16 limits kl")

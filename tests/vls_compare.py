@@ -4,6 +4,9 @@
 * bf16 gradients and bf16 softcap outputs: |gpu - ref| <= ulp_bf16(ref) + 1e-6,
   ulp_bf16(r) = 2^(floor(log2 |r|) - 7) (one unit in the last place of a
   bfloat16 with magnitude |r|).
+* fp16 gradients and fp16 softcap outputs: the same rule with one float16
+  unit, ulp_f16(r) = 2^(max(floor(log2 |r|), -14) - 10) (the float16 spacing,
+  2^-24 in the subnormal range).
 * fp32 gradients and fp32 softcap outputs: 1e-5 + 1e-5 |ref|.
 * Non-finite values match exactly: NaN, +inf and -inf in the same places.
 """
@@ -66,14 +69,23 @@ def ulp_bf16(r: np.ndarray) -> np.ndarray:
     return out
 
 
+def ulp_f16(r: np.ndarray) -> np.ndarray:
+    a = np.abs(r)
+    out = np.full_like(a, 2.0 ** -24)
+    nz = a > 0
+    out[nz] = np.exp2(np.maximum(np.floor(np.log2(a[nz])), -14.0) - 10.0)
+    return out
+
+
 def assert_grad_close(got: torch.Tensor, ref, what: str = ""):
     """Gradient / softcap-output rule for the tensor's own dtype."""
     ref = np.asarray(ref, dtype=np.float64)
-    if got.dtype == torch.bfloat16:
+    if got.dtype in (torch.bfloat16, torch.float16):
         g = to_f64(got)
         assert g.shape == ref.shape, (what, g.shape, ref.shape)
         fin = _nonfinite_match(g, ref, what)
-        _report(what, g, ref, ulp_bf16(ref[fin]) + BF16_ATOL, fin)
+        ulp = ulp_bf16 if got.dtype == torch.bfloat16 else ulp_f16
+        _report(what, g, ref, ulp(ref[fin]) + BF16_ATOL, fin)
     else:
         assert_fp32_close(got, ref, what)
 

@@ -14,6 +14,7 @@ LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "lib", "libv
 
 VLS_F32 = 0
 VLS_BF16 = 1
+VLS_F16 = 2
 VLS_KL_REVERSE = 0
 VLS_KL_FORWARD = 1
 VLS_MAX_TOPK = 1024

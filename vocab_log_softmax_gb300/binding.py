@@ -16,7 +16,7 @@ import torch
 
 from . import _lib
 
-_DT = {torch.float32: _lib.VLS_F32, torch.bfloat16: _lib.VLS_BF16}
+_DT = {torch.float32: _lib.VLS_F32, torch.bfloat16: _lib.VLS_BF16, torch.float16: _lib.VLS_F16}
 _DIR = {"reverse": _lib.VLS_KL_REVERSE, "forward": _lib.VLS_KL_FORWARD}
 
 
@@ -24,7 +24,7 @@ def _dtype(t: torch.Tensor) -> int:
     try:
         return _DT[t.dtype]
     except KeyError:
-        raise TypeError(f"libvls supports float32 and bfloat16 tensors, not {t.dtype}") from None
+        raise TypeError(f"libvls supports float32, bfloat16 and float16 tensors, not {t.dtype}") from None
 
 
 def _rows(t: torch.Tensor) -> tuple[int, int, int]:

@@ -16,7 +16,7 @@ namespace {
 
 constexpr int64_t kMaxGrid = 0x7fffffff;
 
-bool dtype_ok(int dt) { return dt == VLS_F32 || dt == VLS_BF16; }
+bool dtype_ok(int dt) { return dt == VLS_F32 || dt == VLS_BF16 || dt == VLS_F16; }
 
 // cap == 0 disables the softcap in the row calls; NaN, inf and negative
 // values are rejected ("Final Logit Softcap", Summary: the cap must be finite

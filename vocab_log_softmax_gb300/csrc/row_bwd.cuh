@@ -481,11 +481,16 @@ cudaError_t launch_bwd_t(const BwdArgs& a, cudaStream_t s) {
   return cudaGetLastError();
 }
 
-template <int OP>
+template <class T, int OP, int DIR = kFusedNoKl>
+cudaError_t launch_bwd_cap(bool cap, const BwdArgs& a, cudaStream_t s) {
+  return cap ? launch_bwd_t<T, OP, true, DIR>(a, s) : launch_bwd_t<T, OP, false, DIR>(a, s);
+}
+
+template <int OP, int DIR = kFusedNoKl>
 cudaError_t launch_bwd_op(vls_dtype dt, bool cap, const BwdArgs& a, cudaStream_t s) {
-  if (dt == VLS_BF16)
-    return cap ? launch_bwd_t<__nv_bfloat16, OP, true>(a, s) : launch_bwd_t<__nv_bfloat16, OP, false>(a, s);
-  return cap ? launch_bwd_t<float, OP, true>(a, s) : launch_bwd_t<float, OP, false>(a, s);
+  if (dt == VLS_BF16) return launch_bwd_cap<__nv_bfloat16, OP, DIR>(cap, a, s);
+  if (dt == VLS_F16) return launch_bwd_cap<__half, OP, DIR>(cap, a, s);
+  return launch_bwd_cap<float, OP, DIR>(cap, a, s);
 }
 
 }  // namespace vls

@@ -453,11 +453,16 @@ cudaError_t launch_fwd_t(const FwdArgs& a, cudaStream_t s) {
   return cudaLaunchKernelEx(&cfg, row_fwd_kernel<T, OP, CAP, DIR>, a);
 }
 
-template <int OP>
+template <class T, int OP, int DIR = kFusedNoKl>
+cudaError_t launch_fwd_cap(bool cap, const FwdArgs& a, cudaStream_t s) {
+  return cap ? launch_fwd_t<T, OP, true, DIR>(a, s) : launch_fwd_t<T, OP, false, DIR>(a, s);
+}
+
+template <int OP, int DIR = kFusedNoKl>
 cudaError_t launch_fwd_op(vls_dtype dt, bool cap, const FwdArgs& a, cudaStream_t s) {
-  if (dt == VLS_BF16)
-    return cap ? launch_fwd_t<__nv_bfloat16, OP, true>(a, s) : launch_fwd_t<__nv_bfloat16, OP, false>(a, s);
-  return cap ? launch_fwd_t<float, OP, true>(a, s) : launch_fwd_t<float, OP, false>(a, s);
+  if (dt == VLS_BF16) return launch_fwd_cap<__nv_bfloat16, OP, DIR>(cap, a, s);
+  if (dt == VLS_F16) return launch_fwd_cap<__half, OP, DIR>(cap, a, s);
+  return launch_fwd_cap<float, OP, DIR>(cap, a, s);
 }
 
 }  // namespace vls

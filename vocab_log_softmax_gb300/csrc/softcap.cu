@@ -181,6 +181,7 @@ cudaError_t launch_one_wave(K kernel, CapArgs a, cudaStream_t s) {
 
 cudaError_t launch_softcap_fwd(vls_dtype dt, const CapArgs& a, cudaStream_t s) {
   if (dt == VLS_BF16) return launch_one_wave(softcap_fwd_kernel<__nv_bfloat16>, a, s);
+  if (dt == VLS_F16) return launch_one_wave(softcap_fwd_kernel<__half>, a, s);
   return launch_one_wave(softcap_fwd_kernel<float>, a, s);
 }
 
@@ -188,6 +189,10 @@ cudaError_t launch_softcap_bwd(vls_dtype dt, const CapArgs& a, cudaStream_t s) {
   if (dt == VLS_BF16) {
     if (a.gy_f32) return launch_one_wave(softcap_bwd_kernel<__nv_bfloat16, float>, a, s);
     return launch_one_wave(softcap_bwd_kernel<__nv_bfloat16, __nv_bfloat16>, a, s);
+  }
+  if (dt == VLS_F16) {
+    if (a.gy_f32) return launch_one_wave(softcap_bwd_kernel<__half, float>, a, s);
+    return launch_one_wave(softcap_bwd_kernel<__half, __half>, a, s);
   }
   return launch_one_wave(softcap_bwd_kernel<float, float>, a, s);
 }

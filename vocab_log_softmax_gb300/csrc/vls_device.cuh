@@ -7,6 +7,7 @@
 
 #include <cooperative_groups.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
 #include "vls_internal.h"
@@ -107,6 +108,25 @@ __device__ __forceinline__ uint32_t beq2(uint32_t a, uint32_t b) {
   return r;
 }
 
+// float16x2 helpers on raw 32-bit words.
+__device__ __forceinline__ uint32_t hmax2(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("max.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  return r;
+}
+__device__ __forceinline__ uint32_t heq2(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("set.eq.u32.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  return r;
+}
+__device__ __forceinline__ float h2f(uint32_t bits16) {
+  float f;
+  const unsigned short h = static_cast<unsigned short>(bits16);
+  asm("cvt.f32.f16 %0, %1;" : "=f"(f) : "h"(h));
+  return f;
+}
+constexpr uint32_t kNegInfF16x2 = 0xfc00fc00u;
+
 // 16-byte read-only load that skips L1 (each logit is read once per sweep).
 __device__ __forceinline__ uint4 ld_stream16(const void* p) {
   uint4 r;
@@ -182,6 +202,44 @@ struct Raw8<__nv_bfloat16> {
   // nonzero iff some column of pair i has this = finite-or-+inf and q = -inf
   __device__ __forceinline__ uint32_t mismatch(int i, const Raw8& q) const {
     return beq2(q.w[i], kNegInfBf16x2) & ~beq2(w[i], kNegInfBf16x2);
+  }
+};
+
+// float16: converted exactly to fp32 (cvt.f32.f16); -inf is clamped after
+// the conversion, at the fp32 constant kLowest, far below any float16 value,
+// so that it cannot collide with the lowest finite float16 (-65504).
+template <>
+struct Raw8<__half> {
+  uint32_t w[4];
+  __device__ __forceinline__ void load(const __half* p) {
+    const uint4 u = ld_stream16(p);
+    w[0] = u.x; w[1] = u.y; w[2] = u.z; w[3] = u.w;
+  }
+  __device__ __forceinline__ void load_scalar(const __half* p, int valid) {
+    const unsigned short* q = reinterpret_cast<const unsigned short*>(p);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const uint32_t lo = 2 * i < valid ? __ldg(q + 2 * i) : 0xfc00u;
+      const uint32_t hi = 2 * i + 1 < valid ? __ldg(q + 2 * i + 1) : 0xfc00u;
+      w[i] = lo | (hi << 16);
+    }
+  }
+  __device__ __forceinline__ float max() const {
+    const uint32_t m = hmax2(hmax2(w[0], w[1]), hmax2(w[2], w[3]));
+    return fmaxf(h2f(m & 0xffffu), h2f(m >> 16));
+  }
+  __device__ __forceinline__ fp2 pair(int i) const { return pk(h2f(w[i] & 0xffffu), h2f(w[i] >> 16)); }
+  __device__ __forceinline__ fp2 pair_clamped(int i) const {
+    return pk(fmaxf(h2f(w[i] & 0xffffu), kLowest), fmaxf(h2f(w[i] >> 16), kLowest));
+  }
+  __device__ __forceinline__ fp2 pair_abs(int i) const {
+    const uint32_t a = w[i] & 0x7fff7fffu;
+    return pk(h2f(a & 0xffffu), h2f(a >> 16));
+  }
+  __device__ __forceinline__ uint32_t sign_lo(int i) const { return w[i] << 16; }
+  __device__ __forceinline__ uint32_t sign_hi(int i) const { return w[i]; }
+  __device__ __forceinline__ uint32_t mismatch(int i, const Raw8& q) const {
+    return heq2(q.w[i], kNegInfF16x2) & ~heq2(w[i], kNegInfF16x2);
   }
 };
 
@@ -473,6 +531,22 @@ struct Out8<__nv_bfloat16> {
   __device__ static void store1(__nv_bfloat16* p, float v) { *p = __float2bfloat16_rn(v); }
 };
 
+template <>
+struct Out8<__half> {
+  __device__ static void store(__half* p, const fp2 (&o)[4]) {
+    uint32_t w[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      float a, b;
+      upk(o[i], a, b);
+      __half2 h = __floats2half2_rn(a, b);
+      w[i] = *reinterpret_cast<uint32_t*>(&h);
+    }
+    st16(p, make_uint4(w[0], w[1], w[2], w[3]));
+  }
+  __device__ static void store1(__half* p, float v) { *p = __float2half_rn(v); }
+};
+
 // Stores vector `vec` of an output row (whole and aligned: vector stores;
 // otherwise element by element, columns < V only).
 template <class T>
@@ -499,6 +573,10 @@ __device__ __forceinline__ float load1<float>(const float* p) { return __ldg(p);
 template <>
 __device__ __forceinline__ float load1<__nv_bfloat16>(const __nv_bfloat16* p) {
   return __uint_as_float(static_cast<uint32_t>(__ldg(reinterpret_cast<const unsigned short*>(p))) << 16);
+}
+template <>
+__device__ __forceinline__ float load1<__half>(const __half* p) {
+  return h2f(__ldg(reinterpret_cast<const unsigned short*>(p)));
 }
 
 }  // namespace dev
