@@ -15,6 +15,8 @@
 // mixers", RL-Kernel PR #507).
 #pragma once
 
+#include <type_traits>
+
 #include "vls_device.cuh"
 
 namespace vls {
@@ -264,6 +266,25 @@ constexpr bool reads_two() { return OP == kFwdKl || (OP == kFwdFused && DIR != k
 template <int OP, int DIR>
 constexpr int fwd_unroll() { return reads_two<OP, DIR>() ? 2 : 4; }
 
+// Resident CTAs per SM the forward sweep is compiled for, at 256 threads.
+// Without an explicit minimum, ptxas sized these kernels by heuristics that
+// moved with the size of the argument struct (the bf16 entropy sweep went
+// from 32 to 38 registers, the KL sweep from 44 to 56), costing 5-8% of
+// bandwidth.  The bounds below keep the 16-bit sweeps at 32 registers (one
+// tensor), 40 (fused or softcapped one-tensor sweeps) and 48 (bf16 KL);
+// fp32 vectors hold twice the registers and get 64.
+template <class T, int OP, bool CAP, int DIR>
+constexpr int fwd_ctas_at_256() {
+  if (sizeof(T) == 4) return 4;
+  if (reads_two<OP, DIR>())
+    return (CAP || OP == kFwdFused || !std::is_same<T, __nv_bfloat16>::value) ? 4 : 5;
+  return (OP == kFwdFused || (CAP && OP != kFwdLogp)) ? 6 : 8;
+}
+template <class T, int OP, bool CAP, int DIR>
+constexpr int fwd_min_blocks() {
+  return fwd_ctas_at_256<T, OP, CAP, DIR>() * 256 / kFwdThreads > 0 ? fwd_ctas_at_256<T, OP, CAP, DIR>() * 256 / kFwdThreads : 1;
+}
+
 // ---- finalisation, shared with the vocabulary-parallel combine ----
 
 // log p of a target from its raw logit x and the row's (m, log S); NaN for
@@ -295,7 +316,7 @@ __device__ __forceinline__ void from_partial(const vls_partial& p, KlState& s) {
 }
 
 template <class T, int OP, bool CAP, int DIR = kFusedNoKl>
-__global__ void __launch_bounds__(kFwdThreads) row_fwd_kernel(const FwdArgs a) {
+__global__ void __launch_bounds__(kFwdThreads, (fwd_min_blocks<T, OP, CAP, DIR>())) row_fwd_kernel(const FwdArgs a) {
   using Acc = typename FwdAccOf<OP, T, CAP, DIR>::type;
   using S = typename Acc::State;
   constexpr int U = fwd_unroll<OP, DIR>();
