@@ -2,9 +2,10 @@
  * vls.h -- C ABI of libvls, row-wise vocabulary log-softmax statistics on
  * NVIDIA GB300 (sm_103a).
  *
- * A "row" is one token's logits over the vocabulary: N rows of V columns,
- * row r starting at element r*ld of the base pointer, the V columns of a row
- * contiguous (ld >= V; ld > V reads a slice such as logits[:, :V] in place).
+ * A "row" is one token's logits over the vocabulary: N rows of V contiguous
+ * columns.  Where each row starts is given by a vls_rows descriptor (below):
+ * one row stride, or two strides for a [B, T, V] tensor read as N = B*T rows,
+ * so that slices such as logits[:, :V] or logits[:, :-1, :] are read in place.
  * Every call computes in fp32 with one rounding at each store.  The softmax
  * statistics are taken in one read of the logits (online max and sum of
  * exponentials, "Add Triton kernels for vocab-parallel logprobs, entropy and
@@ -63,10 +64,25 @@ typedef enum { VLS_KL_REVERSE = 0, VLS_KL_FORWARD = 1 } vls_kl_dir;
  * adds a large common offset into an fp32 sum.  8 bytes per row. */
 typedef struct { float m; float log_s; } vls_rowstat;
 
+/* Row addressing of a logits operand: row r (0 <= r < N) starts
+ *     (r / group) * ld_group + (r % group) * ld
+ * elements after the operand's base pointer, and its V columns are
+ * contiguous.  A plain [N, V] matrix with row stride ld is {ld, 0, 0} (group
+ * 0: all rows form one group).  A [B, T, V] tensor with element strides
+ * (sB, sT, 1), read as N = B*T rows, is {sT, T, sB}: a slice such as
+ * x[:, :-1, :] keeps its two strides and is read in place where a single row
+ * stride would need a copy ("Add Triton kernels for vocab-parallel logprobs,
+ * entropy and KL", DeepSpeed PR #8838, review "Suggested change": rows
+ * addressed with up to two strides).  Requires ld >= V, group >= 0 and, when
+ * group > 0, ld_group >= V.  Rows may overlap: operands are only read.
+ * Gradients are always written as [N, V] contiguous. */
+typedef struct { int64_t ld; int64_t group; int64_t ld_group; } vls_rows;
+
 enum {
   VLS_OK = 0,
-  VLS_ERR_NULL = 1,     /* a required pointer is NULL (with N > 0)               */
-  VLS_ERR_SHAPE = 2,    /* N < 0, V < 1, ld < V, k < 1 or k > VLS_MAX_TOPK, n < 0,
+  VLS_ERR_NULL = 1,     /* a required pointer (or vls_rows) is NULL (with N > 0) */
+  VLS_ERR_SHAPE = 2,    /* N < 0, V < 1, a vls_rows field out of range, k < 1 or
+                           k > VLS_MAX_TOPK, n < 0,
                            R < 1, a shard outside [0, V_total)                   */
   VLS_ERR_DTYPE = 3,    /* dtype not a vls_dtype; gy dtype neither F32 nor dt     */
   VLS_ERR_CAP = 4,      /* cap NaN, infinite or negative (softcap calls: cap <= 0) */
@@ -105,7 +121,7 @@ int vls_softcap_bwd(const void* x, const void* gy, vls_dtype gy_dt, void* gx, in
  * An id is ignored when it equals ignore_index or lies outside [0, V); its
  * logp is exactly 0.  ids: int64 [N, k] contiguous.  stats: [N], written for
  * the backward.  1 <= k <= VLS_MAX_TOPK. */
-int vls_logp_fwd(const void* logits, int64_t ld, vls_dtype dt, int64_t N, int64_t V,
+int vls_logp_fwd(const void* logits, const vls_rows* rows, vls_dtype dt, int64_t N, int64_t V,
                  const int64_t* ids, int32_t k, int64_t ignore_index, float cap,
                  float* logp, vls_rowstat* stats, void* stream);
 
@@ -118,7 +134,7 @@ int vls_logp_fwd(const void* logits, int64_t ld, vls_dtype dt, int64_t N, int64_
  * written as exact zeros (RL-Kernel PR #495, Behavior changes).  dlogits:
  * [N, V] contiguous, dtype dt.  stats: as written by vls_logp_fwd with the
  * same logits, cap and dtype. */
-int vls_logp_bwd(const void* logits, int64_t ld, vls_dtype dt, int64_t N, int64_t V,
+int vls_logp_bwd(const void* logits, const vls_rows* rows, vls_dtype dt, int64_t N, int64_t V,
                  const int64_t* ids, int32_t k, int64_t ignore_index, float cap,
                  const float* g, const vls_rowstat* stats, void* dlogits, void* stream);
 
@@ -127,12 +143,12 @@ int vls_logp_bwd(const void* logits, int64_t ld, vls_dtype dt, int64_t N, int64_
 /* ------------------------------------------------------------------------ */
 
 /* H[r] = -sum_c p_r[c] log p_r[c] (fp32 [N]); stats [N] for the backward. */
-int vls_entropy_fwd(const void* logits, int64_t ld, vls_dtype dt, int64_t N, int64_t V,
+int vls_entropy_fwd(const void* logits, const vls_rows* rows, vls_dtype dt, int64_t N, int64_t V,
                     float cap, float* H, vls_rowstat* stats, void* stream);
 
 /* dlogits[r, c] = -g[r] * p_r[c] * (log p_r[c] + H[r]) * dz/dx, 0 on -inf
  * columns.  g, H: fp32 [N]; dlogits: [N, V] contiguous, dtype dt. */
-int vls_entropy_bwd(const void* logits, int64_t ld, vls_dtype dt, int64_t N, int64_t V,
+int vls_entropy_bwd(const void* logits, const vls_rows* rows, vls_dtype dt, int64_t N, int64_t V,
                     float cap, const float* g, const float* H, const vls_rowstat* stats,
                     void* dlogits, void* stream);
 
@@ -144,9 +160,9 @@ int vls_entropy_bwd(const void* logits, int64_t ld, vls_dtype dt, int64_t N, int
 /* kl[r] (fp32 [N]) between softmax(a_r) and softmax(b_r), in direction dir.
  * +inf when the first distribution supports a column that the second masks
  * (-inf logit), decided on the logits; NaN when a row of a or b is all -inf.
- * a: rows of stride lda, b: rows of stride ldb, same dtype.  stats_a, stats_b:
+ * a and b: same dtype, each addressed by its own vls_rows.  stats_a, stats_b:
  * [N] for the backward. */
-int vls_kl_fwd(const void* a, int64_t lda, const void* b, int64_t ldb, vls_dtype dt,
+int vls_kl_fwd(const void* a, const vls_rows* rows_a, const void* b, const vls_rows* rows_b, vls_dtype dt,
                int64_t N, int64_t V, vls_kl_dir dir, float cap, float* kl,
                vls_rowstat* stats_a, vls_rowstat* stats_b, void* stream);
 
@@ -155,7 +171,7 @@ int vls_kl_fwd(const void* a, int64_t lda, const void* b, int64_t ldb, vls_dtype
  *            0 where a = -inf, a NaN row when kl[r] is +inf or NaN;
  *   forward: da[r, c] = g (p_a[c] - p_b[c]) * dz/dx, a NaN row when kl[r] is NaN.
  * g, kl: fp32 [N]; da: [N, V] contiguous, dtype dt. */
-int vls_kl_bwd(const void* a, int64_t lda, const void* b, int64_t ldb, vls_dtype dt,
+int vls_kl_bwd(const void* a, const vls_rows* rows_a, const void* b, const vls_rows* rows_b, vls_dtype dt,
                int64_t N, int64_t V, vls_kl_dir dir, float cap, const float* g,
                const float* kl, const vls_rowstat* stats_a, const vls_rowstat* stats_b,
                void* da, void* stream);
@@ -172,7 +188,8 @@ int vls_kl_bwd(const void* a, int64_t lda, const void* b, int64_t ldb, vls_dtype
  * logp [N, k] (NULL to skip; needs ids), H [N] (NULL to skip), kl [N] in
  * direction dir (NULL to skip).  stats_a [N] always; stats_b [N] with kl.
  * Each output equals the corresponding single call's. */
-int vls_fused_fwd(const void* a, int64_t lda, const void* b, int64_t ldb, vls_dtype dt, int64_t N, int64_t V,
+int vls_fused_fwd(const void* a, const vls_rows* rows_a, const void* b, const vls_rows* rows_b,
+                  vls_dtype dt, int64_t N, int64_t V,
                   const int64_t* ids, int32_t k, int64_t ignore_index, vls_kl_dir dir, float cap,
                   float* logp, float* H, float* kl, vls_rowstat* stats_a, vls_rowstat* stats_b,
                   void* stream);
@@ -182,7 +199,8 @@ int vls_fused_fwd(const void* a, int64_t lda, const void* b, int64_t ldb, vls_dt
  * and cast once.  A term is left out when its upstream pointer is NULL
  * (g_logp needs ids; g_H needs H; g_kl needs b, kl and stats_b).  da: [N, V]
  * contiguous, dtype dt. */
-int vls_fused_bwd(const void* a, int64_t lda, const void* b, int64_t ldb, vls_dtype dt, int64_t N, int64_t V,
+int vls_fused_bwd(const void* a, const vls_rows* rows_a, const void* b, const vls_rows* rows_b,
+                  vls_dtype dt, int64_t N, int64_t V,
                   const int64_t* ids, int32_t k, int64_t ignore_index, vls_kl_dir dir, float cap,
                   const float* g_logp, const float* g_H, const float* g_kl, const float* H, const float* kl,
                   const vls_rowstat* stats_a, const vls_rowstat* stats_b, void* da, void* stream);
@@ -202,7 +220,8 @@ int vls_fused_bwd(const void* a, int64_t lda, const void* b, int64_t ldb, vls_dt
 /* writes the same outputs and per-row statistics as the unsharded forward.  */
 /* The backward then runs per shard: vls_entropy_bwd / vls_kl_bwd unchanged  */
 /* on the shard with the combined statistics, vls_logp_bwd_shard for logp.   */
-/* V_shard = 0 (an empty shard) is allowed and gives the identity partial.   */
+/* V_shard = 0 (an empty shard) is allowed and gives the identity partial;   */
+/* its logits pointer and vls_rows may then be NULL.                         */
 /* Results are deterministic for a fixed sharding; they match the unsharded  */
 /* call up to rounding (the reduction tree differs).                         */
 /* ------------------------------------------------------------------------ */
@@ -220,7 +239,7 @@ typedef struct {
  * id that is valid against V_total and lies in this shard, the raw (uncapped)
  * logit of that column, else 0 -- summed over the ranks it is the target's
  * logit (exactly one rank owns a valid id). */
-int vls_logp_partial(const void* logits, int64_t ld, vls_dtype dt, int64_t N, int64_t V_shard,
+int vls_logp_partial(const void* logits, const vls_rows* rows, vls_dtype dt, int64_t N, int64_t V_shard,
                      int64_t vocab_offset, int64_t V_total, const int64_t* ids, int32_t k,
                      int64_t ignore_index, float cap, vls_partial* part, float* zt, void* stream);
 
@@ -233,20 +252,20 @@ int vls_logp_combine(const vls_partial* parts, const float* zt, int32_t R, int64
  * V_total); the one-hot terms land in this shard's columns only, while G
  * sums the upstream gradients of every valid id.  dlogits: [N, V_shard]
  * contiguous.  stats: from vls_logp_combine. */
-int vls_logp_bwd_shard(const void* logits, int64_t ld, vls_dtype dt, int64_t N, int64_t V_shard,
+int vls_logp_bwd_shard(const void* logits, const vls_rows* rows, vls_dtype dt, int64_t N, int64_t V_shard,
                        int64_t vocab_offset, int64_t V_total, const int64_t* ids, int32_t k,
                        int64_t ignore_index, float cap, const float* g, const vls_rowstat* stats,
                        void* dlogits, void* stream);
 
-int vls_entropy_partial(const void* logits, int64_t ld, vls_dtype dt, int64_t N, int64_t V_shard, float cap,
-                        vls_partial* part, void* stream);
+int vls_entropy_partial(const void* logits, const vls_rows* rows, vls_dtype dt, int64_t N, int64_t V_shard,
+                        float cap, vls_partial* part, void* stream);
 
 /* Folds parts [R, N] into H [N] and stats [N]. */
 int vls_entropy_combine(const vls_partial* parts, int32_t R, int64_t N, float* H, vls_rowstat* stats,
                         void* stream);
 
-int vls_kl_partial(const void* a, int64_t lda, const void* b, int64_t ldb, vls_dtype dt, int64_t N,
-                   int64_t V_shard, vls_kl_dir dir, float cap, vls_partial* part, void* stream);
+int vls_kl_partial(const void* a, const vls_rows* rows_a, const void* b, const vls_rows* rows_b,
+                   vls_dtype dt, int64_t N, int64_t V_shard, vls_kl_dir dir, float cap, vls_partial* part, void* stream);
 
 /* Folds parts [R, N] into kl [N], stats_a [N], stats_b [N] (dir as in the partials). */
 int vls_kl_combine(const vls_partial* parts, int32_t R, int64_t N, vls_kl_dir dir, float* kl,

@@ -17,6 +17,7 @@ HEADER = os.path.join(ROOT, "include", "vls.h")
 OK, NULL, SHAPE, DTYPE, CAP, DEVICE, LAUNCH, ARG = range(8)
 F32, BF16 = 0, 1
 P = 0x1000   # a non-NULL pointer value; never dereferenced (errors precede any access)
+R = _lib.rows
 
 
 @pytest.fixture(scope="module")
@@ -53,33 +54,53 @@ def test_status_strings(lib):
 
 def test_logp_argument_errors(lib):
     f = lib.vls_logp_fwd
-    #        logits ld  dt    N  V  ids k  ign  cap  logp stats stream
-    assert f(None, 10, BF16, 4, 10, None, 1, -100, 0.0, None, None, None) == NULL
-    assert f(P, 10, BF16, -1, 10, P, 1, -100, 0.0, P, P, None) == SHAPE
-    assert f(P, 10, BF16, 4, 0, P, 1, -100, 0.0, P, P, None) == SHAPE
-    assert f(P, 9, BF16, 4, 10, P, 1, -100, 0.0, P, P, None) == SHAPE       # ld < V
-    assert f(P, 10, BF16, 4, 10, P, 0, -100, 0.0, P, P, None) == SHAPE      # k < 1
-    assert f(P, 10, BF16, 4, 10, P, _lib.VLS_MAX_TOPK + 1, -100, 0.0, P, P, None) == SHAPE
-    assert f(P, 10, 7, 4, 10, P, 1, -100, 0.0, P, P, None) == DTYPE
+    #        logits rows dt    N  V  ids k  ign  cap  logp stats stream
+    assert f(None, R(10), BF16, 4, 10, None, 1, -100, 0.0, None, None, None) == NULL
+    assert f(P, R(10), BF16, -1, 10, P, 1, -100, 0.0, P, P, None) == SHAPE
+    assert f(P, R(10), BF16, 4, 0, P, 1, -100, 0.0, P, P, None) == SHAPE
+    assert f(P, R(9), BF16, 4, 10, P, 1, -100, 0.0, P, P, None) == SHAPE       # ld < V
+    assert f(P, R(10), BF16, 4, 10, P, 0, -100, 0.0, P, P, None) == SHAPE      # k < 1
+    assert f(P, R(10), BF16, 4, 10, P, _lib.VLS_MAX_TOPK + 1, -100, 0.0, P, P, None) == SHAPE
+    assert f(P, R(10), 7, 4, 10, P, 1, -100, 0.0, P, P, None) == DTYPE
     for bad in (math.nan, math.inf, -1.0):
-        assert f(P, 10, BF16, 4, 10, P, 1, -100, bad, P, P, None) == CAP
-    assert f(None, 10, BF16, 0, 10, None, 1, -100, 0.0, None, None, None) == OK   # empty: no launch
+        assert f(P, R(10), BF16, 4, 10, P, 1, -100, bad, P, P, None) == CAP
+    assert f(None, None, BF16, 0, 10, None, 1, -100, 0.0, None, None, None) == OK   # empty: no launch
     g = lib.vls_logp_bwd
-    assert g(P, 10, BF16, 4, 10, P, 1, -100, 0.0, None, P, P, None) == NULL
-    assert g(P, 10, F32, 4, 10, P, 1, -100, -3.0, P, P, P, None) == CAP
+    assert g(P, R(10), BF16, 4, 10, P, 1, -100, 0.0, None, P, P, None) == NULL
+    assert g(P, R(10), F32, 4, 10, P, 1, -100, -3.0, P, P, P, None) == CAP
 
 
 def test_entropy_kl_argument_errors(lib):
-    assert lib.vls_entropy_fwd(P, 10, F32, 4, 10, 0.0, None, P, None) == NULL
-    assert lib.vls_entropy_bwd(P, 5, F32, 4, 10, 0.0, P, P, P, P, None) == SHAPE
-    assert lib.vls_entropy_fwd(None, 10, F32, 0, 10, 0.0, None, None, None) == OK
+    assert lib.vls_entropy_fwd(P, R(10), F32, 4, 10, 0.0, None, P, None) == NULL
+    assert lib.vls_entropy_bwd(P, R(5), F32, 4, 10, 0.0, P, P, P, P, None) == SHAPE
+    assert lib.vls_entropy_fwd(None, None, F32, 0, 10, 0.0, None, None, None) == OK
     kf = lib.vls_kl_fwd
-    assert kf(P, 10, P, 9, BF16, 4, 10, 0, 0.0, P, P, P, None) == SHAPE          # ldb < V
-    assert kf(P, 10, P, 10, BF16, 4, 10, 2, 0.0, P, P, P, None) == ARG           # bad direction
-    assert kf(P, 10, None, 10, BF16, 4, 10, 0, 0.0, P, P, P, None) == NULL
-    assert kf(P, 10, P, 10, 3, 4, 10, 0, 0.0, P, P, P, None) == DTYPE
+    assert kf(P, R(10), P, R(9), BF16, 4, 10, 0, 0.0, P, P, P, None) == SHAPE          # b: ld < V
+    assert kf(P, R(10), P, R(10), BF16, 4, 10, 2, 0.0, P, P, P, None) == ARG           # bad direction
+    assert kf(P, R(10), None, R(10), BF16, 4, 10, 0, 0.0, P, P, P, None) == NULL
+    assert kf(P, R(10), P, R(10), 3, 4, 10, 0, 0.0, P, P, P, None) == DTYPE
     kb = lib.vls_kl_bwd
-    assert kb(P, 10, P, 10, BF16, 4, 10, 1, math.inf, P, P, P, P, P, None) == CAP
+    assert kb(P, R(10), P, R(10), BF16, 4, 10, 1, math.inf, P, P, P, P, P, None) == CAP
+
+
+def test_row_layout_errors(lib):
+    f = lib.vls_entropy_fwd
+    assert f(P, None, F32, 4, 10, 0.0, P, P, None) == NULL                 # descriptor missing
+    assert f(P, R(10, -1, 40), F32, 4, 10, 0.0, P, P, None) == SHAPE       # negative group
+    assert f(P, R(10, 2, 9), F32, 4, 10, 0.0, P, P, None) == SHAPE         # group stride < V
+    assert f(P, R(9, 2, 40), F32, 4, 10, 0.0, P, P, None) == SHAPE         # row stride < V
+    kf = lib.vls_kl_fwd
+    assert kf(P, R(10, 2, 40), P, R(10, 3, 5), BF16, 4, 10, 0, 0.0, P, P, P, None) == SHAPE
+    assert kf(P, R(10), P, None, BF16, 4, 10, 0, 0.0, P, P, P, None) == NULL
+    # an empty vocabulary shard needs neither logits nor a descriptor
+    assert lib.vls_entropy_partial(None, None, BF16, 4, 0, 0.0, None, None) == NULL   # part missing
+
+
+def test_rows_struct_matches_header():
+    text = open(HEADER).read()
+    assert re.search(r"typedef struct \{ int64_t ld; int64_t group; int64_t ld_group; \} vls_rows;", text)
+    assert ctypes.sizeof(_lib.VlsRows) == 24
+    assert [f[0] for f in _lib.VlsRows._fields_] == ["ld", "group", "ld_group"]
 
 
 def test_softcap_argument_errors(lib):
@@ -104,6 +125,45 @@ def test_binding_rejects_bad_layouts():
         B.vls_entropy_fwd(torch.zeros((6, 4)).t())          # strided vocabulary dimension
     with pytest.raises(ValueError):
         B.vls_entropy_fwd(torch.zeros((3,)))                # not [N, V]
+    with pytest.raises(ValueError):
+        B.vls_entropy_fwd(torch.zeros((2, 6)).expand(3, 2, 6))   # broadcast rows overlap
+
+
+def test_binding_row_descriptors():
+    """[N, V] and [B, T, V] views map to the C ABI's vls_rows; a view whose
+    leading dims collapse to one stride uses the single-stride form."""
+    import torch
+
+    from vocab_log_softmax_gb300 import binding as B
+
+    def desc(t):
+        n, v, r = B._rows(t)
+        return n, v, (r.ld, r.group, r.ld_group)
+
+    x = torch.zeros((4, 9, 16))
+    assert desc(x) == (36, 16, (16, 0, 0))                  # contiguous: one stride
+    assert desc(x[:, :-1]) == (32, 16, (16, 8, 144))        # shifted sequence: two strides
+    assert desc(x[:, 1:, :8]) == (32, 8, (16, 8, 144))      # and a vocabulary slice
+    assert desc(x[1:2, :-1]) == (8, 16, (16, 0, 0))         # one batch entry
+    assert desc(x[:, 2:3]) == (4, 16, (144, 0, 0))          # one position per batch entry
+    assert desc(x.reshape(36, 16)[::2]) == (18, 16, (32, 0, 0))
+    assert desc(torch.zeros((1, 5))) == (1, 5, (5, 0, 0))
+
+
+def test_as_rows_keeps_addressable_views():
+    import torch
+
+    import vocab_log_softmax_gb300 as V
+    base = torch.zeros((4, 9, 16))
+    for view in (base, base[:, :-1], base[:, 1:, :8], base[..., :8]):
+        rows = V._as_rows(view)
+        assert rows.data_ptr() == view.data_ptr() and rows.dim() in (2, 3)
+    y = V._as_rows(torch.zeros((2, 3, 4, 16))[:, :, :-1])   # [2, 3, 3, 16]: leading dims merge to [6, 3]
+    assert tuple(y.shape) == (6, 3, 16) and y.stride() == (64, 16, 1)
+    t = V._as_rows(torch.zeros((16, 4)).t())               # strided vocabulary: copied
+    assert t.is_contiguous()
+    e = V._as_rows(torch.zeros((1, 16)).expand(5, 16))      # broadcast rows: copied
+    assert e.is_contiguous() and e.shape == (5, 16)
 
 
 @pytest.mark.gpu
@@ -112,7 +172,7 @@ def test_host_pointer_is_rejected(lib):
     host = torch.zeros((4, 10))
     out = torch.empty(4, device="cuda")
     st = torch.empty((4, 2), device="cuda")
-    r = lib.vls_entropy_fwd(host.data_ptr(), 10, F32, 4, 10, 0.0, out.data_ptr(), st.data_ptr(), None)
+    r = lib.vls_entropy_fwd(host.data_ptr(), R(10), F32, 4, 10, 0.0, out.data_ptr(), st.data_ptr(), None)
     assert r == DEVICE
 
 

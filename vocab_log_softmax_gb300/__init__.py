@@ -36,17 +36,36 @@ from .binding import (  # noqa: F401
 __all__ = ["logprobs", "entropy", "kl", "softcap", "stats"]
 
 
+def _addressable(rows: torch.Tensor) -> bool:
+    """Whether the kernels can read a [N, V] or [B, T, V] view in place: every
+    row stride at least V (broadcast rows, for one, are not)."""
+    v = rows.shape[-1]
+    return all(size <= 1 or stride >= v for size, stride in zip(rows.shape[:-1], rows.stride()[:-1]))
+
+
 def _as_rows(x: torch.Tensor) -> torch.Tensor:
-    """[..., V] -> [N, V] with a contiguous vocabulary dimension (a view when possible)."""
+    """[..., V] -> a [N, V] view, or a [B, T, V] view read with two row strides
+    (a slice such as ``x[:, :-1]`` stays in place); layouts the kernels cannot
+    address, such as a strided vocabulary dimension, are copied first."""
     if x.dim() == 0:
         raise ValueError("expected at least one dimension (the vocabulary)")
     v = x.shape[-1]
-    if x.dim() >= 2 and v > 1 and x.stride(-1) != 1:
-        x = x.contiguous()      # layouts the kernels cannot address are copied first
-    rows = x.reshape(-1, v)
-    if rows.shape[0] > 1 and v > 1 and rows.stride(1) != 1:
-        rows = rows.contiguous()
-    return rows
+    if x.dim() == 1:
+        x = x.reshape(1, v)
+    if v > 1 and x.stride(-1) != 1:
+        x = x.contiguous()
+    try:
+        rows = x.view(-1, v)
+    except RuntimeError:
+        try:
+            rows = x.view(-1, x.shape[-2], v)
+        except RuntimeError:
+            rows = x.reshape(-1, v)
+    return rows if _addressable(rows) else rows.contiguous()
+
+
+def _nrows(rows: torch.Tensor) -> int:
+    return rows.shape[:-1].numel()
 
 
 def _ids_rows(ids: torch.Tensor, n: int) -> torch.Tensor:
@@ -71,7 +90,7 @@ class _Logprobs(torch.autograd.Function):
     @staticmethod
     def forward(ctx, logits, ids, ignore_index, cap):
         rows = _as_rows(logits)
-        ids2 = _ids_rows(ids, rows.shape[0])
+        ids2 = _ids_rows(ids, _nrows(rows))
         logp, stats = vls_logp_fwd(rows, ids2, ignore_index, cap)
         ctx.save_for_backward(rows, ids2, stats)
         ctx.meta = (ignore_index, cap, logits.shape)
@@ -143,7 +162,7 @@ class _Stats(torch.autograd.Function):
         b = _as_rows(reference.detach()) if reference is not None else None
         ids2 = None
         if ids is not None:
-            ids2 = _ids_rows(ids, a.shape[0])
+            ids2 = _ids_rows(ids, _nrows(a))
         out = vls_fused_fwd(a, b, ids2, logp=ids is not None, entropy=True, direction=direction,
                             ignore_index=ignore_index, cap=cap)
         ctx.save_for_backward(a, b, ids2, out["stats_a"], out.get("stats_b"), out["H"], out.get("kl"))

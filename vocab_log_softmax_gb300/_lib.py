@@ -36,25 +36,39 @@ _i32 = ctypes.c_int32
 _int = ctypes.c_int
 _f = ctypes.c_float
 
+
+class VlsRows(ctypes.Structure):
+    """vls_rows: row r of an operand starts (r // group) * ld_group + (r % group) * ld
+    elements after its base pointer (group 0: r * ld)."""
+
+    _fields_ = [("ld", ctypes.c_int64), ("group", ctypes.c_int64), ("ld_group", ctypes.c_int64)]
+
+
+def rows(ld: int, group: int = 0, ld_group: int = 0) -> VlsRows:
+    return VlsRows(ld, group, ld_group)
+
+
+_r = ctypes.POINTER(VlsRows)
+
 # name -> argument types, in the order of include/vls.h
 SIGNATURES = {
     "vls_softcap_fwd": [_p, _p, _i64, _int, _f, _p],
     "vls_softcap_bwd": [_p, _p, _int, _p, _i64, _int, _f, _p],
-    "vls_logp_fwd": [_p, _i64, _int, _i64, _i64, _p, _i32, _i64, _f, _p, _p, _p],
-    "vls_logp_bwd": [_p, _i64, _int, _i64, _i64, _p, _i32, _i64, _f, _p, _p, _p, _p],
-    "vls_entropy_fwd": [_p, _i64, _int, _i64, _i64, _f, _p, _p, _p],
-    "vls_entropy_bwd": [_p, _i64, _int, _i64, _i64, _f, _p, _p, _p, _p, _p],
-    "vls_kl_fwd": [_p, _i64, _p, _i64, _int, _i64, _i64, _int, _f, _p, _p, _p, _p],
-    "vls_kl_bwd": [_p, _i64, _p, _i64, _int, _i64, _i64, _int, _f, _p, _p, _p, _p, _p, _p],
-    "vls_fused_fwd": [_p, _i64, _p, _i64, _int, _i64, _i64, _p, _i32, _i64, _int, _f, _p, _p, _p, _p, _p, _p],
-    "vls_fused_bwd": [_p, _i64, _p, _i64, _int, _i64, _i64, _p, _i32, _i64, _int, _f, _p, _p, _p, _p, _p, _p, _p,
+    "vls_logp_fwd": [_p, _r, _int, _i64, _i64, _p, _i32, _i64, _f, _p, _p, _p],
+    "vls_logp_bwd": [_p, _r, _int, _i64, _i64, _p, _i32, _i64, _f, _p, _p, _p, _p],
+    "vls_entropy_fwd": [_p, _r, _int, _i64, _i64, _f, _p, _p, _p],
+    "vls_entropy_bwd": [_p, _r, _int, _i64, _i64, _f, _p, _p, _p, _p, _p],
+    "vls_kl_fwd": [_p, _r, _p, _r, _int, _i64, _i64, _int, _f, _p, _p, _p, _p],
+    "vls_kl_bwd": [_p, _r, _p, _r, _int, _i64, _i64, _int, _f, _p, _p, _p, _p, _p, _p],
+    "vls_fused_fwd": [_p, _r, _p, _r, _int, _i64, _i64, _p, _i32, _i64, _int, _f, _p, _p, _p, _p, _p, _p],
+    "vls_fused_bwd": [_p, _r, _p, _r, _int, _i64, _i64, _p, _i32, _i64, _int, _f, _p, _p, _p, _p, _p, _p, _p,
                       _p, _p],
-    "vls_logp_partial": [_p, _i64, _int, _i64, _i64, _i64, _i64, _p, _i32, _i64, _f, _p, _p, _p],
+    "vls_logp_partial": [_p, _r, _int, _i64, _i64, _i64, _i64, _p, _i32, _i64, _f, _p, _p, _p],
     "vls_logp_combine": [_p, _p, _i32, _i64, _p, _i32, _i64, _i64, _f, _p, _p, _p],
-    "vls_logp_bwd_shard": [_p, _i64, _int, _i64, _i64, _i64, _i64, _p, _i32, _i64, _f, _p, _p, _p, _p],
-    "vls_entropy_partial": [_p, _i64, _int, _i64, _i64, _f, _p, _p],
+    "vls_logp_bwd_shard": [_p, _r, _int, _i64, _i64, _i64, _i64, _p, _i32, _i64, _f, _p, _p, _p, _p],
+    "vls_entropy_partial": [_p, _r, _int, _i64, _i64, _f, _p, _p],
     "vls_entropy_combine": [_p, _i32, _i64, _p, _p, _p],
-    "vls_kl_partial": [_p, _i64, _p, _i64, _int, _i64, _i64, _int, _f, _p, _p],
+    "vls_kl_partial": [_p, _r, _p, _r, _int, _i64, _i64, _int, _f, _p, _p],
     "vls_kl_combine": [_p, _i32, _i64, _int, _p, _p, _p, _p],
     "vls_status_string": [_int],
     "vls_version": [],

@@ -5,9 +5,11 @@ Each function takes CUDA tensors, allocates its outputs with torch when they
 are not given, and passes raw pointers, sizes and the current CUDA stream of
 the inputs' device to libvls.  No arithmetic of the method happens here.
 
-Row layout: a logits tensor is [N, V] (or [V] for one row) whose last
-dimension is contiguous; its row stride may exceed V (a slice such as
-``logits[:, :-1]`` is read in place).  Gradients are returned contiguous.
+Row layout: a logits tensor is [N, V], or [B, T, V] read as N = B*T rows,
+with a contiguous last dimension.  Its row strides may exceed V, so slices
+such as ``logits[:, :V]`` or ``logits[:, :-1, :]`` are read in place through
+the C ABI's two-stride row descriptor (vls_rows).  Gradients are returned
+contiguous [N, V].
 """
 
 from __future__ import annotations
@@ -27,16 +29,29 @@ def _dtype(t: torch.Tensor) -> int:
         raise TypeError(f"libvls supports float32, bfloat16 and float16 tensors, not {t.dtype}") from None
 
 
-def _rows(t: torch.Tensor) -> tuple[int, int, int]:
-    """(N, V, row stride) of a 2-D tensor with a contiguous last dimension."""
-    if t.dim() != 2:
-        raise ValueError(f"expected a [N, V] tensor, got shape {tuple(t.shape)}")
-    n, v = t.shape
-    if v > 1 and t.stride(1) != 1:
+def _rows(t: torch.Tensor) -> tuple[int, int, _lib.VlsRows]:
+    """(N, V, vls_rows) of a [N, V] tensor, or of a [B, T, V] tensor read as
+    N = B*T rows with two row strides; the last dimension is contiguous."""
+    if t.dim() not in (2, 3):
+        raise ValueError(f"expected a [N, V] or [B, T, V] tensor, got shape {tuple(t.shape)}")
+    v = t.shape[-1]
+    if v > 1 and t.stride(-1) != 1:
         raise ValueError("the vocabulary dimension must be contiguous (stride 1)")
-    if n > 1 and t.stride(0) < v:
+    if t.dim() == 2:
+        n = t.shape[0]
+        ld = t.stride(0) if n > 1 else v
+        if ld < v:
+            raise ValueError("rows overlap (row stride smaller than V)")
+        return n, v, _lib.rows(ld)
+    b, tt = t.shape[0], t.shape[1]
+    if b == 1 or tt == 1:  # one leading dim of size 1: one row stride
+        return _rows(t[0] if b == 1 else t[:, 0])
+    ld, ldg = t.stride(1), t.stride(0)
+    if ld < v or ldg < v:
         raise ValueError("rows overlap (row stride smaller than V)")
-    return n, v, (t.stride(0) if n > 1 else v)
+    if ldg == tt * ld:  # the leading dims collapse
+        return b * tt, v, _lib.rows(ld)
+    return b * tt, v, _lib.rows(ld, tt, ldg)
 
 
 def _ids2d(ids: torch.Tensor, n: int) -> torch.Tensor:
@@ -90,14 +105,14 @@ def vls_logp_fwd(logits: torch.Tensor, ids: torch.Tensor, ignore_index: int = -1
                  *, logp=None, stats=None, stream=None) -> tuple[torch.Tensor, torch.Tensor]:
     """Returns (logp [N, k] float32, stats [N, 2] float32)."""
     lib = _lib.load()
-    n, v, ld = _rows(logits)
+    n, v, lay = _rows(logits)
     ids = _ids2d(ids, n)
     if ids.dtype != torch.int64 or not ids.is_contiguous():
         raise ValueError("ids must be a contiguous int64 [N, k] tensor")
     k = ids.shape[1]
     logp = torch.empty((n, k), dtype=torch.float32, device=logits.device) if logp is None else logp
     stats = _stats(n, logits.device, stats)
-    st = lib.vls_logp_fwd(_ptr(logits), ld, _dtype(logits), n, v, _ptr(ids), k, int(ignore_index),
+    st = lib.vls_logp_fwd(_ptr(logits), lay, _dtype(logits), n, v, _ptr(ids), k, int(ignore_index),
                           float(cap), _ptr(logp), _ptr(stats), _stream(logits, stream))
     _lib.check("vls_logp_fwd", st)
     return logp, stats
@@ -107,7 +122,7 @@ def vls_logp_bwd(logits: torch.Tensor, ids: torch.Tensor, g: torch.Tensor, stats
                  ignore_index: int = -100, cap: float = 0.0, *, dlogits=None,
                  stream=None) -> torch.Tensor:
     lib = _lib.load()
-    n, v, ld = _rows(logits)
+    n, v, lay = _rows(logits)
     ids = _ids2d(ids, n)
     k = ids.shape[1]
     g = g.reshape(n, k)
@@ -115,7 +130,7 @@ def vls_logp_bwd(logits: torch.Tensor, ids: torch.Tensor, g: torch.Tensor, stats
         raise ValueError("g must be a contiguous float32 [N, k] tensor")
     if dlogits is None:
         dlogits = torch.empty((n, v), dtype=logits.dtype, device=logits.device)
-    st = lib.vls_logp_bwd(_ptr(logits), ld, _dtype(logits), n, v, _ptr(ids), k, int(ignore_index),
+    st = lib.vls_logp_bwd(_ptr(logits), lay, _dtype(logits), n, v, _ptr(ids), k, int(ignore_index),
                           float(cap), _ptr(g), _ptr(stats), _ptr(dlogits), _stream(logits, stream))
     _lib.check("vls_logp_bwd", st)
     return dlogits
@@ -124,10 +139,10 @@ def vls_logp_bwd(logits: torch.Tensor, ids: torch.Tensor, g: torch.Tensor, stats
 def vls_entropy_fwd(logits: torch.Tensor, cap: float = 0.0, *, H=None, stats=None,
                     stream=None) -> tuple[torch.Tensor, torch.Tensor]:
     lib = _lib.load()
-    n, v, ld = _rows(logits)
+    n, v, lay = _rows(logits)
     H = torch.empty((n,), dtype=torch.float32, device=logits.device) if H is None else H
     stats = _stats(n, logits.device, stats)
-    st = lib.vls_entropy_fwd(_ptr(logits), ld, _dtype(logits), n, v, float(cap), _ptr(H), _ptr(stats),
+    st = lib.vls_entropy_fwd(_ptr(logits), lay, _dtype(logits), n, v, float(cap), _ptr(H), _ptr(stats),
                              _stream(logits, stream))
     _lib.check("vls_entropy_fwd", st)
     return H, stats
@@ -136,12 +151,12 @@ def vls_entropy_fwd(logits: torch.Tensor, cap: float = 0.0, *, H=None, stats=Non
 def vls_entropy_bwd(logits: torch.Tensor, g: torch.Tensor, H: torch.Tensor, stats: torch.Tensor,
                     cap: float = 0.0, *, dlogits=None, stream=None) -> torch.Tensor:
     lib = _lib.load()
-    n, v, ld = _rows(logits)
+    n, v, lay = _rows(logits)
     if g.dtype != torch.float32 or not g.is_contiguous():
         raise ValueError("g must be a contiguous float32 [N] tensor")
     if dlogits is None:
         dlogits = torch.empty((n, v), dtype=logits.dtype, device=logits.device)
-    st = lib.vls_entropy_bwd(_ptr(logits), ld, _dtype(logits), n, v, float(cap), _ptr(g), _ptr(H),
+    st = lib.vls_entropy_bwd(_ptr(logits), lay, _dtype(logits), n, v, float(cap), _ptr(g), _ptr(H),
                              _ptr(stats), _ptr(dlogits), _stream(logits, stream))
     _lib.check("vls_entropy_bwd", st)
     return dlogits
@@ -152,8 +167,8 @@ def vls_kl_fwd(a: torch.Tensor, b: torch.Tensor, direction: str = "reverse", cap
                stream=None) -> tuple[torch.Tensor, torch.Tensor, torch.Tensor]:
     """Returns (kl [N], stats_a [N, 2], stats_b [N, 2])."""
     lib = _lib.load()
-    n, v, lda = _rows(a)
-    nb, vb, ldb = _rows(b)
+    n, v, lay_a = _rows(a)
+    nb, vb, lay_b = _rows(b)
     if (nb, vb) != (n, v):
         raise ValueError("a and b must have the same shape")
     if a.dtype != b.dtype:
@@ -161,7 +176,7 @@ def vls_kl_fwd(a: torch.Tensor, b: torch.Tensor, direction: str = "reverse", cap
     kl = torch.empty((n,), dtype=torch.float32, device=a.device) if kl is None else kl
     stats_a = _stats(n, a.device, stats_a)
     stats_b = _stats(n, a.device, stats_b)
-    st = lib.vls_kl_fwd(_ptr(a), lda, _ptr(b), ldb, _dtype(a), n, v, _DIR[direction], float(cap), _ptr(kl),
+    st = lib.vls_kl_fwd(_ptr(a), lay_a, _ptr(b), lay_b, _dtype(a), n, v, _DIR[direction], float(cap), _ptr(kl),
                         _ptr(stats_a), _ptr(stats_b), _stream(a, stream))
     _lib.check("vls_kl_fwd", st)
     return kl, stats_a, stats_b
@@ -171,13 +186,13 @@ def vls_kl_bwd(a: torch.Tensor, b: torch.Tensor, g: torch.Tensor, kl: torch.Tens
                stats_b: torch.Tensor, direction: str = "reverse", cap: float = 0.0, *, da=None,
                stream=None) -> torch.Tensor:
     lib = _lib.load()
-    n, v, lda = _rows(a)
-    _, _, ldb = _rows(b)
+    n, v, lay_a = _rows(a)
+    _, _, lay_b = _rows(b)
     if g.dtype != torch.float32 or not g.is_contiguous():
         raise ValueError("g must be a contiguous float32 [N] tensor")
     if da is None:
         da = torch.empty((n, v), dtype=a.dtype, device=a.device)
-    st = lib.vls_kl_bwd(_ptr(a), lda, _ptr(b), ldb, _dtype(a), n, v, _DIR[direction], float(cap), _ptr(g),
+    st = lib.vls_kl_bwd(_ptr(a), lay_a, _ptr(b), lay_b, _dtype(a), n, v, _DIR[direction], float(cap), _ptr(g),
                         _ptr(kl), _ptr(stats_a), _ptr(stats_b), _ptr(da), _stream(a, stream))
     _lib.check("vls_kl_bwd", st)
     return da
@@ -194,11 +209,11 @@ def vls_fused_fwd(a: torch.Tensor, b: torch.Tensor | None = None, ids: torch.Ten
     dict with 'logp' [N, k] (when ids are given and logp), 'H' [N] (entropy),
     'kl' [N] (when b is given), 'stats_a' and 'stats_b' [N, 2]."""
     lib = _lib.load()
-    n, v, lda = _rows(a)
+    n, v, lay_a = _rows(a)
     want_kl = (b is not None) if kl is None else bool(kl)
-    ldb = 0
+    lay_b = None
     if want_kl:
-        nb, vb, ldb = _rows(b)
+        nb, vb, lay_b = _rows(b)
         if (nb, vb) != (n, v) or b.dtype != a.dtype:
             raise ValueError("a and b must have the same shape and dtype")
     f32 = dict(dtype=torch.float32, device=a.device)
@@ -215,7 +230,7 @@ def vls_fused_fwd(a: torch.Tensor, b: torch.Tensor | None = None, ids: torch.Ten
     if want_kl:
         out["kl"] = torch.empty((n,), **f32)
         out["stats_b"] = torch.empty((n, 2), **f32)
-    st = lib.vls_fused_fwd(_ptr(a), lda, _ptr(b) if want_kl else None, ldb, _dtype(a), n, v,
+    st = lib.vls_fused_fwd(_ptr(a), lay_a, _ptr(b) if want_kl else None, lay_b, _dtype(a), n, v,
                            _ptr(ids) if k else None, k, int(ignore_index), _DIR[direction], float(cap),
                            _ptr(out.get("logp")), _ptr(out.get("H")), _ptr(out.get("kl")), _ptr(out["stats_a"]),
                            _ptr(out.get("stats_b")), _stream(a, stream))
@@ -230,8 +245,8 @@ def vls_fused_bwd(a: torch.Tensor, fwd: dict, b: torch.Tensor | None = None, ids
     """Gradient w.r.t. a of sum(g_logp * logp) + sum(g_H * H) + sum(g_kl * KL);
     `fwd` is vls_fused_fwd's result; absent gradients leave their term out."""
     lib = _lib.load()
-    n, v, lda = _rows(a)
-    ldb = _rows(b)[2] if g_kl is not None else 0
+    n, v, lay_a = _rows(a)
+    lay_b = _rows(b)[2] if g_kl is not None else None
     k = 1
     if g_logp is not None:
         ids = _ids2d(ids, n)
@@ -242,7 +257,7 @@ def vls_fused_bwd(a: torch.Tensor, fwd: dict, b: torch.Tensor | None = None, ids
             raise ValueError("upstream gradients must be contiguous float32")
     if da is None:
         da = torch.empty((n, v), dtype=a.dtype, device=a.device)
-    st = lib.vls_fused_bwd(_ptr(a), lda, _ptr(b) if g_kl is not None else None, ldb, _dtype(a), n, v,
+    st = lib.vls_fused_bwd(_ptr(a), lay_a, _ptr(b) if g_kl is not None else None, lay_b, _dtype(a), n, v,
                            _ptr(ids) if g_logp is not None else None, k, int(ignore_index), _DIR[direction],
                            float(cap), _ptr(g_logp), _ptr(g_H), _ptr(g_kl),
                            _ptr(fwd.get("H")) if g_H is not None else None,
@@ -266,13 +281,12 @@ def _partials(shape, device, out=None) -> torch.Tensor:
     return torch.empty((*shape, PARTIAL_FIELDS), dtype=torch.float32, device=device)
 
 
-def _shard_rows(t: torch.Tensor) -> tuple[int, int, int]:
-    """Like _rows, but a shard may have 0 columns."""
-    if t.dim() != 2:
-        raise ValueError(f"expected a [N, V_shard] tensor, got shape {tuple(t.shape)}")
-    n, v = t.shape
-    if v == 0:
-        return n, 0, 0
+def _shard_rows(t: torch.Tensor) -> tuple[int, int, _lib.VlsRows | None]:
+    """Like _rows, but a shard may have 0 columns (no descriptor then)."""
+    if t.dim() not in (2, 3):
+        raise ValueError(f"expected a [N, V_shard] or [B, T, V_shard] tensor, got shape {tuple(t.shape)}")
+    if t.shape[-1] == 0:
+        return t.shape[:-1].numel(), 0, None
     return _rows(t)
 
 
@@ -285,14 +299,14 @@ def vls_logp_partial(logits: torch.Tensor, ids: torch.Tensor, vocab_offset: int,
                      stream=None) -> tuple[torch.Tensor, torch.Tensor]:
     """Returns (part [N, 6], zt [N, k]) for the shard [vocab_offset, vocab_offset + V_shard)."""
     lib = _lib.load()
-    n, v, ld = _shard_rows(logits)
+    n, v, lay = _shard_rows(logits)
     ids = _ids2d(ids, n)
     if ids.dtype != torch.int64 or not ids.is_contiguous():
         raise ValueError("ids must be a contiguous int64 [N, k] tensor")
     k = ids.shape[1]
     part = _partials((n,), ids.device, part)
     zt = torch.empty((n, k), dtype=torch.float32, device=ids.device) if zt is None else zt
-    st = lib.vls_logp_partial(_ptr_or_none(logits), ld, _dtype(logits), n, v, int(vocab_offset), int(vocab_total),
+    st = lib.vls_logp_partial(_ptr_or_none(logits), lay, _dtype(logits), n, v, int(vocab_offset), int(vocab_total),
                               _ptr(ids), k, int(ignore_index), float(cap), _ptr(part), _ptr(zt),
                               _stream(ids, stream))
     _lib.check("vls_logp_partial", st)
@@ -321,7 +335,7 @@ def vls_logp_bwd_shard(logits: torch.Tensor, ids: torch.Tensor, g: torch.Tensor,
                        vocab_offset: int, vocab_total: int, ignore_index: int = -100, cap: float = 0.0, *,
                        dlogits=None, stream=None) -> torch.Tensor:
     lib = _lib.load()
-    n, v, ld = _shard_rows(logits)
+    n, v, lay = _shard_rows(logits)
     ids = _ids2d(ids, n)
     k = ids.shape[1]
     g = g.reshape(n, k)
@@ -329,7 +343,7 @@ def vls_logp_bwd_shard(logits: torch.Tensor, ids: torch.Tensor, g: torch.Tensor,
         raise ValueError("g must be a contiguous float32 [N, k] tensor")
     if dlogits is None:
         dlogits = torch.empty((n, v), dtype=logits.dtype, device=ids.device)
-    st = lib.vls_logp_bwd_shard(_ptr_or_none(logits), ld, _dtype(logits), n, v, int(vocab_offset),
+    st = lib.vls_logp_bwd_shard(_ptr_or_none(logits), lay, _dtype(logits), n, v, int(vocab_offset),
                                 int(vocab_total), _ptr(ids), k, int(ignore_index), float(cap), _ptr(g),
                                 _ptr(stats), _ptr_or_none(dlogits), _stream(ids, stream))
     _lib.check("vls_logp_bwd_shard", st)
@@ -338,9 +352,9 @@ def vls_logp_bwd_shard(logits: torch.Tensor, ids: torch.Tensor, g: torch.Tensor,
 
 def vls_entropy_partial(logits: torch.Tensor, cap: float = 0.0, *, part=None, stream=None) -> torch.Tensor:
     lib = _lib.load()
-    n, v, ld = _shard_rows(logits)
+    n, v, lay = _shard_rows(logits)
     part = _partials((n,), logits.device, part)
-    st = lib.vls_entropy_partial(_ptr_or_none(logits), ld, _dtype(logits), n, v, float(cap), _ptr(part),
+    st = lib.vls_entropy_partial(_ptr_or_none(logits), lay, _dtype(logits), n, v, float(cap), _ptr(part),
                                  _stream(part, stream))
     _lib.check("vls_entropy_partial", st)
     return part
@@ -359,12 +373,12 @@ def vls_entropy_combine(parts: torch.Tensor, *, H=None, stats=None, stream=None)
 def vls_kl_partial(a: torch.Tensor, b: torch.Tensor, direction: str = "reverse", cap: float = 0.0, *, part=None,
                    stream=None) -> torch.Tensor:
     lib = _lib.load()
-    n, v, lda = _shard_rows(a)
-    _, vb, ldb = _shard_rows(b)
+    n, v, lay_a = _shard_rows(a)
+    _, vb, lay_b = _shard_rows(b)
     if vb != v or a.dtype != b.dtype:
         raise ValueError("a and b shards must have the same shape and dtype")
     part = _partials((n,), a.device, part)
-    st = lib.vls_kl_partial(_ptr_or_none(a), lda, _ptr_or_none(b), ldb, _dtype(a), n, v, _DIR[direction],
+    st = lib.vls_kl_partial(_ptr_or_none(a), lay_a, _ptr_or_none(b), lay_b, _dtype(a), n, v, _DIR[direction],
                             float(cap), _ptr(part), _stream(part, stream))
     _lib.check("vls_kl_partial", st)
     return part

@@ -135,9 +135,25 @@ int launch_status(cudaError_t e) {
   return e == cudaSuccess ? VLS_OK : VLS_ERR_LAUNCH;
 }
 
-int check_rows(int64_t N, int64_t V, int64_t ld) {
-  if (N < 0 || V < 1 || ld < V) return VLS_ERR_SHAPE;
+int check_rows(int64_t N, int64_t V) {
+  if (N < 0 || V < 1) return VLS_ERR_SHAPE;
   return VLS_OK;
+}
+
+// A row descriptor of an operand with V columns: NULL, a row stride below V,
+// a negative group or (with groups) a group stride below V are rejected.
+int check_layout(const vls_rows* r, int64_t V) {
+  if (!r) return VLS_ERR_NULL;
+  if (r->ld < V || r->group < 0 || (r->group > 0 && r->ld_group < V)) return VLS_ERR_SHAPE;
+  return VLS_OK;
+}
+
+// The kernels' form of a checked descriptor: one group (group 0, or a group
+// of at least 2^31 - 1 rows) becomes group 2^31 - 1, above every row index.
+constexpr int64_t kOneGroup = 0x7fffffff;
+vls_rows kernel_rows(const vls_rows& r) {
+  if (r.group == 0 || r.group >= kOneGroup) return vls_rows{r.ld, kOneGroup, 0};
+  return r;
 }
 
 FwdArgs fwd_args(int64_t N, int64_t V, float cap) {
@@ -147,6 +163,7 @@ FwdArgs fwd_args(int64_t N, int64_t V, float cap) {
   a.vocab = V;
   a.cap = cap;
   a.rcap = cap > 0.0f ? 1.0f / cap : 0.0f;
+  a.rx = a.ry = vls_rows{0, kOneGroup, 0};  // until the call sets its operands
   a.vocab_offset = 0;
   a.vocab_total = V;
   fwd_geometry(V, &a.cluster, &a.vec_per_cta);
@@ -160,6 +177,7 @@ BwdArgs bwd_args(int64_t N, int64_t V, int32_t k, float cap) {
   a.vocab = V;
   a.cap = cap;
   a.rcap = cap > 0.0f ? 1.0f / cap : 0.0f;
+  a.rx = a.ry = vls_rows{0, kOneGroup, 0};  // until the call sets its operands
   a.k = k;
   a.vocab_offset = 0;
   a.vocab_total = V;
@@ -168,8 +186,8 @@ BwdArgs bwd_args(int64_t N, int64_t V, int32_t k, float cap) {
 }
 
 // A shard [offset, offset + V_shard) of a V_total-column vocabulary.
-int check_shard(int64_t N, int64_t V_shard, int64_t ld, int64_t offset, int64_t V_total) {
-  if (N < 0 || V_shard < 0 || ld < V_shard || V_total < 1 || offset < 0 || offset + V_shard > V_total)
+int check_shard(int64_t N, int64_t V_shard, int64_t offset, int64_t V_total) {
+  if (N < 0 || V_shard < 0 || V_total < 1 || offset < 0 || offset + V_shard > V_total)
     return VLS_ERR_SHAPE;
   return VLS_OK;
 }
@@ -187,10 +205,11 @@ const char* vls_status_string(int status) {
   switch (status) {
     case VLS_OK: return "VLS_OK";
     case VLS_ERR_NULL: return "VLS_ERR_NULL: a required pointer is NULL";
-    case VLS_ERR_SHAPE: return "VLS_ERR_SHAPE: bad N, V, ld, k or n";
+    case VLS_ERR_SHAPE: return "VLS_ERR_SHAPE: bad N, V, row layout, k or n";
     case VLS_ERR_DTYPE: return "VLS_ERR_DTYPE: unsupported dtype";
     case VLS_ERR_CAP: return "VLS_ERR_CAP: cap must be finite and non-negative (softcap calls: positive)";
-    case VLS_ERR_DEVICE: return "VLS_ERR_DEVICE: pointer not device memory, or pointers/stream on different devices";
+    case VLS_ERR_DEVICE:
+      return "VLS_ERR_DEVICE: pointer not device memory, or pointers/stream on different devices";
     case VLS_ERR_LAUNCH: return "VLS_ERR_LAUNCH: CUDA launch failed";
     case VLS_ERR_ARG: return "VLS_ERR_ARG: bad argument";
     default: return "VLS_ERR_UNKNOWN";
@@ -228,14 +247,16 @@ int vls_softcap_bwd(const void* x, const void* gy, vls_dtype gy_dt, void* gx, in
   return launch_status(launch_softcap_bwd(dt, a, static_cast<cudaStream_t>(stream)));
 }
 
-int vls_logp_fwd(const void* logits, int64_t ld, vls_dtype dt, int64_t N, int64_t V, const int64_t* ids,
-                 int32_t k, int64_t ignore_index, float cap, float* logp, vls_rowstat* stats,
+int vls_logp_fwd(const void* logits, const vls_rows* rows, vls_dtype dt, int64_t N, int64_t V,
+                 const int64_t* ids, int32_t k, int64_t ignore_index, float cap, float* logp,
+                 vls_rowstat* stats,
                  void* stream) {
-  if (int e = check_rows(N, V, ld)) return e;
+  if (int e = check_rows(N, V)) return e;
   if (k < 1 || k > VLS_MAX_TOPK) return VLS_ERR_SHAPE;
   if (!dtype_ok(dt)) return VLS_ERR_DTYPE;
   if (int e = check_row_cap(cap)) return e;
   if (N == 0) return VLS_OK;
+  if (int e = check_layout(rows, V)) return e;
   if (!logits || !ids || !logp || !stats) return VLS_ERR_NULL;
   FwdArgs a = fwd_args(N, V, cap);
   if (N * a.cluster > kMaxGrid) return VLS_ERR_SHAPE;
@@ -244,7 +265,7 @@ int vls_logp_fwd(const void* logits, int64_t ld, vls_dtype dt, int64_t N, int64_
   DeviceGuard guard;
   if (int e = guard.enter(dev)) return e;
   a.x = logits;
-  a.ldx = ld;
+  a.rx = kernel_rows(*rows);
   a.ids = ids;
   a.k = k;
   a.ignore_index = ignore_index;
@@ -253,14 +274,16 @@ int vls_logp_fwd(const void* logits, int64_t ld, vls_dtype dt, int64_t N, int64_
   return launch_status(launch_fwd_logp(dt, cap > 0.0f, a, static_cast<cudaStream_t>(stream)));
 }
 
-int vls_logp_bwd(const void* logits, int64_t ld, vls_dtype dt, int64_t N, int64_t V, const int64_t* ids,
-                 int32_t k, int64_t ignore_index, float cap, const float* g, const vls_rowstat* stats,
+int vls_logp_bwd(const void* logits, const vls_rows* rows, vls_dtype dt, int64_t N, int64_t V,
+                 const int64_t* ids, int32_t k, int64_t ignore_index, float cap, const float* g,
+                 const vls_rowstat* stats,
                  void* dlogits, void* stream) {
-  if (int e = check_rows(N, V, ld)) return e;
+  if (int e = check_rows(N, V)) return e;
   if (k < 1 || k > VLS_MAX_TOPK) return VLS_ERR_SHAPE;
   if (!dtype_ok(dt)) return VLS_ERR_DTYPE;
   if (int e = check_row_cap(cap)) return e;
   if (N == 0) return VLS_OK;
+  if (int e = check_layout(rows, V)) return e;
   if (!logits || !ids || !g || !stats || !dlogits) return VLS_ERR_NULL;
   BwdArgs a = bwd_args(N, V, k, cap);
   if (N * a.chunks > kMaxGrid) return VLS_ERR_SHAPE;
@@ -269,7 +292,7 @@ int vls_logp_bwd(const void* logits, int64_t ld, vls_dtype dt, int64_t N, int64_
   DeviceGuard guard;
   if (int e = guard.enter(dev)) return e;
   a.x = logits;
-  a.ldx = ld;
+  a.rx = kernel_rows(*rows);
   a.ids = ids;
   a.ignore_index = ignore_index;
   a.g = g;
@@ -278,12 +301,13 @@ int vls_logp_bwd(const void* logits, int64_t ld, vls_dtype dt, int64_t N, int64_
   return launch_status(launch_bwd_logp(dt, cap > 0.0f, a, static_cast<cudaStream_t>(stream)));
 }
 
-int vls_entropy_fwd(const void* logits, int64_t ld, vls_dtype dt, int64_t N, int64_t V, float cap,
+int vls_entropy_fwd(const void* logits, const vls_rows* rows, vls_dtype dt, int64_t N, int64_t V, float cap,
                     float* H, vls_rowstat* stats, void* stream) {
-  if (int e = check_rows(N, V, ld)) return e;
+  if (int e = check_rows(N, V)) return e;
   if (!dtype_ok(dt)) return VLS_ERR_DTYPE;
   if (int e = check_row_cap(cap)) return e;
   if (N == 0) return VLS_OK;
+  if (int e = check_layout(rows, V)) return e;
   if (!logits || !H || !stats) return VLS_ERR_NULL;
   FwdArgs a = fwd_args(N, V, cap);
   if (N * a.cluster > kMaxGrid) return VLS_ERR_SHAPE;
@@ -292,19 +316,20 @@ int vls_entropy_fwd(const void* logits, int64_t ld, vls_dtype dt, int64_t N, int
   DeviceGuard guard;
   if (int e = guard.enter(dev)) return e;
   a.x = logits;
-  a.ldx = ld;
+  a.rx = kernel_rows(*rows);
   a.out = H;
   a.stats_x = stats;
   return launch_status(launch_fwd_entropy(dt, cap > 0.0f, a, static_cast<cudaStream_t>(stream)));
 }
 
-int vls_entropy_bwd(const void* logits, int64_t ld, vls_dtype dt, int64_t N, int64_t V, float cap,
+int vls_entropy_bwd(const void* logits, const vls_rows* rows, vls_dtype dt, int64_t N, int64_t V, float cap,
                     const float* g, const float* H, const vls_rowstat* stats, void* dlogits,
                     void* stream) {
-  if (int e = check_rows(N, V, ld)) return e;
+  if (int e = check_rows(N, V)) return e;
   if (!dtype_ok(dt)) return VLS_ERR_DTYPE;
   if (int e = check_row_cap(cap)) return e;
   if (N == 0) return VLS_OK;
+  if (int e = check_layout(rows, V)) return e;
   if (!logits || !g || !H || !stats || !dlogits) return VLS_ERR_NULL;
   BwdArgs a = bwd_args(N, V, 1, cap);
   if (N * a.chunks > kMaxGrid) return VLS_ERR_SHAPE;
@@ -313,7 +338,7 @@ int vls_entropy_bwd(const void* logits, int64_t ld, vls_dtype dt, int64_t N, int
   DeviceGuard guard;
   if (int e = guard.enter(dev)) return e;
   a.x = logits;
-  a.ldx = ld;
+  a.rx = kernel_rows(*rows);
   a.g = g;
   a.fout = H;
   a.stats_x = stats;
@@ -321,15 +346,17 @@ int vls_entropy_bwd(const void* logits, int64_t ld, vls_dtype dt, int64_t N, int
   return launch_status(launch_bwd_entropy(dt, cap > 0.0f, a, static_cast<cudaStream_t>(stream)));
 }
 
-int vls_kl_fwd(const void* pa, int64_t lda, const void* pb, int64_t ldb, vls_dtype dt, int64_t N, int64_t V,
+int vls_kl_fwd(const void* pa, const vls_rows* rows_a, const void* pb, const vls_rows* rows_b,
+               vls_dtype dt, int64_t N, int64_t V,
                vls_kl_dir dir, float cap, float* kl, vls_rowstat* stats_a, vls_rowstat* stats_b,
                void* stream) {
-  if (int e = check_rows(N, V, lda)) return e;
-  if (ldb < V) return VLS_ERR_SHAPE;
+  if (int e = check_rows(N, V)) return e;
   if (!dtype_ok(dt)) return VLS_ERR_DTYPE;
   if (dir != VLS_KL_REVERSE && dir != VLS_KL_FORWARD) return VLS_ERR_ARG;
   if (int e = check_row_cap(cap)) return e;
   if (N == 0) return VLS_OK;
+  if (int e = check_layout(rows_a, V)) return e;
+  if (int e = check_layout(rows_b, V)) return e;
   if (!pa || !pb || !kl || !stats_a || !stats_b) return VLS_ERR_NULL;
   FwdArgs a = fwd_args(N, V, cap);
   if (N * a.cluster > kMaxGrid) return VLS_ERR_SHAPE;
@@ -340,24 +367,26 @@ int vls_kl_fwd(const void* pa, int64_t lda, const void* pb, int64_t ldb, vls_dty
   // the sweep's first argument is the distribution the expectation is over
   const bool rev = dir == VLS_KL_REVERSE;
   a.x = rev ? pa : pb;
-  a.ldx = rev ? lda : ldb;
+  a.rx = kernel_rows(rev ? *rows_a : *rows_b);
   a.y = rev ? pb : pa;
-  a.ldy = rev ? ldb : lda;
+  a.ry = kernel_rows(rev ? *rows_b : *rows_a);
   a.stats_x = rev ? stats_a : stats_b;
   a.stats_y = rev ? stats_b : stats_a;
   a.out = kl;
   return launch_status(launch_fwd_kl(dt, cap > 0.0f, a, static_cast<cudaStream_t>(stream)));
 }
 
-int vls_kl_bwd(const void* pa, int64_t lda, const void* pb, int64_t ldb, vls_dtype dt, int64_t N, int64_t V,
+int vls_kl_bwd(const void* pa, const vls_rows* rows_a, const void* pb, const vls_rows* rows_b,
+               vls_dtype dt, int64_t N, int64_t V,
                vls_kl_dir dir, float cap, const float* g, const float* kl, const vls_rowstat* stats_a,
                const vls_rowstat* stats_b, void* da, void* stream) {
-  if (int e = check_rows(N, V, lda)) return e;
-  if (ldb < V) return VLS_ERR_SHAPE;
+  if (int e = check_rows(N, V)) return e;
   if (!dtype_ok(dt)) return VLS_ERR_DTYPE;
   if (dir != VLS_KL_REVERSE && dir != VLS_KL_FORWARD) return VLS_ERR_ARG;
   if (int e = check_row_cap(cap)) return e;
   if (N == 0) return VLS_OK;
+  if (int e = check_layout(rows_a, V)) return e;
+  if (int e = check_layout(rows_b, V)) return e;
   if (!pa || !pb || !g || !kl || !stats_a || !stats_b || !da) return VLS_ERR_NULL;
   BwdArgs a = bwd_args(N, V, 1, cap);
   if (N * a.chunks > kMaxGrid) return VLS_ERR_SHAPE;
@@ -366,9 +395,9 @@ int vls_kl_bwd(const void* pa, int64_t lda, const void* pb, int64_t ldb, vls_dty
   DeviceGuard guard;
   if (int e = guard.enter(dev)) return e;
   a.x = pa;
-  a.ldx = lda;
+  a.rx = kernel_rows(*rows_a);
   a.y = pb;
-  a.ldy = ldb;
+  a.ry = kernel_rows(*rows_b);
   a.g = g;
   a.fout = kl;
   a.stats_x = stats_a;
@@ -383,17 +412,21 @@ int vls_kl_bwd(const void* pa, int64_t lda, const void* pb, int64_t ldb, vls_dty
 // fused statistics
 // ---------------------------------------------------------------------------
 
-int vls_fused_fwd(const void* pa, int64_t lda, const void* pb, int64_t ldb, vls_dtype dt, int64_t N, int64_t V,
+int vls_fused_fwd(const void* pa, const vls_rows* rows_a, const void* pb, const vls_rows* rows_b,
+                  vls_dtype dt, int64_t N, int64_t V,
                   const int64_t* ids, int32_t k, int64_t ignore_index, vls_kl_dir dir, float cap, float* logp,
                   float* H, float* kl, vls_rowstat* stats_a, vls_rowstat* stats_b, void* stream) {
-  if (int e = check_rows(N, V, lda)) return e;
+  if (int e = check_rows(N, V)) return e;
   const bool want_kl = kl != nullptr;
-  if (want_kl && ldb < V) return VLS_ERR_SHAPE;
   if (logp && (k < 1 || k > VLS_MAX_TOPK)) return VLS_ERR_SHAPE;
   if (!dtype_ok(dt)) return VLS_ERR_DTYPE;
   if (want_kl && dir != VLS_KL_REVERSE && dir != VLS_KL_FORWARD) return VLS_ERR_ARG;
   if (int e = check_row_cap(cap)) return e;
   if (N == 0) return VLS_OK;
+  if (int e = check_layout(rows_a, V)) return e;
+  if (want_kl) {
+    if (int e = check_layout(rows_b, V)) return e;
+  }
   if (!pa || !stats_a || (logp && !ids) || (want_kl && (!pb || !stats_b))) return VLS_ERR_NULL;
   FwdArgs a = fwd_args(N, V, cap);
   if (N * a.cluster > kMaxGrid) return VLS_ERR_SHAPE;
@@ -405,9 +438,9 @@ int vls_fused_fwd(const void* pa, int64_t lda, const void* pb, int64_t ldb, vls_
   DeviceGuard guard;
   if (int e = guard.enter(dev)) return e;
   a.x = pa;
-  a.ldx = lda;
+  a.rx = kernel_rows(*rows_a);
   a.y = want_kl ? pb : nullptr;
-  a.ldy = want_kl ? ldb : 0;
+  if (want_kl) a.ry = kernel_rows(*rows_b);
   a.ids = ids;
   a.k = logp ? k : 0;
   a.ignore_index = ignore_index;
@@ -420,19 +453,23 @@ int vls_fused_fwd(const void* pa, int64_t lda, const void* pb, int64_t ldb, vls_
   return launch_status(launch_fwd_fused(fk, dt, cap > 0.0f, a, static_cast<cudaStream_t>(stream)));
 }
 
-int vls_fused_bwd(const void* pa, int64_t lda, const void* pb, int64_t ldb, vls_dtype dt, int64_t N, int64_t V,
+int vls_fused_bwd(const void* pa, const vls_rows* rows_a, const void* pb, const vls_rows* rows_b,
+                  vls_dtype dt, int64_t N, int64_t V,
                   const int64_t* ids, int32_t k, int64_t ignore_index, vls_kl_dir dir, float cap,
                   const float* g_logp, const float* g_H, const float* g_kl, const float* H, const float* kl,
                   const vls_rowstat* stats_a, const vls_rowstat* stats_b, void* da, void* stream) {
-  if (int e = check_rows(N, V, lda)) return e;
+  if (int e = check_rows(N, V)) return e;
   const bool want_kl = g_kl != nullptr;
-  if (want_kl && ldb < V) return VLS_ERR_SHAPE;
   if (g_logp && (k < 1 || k > VLS_MAX_TOPK)) return VLS_ERR_SHAPE;
   if (!dtype_ok(dt)) return VLS_ERR_DTYPE;
   if (!g_logp && !g_H && !g_kl) return VLS_ERR_ARG;
   if (want_kl && dir != VLS_KL_REVERSE && dir != VLS_KL_FORWARD) return VLS_ERR_ARG;
   if (int e = check_row_cap(cap)) return e;
   if (N == 0) return VLS_OK;
+  if (int e = check_layout(rows_a, V)) return e;
+  if (want_kl) {
+    if (int e = check_layout(rows_b, V)) return e;
+  }
   if (!pa || !stats_a || !da || (g_logp && !ids) || (g_H && !H) || (want_kl && (!pb || !kl || !stats_b)))
     return VLS_ERR_NULL;
   BwdArgs a = bwd_args(N, V, g_logp ? k : 1, cap);
@@ -445,9 +482,9 @@ int vls_fused_bwd(const void* pa, int64_t lda, const void* pb, int64_t ldb, vls_
   DeviceGuard guard;
   if (int e = guard.enter(dev)) return e;
   a.x = pa;
-  a.ldx = lda;
+  a.rx = kernel_rows(*rows_a);
   a.y = want_kl ? pb : nullptr;
-  a.ldy = want_kl ? ldb : 0;
+  if (want_kl) a.ry = kernel_rows(*rows_b);
   a.ids = ids;
   a.k = g_logp ? k : 1;
   a.ignore_index = ignore_index;
@@ -467,14 +504,17 @@ int vls_fused_bwd(const void* pa, int64_t lda, const void* pb, int64_t ldb, vls_
 // vocabulary-parallel split phase
 // ---------------------------------------------------------------------------
 
-int vls_logp_partial(const void* logits, int64_t ld, vls_dtype dt, int64_t N, int64_t V_shard,
+int vls_logp_partial(const void* logits, const vls_rows* rows, vls_dtype dt, int64_t N, int64_t V_shard,
                      int64_t vocab_offset, int64_t V_total, const int64_t* ids, int32_t k,
                      int64_t ignore_index, float cap, vls_partial* part, float* zt, void* stream) {
-  if (int e = check_shard(N, V_shard, ld, vocab_offset, V_total)) return e;
+  if (int e = check_shard(N, V_shard, vocab_offset, V_total)) return e;
   if (k < 1 || k > VLS_MAX_TOPK) return VLS_ERR_SHAPE;
   if (!dtype_ok(dt)) return VLS_ERR_DTYPE;
   if (int e = check_row_cap(cap)) return e;
   if (N == 0) return VLS_OK;
+  if (V_shard > 0) {
+    if (int e = check_layout(rows, V_shard)) return e;
+  }
   if ((!logits && V_shard > 0) || !ids || !part || !zt) return VLS_ERR_NULL;
   FwdArgs a = fwd_args(N, V_shard, cap);
   if (N * a.cluster > kMaxGrid) return VLS_ERR_SHAPE;
@@ -483,7 +523,7 @@ int vls_logp_partial(const void* logits, int64_t ld, vls_dtype dt, int64_t N, in
   DeviceGuard guard;
   if (int e = guard.enter(dev)) return e;
   a.x = logits;
-  a.ldx = ld;
+  if (V_shard > 0) a.rx = kernel_rows(*rows);
   a.ids = ids;
   a.k = k;
   a.ignore_index = ignore_index;
@@ -521,15 +561,16 @@ int vls_logp_combine(const vls_partial* parts, const float* zt, int32_t R, int64
   return launch_status(launch_combine(kFwdLogp, a, static_cast<cudaStream_t>(stream)));
 }
 
-int vls_logp_bwd_shard(const void* logits, int64_t ld, vls_dtype dt, int64_t N, int64_t V_shard,
+int vls_logp_bwd_shard(const void* logits, const vls_rows* rows, vls_dtype dt, int64_t N, int64_t V_shard,
                        int64_t vocab_offset, int64_t V_total, const int64_t* ids, int32_t k,
                        int64_t ignore_index, float cap, const float* g, const vls_rowstat* stats,
                        void* dlogits, void* stream) {
-  if (int e = check_shard(N, V_shard, ld, vocab_offset, V_total)) return e;
+  if (int e = check_shard(N, V_shard, vocab_offset, V_total)) return e;
   if (k < 1 || k > VLS_MAX_TOPK) return VLS_ERR_SHAPE;
   if (!dtype_ok(dt)) return VLS_ERR_DTYPE;
   if (int e = check_row_cap(cap)) return e;
   if (N == 0 || V_shard == 0) return VLS_OK;
+  if (int e = check_layout(rows, V_shard)) return e;
   if (!logits || !ids || !g || !stats || !dlogits) return VLS_ERR_NULL;
   BwdArgs a = bwd_args(N, V_shard, k, cap);
   if (N * a.chunks > kMaxGrid) return VLS_ERR_SHAPE;
@@ -538,7 +579,7 @@ int vls_logp_bwd_shard(const void* logits, int64_t ld, vls_dtype dt, int64_t N, 
   DeviceGuard guard;
   if (int e = guard.enter(dev)) return e;
   a.x = logits;
-  a.ldx = ld;
+  a.rx = kernel_rows(*rows);
   a.ids = ids;
   a.ignore_index = ignore_index;
   a.g = g;
@@ -549,12 +590,16 @@ int vls_logp_bwd_shard(const void* logits, int64_t ld, vls_dtype dt, int64_t N, 
   return launch_status(launch_bwd_logp(dt, cap > 0.0f, a, static_cast<cudaStream_t>(stream)));
 }
 
-int vls_entropy_partial(const void* logits, int64_t ld, vls_dtype dt, int64_t N, int64_t V_shard, float cap,
+int vls_entropy_partial(const void* logits, const vls_rows* rows, vls_dtype dt, int64_t N, int64_t V_shard,
+                        float cap,
                         vls_partial* part, void* stream) {
-  if (N < 0 || V_shard < 0 || ld < V_shard) return VLS_ERR_SHAPE;
+  if (N < 0 || V_shard < 0) return VLS_ERR_SHAPE;
   if (!dtype_ok(dt)) return VLS_ERR_DTYPE;
   if (int e = check_row_cap(cap)) return e;
   if (N == 0) return VLS_OK;
+  if (V_shard > 0) {
+    if (int e = check_layout(rows, V_shard)) return e;
+  }
   if ((!logits && V_shard > 0) || !part) return VLS_ERR_NULL;
   FwdArgs a = fwd_args(N, V_shard, cap);
   if (N * a.cluster > kMaxGrid) return VLS_ERR_SHAPE;
@@ -563,7 +608,7 @@ int vls_entropy_partial(const void* logits, int64_t ld, vls_dtype dt, int64_t N,
   DeviceGuard guard;
   if (int e = guard.enter(dev)) return e;
   a.x = logits;
-  a.ldx = ld;
+  if (V_shard > 0) a.rx = kernel_rows(*rows);
   a.part = part;
   return launch_status(launch_fwd_entropy(dt, cap > 0.0f, a, static_cast<cudaStream_t>(stream)));
 }
@@ -587,13 +632,18 @@ int vls_entropy_combine(const vls_partial* parts, int32_t R, int64_t N, float* H
   return launch_status(launch_combine(kFwdEntropy, a, static_cast<cudaStream_t>(stream)));
 }
 
-int vls_kl_partial(const void* pa, int64_t lda, const void* pb, int64_t ldb, vls_dtype dt, int64_t N,
+int vls_kl_partial(const void* pa, const vls_rows* rows_a, const void* pb, const vls_rows* rows_b,
+                   vls_dtype dt, int64_t N,
                    int64_t V_shard, vls_kl_dir dir, float cap, vls_partial* part, void* stream) {
-  if (N < 0 || V_shard < 0 || lda < V_shard || ldb < V_shard) return VLS_ERR_SHAPE;
+  if (N < 0 || V_shard < 0) return VLS_ERR_SHAPE;
   if (!dtype_ok(dt)) return VLS_ERR_DTYPE;
   if (dir != VLS_KL_REVERSE && dir != VLS_KL_FORWARD) return VLS_ERR_ARG;
   if (int e = check_row_cap(cap)) return e;
   if (N == 0) return VLS_OK;
+  if (V_shard > 0) {
+    if (int e = check_layout(rows_a, V_shard)) return e;
+    if (int e = check_layout(rows_b, V_shard)) return e;
+  }
   if (((!pa || !pb) && V_shard > 0) || !part) return VLS_ERR_NULL;
   FwdArgs a = fwd_args(N, V_shard, cap);
   if (N * a.cluster > kMaxGrid) return VLS_ERR_SHAPE;
@@ -604,9 +654,11 @@ int vls_kl_partial(const void* pa, int64_t lda, const void* pb, int64_t ldb, vls
   if (int e = guard.enter(dev)) return e;
   const bool rev = dir == VLS_KL_REVERSE;
   a.x = rev ? pa : pb;
-  a.ldx = rev ? lda : ldb;
   a.y = rev ? pb : pa;
-  a.ldy = rev ? ldb : lda;
+  if (V_shard > 0) {
+    a.rx = kernel_rows(rev ? *rows_a : *rows_b);
+    a.ry = kernel_rows(rev ? *rows_b : *rows_a);
+  }
   a.part = part;
   return launch_status(launch_fwd_kl(dt, cap > 0.0f, a, static_cast<cudaStream_t>(stream)));
 }

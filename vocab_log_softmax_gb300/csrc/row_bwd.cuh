@@ -233,8 +233,8 @@ __global__ void __launch_bounds__(kRowThreads, CAP ? kCapMinBlocks : 6) row_bwd_
   const int64_t nvec = (V + 7) >> 3;
   const int64_t vb = static_cast<int64_t>(q) * a.vec_per_cta;
   const int64_t ve = min(vb + a.vec_per_cta, nvec);
-  const T* xr = static_cast<const T*>(a.x) + row * a.ldx;
-  const T* yr = KL ? static_cast<const T*>(a.y) + row * a.ldy : xr;
+  const T* xr = row_ptr<T>(a.x, a.rx, row);
+  const T* yr = KL ? row_ptr<T>(a.y, a.ry, row) : xr;
   T* dr = static_cast<T*>(a.dx) + row * V;
   const bool al = aligned16(xr) && aligned16(dr) && aligned16(yr);
   const CapK K = cap_consts(CAP ? a.cap : 1.0f);

@@ -282,7 +282,8 @@ constexpr int fwd_ctas_at_256() {
 }
 template <class T, int OP, bool CAP, int DIR>
 constexpr int fwd_min_blocks() {
-  return fwd_ctas_at_256<T, OP, CAP, DIR>() * 256 / kFwdThreads > 0 ? fwd_ctas_at_256<T, OP, CAP, DIR>() * 256 / kFwdThreads : 1;
+  constexpr int b = fwd_ctas_at_256<T, OP, CAP, DIR>() * 256 / kFwdThreads;
+  return b > 0 ? b : 1;
 }
 
 // ---- finalisation, shared with the vocabulary-parallel combine ----
@@ -330,8 +331,8 @@ __global__ void __launch_bounds__(kFwdThreads, (fwd_min_blocks<T, OP, CAP, DIR>(
   const int q = static_cast<int>(blockIdx.x - row * C);
   if (C > 1) cluster_arrive_relaxed();
 
-  const T* xr = static_cast<const T*>(a.x) + row * a.ldx;
-  const T* yr = KL ? static_cast<const T*>(a.y) + row * a.ldy : xr;
+  const T* xr = row_ptr<T>(a.x, a.rx, row);
+  const T* yr = KL ? row_ptr<T>(a.y, a.ry, row) : xr;
   const int64_t V = a.vocab;
   const int64_t nvec = (V + 7) >> 3;
   const int64_t vb = static_cast<int64_t>(q) * a.vec_per_cta;

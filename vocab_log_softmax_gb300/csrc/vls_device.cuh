@@ -151,6 +151,19 @@ __device__ __forceinline__ bool aligned16(const void* p) {
   return (reinterpret_cast<uintptr_t>(p) & 15u) == 0;
 }
 
+// First element of row r of an operand addressed by a vls_rows descriptor:
+// (r / group) * ld_group + (r % group) * ld.  Row indices stay below the
+// 2^31 grid limit, so the split is a 32-bit division.  The C layer turns a
+// single group (group 0) into group 2^31 - 1, so one branch-free path serves
+// both forms (a branch here cost the register-bound backward maps spills).
+template <class T>
+__device__ __forceinline__ const T* row_ptr(const void* base, const vls_rows& l, int64_t r) {
+  const uint32_t d = static_cast<uint32_t>(l.group);
+  const uint32_t q = static_cast<uint32_t>(r) / d;
+  const uint32_t t = static_cast<uint32_t>(r) - q * d;
+  return static_cast<const T*>(base) + (static_cast<int64_t>(q) * l.ld_group + static_cast<int64_t>(t) * l.ld);
+}
+
 __device__ __forceinline__ bool valid_id(int64_t id, int64_t V, int64_t ignore_index) {
   return id != ignore_index && id >= 0 && id < V;
 }

@@ -47,10 +47,10 @@ struct FwdArgs {
   // logits (logp / entropy), or the first KL argument: the distribution the
   // expectation is taken over (a for reverse KL, b for forward KL)
   const void* x;
-  int64_t ldx;
+  vls_rows rx;
   // second KL argument (KL only)
   const void* y;
-  int64_t ldy;
+  vls_rows ry;
   int64_t rows;
   int64_t vocab;
   float cap;   // 0 = no softcap
@@ -83,9 +83,9 @@ struct FwdArgs {
 
 struct BwdArgs {
   const void* x;  // logits / policy a
-  int64_t ldx;
+  vls_rows rx;
   const void* y;  // reference b (KL only)
-  int64_t ldy;
+  vls_rows ry;
   int64_t rows;
   int64_t vocab;
   float cap;
