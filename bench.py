@@ -453,45 +453,85 @@ def run_config(args) -> None:
                       "peak_gbs": peak, "peak_kind": kind, "ops": ops}), flush=True)
 
 
-def time_e2e(step: Step, steps: int, device):
-    """Same step through the same calls, with every input copied in from
-    pinned host memory and every result copied back, inside the timed region."""
+E2E_CHUNKS = 8
+E2E_COPY_STREAMS = 1
+
+
+def time_e2e(step: Step, steps: int, device, chunks: int = E2E_CHUNKS, copy_streams: int = E2E_COPY_STREAMS):
+    """The same step through the same calls with HOST buffers: every input is
+    copied in from pinned host memory and every result (forward outputs, each
+    op's gradient, the softcap output) is copied back to pinned host memory
+    inside the timed region.  Rows are independent, so the batch is cut into
+    row chunks pipelined over three streams: chunk c's inputs are copied in
+    while chunk c-1 computes and chunk c-2's results are copied out (the two
+    copy directions run on separate copy engines; ``copy_streams`` > 1 deals
+    the chunks round-robin over that many streams per direction).  Each op
+    writes its own gradient buffer, so no readback waits for a later op."""
     import torch
+    n = step.n
+    bounds = [(n * c // chunks, n * (c + 1) // chunks) for c in range(chunks)]
     pinned_in = {k: t.detach().cpu().pin_memory() for k, t in step.inp.items()}
-    res = step.results()
-    pinned_out = [torch.empty(r.shape, dtype=r.dtype, pin_memory=True) for r in res[:-2]]
-    big = torch.empty(step.out["d"].shape, dtype=step.out["d"].dtype, pin_memory=True)
     h2d = sum(t.numel() * t.element_size() for t in pinned_in.values())
-    launches = step.launches()
-    grad_ops = {"bwd"}
+    i, o = step.inp, step.out
+    grad = {op: torch.empty_like(o["d"]) for op in OPS}
+    dev_out = {"lp": o["lp"], "H": o["H"], "klr": o["klr"], "klf": o["klf"], "lpc": o["lpc"], "y": o["y"]}
+    dev_out.update({"d_" + op: grad[op] for op in OPS})
+    host_out = {k: torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for k, t in dev_out.items()}
+    d2h = sum(t.numel() * t.element_size() for t in host_out.values())
+
+    from vocab_log_softmax_gb300 import binding as B
+
+    def launches(lo, hi):
+        r = slice(lo, hi)
+        st, st2 = o["st"][r], o["st2"][r]
+        B.vls_logp_fwd(i["x"][r], i["ids"][r], -100, 0.0, logp=o["lp"][r], stats=st)
+        B.vls_logp_bwd(i["x"][r], i["ids"][r], i["g"][r], st, -100, 0.0, dlogits=grad["logp"][r])
+        B.vls_entropy_fwd(i["a"][r], 0.0, H=o["H"][r], stats=st)
+        B.vls_entropy_bwd(i["a"][r], i["g_row"][r], o["H"][r], st, 0.0, dlogits=grad["entropy"][r])
+        for op, d, kl in (("kl_reverse", "reverse", o["klr"]), ("kl_forward", "forward", o["klf"])):
+            B.vls_kl_fwd(i["a"][r], i["b"][r], d, 0.0, kl=kl[r], stats_a=st, stats_b=st2)
+            B.vls_kl_bwd(i["a"][r], i["b"][r], i["g_row"][r], kl[r], st, st2, d, 0.0, da=grad[op][r])
+        B.vls_logp_fwd(i["xc"][r], i["ids_c"][r], -100, CAP, logp=o["lpc"][r], stats=st)
+        B.vls_logp_bwd(i["xc"][r], i["ids_c"][r], i["g_c"][r], st, -100, CAP, dlogits=grad["cap_logp"][r])
+        B.vls_softcap_fwd(i["xc"][r], CAP, y=o["y"][r])
+        B.vls_softcap_bwd(i["xc"][r], i["gy"][r], CAP, gx=grad["softcap"][r])
+
+    comp = torch.cuda.current_stream(device)
+    s_ins = [torch.cuda.Stream(device) for _ in range(copy_streams)]
+    s_outs = [torch.cuda.Stream(device) for _ in range(copy_streams)]
+    ev = {k: [torch.cuda.Event() for _ in bounds] for k in ("in", "comp", "out")}
 
     def one():
-        for k, t in pinned_in.items():
-            step.inp[k].copy_(t, non_blocking=True)
-        d2h = 0
-        for op, ps, f in launches:
-            f()
-            if ps in grad_ops:          # the shared gradient buffer is read back after each backward
-                big.copy_(step.out["d"], non_blocking=True)
-                d2h += big.numel() * big.element_size()
-        big.copy_(step.out["y"], non_blocking=True)
-        d2h += big.numel() * big.element_size()
-        for h, r in zip(pinned_out, res[:-2]):
-            h.copy_(r, non_blocking=True)
-            d2h += h.numel() * h.element_size()
-        return d2h
+        for c, (lo, hi) in enumerate(bounds):
+            s_in, s_out = s_ins[c % copy_streams], s_outs[c % copy_streams]
+            s_in.wait_event(ev["comp"][c])            # the previous step has read chunk c's inputs
+            with torch.cuda.stream(s_in):
+                for k, t in pinned_in.items():
+                    i[k][lo:hi].copy_(t[lo:hi], non_blocking=True)
+            ev["in"][c].record(s_in)
+            comp.wait_event(ev["in"][c])
+            comp.wait_event(ev["out"][c])             # the previous step's chunk c results are read back
+            launches(lo, hi)
+            ev["comp"][c].record(comp)
+            s_out.wait_event(ev["comp"][c])
+            with torch.cuda.stream(s_out):
+                for k, t in dev_out.items():
+                    host_out[k][lo:hi].copy_(t[lo:hi], non_blocking=True)
+            ev["out"][c].record(s_out)
 
     one()
     torch.cuda.synchronize()
-    stream = torch.cuda.current_stream(device)
-    s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    s0.record(stream)
-    d2h = 0
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record(comp)
+    for st in s_ins + s_outs:
+        st.wait_event(t0)
     for _ in range(steps):
-        d2h = one()
-    s1.record(stream)
+        one()
+    for e in ev["out"]:
+        comp.wait_event(e)
+    t1.record(comp)
     torch.cuda.synchronize()
-    return s0.elapsed_time(s1) / steps, h2d, d2h
+    return t0.elapsed_time(t1) / steps, h2d, d2h
 
 
 # ----------------------------------------------------------------------------
@@ -603,6 +643,9 @@ def main() -> None:
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--rows", type=int, default=N_ROWS, help="rows per GPU (default 8192)")
     ap.add_argument("--e2e-steps", type=int, default=3)
+    ap.add_argument("--e2e-chunks", type=int, default=E2E_CHUNKS, help="row chunks of the host-buffer pipeline")
+    ap.add_argument("--e2e-copy-streams", type=int, default=E2E_COPY_STREAMS,
+                    help="copy streams per direction in the host-buffer pipeline")
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timing leg")
     ap.add_argument("--workload", default="step",
                     choices=["step", "logp_small", "logp_offset", "kl_masked", "softcap_wide", "long_seq", "fused"],
@@ -660,10 +703,11 @@ def main() -> None:
                 "share_of_step": round(dom_ms / ms, 4),
                 "step_frac": round(sb / (ms / 1e3) / 1e9 / peak, 4)}
 
-    e2e_ms, h2d, d2h = time_e2e(step, args.e2e_steps, device)
+    e2e_ms, h2d, d2h = time_e2e(step, args.e2e_steps, device, args.e2e_chunks, args.e2e_copy_streams)
     e2e_ms = max_over_ranks(e2e_ms, device)
     e2e = {"value": round(aggregate(sb, world, e2e_ms / 1e3), 4), "unit": "TB/s", "h2d_bytes_per_step": h2d,
-           "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 3), "steps": args.e2e_steps}
+           "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 3), "steps": args.e2e_steps,
+           "pipeline": {"row_chunks": args.e2e_chunks, "copy_streams_per_direction": args.e2e_copy_streams}}
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
