@@ -11,6 +11,9 @@ from .vocab_stats import (  # noqa: F401
     is_valid_id,
     kl_bwd,
     kl_fwd,
+    linear_logits,
+    linear_logp_bwd,
+    linear_logp_fwd,
     logp_bwd,
     logp_fwd,
     round_to_bf16_bits,

@@ -46,6 +46,13 @@ Readings where the pages are silent (each also listed in the design notes):
   and the softmax term is weighted by the sum of all valid upstream
   gradients.  With k = 1 this is ``g*(one_hot - softmax)``.
 
+* Fused linear + logprobs: the pages name a ``linear_logp`` op ("perf(logp):
+  fused zero-workspace backward ...", RL-Kernel PR #495, Summary, listed as
+  not touched) without defining it.  The plainest reading is the target
+  log-probabilities of the logits a linear vocabulary head produces,
+  ``z = h @ W^T`` (h: [N, D] hidden states, W: [V, D] head weights), with
+  the gradient flowing to both h and W.
+
 Parity pins for every function here live in ``tests/test_oracle.py``.
 """
 
@@ -323,3 +330,29 @@ def kl_bwd(a: np.ndarray, b: np.ndarray, g: np.ndarray, direction: str = "revers
             row = g[i] * (np.exp(lpa) - np.exp(lpb))
         d[i] = row * _cap_chain(a[i], cap)
     return d
+
+
+# ----------------------------------------------------------------------------
+# fused linear head + target log-probabilities (reading: z = h @ W^T)
+# ----------------------------------------------------------------------------
+
+def linear_logits(h: np.ndarray, w: np.ndarray) -> np.ndarray:
+    """z = h @ W^T in float64: h [N, D], W [V, D] -> [N, V]."""
+    h = np.atleast_2d(np.asarray(h, dtype=np.float64))
+    w = np.atleast_2d(np.asarray(w, dtype=np.float64))
+    return h @ w.T
+
+
+def linear_logp_fwd(h: np.ndarray, w: np.ndarray, ids: np.ndarray, ignore_index: int = -100) -> np.ndarray:
+    """logp_fwd of the logits z = h @ W^T (never formed on the GPU)."""
+    return logp_fwd(linear_logits(h, w), ids, ignore_index)
+
+
+def linear_logp_bwd(h: np.ndarray, w: np.ndarray, ids: np.ndarray, g: np.ndarray,
+                    ignore_index: int = -100) -> tuple[np.ndarray, np.ndarray]:
+    """(dh, dW) for upstream g [N, k]: with dz = logp_bwd(z, ids, g) [N, V],
+    dh = dz @ W and dW = dz^T @ h (the chain rule through z = h @ W^T)."""
+    h = np.atleast_2d(np.asarray(h, dtype=np.float64))
+    w = np.atleast_2d(np.asarray(w, dtype=np.float64))
+    dz = logp_bwd(linear_logits(h, w), ids, g, ignore_index)
+    return dz @ w, dz.T @ h

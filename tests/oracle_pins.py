@@ -13,7 +13,9 @@ copy of the oracle are caught.  The pins are:
   ``log_softmax`` + ``gather``;
 * invariants: shift invariance, sum of probabilities = 1, zero row sums of
   gradients, Gibbs' inequality, odd symmetry of the softcap;
-* central finite differences in fp64 on tiny rows for every backward.
+* central finite differences in fp64 on tiny rows for every backward;
+* for the linear head, dot products and log-sum-exp written out with
+  Python's math on a tiny case, and torch fp64 autograd.
 """
 
 from __future__ import annotations
@@ -358,6 +360,60 @@ def check_softcap_grad_cap_free(impl):
     d20 = impl.softcap_grad(20.0 * u, np.ones_like(u), 20.0)
     d30 = impl.softcap_grad(30.0 * u, np.ones_like(u), 30.0)
     assert np.allclose(d20, d30, rtol=1e-14, atol=0)
+
+
+# ---- fused linear head + logprobs (z = h @ W^T) ----
+
+def _tiny_linear():
+    h = np.array([[1.0, -2.0, 0.5], [0.0, 3.0, -1.0]])
+    w = np.array([[2.0, 0.0, -1.0], [1.0, 1.0, 1.0], [-3.0, 0.5, 2.0], [0.0, -1.0, 4.0]])
+    ids = np.array([[2], [0]])
+    return h, w, ids
+
+
+def check_linear_logp_brute_force(impl):
+    """Dot products and log-sum-exp written out with Python's math on a 2 x 3 x 4 case."""
+    h, w, ids = _tiny_linear()
+    got = impl.linear_logp_fwd(h, w, ids)
+    for i in range(2):
+        z = [sum(h[i, d] * w[c, d] for d in range(3)) for c in range(4)]
+        lse = max(z) + math.log(sum(math.exp(t - max(z)) for t in z))
+        assert abs(got[i, 0] - (z[int(ids[i, 0])] - lse)) < 1e-12
+
+
+def check_linear_logp_zero_hidden(impl):
+    """h = 0 gives uniform logits: log p = -ln V for every valid id, 0 for ignored ones."""
+    w = np.random.default_rng(3).standard_normal((37, 8))
+    ids = np.array([[5, -100], [36, 0]])
+    got = impl.linear_logp_fwd(np.zeros((2, 8)), w, ids)
+    assert _close(got, [[-math.log(37), 0.0], [-math.log(37), -math.log(37)]])
+
+
+def check_linear_logp_vs_torch(impl):
+    """torch fp64 autograd of log_softmax(h @ W^T).gather: forward, dh and dW."""
+    import torch
+    rng = np.random.default_rng(11)
+    h, w = rng.standard_normal((5, 6)), 0.7 * rng.standard_normal((9, 6))
+    ids = np.array([[1, 1], [8, -100], [0, 3], [4, 4], [7, 2]])
+    g = rng.standard_normal((5, 2))
+    th, tw = torch.tensor(h, requires_grad=True), torch.tensor(w, requires_grad=True)
+    tid = torch.tensor(np.where(ids < 0, 0, ids))
+    lp = torch.log_softmax(th @ tw.T, dim=1).gather(1, tid) * torch.tensor(ids >= 0, dtype=torch.float64)
+    (lp * torch.tensor(g)).sum().backward()
+    assert _close(impl.linear_logp_fwd(h, w, ids), lp.detach().numpy(), rtol=1e-12, atol=1e-12)
+    dh, dw = impl.linear_logp_bwd(h, w, ids, g)
+    assert _close(dh, th.grad.numpy(), rtol=1e-10, atol=1e-12)
+    assert _close(dw, tw.grad.numpy(), rtol=1e-10, atol=1e-12)
+
+
+def check_linear_logp_bwd_fd(impl):
+    """Central finite differences of sum(g * logp) in h and in W."""
+    h, w, ids = _tiny_linear()
+    g = np.array([[0.7], [-1.3]])
+    dh, dw = impl.linear_logp_bwd(h, w, ids, g)
+    fh = _fd(lambda x: float(np.sum(g * impl.linear_logp_fwd(x, w, ids))), h.copy())
+    fw = _fd(lambda x: float(np.sum(g * impl.linear_logp_fwd(h, x, ids))), w.copy())
+    assert np.allclose(dh, fh, rtol=1e-6, atol=1e-7) and np.allclose(dw, fw, rtol=1e-6, atol=1e-7)
 
 
 ALL_CHECKS = [v for k, v in sorted(globals().items()) if k.startswith("check_")]

@@ -113,7 +113,29 @@ def _softcap_no_outer_cap(x, cap):
     return np.tanh(np.asarray(x, dtype=np.float64) / cap)
 
 
+def _linear_logp_fwd_scaled(h, w, ids, ignore_index=-100):
+    # logits scaled by 1/sqrt(D), as an attention score would be
+    h = np.atleast_2d(np.asarray(h, dtype=np.float64))
+    return vs.logp_fwd(vs.linear_logits(h, w) / np.sqrt(h.shape[1]), ids, ignore_index)
+
+
+def _linear_logp_bwd_dw_rows_reversed(h, w, ids, g, ignore_index=-100):
+    # the vocabulary index of dW taken in the wrong order
+    dh, dw = vs.linear_logp_bwd(h, w, ids, g, ignore_index)
+    return dh, dw[::-1]
+
+
+def _linear_logp_bwd_dh_without_softmax(h, w, ids, g, ignore_index=-100):
+    # dh from the one-hot term only
+    z = vs.linear_logits(h, w)
+    dz = _logp_bwd_without_softmax_term(z, ids, g, ignore_index)
+    return dz @ np.asarray(w, dtype=np.float64), vs.linear_logp_bwd(h, w, ids, g, ignore_index)[1]
+
+
 MUTANTS = {
+    "linear_logp_fwd: logits scaled by 1/sqrt(D)": dict(linear_logp_fwd=_linear_logp_fwd_scaled),
+    "linear_logp_bwd: dW vocabulary rows reversed": dict(linear_logp_bwd=_linear_logp_bwd_dw_rows_reversed),
+    "linear_logp_bwd: dh without the softmax term": dict(linear_logp_bwd=_linear_logp_bwd_dh_without_softmax),
     "logp_bwd: softmax term dropped": dict(logp_bwd=_logp_bwd_without_softmax_term),
     "logp_bwd: sign flipped": dict(logp_bwd=_logp_bwd_sign_flip),
     "logp_bwd: softmax weight = first g": dict(logp_bwd=_logp_bwd_first_g_only),
