@@ -204,6 +204,16 @@ def hbm_peak() -> tuple[float, str]:
         return 6800.0, "fallback"
 
 
+def tensor_peak() -> tuple[float, str]:
+    """Dense bf16 tensor-core peak in TFLOP/s: the measured burst figure, else the fallback."""
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["bf16_tflops"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return 1900.0, "fallback"
+
+
 def source_hash() -> str:
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "vocab_log_softmax_gb300", "csrc")
@@ -415,6 +425,29 @@ class ConfigRun:
                   ("separate logp bwd", bl["bwd"], lambda: B.vls_logp_bwd(a_, ids, gl, st1, dlogits=d)),
                   ("separate entropy bwd", be["bwd"], lambda: B.vls_entropy_bwd(a_, g, H, st1, dlogits=d)),
                   ("separate KL bwd", bk["bwd"], lambda: B.vls_kl_bwd(a_, b_, g, kl, st2, st3, da=d))]
+        elif name == "linear_logp":
+            # fused linear head + logprobs on the tensor cores, against cuBLAS logits + the logp sweep
+            w = workloads.linear_head(device)
+            h, wt, ids = w["h"], w["w"], w["ids"]
+            n, dd = h.shape
+            v = wt.shape[0]
+            s = B.vls_linear_logp_chunks(v)
+            part = torch.empty((s, n, 6), **f32)
+            zt = torch.empty((s, n, 1), **f32)
+            status = torch.zeros(1, dtype=torch.int32, device=device)
+            lp, st = torch.empty((n, 1), **f32), torch.empty((n, 2), **f32)
+            z = torch.empty((n, v), dtype=torch.bfloat16, device=device)
+            flops = 2 * n * v * dd
+            io = (n + v) * dd * 2
+
+            def fused():
+                B.vls_linear_logp_partial(h, wt, ids, part=part, zt=zt, status=status)
+                B.vls_logp_combine(part, zt, ids, v, logp=lp, stats=st)
+
+            L += [("fused linear logp (partials + combine)", io, fused, flops),
+                  ("cuBLAS h @ W^T to bf16 logits", io + n * v * 2, lambda: torch.mm(h, wt.t(), out=z), flops),
+                  ("logp fwd over those logits", n * v * 2, lambda: B.vls_logp_fwd(z, ids, logp=lp, stats=st))]
+            self.status = status
         else:
             raise SystemExit(f"unknown workload {name}")
         self.launches = L
@@ -427,26 +460,32 @@ def run_config(args) -> None:
     device = torch.device("cuda", 0)
     run = ConfigRun(args.workload, device)
     for _ in range(args.warmup):
-        for _, _, f in run.launches:
+        for _, _, f, *_ in run.launches:
             f()
     torch.cuda.synchronize()
     stream = torch.cuda.current_stream(device)
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(run.launches) + 1)] for _ in range(args.steps)]
     for s in range(args.steps):
-        for j, (_, _, f) in enumerate(run.launches):
+        for j, (_, _, f, *_) in enumerate(run.launches):
             ev[s][j].record(stream)
             f()
         ev[s][-1].record(stream)
     torch.cuda.synchronize()
     peak, kind = hbm_peak()
+    tpeak, tkind = tensor_peak()
     ops = {}
-    for j, (label, nbytes, _) in enumerate(run.launches):
+    for j, (label, nbytes, _, *fl) in enumerate(run.launches):
         ts = sorted(ev[s][j].elapsed_time(ev[s][j + 1]) for s in range(args.steps))
         med = ts[len(ts) // 2]
         ops[label] = {"ms_median": round(med, 4), "ms_p10": round(ts[len(ts) // 10], 4),
                       "ms_p90": round(ts[(9 * len(ts)) // 10], 4), "tbs": round(nbytes / med / 1e9, 3),
                       "frac_of_measured": round(nbytes / med / 1e6 / peak, 4), "bytes": nbytes}
-    total_b = sum(b for _, b, _ in run.launches)
+        if fl:   # a contraction: its tensor-core roofline
+            ops[label].update({"tflops": round(fl[0] / med / 1e9, 1), "flops": fl[0],
+                               "frac_of_bf16_peak": round(fl[0] / med / 1e9 / tpeak, 4), "bf16_peak_kind": tkind})
+    if getattr(run, "status", None) is not None and int(run.status.item()) != 0:
+        raise SystemExit(f"{run.name}: a bounded wait in the kernel ran out (status {int(run.status.item())})")
+    total_b = sum(b for _, b, *_ in run.launches)
     total_ms = sum(o["ms_median"] for o in ops.values())
     print(json.dumps({"workload": run.name, "rows": run.rows, "vocab": run.vocab, "steps": args.steps,
                       "fwd_bwd_ms": round(total_ms, 4), "tbs": round(total_b / total_ms / 1e9, 3),
@@ -648,7 +687,8 @@ def main() -> None:
                     help="copy streams per direction in the host-buffer pipeline")
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timing leg")
     ap.add_argument("--workload", default="step",
-                    choices=["step", "logp_small", "logp_offset", "kl_masked", "softcap_wide", "long_seq", "fused"],
+                    choices=["step", "logp_small", "logp_offset", "kl_masked", "softcap_wide", "long_seq", "fused",
+                             "linear_logp"],
                     help="step (default): the benchmark step; otherwise per-op times of one workload")
     args = ap.parse_args()
     if args.workload != "step" and args.impl == "ours":

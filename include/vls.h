@@ -272,6 +272,43 @@ int vls_kl_combine(const vls_partial* parts, int32_t R, int64_t N, vls_kl_dir di
                    vls_rowstat* stats_a, vls_rowstat* stats_b, void* stream);
 
 /* ------------------------------------------------------------------------ */
+/* Fused linear head + target log-probabilities.  The pages name a           */
+/* linear_logp op without defining it ("perf(logp): fused zero-workspace     */
+/* backward ...", RL-Kernel PR #495, Summary); it is read here as the        */
+/* logprobs of the logits z = h @ W^T of a linear vocabulary head, where z   */
+/* is never written to memory.  The tensor cores (tcgen05) form z tile by    */
+/* tile and the statistics of vls_logp_fwd are folded from those tiles.      */
+/* The forward is split phase: the vocabulary is cut into fixed chunks       */
+/* (vls_linear_logp_chunks), vls_linear_logp_partial writes one vls_partial  */
+/* per chunk and row plus the owned targets' logits, and vls_logp_combine    */
+/* (R = the chunk count, V_total = V) folds them in chunk order into logp    */
+/* and stats, exactly as for vocabulary shards.                              */
+/* ------------------------------------------------------------------------ */
+
+/* Largest top-k the linear call accepts. */
+#define VLS_LINEAR_MAX_TOPK 16
+
+/* Number of vocabulary chunks S of a V-column head (a function of V only, so
+ * results do not depend on N); parts and zt of vls_linear_logp_partial hold
+ * S rows of N entries.  Returns -1 when V < 1. */
+int64_t vls_linear_logp_chunks(int64_t V);
+
+/* h: [N, D] hidden states, row stride ldh; W: [V, D] head weights, row
+ * stride ldw; both of dtype dt, VLS_BF16 or VLS_F16 (fp32 accumulation).
+ * h, W and their row strides must be 16-byte aligned (ldh, ldw multiples of
+ * 8 elements), as the tensor-memory-access loads require.  ids: int64 [N, k],
+ * 1 <= k <= VLS_LINEAR_MAX_TOPK, ignored as in vls_logp_fwd.  part: [S, N];
+ * zt: fp32 [S, N, k] (the raw logit of each valid id in the chunk that holds
+ * it, 0 in the others).  status: one device uint32 the caller zeroes; the
+ * kernel sets bit 0 if one of its internal waits ran out (a fault of the
+ * kernel, not of the inputs), and the partials are then invalid.  Needs a
+ * GPU with tcgen05 (sm_100 family); the library is built for sm_103a. */
+int vls_linear_logp_partial(const void* h, int64_t ldh, const void* W, int64_t ldw, vls_dtype dt,
+                            int64_t N, int64_t D, int64_t V, const int64_t* ids, int32_t k,
+                            int64_t ignore_index, vls_partial* part, float* zt, uint32_t* status,
+                            void* stream);
+
+/* ------------------------------------------------------------------------ */
 /* Status                                                                    */
 /* ------------------------------------------------------------------------ */
 

@@ -1,0 +1,136 @@
+"""Fused linear head + logprobs on the tensor cores against the oracle
+(logits z = h @ W^T formed in fp64 there, never stored on the GPU).
+
+Tolerance.  The logits are fp32 sums of D exact bf16 / fp16 products, in an
+order the tensor cores fix.  Any order of an fp32 sum of D terms is within
+D * 2^-24 * sum |terms| of the exact sum (the standard worst-case bound of
+recursive summation), so a log-probability, which is z_target - max z - log S,
+moves by at most twice the largest such bound over the row's columns.  The
+tests add that bound to the logprob rule of the other calls
+(1e-5 + 1e-5 |ref|).  With small integer inputs every logit is exact in fp32,
+the bound is 0, and the plain rule applies: any misplaced product, tile or
+chunk changes an integer and fails.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from vls_compare import assert_fp32_close, bitwise_equal, to_f64
+from vocab_log_softmax_gb300 import binding as B
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+U = 2.0 ** -24
+
+
+def _gen(seed):
+    return torch.Generator(device=DEV).manual_seed(seed)
+
+
+def _ids(n, v, k, seed, ignore_frac=0.0):
+    g = _gen(seed)
+    ids = torch.randint(0, v, (n, k), generator=g, device=DEV)
+    if ignore_frac:
+        mask = torch.rand((n, k), generator=g, device=DEV) < ignore_frac
+        ids[mask] = -100
+    return ids
+
+
+def _summation_bound(h, w):
+    """Per row: 2 * D * 2^-24 * max_c sum_i |h_ri W_ci| (float64)."""
+    hh, ww = np.abs(to_f64(h)), np.abs(to_f64(w))
+    return 2.0 * h.shape[1] * U * (hh @ ww.T).max(axis=1)
+
+
+def _check(h, w, ids, what, ignore=-100, exact=False):
+    logp, stats, status = B.vls_linear_logp_fwd(h, w, ids, ignore)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0, f"{what}: a wait in the kernel ran out"
+    ref = oracle.linear_logp_fwd(to_f64(h), to_f64(w), ids.cpu().numpy(), ignore)
+    extra = 0.0 if exact else _summation_bound(h, w)[:, None]
+    assert_fp32_close(logp, ref, what, atol=1e-5 + extra)
+    z = oracle.linear_logits(to_f64(h), to_f64(w))
+    m_ref = z.max(axis=1)
+    lse = m_ref + np.log(np.exp(z - m_ref[:, None]).sum(axis=1))
+    got = stats.cpu().numpy().astype(np.float64)
+    tol = 1e-5 + 1e-5 * np.abs(lse) + (0.0 if exact else _summation_bound(h, w))
+    assert np.all(np.abs(got[:, 0] + got[:, 1] - lse) <= tol), what + " stats"
+    return logp, stats
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float16], ids=["bf16", "f16"])
+def test_exact_integer_inputs(dtype):
+    """Entries in {-1, 0, 1}: every logit is an exact integer in fp32."""
+    n, d, v = 300, 200, 5000          # 3 row tiles (ragged), D not a multiple of 64, 3 chunks, ragged last tile
+    g = _gen(1)
+    h = torch.randint(-1, 2, (n, d), generator=g, device=DEV).to(dtype)
+    w = torch.randint(-1, 2, (v, d), generator=g, device=DEV).to(dtype)
+    _check(h, w, _ids(n, v, 1, 2, 0.1), "integer linear logp", exact=True)
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float16], ids=["bf16", "f16"])
+@pytest.mark.parametrize("n,d,v", [(129, 1000, 2049), (8, 64, 256), (1, 8, 1), (520, 4096, 16000)])
+def test_random_inputs(n, d, v, dtype):
+    g = _gen(n + d + v)
+    h = torch.randn((n, d), generator=g, device=DEV).to(dtype)
+    w = (3.0 / d ** 0.5 * torch.randn((v, d), generator=g, device=DEV)).to(dtype)
+    _check(h, w, _ids(n, v, 1, 3, 0.05), f"linear logp N={n} D={d} V={v}")
+
+
+def test_topk_duplicates_ignores_out_of_range():
+    n, d, v = 200, 128, 3000
+    g = _gen(7)
+    h = torch.randn((n, d), generator=g, device=DEV).to(torch.bfloat16)
+    w = (0.3 * torch.randn((v, d), generator=g, device=DEV)).to(torch.bfloat16)
+    ids = _ids(n, v, 16, 8, 0.1)
+    ids[:, 5] = ids[:, 4]                  # duplicates
+    ids[::3, 7] = v + 5                    # out of range
+    ids[1::7, 9] = -7                      # negative
+    _check(h, w, ids, "linear logp top-16")
+    _check(h, w, ids, "linear logp ignore=3", ignore=3)
+
+
+def test_strided_rows_and_batch_invariance():
+    """Rows read in place from wider buffers; any subset or order of rows
+    gives the same bits (each row's statistics depend on that row only)."""
+    n, d, v = 300, 256, 4100
+    g = _gen(11)
+    hbuf = torch.randn((n, d + 8), generator=g, device=DEV).to(torch.bfloat16)
+    wbuf = (0.2 * torch.randn((v, d + 16), generator=g, device=DEV)).to(torch.bfloat16)
+    h, w = hbuf[:, :d], wbuf[:, :d]
+    ids = _ids(n, v, 2, 12)
+    lp, st = _check(h, w, ids, "strided linear logp")
+    lpc, stc, _ = B.vls_linear_logp_fwd(h.contiguous(), w.contiguous(), ids)
+    assert bitwise_equal(lp, lpc) and bitwise_equal(st, stc)
+    perm = torch.randperm(n, generator=torch.Generator().manual_seed(0)).to(DEV)
+    for rows in (perm, perm[:1], perm[:130], torch.arange(n - 1, -1, -1, device=DEV)):
+        lps, sts, _ = B.vls_linear_logp_fwd(h[rows].contiguous(), w, ids[rows].contiguous())
+        assert bitwise_equal(lps, lp[rows]) and bitwise_equal(sts, st[rows])
+
+
+def test_chunk_count_depends_on_v_only():
+    assert B.vls_linear_logp_chunks(1) == 1
+    assert B.vls_linear_logp_chunks(2048) == 1
+    assert B.vls_linear_logp_chunks(2049) == 2
+    assert B.vls_linear_logp_chunks(151936) == 75
+
+
+def test_full_size_sampled_rows():
+    """N=8192, D=4096, V=151936 (a Qwen-size head) in the launch shape the
+    bench times; 6 sampled rows checked against the oracle one by one."""
+    n, d, v = 8192, 4096, 151936
+    g = _gen(21)
+    h = torch.randn((n, d), generator=g, device=DEV).to(torch.bfloat16)
+    w = (3.0 / d ** 0.5 * torch.randn((v, d), generator=g, device=DEV)).to(torch.bfloat16)
+    ids = _ids(n, v, 1, 22, 0.05)
+    logp, stats, status = B.vls_linear_logp_fwd(h, w, ids)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    wf = to_f64(w)
+    for r in (0, 1, 127, 128, 4097, n - 1):
+        hr = to_f64(h[r:r + 1])
+        ref = oracle.linear_logp_fwd(hr, wf, ids[r:r + 1].cpu().numpy())
+        bound = 2.0 * d * U * (np.abs(hr) @ np.abs(wf).T).max()
+        assert_fp32_close(logp[r:r + 1], ref, f"row {r}", atol=1e-5 + bound)

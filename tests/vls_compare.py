@@ -54,10 +54,12 @@ def _report(what, got, ref, tol, fin):
             f"gpu {got[fin][i]!r} ref {ref[fin][i]!r} err {err[i]:.3e} tol {tol[i]:.3e}")
 
 
-def assert_fp32_close(got, ref, what: str = "", rtol: float = FWD_RTOL, atol: float = FWD_ATOL):
+def assert_fp32_close(got, ref, what: str = "", rtol: float = FWD_RTOL, atol=FWD_ATOL):
+    """atol may be an array that broadcasts against ref (a per-row bound)."""
     got, ref = to_f64(got), np.asarray(ref, dtype=np.float64)
     assert got.shape == ref.shape, (what, got.shape, ref.shape)
     fin = _nonfinite_match(got, ref, what)
+    atol = np.broadcast_to(np.asarray(atol, dtype=np.float64), ref.shape)[fin]
     _report(what, got, ref, atol + rtol * np.abs(ref[fin]), fin)
 
 

@@ -70,9 +70,14 @@ SIGNATURES = {
     "vls_entropy_combine": [_p, _i32, _i64, _p, _p, _p],
     "vls_kl_partial": [_p, _r, _p, _r, _int, _i64, _i64, _int, _f, _p, _p],
     "vls_kl_combine": [_p, _i32, _i64, _int, _p, _p, _p, _p],
+    "vls_linear_logp_chunks": [_i64],
+    "vls_linear_logp_partial": [_p, _i64, _p, _i64, _int, _i64, _i64, _i64, _p, _i32, _i64, _p, _p, _p, _p],
     "vls_status_string": [_int],
     "vls_version": [],
 }
+
+RESTYPES = {"vls_status_string": ctypes.c_char_p, "vls_linear_logp_chunks": ctypes.c_int64}
+VLS_LINEAR_MAX_TOPK = 16
 
 _lib = None
 
@@ -102,7 +107,7 @@ def load() -> ctypes.CDLL:
     for name, argtypes in SIGNATURES.items():
         fn = getattr(lib, name)
         fn.argtypes = argtypes
-        fn.restype = ctypes.c_char_p if name == "vls_status_string" else ctypes.c_int
+        fn.restype = RESTYPES.get(name, ctypes.c_int)
     _lib = lib
     return lib
 

@@ -397,6 +397,53 @@ def vls_kl_combine(parts: torch.Tensor, direction: str = "reverse", *, kl=None, 
     return kl, stats_a, stats_b
 
 
+# ---------------------------------------------------------------------------
+# fused linear head + logprobs
+# ---------------------------------------------------------------------------
+
+def vls_linear_logp_chunks(vocab: int) -> int:
+    return int(_lib.load().vls_linear_logp_chunks(int(vocab)))
+
+
+def _matrix(t: torch.Tensor, what: str) -> tuple[int, int, int]:
+    """(rows, D, row stride) of a 2-D tensor with a contiguous last dimension."""
+    if t.dim() != 2 or (t.shape[1] > 1 and t.stride(1) != 1):
+        raise ValueError(f"{what} must be a 2-D tensor with a contiguous last dimension")
+    return t.shape[0], t.shape[1], (t.stride(0) if t.shape[0] > 1 else t.shape[1])
+
+
+def vls_linear_logp_partial(h: torch.Tensor, w: torch.Tensor, ids: torch.Tensor, ignore_index: int = -100, *,
+                            part=None, zt=None, status=None, stream=None):
+    """(part [S, N, 6], zt [S, N, k], status [1] int32) of the linear head z = h @ w^T."""
+    lib = _lib.load()
+    n, d, ldh = _matrix(h, "h")
+    v, dw, ldw = _matrix(w, "W")
+    if dw != d:
+        raise ValueError(f"h has D={d} but W has D={dw}")
+    if h.dtype != w.dtype or h.dtype not in (torch.bfloat16, torch.float16):
+        raise TypeError("h and W must both be bfloat16 or both float16")
+    ids = _ids2d(ids, n)
+    if ids.dtype != torch.int64 or not ids.is_contiguous():
+        raise ValueError("ids must be a contiguous int64 [N, k] tensor")
+    k = ids.shape[1]
+    s = vls_linear_logp_chunks(v) if v > 0 else 0
+    part = _partials((s, n), h.device, part)
+    zt = torch.empty((s, n, k), dtype=torch.float32, device=h.device) if zt is None else zt
+    status = torch.zeros(1, dtype=torch.int32, device=h.device) if status is None else status
+    st = lib.vls_linear_logp_partial(_ptr(h), ldh, _ptr(w), ldw, _dtype(h), n, d, v, _ptr(ids), k,
+                                     int(ignore_index), _ptr(part), _ptr(zt), _ptr(status), _stream(h, stream))
+    _lib.check("vls_linear_logp_partial", st)
+    return part, zt, status
+
+
+def vls_linear_logp_fwd(h: torch.Tensor, w: torch.Tensor, ids: torch.Tensor, ignore_index: int = -100, *,
+                        stream=None) -> tuple[torch.Tensor, torch.Tensor, torch.Tensor]:
+    """(logp [N, k], stats [N, 2], status [1]): the two C calls in sequence."""
+    part, zt, status = vls_linear_logp_partial(h, w, ids, ignore_index, stream=stream)
+    logp, stats = vls_logp_combine(part, zt, ids, w.shape[0], ignore_index, 0.0, stream=stream)
+    return logp, stats, status
+
+
 def vls_status_string(status: int) -> str:
     return _lib.load().vls_status_string(int(status)).decode()
 

@@ -685,4 +685,28 @@ int vls_kl_combine(const vls_partial* parts, int32_t R, int64_t N, vls_kl_dir di
   return launch_status(launch_combine(kFwdKl, a, static_cast<cudaStream_t>(stream)));
 }
 
+// ---------------------------------------------------------------------------
+// fused linear head + logprobs
+// ---------------------------------------------------------------------------
+
+int64_t vls_linear_logp_chunks(int64_t V) { return V < 1 ? -1 : linear_chunks(V); }
+
+int vls_linear_logp_partial(const void* h, int64_t ldh, const void* W, int64_t ldw, vls_dtype dt, int64_t N,
+                            int64_t D, int64_t V, const int64_t* ids, int32_t k, int64_t ignore_index,
+                            vls_partial* part, float* zt, uint32_t* status, void* stream) {
+  if (N < 0 || D < 1 || V < 1 || ldh < D || ldw < D || k < 1 || k > VLS_LINEAR_MAX_TOPK) return VLS_ERR_SHAPE;
+  if (N > kMaxGrid || V > kMaxGrid) return VLS_ERR_SHAPE;   // TMA row coordinates are 32-bit
+  if (dt != VLS_BF16 && dt != VLS_F16) return VLS_ERR_DTYPE;
+  if (N == 0) return VLS_OK;
+  if (!h || !W || !ids || !part || !zt || !status) return VLS_ERR_NULL;
+  if ((reinterpret_cast<uintptr_t>(h) | reinterpret_cast<uintptr_t>(W)) & 15u) return VLS_ERR_ARG;
+  if ((ldh % 8) || (ldw % 8)) return VLS_ERR_ARG;
+  int dev;
+  if (int e = resolve_device({h, W, ids, part, zt, status}, stream, &dev)) return e;
+  DeviceGuard guard;
+  if (int e = guard.enter(dev)) return e;
+  LinearArgs a{h, ldh, W, ldw, dt, N, D, V, ids, k, ignore_index, part, zt, status};
+  return launch_status(launch_linear_logp(a, sm_count(dev), static_cast<cudaStream_t>(stream)));
+}
+
 }  // extern "C"

@@ -139,6 +139,28 @@ struct CapArgs {
   int grid;         // the SM count on entry to the launcher, the grid size after
 };
 
+// Fused linear head + logprobs (tcgen05): vocabulary chunks of
+// kLinChunkTiles tiles of 256 columns each give one vls_partial per row.
+constexpr int kLinChunkTiles = 8;
+constexpr int kLinMaxTopk = VLS_LINEAR_MAX_TOPK;
+
+struct LinearArgs {
+  const void* h;       // [N, D], row stride ldh
+  int64_t ldh;
+  const void* W;       // [V, D], row stride ldw
+  int64_t ldw;
+  vls_dtype dt;        // VLS_BF16 or VLS_F16
+  int64_t N, D, V;
+  const int64_t* ids;  // [N, k]
+  int32_t k;
+  int64_t ignore_index;
+  vls_partial* part;   // [S, N]
+  float* zt;           // [S, N, k]
+  uint32_t* status;
+};
+
+int64_t linear_chunks(int64_t V);
+
 // Launchers: one per kernel family, dispatching on dtype and softcap.  They
 // return a cudaError_t of the launch.
 cudaError_t launch_fwd_logp(vls_dtype dt, bool cap, const FwdArgs& a, cudaStream_t s);
@@ -152,5 +174,6 @@ cudaError_t launch_fwd_fused(FusedKl kl, vls_dtype dt, bool cap, const FwdArgs& 
 cudaError_t launch_bwd_fused(FusedKl kl, vls_dtype dt, bool cap, const BwdArgs& a, cudaStream_t s);
 cudaError_t launch_softcap_fwd(vls_dtype dt, const CapArgs& a, cudaStream_t s);
 cudaError_t launch_softcap_bwd(vls_dtype dt, const CapArgs& a, cudaStream_t s);
+cudaError_t launch_linear_logp(const LinearArgs& a, int sms, cudaStream_t s);
 
 }  // namespace vls

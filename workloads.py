@@ -29,6 +29,11 @@ Workloads (rows N x vocabulary V):
   k=256 ids per row = 224 distinct ids + 32 repeats of some of them,
   shuffled; grads N(0, 1).  (seed 4)
 
+* ``linear_head`` h: 8192 x 4096 bf16 hidden states N(0, 1); W: 151936 x
+  4096 bf16 head weights N(0, 9 / 4096), so the logits h @ W^T are about
+  N(0, 3^2); a Qwen-size head (vocabulary 151936, hidden 4096); targets
+  uniform, 5% of rows -100; grad N(0, 1).  (seed 5)
+
 Every builder takes ``n`` and ``v`` overrides so that reduced copies of a
 workload (the parity tests' sizes) follow the same recipe.
 """
@@ -161,3 +166,18 @@ def long_seq(device="cuda", n: int = 32768, v: int = 151936, seed: int = 4, k: i
         "gk": _randn((n, k), g, device),
         "g_row": _randn((n,), g, device),
     }
+
+
+def linear_head(device="cuda", n: int = 8192, d: int = 4096, v: int = 151936, seed: int = 5) -> dict:
+    h = torch.empty((n, d), dtype=torch.bfloat16, device=device)
+    for blk, r0, r1 in _blocks(n):
+        h[r0:r1] = _randn((r1 - r0, d), _gen(device, seed, blk), device).to(torch.bfloat16)
+    w = torch.empty((v, d), dtype=torch.bfloat16, device=device)
+    scale = 3.0 / d ** 0.5
+    for blk, r0, r1 in _blocks(v):
+        w[r0:r1] = (scale * _randn((r1 - r0, d), _gen(device, seed, (1 << 16) + blk), device)).to(torch.bfloat16)
+    g = _gen(device, seed, 1 << 20)
+    ids = torch.randint(0, v, (n, 1), generator=g, device=device, dtype=torch.int64)
+    ign = torch.randperm(n, generator=g, device=device)[: n // 20]
+    ids[ign] = -100
+    return {"h": h, "w": w, "ids": ids, "g": _randn((n, 1), g, device)}
