@@ -89,7 +89,9 @@ enum {
   VLS_ERR_DEVICE = 5,   /* a pointer is not device memory, or pointers / stream
                            sit on different devices                               */
   VLS_ERR_LAUNCH = 6,   /* the CUDA launch failed (cudaGetLastError after launch) */
-  VLS_ERR_ARG = 7       /* another bad argument (e.g. an unknown KL direction)    */
+  VLS_ERR_ARG = 7,      /* another bad argument (e.g. an unknown KL direction)    */
+  VLS_ERR_TOO_LARGE = 8 /* the call needs more than the fixed scratch of
+                           vls_linear_logp_fwd_noalloc                            */
 };
 
 /* Largest top-k the logprob calls accept. */
@@ -307,6 +309,28 @@ int vls_linear_logp_partial(const void* h, int64_t ldh, const void* W, int64_t l
                             int64_t N, int64_t D, int64_t V, const int64_t* ids, int32_t k,
                             int64_t ignore_index, vls_partial* part, float* zt, uint32_t* status,
                             void* stream);
+
+/* The whole linear-head logprob forward (the partial call, then the combine)
+ * without any buffer from the caller beyond its inputs and outputs.  The
+ * pages have no counterpart to this call: it exists for callers that cannot
+ * allocate device memory, such as a serving engine that has given all of it
+ * to its own pool and forbids further cudaMalloc calls, or a program held to
+ * a fixed device-memory budget.  The intermediate partials live in one fixed
+ * array of the library (32 MiB, held on every GPU that loads the library
+ * until the process exits), which bounds a call: N * S <= 2^20 and
+ * N * S * k <= 2^21 with S = vls_linear_logp_chunks(V) (for V = 151936,
+ * S = 75: up to 13981 rows at k = 1); larger calls return VLS_ERR_TOO_LARGE
+ * before touching the GPU.  Arguments, outputs and status are those of
+ * vls_linear_logp_partial and vls_logp_combine: logp [N, k] and stats [N].
+ * The first call on a device looks up the array's address there (a runtime
+ * query, no allocation), so make that first call before any stream capture.
+ * Every call uses the same array: calls whose work overlaps on the GPU (on
+ * different streams or from different threads) race and must be ordered by
+ * the caller. */
+int vls_linear_logp_fwd_noalloc(const void* h, int64_t ldh, const void* W, int64_t ldw, vls_dtype dt,
+                                int64_t N, int64_t D, int64_t V, const int64_t* ids, int32_t k,
+                                int64_t ignore_index, float* logp, vls_rowstat* stats, uint32_t* status,
+                                void* stream);
 
 /* ------------------------------------------------------------------------ */
 /* Status                                                                    */

@@ -28,6 +28,7 @@ STATUS = {
     5: "VLS_ERR_DEVICE",
     6: "VLS_ERR_LAUNCH",
     7: "VLS_ERR_ARG",
+    8: "VLS_ERR_TOO_LARGE",
 }
 
 _p = ctypes.c_void_p
@@ -72,6 +73,7 @@ SIGNATURES = {
     "vls_kl_combine": [_p, _i32, _i64, _int, _p, _p, _p, _p],
     "vls_linear_logp_chunks": [_i64],
     "vls_linear_logp_partial": [_p, _i64, _p, _i64, _int, _i64, _i64, _i64, _p, _i32, _i64, _p, _p, _p, _p],
+    "vls_linear_logp_fwd_noalloc": [_p, _i64, _p, _i64, _int, _i64, _i64, _i64, _p, _i32, _i64, _p, _p, _p, _p],
     "vls_status_string": [_int],
     "vls_version": [],
 }
@@ -115,6 +117,6 @@ def load() -> ctypes.CDLL:
 def check(fn: str, status: int) -> None:
     if status == 0:
         return
-    if status in (1, 2, 3, 4, 7):
+    if status in (1, 2, 3, 4, 7, 8):
         raise VlsArgumentError(fn, status)
     raise VlsError(fn, status)

@@ -444,6 +444,28 @@ def vls_linear_logp_fwd(h: torch.Tensor, w: torch.Tensor, ids: torch.Tensor, ign
     return logp, stats, status
 
 
+def vls_linear_logp_fwd_noalloc(h: torch.Tensor, w: torch.Tensor, ids: torch.Tensor, ignore_index: int = -100, *,
+                                logp=None, stats=None, status=None, stream=None):
+    """vls_linear_logp_fwd through the C entry point that needs no buffer
+    beyond the inputs and outputs (its intermediates sit in a fixed array of
+    the library).  Returns (logp [N, k], stats [N, 2], status [1])."""
+    lib = _lib.load()
+    n, d, ldh = _matrix(h, "h")
+    v, dw, ldw = _matrix(w, "W")
+    if dw != d:
+        raise ValueError(f"h has D={d} but W has D={dw}")
+    ids = _ids2d(ids, n)
+    k = ids.shape[1]
+    logp = torch.empty((n, k), dtype=torch.float32, device=h.device) if logp is None else logp
+    stats = _stats(n, h.device, stats)
+    status = torch.zeros(1, dtype=torch.int32, device=h.device) if status is None else status
+    st = lib.vls_linear_logp_fwd_noalloc(_ptr(h), ldh, _ptr(w), ldw, _dtype(h), n, d, v, _ptr(ids), k,
+                                         int(ignore_index), _ptr(logp), _ptr(stats), _ptr(status),
+                                         _stream(h, stream))
+    _lib.check("vls_linear_logp_fwd_noalloc", st)
+    return logp, stats, status
+
+
 def vls_status_string(status: int) -> str:
     return _lib.load().vls_status_string(int(status)).decode()
 

@@ -212,6 +212,7 @@ const char* vls_status_string(int status) {
       return "VLS_ERR_DEVICE: pointer not device memory, or pointers/stream on different devices";
     case VLS_ERR_LAUNCH: return "VLS_ERR_LAUNCH: CUDA launch failed";
     case VLS_ERR_ARG: return "VLS_ERR_ARG: bad argument";
+    case VLS_ERR_TOO_LARGE: return "VLS_ERR_TOO_LARGE: the call needs more than the no-alloc call's fixed scratch";
     default: return "VLS_ERR_UNKNOWN";
   }
 }
