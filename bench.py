@@ -444,7 +444,13 @@ class ConfigRun:
                 B.vls_linear_logp_partial(h, wt, ids, part=part, zt=zt, status=status)
                 B.vls_logp_combine(part, zt, ids, v, logp=lp, stats=st)
 
+            g = w["g"]
+            dh, dw = torch.empty_like(h), torch.empty_like(wt)
+            ws = torch.empty((B.vls_linear_logp_bwd_workspace(n, dd, v),), dtype=torch.uint8, device=device)
             L += [("fused linear logp (partials + combine)", io, fused, flops),
+                  ("fused linear logp bwd (dz map, dh, dW)", io + (n + v) * dd * 2 + 4 * n * v * 2,
+                   lambda: B.vls_linear_logp_bwd(h, wt, ids, g, st, dh=dh, dW=dw, workspace=ws, status=status),
+                   3 * flops),
                   ("cuBLAS h @ W^T to bf16 logits", io + n * v * 2, lambda: torch.mm(h, wt.t(), out=z), flops),
                   ("logp fwd over those logits", n * v * 2, lambda: B.vls_logp_fwd(z, ids, logp=lp, stats=st))]
             self.status = status

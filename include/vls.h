@@ -310,6 +310,28 @@ int vls_linear_logp_partial(const void* h, int64_t ldh, const void* W, int64_t l
                             int64_t ignore_index, vls_partial* part, float* zt, uint32_t* status,
                             void* stream);
 
+/* Bytes of device workspace vls_linear_logp_bwd needs (h^T, W^T, dz and
+ * dz^T in the operand dtype, each 256-byte aligned): about
+ * 2 (D N + D V + 2 N V).  Returns -1 for sizes out of range. */
+int64_t vls_linear_logp_bwd_workspace(int64_t N, int64_t D, int64_t V);
+
+/* Gradients of sum_{r,j} g[r, j] logp[r, j] with respect to h and W, where
+ * logp is vls_linear_logp's output for the same h, W, ids and ignore_index
+ * and stats its (m, log S):
+ *     dz = g one-hot - G p   (G = sum of the valid g of the row),
+ *     dh = dz @ W  [N, D],   dW = dz^T @ h  [V, D],
+ * with the logits recomputed on the tensor cores from h and W.  dz is formed
+ * in fp32 and rounded once to dt before the two products, which accumulate
+ * in fp32 and round once to dt at the store.  g: fp32 [N, k]; dh, dW:
+ * contiguous, dtype dt.  workspace: at least
+ * vls_linear_logp_bwd_workspace(N, D, V) bytes, 256-byte aligned, the
+ * caller's; its contents on entry do not matter.  status as for
+ * vls_linear_logp_partial.  Row counts N and V are at most 2^21 - 32. */
+int vls_linear_logp_bwd(const void* h, int64_t ldh, const void* W, int64_t ldw, vls_dtype dt, int64_t N,
+                        int64_t D, int64_t V, const int64_t* ids, int32_t k, int64_t ignore_index,
+                        const float* g, const vls_rowstat* stats, void* dh, void* dW, void* workspace,
+                        int64_t workspace_bytes, uint32_t* status, void* stream);
+
 /* The whole linear-head logprob forward (the partial call, then the combine)
  * without any buffer from the caller beyond its inputs and outputs.  The
  * pages have no counterpart to this call: it exists for callers that cannot

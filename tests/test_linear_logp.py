@@ -134,3 +134,88 @@ def test_full_size_sampled_rows():
         ref = oracle.linear_logp_fwd(hr, wf, ids[r:r + 1].cpu().numpy())
         bound = 2.0 * d * U * (np.abs(hr) @ np.abs(wf).T).max()
         assert_fp32_close(logp[r:r + 1], ref, f"row {r}", atol=1e-5 + bound)
+
+
+# ---------------------------------------------------------------------------
+# backward: dh = dz @ W, dW = dz^T @ h with dz = g one-hot - G p
+# ---------------------------------------------------------------------------
+
+def _ulp16(r, dtype):
+    from vls_compare import ulp_bf16, ulp_f16
+    return ulp_bf16(r) if dtype == torch.bfloat16 else ulp_f16(r)
+
+
+def _check_bwd(h, w, ids, g, what, ignore=-100):
+    """dh and dW against the oracle.  Bound: dz is formed in fp32 from logits
+    within the summation bound, then rounded once to the 16-bit dtype
+    (relative 2^-9 for bf16, 2^-11 for fp16; taken as 2^-8 and 2^-10); the
+    products sum in fp32 (K 2^-24 sum |terms|), then round once more."""
+    logp, stats, st0 = B.vls_linear_logp_fwd(h, w, ids, ignore)
+    dh, dw, st1 = B.vls_linear_logp_bwd(h, w, ids, g, stats, ignore)
+    torch.cuda.synchronize()
+    assert int(st0.item()) == 0 and int(st1.item()) == 0, what + ": a wait ran out"
+    x, wf = to_f64(h), to_f64(w)
+    idn, gn = ids.cpu().numpy(), g.cpu().numpy().astype(np.float64)
+    ref_dh, ref_dw = oracle.linear_logp_bwd(x, wf, idn, gn, ignore)
+    z = oracle.linear_logits(x, wf)
+    dz = oracle.logp_bwd(z, idn, gn, ignore)
+    p = np.exp(z - z.max(axis=1, keepdims=True))
+    p /= p.sum(axis=1, keepdims=True)
+    valid = (idn != ignore) & (idn >= 0) & (idn < wf.shape[0])
+    G = np.abs((gn * valid).sum(axis=1))
+    rel = 2.0 ** -8 if h.dtype == torch.bfloat16 else 2.0 ** -10
+    bz = h.shape[1] * U * (np.abs(x) @ np.abs(wf).T).max(axis=1)
+    err_dz = np.abs(dz) * rel + G[:, None] * p * (2.0 * bz[:, None] + 2.0 ** -20)
+    tol_dh = err_dz @ np.abs(wf) + wf.shape[0] * U * (np.abs(dz) @ np.abs(wf))
+    tol_dw = err_dz.T @ np.abs(x) + x.shape[0] * U * (np.abs(dz).T @ np.abs(x))
+    for got, ref, tol, name in ((dh, ref_dh, tol_dh, "dh"), (dw, ref_dw, tol_dw, "dW")):
+        gotn = to_f64(got)
+        bound = tol + _ulp16(ref, h.dtype) + 1e-6
+        bad = np.abs(gotn - ref) > bound
+        assert not bad.any(), (f"{what} {name}: {int(bad.sum())} of {bad.size} out of bound; worst "
+                               f"{np.max(np.abs(gotn - ref) - bound):.3e}")
+    return dh, dw
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float16], ids=["bf16", "f16"])
+@pytest.mark.parametrize("n,d,v,k", [(300, 256, 5003, 2), (129, 1000, 2049, 1), (8, 64, 256, 3)])
+def test_backward(n, d, v, k, dtype):
+    g = _gen(n * 7 + v)
+    h = torch.randn((n, d), generator=g, device=DEV).to(dtype)
+    w = (3.0 / d ** 0.5 * torch.randn((v, d), generator=g, device=DEV)).to(dtype)
+    ids = _ids(n, v, k, 31, 0.1)
+    if k > 1:
+        ids[:, 1] = ids[:, 0]               # duplicates add their upstream gradients
+    gr = torch.randn((n, k), generator=g, device=DEV)
+    _check_bwd(h, w, ids, gr, f"linear bwd N={n} D={d} V={v} k={k}")
+
+
+def test_backward_ignored_rows_give_zero_dh():
+    n, d, v = 200, 128, 3000
+    g = _gen(41)
+    h = torch.randn((n, d), generator=g, device=DEV).to(torch.bfloat16)
+    w = (0.3 * torch.randn((v, d), generator=g, device=DEV)).to(torch.bfloat16)
+    ids = _ids(n, v, 1, 42)
+    ids[::4] = -100
+    ids[1::9] = v + 3
+    gr = torch.randn((n, 1), generator=g, device=DEV)
+    dh, _ = _check_bwd(h, w, ids, gr, "linear bwd with ignored rows")
+    dead = ((ids[:, 0] == -100) | (ids[:, 0] >= v)).nonzero().flatten()
+    assert bool(torch.all(dh[dead] == 0))
+
+
+def test_autograd_linear_logprobs():
+    import vocab_log_softmax_gb300 as V
+    n, d, v = 2 * 96, 256, 4100
+    g = _gen(51)
+    h = torch.randn((2, 96, d), generator=g, device=DEV).to(torch.bfloat16).requires_grad_(True)
+    w = (0.2 * torch.randn((v, d), generator=g, device=DEV)).to(torch.bfloat16).requires_grad_(True)
+    ids = _ids(n, v, 1, 52).reshape(2, 96)
+    gr = torch.randn((2, 96), generator=g, device=DEV)
+    lp = V.linear_logprobs(h, w, ids)
+    (lp * gr).sum().backward()
+    ref_lp, st, _ = B.vls_linear_logp_fwd(h.detach().reshape(n, d), w.detach(), ids.reshape(n, 1))
+    dh, dw, _ = B.vls_linear_logp_bwd(h.detach().reshape(n, d), w.detach(), ids.reshape(n, 1),
+                                      gr.reshape(n, 1).contiguous(), st)
+    assert bitwise_equal(lp.reshape(n, 1), ref_lp)
+    assert bitwise_equal(h.grad.reshape(n, d), dh) and bitwise_equal(w.grad, dw)

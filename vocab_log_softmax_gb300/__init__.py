@@ -19,6 +19,8 @@ import torch
 
 from ._lib import VlsArgumentError, VlsError  # noqa: F401
 from .binding import (  # noqa: F401
+    vls_linear_logp_bwd,
+    vls_linear_logp_fwd,
     vls_entropy_bwd,
     vls_entropy_fwd,
     vls_fused_bwd,
@@ -33,7 +35,7 @@ from .binding import (  # noqa: F401
     vls_version,
 )
 
-__all__ = ["logprobs", "entropy", "kl", "softcap", "stats"]
+__all__ = ["logprobs", "entropy", "kl", "softcap", "stats", "linear_logprobs"]
 
 
 def _addressable(rows: torch.Tensor) -> bool:
@@ -229,3 +231,38 @@ def kl(policy: torch.Tensor, reference: torch.Tensor, direction: str = "reverse"
 def softcap(x: torch.Tensor, cap: float = 30.0) -> torch.Tensor:
     """cap * tanh(x / cap), elementwise, in x's dtype."""
     return _Softcap.apply(x, _cap(cap))
+
+
+class _LinearLogprobs(torch.autograd.Function):
+    @staticmethod
+    def forward(ctx, hidden, weight, ids, ignore_index):
+        h = hidden.reshape(-1, hidden.shape[-1])
+        if h.shape[-1] > 1 and h.stride(-1) != 1:
+            h = h.contiguous()
+        w = weight if weight.stride(-1) == 1 else weight.contiguous()
+        ids2 = _ids_rows(ids, h.shape[0])
+        logp, st, _ = vls_linear_logp_fwd(h, w, ids2, ignore_index)
+        ctx.save_for_backward(h, w, ids2, st)
+        ctx.meta = (ignore_index, hidden.shape)
+        return logp.reshape(ids.shape)
+
+    @staticmethod
+    def backward(ctx, grad):
+        h, w, ids2, st = ctx.saved_tensors
+        ignore_index, shape = ctx.meta
+        g = grad.reshape(ids2.shape).to(torch.float32).contiguous()
+        dh, dw, _ = vls_linear_logp_bwd(h, w, ids2, g, st, ignore_index)
+        return dh.reshape(shape), dw, None, None
+
+
+def linear_logprobs(hidden: torch.Tensor, weight: torch.Tensor, ids: torch.Tensor,
+                    ignore_index: int = -100) -> torch.Tensor:
+    """log_softmax(hidden @ weight^T)[..., ids] without storing the logits.
+
+    hidden: [..., D] and weight: [V, D], both bfloat16 or both float16; ids
+    shaped like hidden's leading dims ([...] or [..., k], k <= 16).  The
+    gradient flows to hidden and weight.  The kernels' bounded waits report
+    through a status word that this API does not read (no host
+    synchronisation); ``binding.vls_linear_logp_fwd`` / ``_bwd`` return it.
+    """
+    return _LinearLogprobs.apply(hidden, weight, ids, int(ignore_index))

@@ -73,12 +73,16 @@ SIGNATURES = {
     "vls_kl_combine": [_p, _i32, _i64, _int, _p, _p, _p, _p],
     "vls_linear_logp_chunks": [_i64],
     "vls_linear_logp_partial": [_p, _i64, _p, _i64, _int, _i64, _i64, _i64, _p, _i32, _i64, _p, _p, _p, _p],
+    "vls_linear_logp_bwd_workspace": [_i64, _i64, _i64],
+    "vls_linear_logp_bwd": [_p, _i64, _p, _i64, _int, _i64, _i64, _i64, _p, _i32, _i64, _p, _p, _p, _p, _p, _i64,
+                            _p, _p],
     "vls_linear_logp_fwd_noalloc": [_p, _i64, _p, _i64, _int, _i64, _i64, _i64, _p, _i32, _i64, _p, _p, _p, _p],
     "vls_status_string": [_int],
     "vls_version": [],
 }
 
-RESTYPES = {"vls_status_string": ctypes.c_char_p, "vls_linear_logp_chunks": ctypes.c_int64}
+RESTYPES = {"vls_status_string": ctypes.c_char_p, "vls_linear_logp_chunks": ctypes.c_int64,
+            "vls_linear_logp_bwd_workspace": ctypes.c_int64}
 VLS_LINEAR_MAX_TOPK = 16
 
 _lib = None

@@ -444,6 +444,37 @@ def vls_linear_logp_fwd(h: torch.Tensor, w: torch.Tensor, ids: torch.Tensor, ign
     return logp, stats, status
 
 
+def vls_linear_logp_bwd_workspace(n: int, d: int, v: int) -> int:
+    return int(_lib.load().vls_linear_logp_bwd_workspace(int(n), int(d), int(v)))
+
+
+def vls_linear_logp_bwd(h: torch.Tensor, w: torch.Tensor, ids: torch.Tensor, g: torch.Tensor, stats: torch.Tensor,
+                        ignore_index: int = -100, *, dh=None, dW=None, workspace=None, status=None, stream=None):
+    """(dh [N, D], dW [V, D], status [1]) of sum(g * logp) for the linear head
+    z = h @ w^T; `stats` is vls_linear_logp_fwd's."""
+    lib = _lib.load()
+    n, d, ldh = _matrix(h, "h")
+    v, dw, ldw = _matrix(w, "W")
+    if dw != d or h.dtype != w.dtype:
+        raise ValueError("h and W must share D and dtype")
+    ids = _ids2d(ids, n)
+    k = ids.shape[1]
+    g = g.reshape(n, k)
+    if g.dtype != torch.float32 or not g.is_contiguous():
+        raise ValueError("g must be a contiguous float32 [N, k] tensor")
+    dh = torch.empty((n, d), dtype=h.dtype, device=h.device) if dh is None else dh
+    dW = torch.empty((v, d), dtype=h.dtype, device=h.device) if dW is None else dW
+    need = vls_linear_logp_bwd_workspace(n, d, v)
+    if workspace is None:
+        workspace = torch.empty((max(need, 1),), dtype=torch.uint8, device=h.device)
+    status = torch.zeros(1, dtype=torch.int32, device=h.device) if status is None else status
+    st = lib.vls_linear_logp_bwd(_ptr(h), ldh, _ptr(w), ldw, _dtype(h), n, d, v, _ptr(ids), k, int(ignore_index),
+                                 _ptr(g), _ptr(stats), _ptr(dh), _ptr(dW), _ptr(workspace),
+                                 workspace.numel() * workspace.element_size(), _ptr(status), _stream(h, stream))
+    _lib.check("vls_linear_logp_bwd", st)
+    return dh, dW, status
+
+
 def vls_linear_logp_fwd_noalloc(h: torch.Tensor, w: torch.Tensor, ids: torch.Tensor, ignore_index: int = -100, *,
                                 logp=None, stats=None, status=None, stream=None):
     """vls_linear_logp_fwd through the C entry point that needs no buffer

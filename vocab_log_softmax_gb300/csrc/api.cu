@@ -710,4 +710,33 @@ int vls_linear_logp_partial(const void* h, int64_t ldh, const void* W, int64_t l
   return launch_status(launch_linear_logp(a, sm_count(dev), static_cast<cudaStream_t>(stream)));
 }
 
+// largest row count of the transposes' 2-D grid (65535 blocks of 32 rows)
+constexpr int64_t kMaxTransposeRows = int64_t(65535) * 32;
+
+int64_t vls_linear_logp_bwd_workspace(int64_t N, int64_t D, int64_t V) {
+  if (N < 0 || D < 1 || V < 1 || N > kMaxTransposeRows || V > kMaxTransposeRows) return -1;
+  return static_cast<int64_t>(linear_bwd_workspace(N, D, V));
+}
+
+int vls_linear_logp_bwd(const void* h, int64_t ldh, const void* W, int64_t ldw, vls_dtype dt, int64_t N, int64_t D,
+                        int64_t V, const int64_t* ids, int32_t k, int64_t ignore_index, const float* g,
+                        const vls_rowstat* stats, void* dh, void* dW, void* workspace, int64_t workspace_bytes,
+                        uint32_t* status, void* stream) {
+  if (N < 0 || D < 1 || V < 1 || ldh < D || ldw < D || k < 1 || k > VLS_LINEAR_MAX_TOPK) return VLS_ERR_SHAPE;
+  if (N > kMaxTransposeRows || V > kMaxTransposeRows) return VLS_ERR_SHAPE;
+  if (dt != VLS_BF16 && dt != VLS_F16) return VLS_ERR_DTYPE;
+  if (N == 0) return VLS_OK;
+  if (!h || !W || !ids || !g || !stats || !dh || !dW || !workspace || !status) return VLS_ERR_NULL;
+  if (workspace_bytes < vls_linear_logp_bwd_workspace(N, D, V)) return VLS_ERR_SHAPE;
+  if ((reinterpret_cast<uintptr_t>(h) | reinterpret_cast<uintptr_t>(W)) & 15u) return VLS_ERR_ARG;
+  if (reinterpret_cast<uintptr_t>(workspace) & 255u) return VLS_ERR_ARG;
+  if ((ldh % 8) || (ldw % 8)) return VLS_ERR_ARG;
+  int dev;
+  if (int e = resolve_device({h, W, ids, g, stats, dh, dW, workspace, status}, stream, &dev)) return e;
+  DeviceGuard guard;
+  if (int e = guard.enter(dev)) return e;
+  LinearBwdArgs a{h, ldh, W, ldw, dt, N, D, V, ids, k, ignore_index, g, stats, dh, dW, workspace, status};
+  return launch_status(launch_linear_logp_bwd(a, sm_count(dev), static_cast<cudaStream_t>(stream)));
+}
+
 }  // extern "C"

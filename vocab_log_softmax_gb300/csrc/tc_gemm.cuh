@@ -1,0 +1,262 @@
+// A persistent tcgen05 GEMM mainloop with a pluggable epilogue:
+//     C[M, Ncols] = A[M, K] * B[Ncols, K]^T,
+// A and B 16-bit, both K-major (K contiguous), fp32 accumulation in tensor
+// memory.  The output tile is never stored by the mainloop: an epilogue
+// object receives it, 32 columns of one row per thread at a time, and does
+// what its operation needs (fold a softmax, form a gradient, store).
+//
+// Work is cut into units of (128 rows) x (a chunk of `chunk_tiles` column
+// tiles of 256), rows fastest, walked by a grid of at most one CTA per SM.
+// Roles (192 threads): warp 0 issues TMA loads of 64-wide K slices of A
+// (128 x 64) and B (256 x 64) into a 4-stage shared-memory ring (128-byte
+// swizzle); warp 1 owns 512 tensor-memory columns and one of its threads
+// issues 128x256x16 kind::f16 MMAs into one of two accumulators; warps 2-5
+// read a finished accumulator (one row per thread) and hand it to the
+// epilogue, then free it, so one tile's epilogue overlaps the next tile's
+// MMAs.  Every wait is bounded (tc_device.cuh).
+#pragma once
+
+#include "tc_device.cuh"
+#include "vls_device.cuh"
+
+namespace vls {
+namespace tcg {
+
+constexpr int kBM = 128;            // rows per tile (MMA M)
+constexpr int kBN = 256;            // columns per tile (MMA N)
+constexpr int kBK = 64;             // K per stage: one 128-byte swizzled row of 16-bit elements
+constexpr int kUK = 16;             // K per MMA instruction (kind::f16)
+constexpr int kStages = 4;
+constexpr int kThreads = 192;       // warp 0: TMA, warp 1: MMA, warps 2-5: epilogue
+constexpr uint32_t kStageA = kBM * kBK * 2;   // 16 KB
+constexpr uint32_t kStageB = kBN * kBK * 2;   // 32 KB
+constexpr uint32_t kTmemCols = 2 * kBN;       // two fp32 accumulators of 256 columns
+constexpr int kNumBars = 2 * kStages + 4 + 1; // full, empty, acc_full x2, acc_empty x2, done
+constexpr size_t kSmem = 1024 /* alignment slack */ + kStages * (kStageA + kStageB) + kNumBars * 8 + 16;
+
+struct Sched {
+  int64_t M;          // valid rows of the output
+  int64_t Ncols;      // valid columns of the output
+  int n_row_tiles, n_col_tiles, chunk_tiles, n_chunks, n_units, nk;
+  uint32_t* status;   // device status word (tc::kStatusTimeout after a wait ran out)
+};
+
+inline Sched make_sched(int64_t M, int64_t Ncols, int64_t K, int chunk_tiles, uint32_t* status) {
+  Sched s;
+  s.M = M;
+  s.Ncols = Ncols;
+  s.n_row_tiles = static_cast<int>((M + kBM - 1) / kBM);
+  s.n_col_tiles = static_cast<int>((Ncols + kBN - 1) / kBN);
+  s.chunk_tiles = chunk_tiles;
+  s.n_chunks = (s.n_col_tiles + chunk_tiles - 1) / chunk_tiles;
+  s.n_units = s.n_row_tiles * s.n_chunks;
+  s.nk = static_cast<int>((K + kBK - 1) / kBK);
+  s.status = status;
+  return s;
+}
+
+// Epilogue interface (one object per launch, copied to every thread):
+//   struct State;                                           per-thread, per-unit state
+//   State begin(int64_t row, bool row_ok, int chunk);       at each unit
+//   void  cols(State&, const float (&v)[32], int64_t row, bool row_ok, int64_t col0, int nvalid);
+//                                                           32 columns of the row (nvalid < 32 at the edge)
+//   void  end(State&, int64_t row, bool row_ok, int chunk); after the unit's last tile
+template <bool BF16, class Epi>
+__global__ void __launch_bounds__(kThreads, 1)
+    gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
+                const Sched sc, const Epi epi) {
+  extern __shared__ unsigned char smem_raw[];
+  if (static_cast<int>(blockIdx.x) >= sc.n_units) return;  // whole CTA, before any barrier
+
+  const uint32_t raw = tc::smem_u32(smem_raw);
+  unsigned char* smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
+  const uint32_t sbase = tc::smem_u32(smem);
+  const uint32_t sA = sbase;                           // kStages x kStageA
+  const uint32_t sB = sbase + kStages * kStageA;       // kStages x kStageB
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kStages * (kStageA + kStageB));
+  const uint32_t bar0 = tc::smem_u32(bars);
+  auto full = [&](int s) { return bar0 + 8u * s; };
+  auto empty = [&](int s) { return bar0 + 8u * (kStages + s); };
+  auto acc_full = [&](int b) { return bar0 + 8u * (2 * kStages + b); };
+  auto acc_empty = [&](int b) { return bar0 + 8u * (2 * kStages + 2 + b); };
+  const uint32_t done_bar = bar0 + 8u * (2 * kStages + 4);
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + kNumBars);
+  volatile uint32_t* abort_flag = tmem_holder + 1;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      tc::mbar_init(full(s), 1);
+      tc::mbar_init(empty(s), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      tc::mbar_init(acc_full(b), 1);
+      tc::mbar_init(acc_empty(b), 4);   // one arrival per epilogue warp
+    }
+    tc::mbar_init(done_bar, 1);
+    *abort_flag = 0u;
+    tc::mbar_init_fence();
+    tc::prefetch_tensormap(&tm_a);
+    tc::prefetch_tensormap(&tm_b);
+  }
+  if (warp == 1) tc::tmem_alloc(tc::smem_u32(tmem_holder), kTmemCols);
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tmem = *tmem_holder;
+
+  if (warp == 0) {
+    // ---------------- TMA producer ----------------
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t issued = 0;   // loads issued, for the drain below
+      bool ok = true;
+      for (int u = blockIdx.x; ok && u < sc.n_units; u += gridDim.x) {
+        const int chunk = u / sc.n_row_tiles, rt = u - chunk * sc.n_row_tiles;
+        const int t_end = min((chunk + 1) * sc.chunk_tiles, sc.n_col_tiles);
+        for (int t = chunk * sc.chunk_tiles; ok && t < t_end; ++t) {
+          for (int kb = 0; kb < sc.nk; ++kb) {
+            if (!tc::wait(empty(stage), phase ^ 1u, abort_flag, sc.status)) {
+              ok = false;
+              break;
+            }
+            tc::mbar_expect_tx(full(stage), kStageA + kStageB);
+            tc::tma_load_2d(sA + stage * kStageA, &tm_a, kb * kBK, rt * kBM, full(stage));
+            tc::tma_load_2d(sB + stage * kStageB, &tm_b, kb * kBK, t * kBN, full(stage));
+            ++issued;
+            if (++stage == kStages) {
+              stage = 0;
+              phase ^= 1u;
+            }
+          }
+        }
+      }
+      // After an abort, wait for the loads still in flight before the CTA
+      // releases its shared memory: the last load issued into each stage.
+      if (!ok) {
+        for (int s = 0; s < kStages; ++s) {
+          if (issued > static_cast<uint32_t>(s)) {
+            const uint32_t last = (issued - 1 - s) / kStages;   // index of the last load into stage s
+            tc::wait_drain(full(s), last & 1u, sc.status);
+          }
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ---------------- MMA issuer ----------------
+    if (lane == 0) {
+      constexpr uint32_t idesc = tc::idesc_f16(BF16, kBM, kBN);
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t tc_count = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; ok && u < sc.n_units; u += gridDim.x) {
+        const int chunk = u / sc.n_row_tiles;
+        const int t_end = min((chunk + 1) * sc.chunk_tiles, sc.n_col_tiles);
+        for (int t = chunk * sc.chunk_tiles; ok && t < t_end; ++t, ++tc_count) {
+          const uint32_t buf = tc_count & 1u, use = (tc_count >> 1) & 1u;
+          if (!tc::wait(acc_empty(buf), use ^ 1u, abort_flag, sc.status)) {
+            ok = false;
+            break;
+          }
+          tc::fence_after_sync();
+          const uint32_t d = tmem + buf * kBN;
+          for (int kb = 0; kb < sc.nk; ++kb) {
+            if (!tc::wait(full(stage), phase, abort_flag, sc.status)) {
+              ok = false;
+              break;
+            }
+            tc::fence_after_sync();
+            const uint64_t da = tc::sdesc_sw128(sA + stage * kStageA);
+            const uint64_t db = tc::sdesc_sw128(sB + stage * kStageB);
+#pragma unroll
+            for (int kk = 0; kk < kBK / kUK; ++kk) {
+              // 16 elements = 32 bytes further along the swizzled row: +2 in the address field
+              tc::mma_f16(d, da + 2ull * kk, db + 2ull * kk, idesc, (kb | kk) != 0 ? 1u : 0u);
+            }
+            tc::mma_commit(empty(stage));   // frees the stage once these MMAs have read it
+            if (++stage == kStages) {
+              stage = 0;
+              phase ^= 1u;
+            }
+          }
+          if (ok) tc::mma_commit(acc_full(buf));
+        }
+      }
+      // every MMA this thread issued has completed before tensor memory is freed
+      tc::mma_commit(done_bar);
+      tc::wait_drain(done_bar, 0u, sc.status);
+    }
+  } else {
+    // ---------------- epilogue: warps 2-5 ----------------
+    const int quarter = warp & 3;                 // the tensor-memory lanes this warp may read
+    const int r_in_tile = quarter * 32 + lane;
+    const uint32_t lane_addr = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
+    uint32_t tc_count = 0;
+    bool ok = true;
+    for (int u = blockIdx.x; ok && u < sc.n_units; u += gridDim.x) {
+      const int chunk = u / sc.n_row_tiles, rt = u - chunk * sc.n_row_tiles;
+      const int t_beg = chunk * sc.chunk_tiles, t_end = min(t_beg + sc.chunk_tiles, sc.n_col_tiles);
+      const int64_t row = static_cast<int64_t>(rt) * kBM + r_in_tile;
+      const bool row_ok = row < sc.M;
+      typename Epi::State st = epi.begin(row, row_ok, chunk);
+      for (int t = t_beg; t < t_end; ++t, ++tc_count) {
+        const uint32_t buf = tc_count & 1u, use = (tc_count >> 1) & 1u;
+        // one lane waits and the warp follows it, so the warp-wide tensor-memory
+        // loads below are never reached by part of a warp
+        const bool got = lane == 0 ? tc::wait(acc_full(buf), use, abort_flag, sc.status) : true;
+        if (!__shfl_sync(0xffffffffu, got ? 1 : 0, 0)) {
+          ok = false;
+          break;
+        }
+        __syncwarp();
+        tc::fence_after_sync();
+        for (int c = 0; c < kBN / 32; ++c) {
+          float v[32];
+          tc::tmem_ld32(lane_addr + buf * kBN + c * 32, v);
+          const int64_t cbase = static_cast<int64_t>(t) * kBN + c * 32;
+          const int64_t left = sc.Ncols - cbase;
+          const int nvalid = left <= 0 ? 0 : (left >= 32 ? 32 : static_cast<int>(left));
+          epi.cols(st, v, row, row_ok, cbase, nvalid);
+        }
+        tc::fence_before_sync();
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive(acc_empty(buf));
+      }
+      if (ok) epi.end(st, row, row_ok, chunk);
+    }
+  }
+
+  tc::fence_before_sync();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc::fence_after_sync();
+    tc::tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+// Tensor map of a [rows, K] 16-bit row-major matrix with row stride ld
+// (elements): a box of 64 x box_rows elements, 128-byte swizzle, zero fill
+// outside the matrix.
+bool encode_kmajor(CUtensorMap* map, const void* base, bool bf16, int64_t rows, int64_t K, int64_t ld,
+                   int box_rows);
+
+template <bool BF16, class Epi>
+cudaError_t launch_gemm(const void* A, int64_t lda, int64_t M, const void* Bm, int64_t ldb, int64_t Ncols,
+                        int64_t K, int chunk_tiles, uint32_t* status, const Epi& epi, int sms, cudaStream_t s) {
+  CUtensorMap tm_a, tm_b;
+  if (!encode_kmajor(&tm_a, A, BF16, M, K, lda, kBM) || !encode_kmajor(&tm_b, Bm, BF16, Ncols, K, ldb, kBN))
+    return cudaErrorInvalidValue;
+  const Sched sc = make_sched(M, Ncols, K, chunk_tiles, status);
+  auto kern = gemm_kernel<BF16, Epi>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(kSmem));
+  if (e != cudaSuccess) return e;
+  const int grid = sc.n_units < sms ? sc.n_units : sms;
+  kern<<<grid, kThreads, kSmem, s>>>(tm_a, tm_b, sc, epi);
+  return cudaGetLastError();
+}
+
+}  // namespace tcg
+}  // namespace vls

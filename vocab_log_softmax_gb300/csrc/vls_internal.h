@@ -161,6 +161,26 @@ struct LinearArgs {
 
 int64_t linear_chunks(int64_t V);
 
+struct LinearBwdArgs {
+  const void* h;
+  int64_t ldh;
+  const void* W;
+  int64_t ldw;
+  vls_dtype dt;
+  int64_t N, D, V;
+  const int64_t* ids;        // [N, k]
+  int32_t k;
+  int64_t ignore_index;
+  const float* g;            // [N, k]
+  const vls_rowstat* stats;  // [N], from the forward
+  void* dh;                  // [N, D] contiguous, dtype dt
+  void* dW;                  // [V, D] contiguous, dtype dt
+  void* workspace;           // linear_bwd_workspace(N, D, V) bytes, 256-byte aligned
+  uint32_t* status;
+};
+
+size_t linear_bwd_workspace(int64_t N, int64_t D, int64_t V);
+
 // Launchers: one per kernel family, dispatching on dtype and softcap.  They
 // return a cudaError_t of the launch.
 cudaError_t launch_fwd_logp(vls_dtype dt, bool cap, const FwdArgs& a, cudaStream_t s);
@@ -175,5 +195,6 @@ cudaError_t launch_bwd_fused(FusedKl kl, vls_dtype dt, bool cap, const BwdArgs& 
 cudaError_t launch_softcap_fwd(vls_dtype dt, const CapArgs& a, cudaStream_t s);
 cudaError_t launch_softcap_bwd(vls_dtype dt, const CapArgs& a, cudaStream_t s);
 cudaError_t launch_linear_logp(const LinearArgs& a, int sms, cudaStream_t s);
+cudaError_t launch_linear_logp_bwd(const LinearBwdArgs& a, int sms, cudaStream_t s);
 
 }  // namespace vls
