@@ -710,8 +710,8 @@ int vls_linear_logp_partial(const void* h, int64_t ldh, const void* W, int64_t l
   return launch_status(launch_linear_logp(a, sm_count(dev), static_cast<cudaStream_t>(stream)));
 }
 
-// largest row count of the transposes' 2-D grid (65535 blocks of 32 rows)
-constexpr int64_t kMaxTransposeRows = int64_t(65535) * 32;
+// largest row count of the transposes' 2-D grid (65535 blocks of 64 rows)
+constexpr int64_t kMaxTransposeRows = int64_t(65535) * 64;
 
 int64_t vls_linear_logp_bwd_workspace(int64_t N, int64_t D, int64_t V) {
   if (N < 0 || D < 1 || V < 1 || N > kMaxTransposeRows || V > kMaxTransposeRows) return -1;

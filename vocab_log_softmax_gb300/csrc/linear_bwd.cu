@@ -7,7 +7,8 @@
 //
 // Steps, all on tcgen05 through the mainloop of tc_gemm.cuh, whose operands
 // are K-major:
-//  1. h^T [D, N] and W^T [D, V] by a shared-memory tiled transpose;
+//  1. h^T [D, N] and W^T [D, V] by a shared-memory tiled transpose (64 x 64
+//     tiles, 16-byte accesses);
 //  2. the dz map: the forward's GEMM z = h @ W^T with an epilogue that forms
 //     dz in fp32, casts it once to the operand dtype and writes it both as
 //     dz [N, V] and as dz^T [V, N];
@@ -144,31 +145,53 @@ struct DzEpi {
 };
 
 // y[c, r] = x[r, c] for a [rows, cols] 16-bit matrix with row stride ldx
-// into y with row stride ldy, through 32 x 32 shared-memory tiles.
-template <class T>
-__global__ void __launch_bounds__(256) transpose_kernel(const T* __restrict__ x, int64_t rows, int64_t cols,
-                                                         int64_t ldx, T* __restrict__ y, int64_t ldy) {
-  __shared__ T tile[32][33];
-  const int64_t r0 = static_cast<int64_t>(blockIdx.y) * 32, c0 = static_cast<int64_t>(blockIdx.x) * 32;
-  const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;   // 32 x 8 threads
+// into y with row stride ldy, through 64 x 64 shared-memory tiles: 16-byte
+// loads along x's rows, 16-byte stores along y's rows (element by element at
+// ragged edges).  x, y and both strides must be 16-byte aligned.
+__global__ void __launch_bounds__(256) transpose_kernel(const uint16_t* __restrict__ x, int64_t rows, int64_t cols,
+                                                         int64_t ldx, uint16_t* __restrict__ y, int64_t ldy) {
+  __shared__ __align__(16) uint16_t tile[64][72];   // 144-byte rows: 16-byte aligned, banks staggered
+  const int64_t r0 = static_cast<int64_t>(blockIdx.y) * 64, c0 = static_cast<int64_t>(blockIdx.x) * 64;
 #pragma unroll
-  for (int i = 0; i < 32; i += 8) {
-    const int64_t r = r0 + ty + i, c = c0 + tx;
-    if (r < rows && c < cols) tile[ty + i][tx] = x[r * ldx + c];
+  for (int i = 0; i < 2; ++i) {
+    const int vec = threadIdx.x + 256 * i, r = vec >> 3, c8 = (vec & 7) * 8;
+    const int64_t gr = r0 + r, gc = c0 + c8;
+    if (gr < rows && gc + 8 <= cols) {
+      *reinterpret_cast<uint4*>(&tile[r][c8]) = __ldg(reinterpret_cast<const uint4*>(x + gr * ldx + gc));
+    } else {
+#pragma unroll
+      for (int e = 0; e < 8; ++e) tile[r][c8 + e] = (gr < rows && gc + e < cols) ? x[gr * ldx + gc + e] : 0;
+    }
   }
   __syncthreads();
 #pragma unroll
-  for (int i = 0; i < 32; i += 8) {
-    const int64_t c = c0 + ty + i, r = r0 + tx;
-    if (r < rows && c < cols) y[c * ldy + r] = tile[tx][ty + i];
+  for (int i = 0; i < 2; ++i) {
+    const int vec = threadIdx.x + 256 * i, oc = vec >> 3, r8 = (vec & 7) * 8;
+    const int64_t gc = c0 + oc, gr = r0 + r8;
+    if (gc >= cols) continue;
+    uint16_t v[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) v[e] = tile[r8 + e][oc];
+    if (gr + 8 <= rows) {
+      uint4 w;
+      w.x = v[0] | (static_cast<uint32_t>(v[1]) << 16);
+      w.y = v[2] | (static_cast<uint32_t>(v[3]) << 16);
+      w.z = v[4] | (static_cast<uint32_t>(v[5]) << 16);
+      w.w = v[6] | (static_cast<uint32_t>(v[7]) << 16);
+      *reinterpret_cast<uint4*>(y + gc * ldy + gr) = w;
+    } else {
+#pragma unroll
+      for (int e = 0; e < 8; ++e)
+        if (gr + e < rows) y[gc * ldy + gr + e] = v[e];
+    }
   }
 }
 
-template <class T>
 cudaError_t transpose(const void* x, int64_t rows, int64_t cols, int64_t ldx, void* y, int64_t ldy,
                       cudaStream_t s) {
-  const dim3 grid(static_cast<unsigned>((cols + 31) / 32), static_cast<unsigned>((rows + 31) / 32));
-  transpose_kernel<T><<<grid, 256, 0, s>>>(static_cast<const T*>(x), rows, cols, ldx, static_cast<T*>(y), ldy);
+  const dim3 grid(static_cast<unsigned>((cols + 63) / 64), static_cast<unsigned>((rows + 63) / 64));
+  transpose_kernel<<<grid, 256, 0, s>>>(static_cast<const uint16_t*>(x), rows, cols, ldx, static_cast<uint16_t*>(y),
+                                        ldy);
   return cudaGetLastError();
 }
 
@@ -202,16 +225,16 @@ cudaError_t bwd_t(const LinearBwdArgs& a, int sms, cudaStream_t s) {
   T* dzt = reinterpret_cast<T*>(ws + w.dzt);
   const int64_t ldn = pad8(a.N), ldv = pad8(a.V);
   cudaError_t e;
-  if ((e = transpose<T>(a.h, a.N, a.D, a.ldh, hT, ldn, s)) != cudaSuccess) return e;
-  if ((e = transpose<T>(a.W, a.V, a.D, a.ldw, WT, ldv, s)) != cudaSuccess) return e;
+  if ((e = transpose(a.h, a.N, a.D, a.ldh, hT, ldn, s)) != cudaSuccess) return e;
+  if ((e = transpose(a.W, a.V, a.D, a.ldw, WT, ldv, s)) != cudaSuccess) return e;
   const DzEpi<T> dze{a.ids, a.k, a.ignore_index, a.V, a.g, a.stats, dz, ldv, dzt, ldn};
-  if ((e = tcg::launch_gemm<BF16>(a.h, a.ldh, a.N, a.W, a.ldw, a.V, a.D, kLinChunkTiles, a.status, dze, sms, s)) !=
+  if ((e = tcg::launch_gemm<BF16>(a.h, a.ldh, a.N, a.W, a.ldw, a.V, a.D, kLinChunkTiles, false, a.status, dze, sms, s)) !=
       cudaSuccess)
     return e;
   const StoreEpi<T> dhe{static_cast<T*>(a.dh), a.D};
-  if ((e = tcg::launch_gemm<BF16>(dz, ldv, a.N, WT, ldv, a.D, a.V, 1, a.status, dhe, sms, s)) != cudaSuccess) return e;
+  if ((e = tcg::launch_gemm<BF16>(dz, ldv, a.N, WT, ldv, a.D, a.V, 1, true, a.status, dhe, sms, s)) != cudaSuccess) return e;
   const StoreEpi<T> dwe{static_cast<T*>(a.dW), a.D};
-  return tcg::launch_gemm<BF16>(dzt, ldn, a.V, hT, ldn, a.D, a.N, 1, a.status, dwe, sms, s);
+  return tcg::launch_gemm<BF16>(dzt, ldn, a.V, hT, ldn, a.D, a.N, 1, true, a.status, dwe, sms, s);
 }
 
 }  // namespace

@@ -38,7 +38,20 @@ struct Sched {
   int64_t M;          // valid rows of the output
   int64_t Ncols;      // valid columns of the output
   int n_row_tiles, n_col_tiles, chunk_tiles, n_chunks, n_units, nk;
+  int cols_fastest;   // unit order: 0 = row tiles fastest (B chunk shared by the CTAs in flight),
+                      // 1 = column chunks fastest (A row panel shared)
   uint32_t* status;   // device status word (tc::kStatusTimeout after a wait ran out)
+
+  // (row tile, column chunk) of unit u
+  __device__ __forceinline__ void unit(int u, int& rt, int& chunk) const {
+    if (cols_fastest) {
+      rt = u / n_chunks;
+      chunk = u - rt * n_chunks;
+    } else {
+      chunk = u / n_row_tiles;
+      rt = u - chunk * n_row_tiles;
+    }
+  }
 };
 
 inline Sched make_sched(int64_t M, int64_t Ncols, int64_t K, int chunk_tiles, uint32_t* status) {
@@ -51,6 +64,7 @@ inline Sched make_sched(int64_t M, int64_t Ncols, int64_t K, int chunk_tiles, ui
   s.n_chunks = (s.n_col_tiles + chunk_tiles - 1) / chunk_tiles;
   s.n_units = s.n_row_tiles * s.n_chunks;
   s.nk = static_cast<int>((K + kBK - 1) / kBK);
+  s.cols_fastest = 0;
   s.status = status;
   return s;
 }
@@ -113,7 +127,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t issued = 0;   // loads issued, for the drain below
       bool ok = true;
       for (int u = blockIdx.x; ok && u < sc.n_units; u += gridDim.x) {
-        const int chunk = u / sc.n_row_tiles, rt = u - chunk * sc.n_row_tiles;
+        int rt, chunk;
+        sc.unit(u, rt, chunk);
         const int t_end = min((chunk + 1) * sc.chunk_tiles, sc.n_col_tiles);
         for (int t = chunk * sc.chunk_tiles; ok && t < t_end; ++t) {
           for (int kb = 0; kb < sc.nk; ++kb) {
@@ -152,7 +167,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t tc_count = 0;
       bool ok = true;
       for (int u = blockIdx.x; ok && u < sc.n_units; u += gridDim.x) {
-        const int chunk = u / sc.n_row_tiles;
+        int rt, chunk;
+        sc.unit(u, rt, chunk);
         const int t_end = min((chunk + 1) * sc.chunk_tiles, sc.n_col_tiles);
         for (int t = chunk * sc.chunk_tiles; ok && t < t_end; ++t, ++tc_count) {
           const uint32_t buf = tc_count & 1u, use = (tc_count >> 1) & 1u;
@@ -196,7 +212,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t tc_count = 0;
     bool ok = true;
     for (int u = blockIdx.x; ok && u < sc.n_units; u += gridDim.x) {
-      const int chunk = u / sc.n_row_tiles, rt = u - chunk * sc.n_row_tiles;
+      int rt, chunk;
+      sc.unit(u, rt, chunk);
       const int t_beg = chunk * sc.chunk_tiles, t_end = min(t_beg + sc.chunk_tiles, sc.n_col_tiles);
       const int64_t row = static_cast<int64_t>(rt) * kBM + r_in_tile;
       const bool row_ok = row < sc.M;
@@ -237,19 +254,251 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
+// ---------------------------------------------------------------------------
+// The same GEMM on CTA pairs (2-SM MMA, tcgen05 cta_group::2).  A cluster of
+// two CTAs computes 256 x 256 tiles: each CTA loads 128 rows of A and 128 of
+// the tile's 256 columns of B, the pair's leader (rank 0) issues 256x256x16
+// MMAs that read both CTAs' shared memory, and each CTA's tensor memory holds
+// its own 128 rows of the accumulator.  Per CTA and K step this moves 32 KB
+// into shared memory instead of 48 KB, which is what lets the tensor pipe
+// run past the shared-memory bandwidth limit of the 1-SM form.
+//   - loads of both CTAs complete on the leader's `full` barriers;
+//   - MMA commits arrive on the `empty` / `acc_full` barriers of both CTAs;
+//   - both CTAs' epilogue warps arrive on the leader's `acc_empty` (8 arrivals).
+// ---------------------------------------------------------------------------
+
+constexpr int kStages2 = 6;
+constexpr uint32_t kStageA2 = kBM * kBK * 2;         // 16 KB: this CTA's 128 rows of A
+constexpr uint32_t kStageB2 = (kBN / 2) * kBK * 2;   // 16 KB: this CTA's 128 columns of B
+constexpr int kNumBars2 = 2 * kStages2 + 4 + 1;
+constexpr size_t kSmem2 = 1024 + kStages2 * (kStageA2 + kStageB2) + kNumBars2 * 8 + 16;
+
+template <bool BF16, class Epi>
+__global__ void __launch_bounds__(kThreads, 1)
+    gemm2_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
+                 const Sched sc, const Epi epi) {
+  extern __shared__ unsigned char smem_raw[];
+  const int pair = static_cast<int>(blockIdx.x >> 1), n_pairs = static_cast<int>(gridDim.x >> 1);
+  if (pair >= sc.n_units) return;   // both CTAs of the pair, before any barrier
+  const uint32_t rank = tc::cluster_rank();
+  const bool leader = rank == 0;
+
+  const uint32_t raw = tc::smem_u32(smem_raw);
+  unsigned char* smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
+  const uint32_t sbase = tc::smem_u32(smem);
+  const uint32_t sA = sbase;
+  const uint32_t sB = sbase + kStages2 * kStageA2;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kStages2 * (kStageA2 + kStageB2));
+  const uint32_t bar0 = tc::smem_u32(bars);
+  auto full = [&](int s) { return bar0 + 8u * s; };
+  auto empty = [&](int s) { return bar0 + 8u * (kStages2 + s); };
+  auto acc_full = [&](int b) { return bar0 + 8u * (2 * kStages2 + b); };
+  auto acc_empty = [&](int b) { return bar0 + 8u * (2 * kStages2 + 2 + b); };
+  const uint32_t done_bar = bar0 + 8u * (2 * kStages2 + 4);
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + kNumBars2);
+  volatile uint32_t* abort_flag = tmem_holder + 1;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages2; ++s) {
+      tc::mbar_init(full(s), 1);    // the leader's: its expect_tx plus both CTAs' bytes
+      tc::mbar_init(empty(s), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      tc::mbar_init(acc_full(b), 1);
+      tc::mbar_init(acc_empty(b), 8);   // the leader's: four epilogue warps in each CTA
+    }
+    tc::mbar_init(done_bar, 1);
+    *abort_flag = 0u;
+    tc::mbar_init_fence();
+    tc::prefetch_tensormap(&tm_a);
+    tc::prefetch_tensormap(&tm_b);
+  }
+  if (warp == 1) tc::tmem_alloc_pair(tc::smem_u32(tmem_holder), kTmemCols);
+  tc::fence_before_sync();
+  tc::cluster_sync_all();   // both CTAs' barriers initialised, tensor memory allocated in both
+  tc::fence_after_sync();
+  const uint32_t tmem = *tmem_holder;
+
+  if (warp == 0) {
+    // ---------------- TMA producer (both CTAs) ----------------
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      for (int u = pair; ok && u < sc.n_units; u += n_pairs) {
+        int rt, chunk;
+        sc.unit(u, rt, chunk);
+        const int t_end = min((chunk + 1) * sc.chunk_tiles, sc.n_col_tiles);
+        for (int t = chunk * sc.chunk_tiles; ok && t < t_end; ++t) {
+          for (int kb = 0; kb < sc.nk; ++kb) {
+            if (!tc::wait(empty(stage), phase ^ 1u, abort_flag, sc.status)) {
+              ok = false;
+              break;
+            }
+            if (leader) tc::mbar_expect_tx(full(stage), 2 * (kStageA2 + kStageB2));
+            const uint32_t lead_full = tc::map_to_rank(full(stage), 0);
+            tc::tma_load_2d_pair(sA + stage * kStageA2, &tm_a, kb * kBK, rt * 2 * kBM + rank * kBM, lead_full);
+            tc::tma_load_2d_pair(sB + stage * kStageB2, &tm_b, kb * kBK, t * kBN + rank * (kBN / 2), lead_full);
+            if (++stage == kStages2) {
+              stage = 0;
+              phase ^= 1u;
+            }
+          }
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ---------------- MMA issuer (the leader) ----------------
+    if (lane == 0 && leader) {
+      constexpr uint32_t idesc = tc::idesc_f16(BF16, 2 * kBM, kBN);
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t tc_count = 0;
+      bool ok = true;
+      for (int u = pair; ok && u < sc.n_units; u += n_pairs) {
+        int rt, chunk;
+        sc.unit(u, rt, chunk);
+        const int t_end = min((chunk + 1) * sc.chunk_tiles, sc.n_col_tiles);
+        for (int t = chunk * sc.chunk_tiles; ok && t < t_end; ++t, ++tc_count) {
+          const uint32_t buf = tc_count & 1u, use = (tc_count >> 1) & 1u;
+          if (!tc::wait(acc_empty(buf), use ^ 1u, abort_flag, sc.status)) {
+            ok = false;
+            break;
+          }
+          tc::fence_after_sync();
+          const uint32_t d = tmem + buf * kBN;
+          for (int kb = 0; kb < sc.nk; ++kb) {
+            if (!tc::wait(full(stage), phase, abort_flag, sc.status)) {
+              ok = false;
+              break;
+            }
+            tc::fence_after_sync();
+            const uint64_t da = tc::sdesc_sw128(sA + stage * kStageA2);
+            const uint64_t db = tc::sdesc_sw128(sB + stage * kStageB2);
+#pragma unroll
+            for (int kk = 0; kk < kBK / kUK; ++kk)
+              tc::mma_f16_pair(d, da + 2ull * kk, db + 2ull * kk, idesc, (kb | kk) != 0 ? 1u : 0u);
+            tc::mma_commit_pair(empty(stage));   // frees this stage in both CTAs
+            if (++stage == kStages2) {
+              stage = 0;
+              phase ^= 1u;
+            }
+          }
+          if (ok) tc::mma_commit_pair(acc_full(buf));
+        }
+      }
+      // every pair MMA has completed before either CTA frees its memory
+      tc::mma_commit_pair(done_bar);
+      tc::wait_drain(done_bar, 0u, sc.status);
+    }
+  } else {
+    // ---------------- epilogue: warps 2-5 of both CTAs ----------------
+    const int quarter = warp & 3;
+    const int r_in_tile = quarter * 32 + lane;
+    const uint32_t lane_addr = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
+    uint32_t tc_count = 0;
+    bool ok = true;
+    for (int u = pair; ok && u < sc.n_units; u += n_pairs) {
+      int rt, chunk;
+      sc.unit(u, rt, chunk);
+      const int t_beg = chunk * sc.chunk_tiles, t_end = min(t_beg + sc.chunk_tiles, sc.n_col_tiles);
+      const int64_t row = static_cast<int64_t>(rt) * 2 * kBM + rank * kBM + r_in_tile;
+      const bool row_ok = row < sc.M;
+      typename Epi::State st = epi.begin(row, row_ok, chunk);
+      for (int t = t_beg; t < t_end; ++t, ++tc_count) {
+        const uint32_t buf = tc_count & 1u, use = (tc_count >> 1) & 1u;
+        const bool got = lane == 0 ? tc::wait(acc_full(buf), use, abort_flag, sc.status) : true;
+        if (!__shfl_sync(0xffffffffu, got ? 1 : 0, 0)) {
+          ok = false;
+          break;
+        }
+        __syncwarp();
+        tc::fence_after_sync();
+        for (int c = 0; c < kBN / 32; ++c) {
+          float v[32];
+          tc::tmem_ld32(lane_addr + buf * kBN + c * 32, v);
+          const int64_t cbase = static_cast<int64_t>(t) * kBN + c * 32;
+          const int64_t left = sc.Ncols - cbase;
+          const int nvalid = left <= 0 ? 0 : (left >= 32 ? 32 : static_cast<int>(left));
+          epi.cols(st, v, row, row_ok, cbase, nvalid);
+        }
+        tc::fence_before_sync();
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive_cluster(tc::map_to_rank(acc_empty(buf), 0));
+      }
+      if (ok) epi.end(st, row, row_ok, chunk);
+    }
+  }
+
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::cluster_sync_all();   // no CTA leaves while its pair may still read its memory
+  if (warp == 1) {
+    __syncwarp();
+    tc::fence_after_sync();
+    tc::tmem_dealloc_pair(tmem, kTmemCols);
+  }
+}
+
 // Tensor map of a [rows, K] 16-bit row-major matrix with row stride ld
 // (elements): a box of 64 x box_rows elements, 128-byte swizzle, zero fill
 // outside the matrix.
 bool encode_kmajor(CUtensorMap* map, const void* base, bool bf16, int64_t rows, int64_t K, int64_t ld,
                    int box_rows);
 
+// 1 for the 1-SM kernel, 2 for CTA pairs (VLS_TC_CTA_GROUP; default 2).
+int cta_group();
+
+template <bool BF16, class Epi>
+cudaError_t launch_gemm2(const void* A, int64_t lda, int64_t M, const void* Bm, int64_t ldb, int64_t Ncols,
+                         int64_t K, int chunk_tiles, bool cols_fastest, uint32_t* status, const Epi& epi, int sms,
+                         cudaStream_t s) {
+  CUtensorMap tm_a, tm_b;
+  if (!encode_kmajor(&tm_a, A, BF16, M, K, lda, kBM) || !encode_kmajor(&tm_b, Bm, BF16, Ncols, K, ldb, kBN / 2))
+    return cudaErrorInvalidValue;
+  Sched sc = make_sched(M, Ncols, K, chunk_tiles, status);
+  sc.n_row_tiles = static_cast<int>((M + 2 * kBM - 1) / (2 * kBM));   // 256-row tiles
+  sc.n_units = sc.n_row_tiles * sc.n_chunks;
+  sc.cols_fastest = cols_fastest ? 1 : 0;
+  auto kern = gemm2_kernel<BF16, Epi>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(kSmem2));
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = kSmem2;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  // a persistent grid: only as many pairs as can be resident at once (a GPC
+  // with an odd number of free SMs leaves one idle)
+  cfg.gridDim = dim3(static_cast<unsigned>(sms & ~1));
+  int resident = 0;
+  if (cudaOccupancyMaxActiveClusters(&resident, kern, &cfg) != cudaSuccess || resident < 1) {
+    cudaGetLastError();
+    resident = sms / 2;
+  }
+  const int pairs = sc.n_units < resident ? sc.n_units : resident;
+  cfg.gridDim = dim3(static_cast<unsigned>(2 * pairs));
+  return cudaLaunchKernelEx(&cfg, kern, tm_a, tm_b, sc, epi);
+}
+
 template <bool BF16, class Epi>
 cudaError_t launch_gemm(const void* A, int64_t lda, int64_t M, const void* Bm, int64_t ldb, int64_t Ncols,
-                        int64_t K, int chunk_tiles, uint32_t* status, const Epi& epi, int sms, cudaStream_t s) {
+                        int64_t K, int chunk_tiles, bool cols_fastest, uint32_t* status, const Epi& epi, int sms,
+                        cudaStream_t s) {
+  if (cta_group() == 2 && sms >= 2)
+    return launch_gemm2<BF16>(A, lda, M, Bm, ldb, Ncols, K, chunk_tiles, cols_fastest, status, epi, sms, s);
   CUtensorMap tm_a, tm_b;
   if (!encode_kmajor(&tm_a, A, BF16, M, K, lda, kBM) || !encode_kmajor(&tm_b, Bm, BF16, Ncols, K, ldb, kBN))
     return cudaErrorInvalidValue;
-  const Sched sc = make_sched(M, Ncols, K, chunk_tiles, status);
+  Sched sc = make_sched(M, Ncols, K, chunk_tiles, status);
+  sc.cols_fastest = cols_fastest ? 1 : 0;
   auto kern = gemm_kernel<BF16, Epi>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(kSmem));
   if (e != cudaSuccess) return e;
