@@ -326,7 +326,7 @@ int64_t vls_linear_logp_bwd_workspace(int64_t N, int64_t D, int64_t V);
  * contiguous, dtype dt.  workspace: at least
  * vls_linear_logp_bwd_workspace(N, D, V) bytes, 256-byte aligned, the
  * caller's; its contents on entry do not matter.  status as for
- * vls_linear_logp_partial.  Row counts N and V are at most 2^21 - 32. */
+ * vls_linear_logp_partial.  Row counts N and V are at most 65535 * 64. */
 int vls_linear_logp_bwd(const void* h, int64_t ldh, const void* W, int64_t ldw, vls_dtype dt, int64_t N,
                         int64_t D, int64_t V, const int64_t* ids, int32_t k, int64_t ignore_index,
                         const float* g, const vls_rowstat* stats, void* dh, void* dW, void* workspace,
