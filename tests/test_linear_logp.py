@@ -219,3 +219,19 @@ def test_autograd_linear_logprobs():
                                       gr.reshape(n, 1).contiguous(), st)
     assert bitwise_equal(lp.reshape(n, 1), ref_lp)
     assert bitwise_equal(h.grad.reshape(n, d), dh) and bitwise_equal(w.grad, dw)
+
+
+def test_one_sm_kernel_in_a_fresh_process():
+    """The 1-SM form of the tensor-core GEMM (VLS_TC_CTA_GROUP=1, read once
+    per process) passes the exact-integer and backward parity checks too."""
+    import os
+    import subprocess
+    import sys
+    here = os.path.dirname(os.path.abspath(__file__))
+    env = dict(os.environ, VLS_TC_CTA_GROUP="1")
+    r = subprocess.run([sys.executable, "-m", "pytest", "-q", "-x", "-p", "no:cacheprovider",
+                        os.path.join(here, "test_linear_logp.py"),
+                        "-k", "exact_integer or (test_backward and 300) or strided_rows"],
+                       env=env, capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0, r.stdout[-3000:] + r.stderr[-2000:]
+    assert " passed" in r.stdout and "failed" not in r.stdout
