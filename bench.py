@@ -458,6 +458,75 @@ class ConfigRun:
             raise SystemExit(f"unknown workload {name}")
         self.launches = L
         self.rows, self.vocab = n, v
+        if name == "fused":
+            w = {"a": w["a"], "b": w["b"], "g": w["g"], "ids": wl["ids"], "gl": wl["g"]}
+        self.autograd = self._autograd_thunks(name, w, device)
+
+    @staticmethod
+    def _autograd_thunks(name, w, device):
+        """(label, bytes, thunk): the public autograd API, forward and backward,
+        for the workload's main op -- the path a training loop calls."""
+        import torch
+
+        import vocab_log_softmax_gb300 as V
+
+        leaves = []
+
+        def fwd_bwd(make):
+            def run():
+                for t in leaves:        # a training step starts from cleared gradients
+                    t.grad = None
+                out, g = make()
+                out.backward(g)
+            return run
+
+        def leaf(t):
+            t = t.detach().requires_grad_(True)
+            leaves.append(t)
+            return t
+
+        if name in ("logp_small", "logp_offset", "long_seq"):
+            x = leaf(w["logits"])
+            ids = w["ids"] if "ids" in w else w["ids1"]
+            g = (w["g"] if "g" in w else w["g1"]).reshape(ids.shape)
+            n, v = x.shape
+            b = op_bytes("logp", n, v, es=x.element_size())
+            return [("autograd logprobs fwd+bwd", b["fwd"] + b["bwd"], fwd_bwd(lambda: (V.logprobs(x, ids), g)))]
+        if name == "kl_masked":
+            a = leaf(w["a"])
+            n, v = a.shape
+            be, bk = op_bytes("entropy", n, v), op_bytes("kl_reverse", n, v)
+            return [("autograd entropy fwd+bwd", be["fwd"] + be["bwd"], fwd_bwd(lambda: (V.entropy(a), w["g"]))),
+                    ("autograd reverse KL fwd+bwd", bk["fwd"] + bk["bwd"],
+                     fwd_bwd(lambda: (V.kl(a, w["b"], "reverse"), w["g"])))]
+        if name == "softcap_wide":
+            x = leaf(w["logits"])
+            n, v = x.shape
+            b, bs = op_bytes("cap_logp", n, v), op_bytes("softcap", n, v)
+            g = w["g"].reshape(w["ids"].shape)
+            return [("autograd cap30 logprobs fwd+bwd", b["fwd"] + b["bwd"],
+                     fwd_bwd(lambda: (V.logprobs(x, w["ids"], softcap=30.0), g))),
+                    ("autograd softcap fwd+bwd", bs["fwd"] + bs["bwd"],
+                     fwd_bwd(lambda: (V.softcap(x, 30.0), w["gy_bf16"])))]
+        if name == "fused":
+            a = leaf(w["a"])
+            n, v = a.shape
+            gl = w["gl"].reshape(w["ids"].shape)
+
+            def stats_run():
+                a.grad = None
+                lp, H, kl = V.stats(a, w["ids"], reference=w["b"])
+                torch.autograd.backward([lp, H, kl], [gl, w["g"], w["g"]])
+            return [("autograd stats (logp+H+KL) fwd+bwd", 5 * n * v * 2, stats_run)]
+        if name == "linear_logp":
+            h = leaf(w["h"])
+            wt = leaf(w["w"])
+            g = w["g"].reshape(w["ids"].shape)
+            n, d = h.shape
+            return [("autograd linear_logprobs fwd+bwd", (n + wt.shape[0]) * d * 2 * 3,
+                     fwd_bwd(lambda: (V.linear_logprobs(h, wt, w["ids"]), g)),
+                     4 * 2 * n * wt.shape[0] * d)]
+        return []
 
 
 def run_config(args) -> None:
@@ -493,9 +562,70 @@ def run_config(args) -> None:
         raise SystemExit(f"{run.name}: a bounded wait in the kernel ran out (status {int(run.status.item())})")
     total_b = sum(b for _, b, *_ in run.launches)
     total_ms = sum(o["ms_median"] for o in ops.values())
+    # an op's forward and backward timed back to back (one event pair around both)
+    pairs = {}
+    for j in range(len(run.launches) - 1):
+        lf, lb = run.launches[j][0], run.launches[j + 1][0]
+        if lf.endswith(" fwd") and lb == lf[:-4] + " bwd":
+            ts = sorted(ev[s][j].elapsed_time(ev[s][j + 2]) for s in range(args.steps))
+            nb = run.launches[j][1] + run.launches[j + 1][1]
+            pairs[lf[:-4] + " fwd+bwd"] = {"ms_median": round(ts[len(ts) // 2], 4), "ms_p10": round(ts[len(ts) // 10], 4),
+                                           "ms_p90": round(ts[(9 * len(ts)) // 10], 4),
+                                           "tbs": round(nb / ts[len(ts) // 2] / 1e9, 3)}
+    autograd = {}
+    for label, nbytes, f, *fl in run.autograd:
+        ts = time_thunk(f, args.steps, args.warmup, stream)
+        med = ts[len(ts) // 2]
+        autograd[label] = {"ms_median": round(med, 4), "ms_p10": round(ts[len(ts) // 10], 4),
+                           "ms_p90": round(ts[(9 * len(ts)) // 10], 4), "tbs": round(nbytes / med / 1e9, 3)}
+        if fl:
+            autograd[label]["tflops"] = round(fl[0] / med / 1e9, 1)
+    graph = graph_replay(run, args.steps, stream) if run.name == "logp_small" else None
     print(json.dumps({"workload": run.name, "rows": run.rows, "vocab": run.vocab, "steps": args.steps,
                       "fwd_bwd_ms": round(total_ms, 4), "tbs": round(total_b / total_ms / 1e9, 3),
-                      "peak_gbs": peak, "peak_kind": kind, "ops": ops}), flush=True)
+                      "peak_gbs": peak, "peak_kind": kind, "ops": ops, "fwd_bwd_back_to_back": pairs,
+                      "autograd": autograd, "graph_replay": graph}), flush=True)
+
+
+def time_thunk(f, steps: int, warmup: int, stream) -> list:
+    """Sorted CUDA-event times (ms) of f() over `steps` calls after `warmup`."""
+    import torch
+    for _ in range(warmup):
+        f()
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    for a, b in ev:
+        a.record(stream)
+        f()
+        b.record(stream)
+    torch.cuda.synchronize()
+    return sorted(a.elapsed_time(b) for a, b in ev)
+
+
+def graph_replay(run, steps: int, stream) -> dict:
+    """The workload's launches captured once in a CUDA graph and replayed: the
+    per-replay time without host launch overhead (for launch-bound sizes)."""
+    import torch
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        for _ in range(3):
+            for _, _, f, *_ in run.launches:
+                f()
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    try:
+        with torch.cuda.graph(graph):
+            for _, _, f, *_ in run.launches:
+                f()
+    except RuntimeError as e:
+        return {"unavailable": str(e).splitlines()[0][:200]}
+    ts = time_thunk(graph.replay, steps, 3, torch.cuda.current_stream())
+    nb = sum(b for _, b, *_ in run.launches)
+    med = ts[len(ts) // 2]
+    return {"launches_per_replay": len(run.launches), "ms_median": round(med, 4), "ms_p10": round(ts[len(ts) // 10], 4),
+            "ms_p90": round(ts[(9 * len(ts)) // 10], 4), "tbs": round(nb / med / 1e9, 3)}
 
 
 E2E_CHUNKS = 8

@@ -36,6 +36,12 @@
  *  - Results are deterministic and batch invariant: a row's outputs depend
  *    only on that row's data, V and the dtype, bit for bit, not on N, on the
  *    row's position or on the alignment of the row in memory.
+ *  - CUDA graphs: the calls may be recorded by stream capture (any capture
+ *    mode).  While `stream` is capturing, the launch goes to the current
+ *    device and pointers are not checked against it (the runtime refuses
+ *    those queries inside a capture).  Make one call of each kind before
+ *    capturing, so the first-use set-up of the tensor-core kernels happens
+ *    outside it.
  *  - Errors: each call returns VLS_OK (0) or one of the VLS_ERR_* codes
  *    below; it never aborts, throws or prints.  Argument errors are found
  *    before any CUDA call.  vls_status_string() names a code.

@@ -76,6 +76,26 @@ int sm_count(int dev) {
 
 // Finds the one device that holds every non-NULL pointer and owns the stream.
 int resolve_device(std::initializer_list<const void*> ptrs, void* stream, int* dev_out) {
+  // While a stream is being captured into a CUDA graph the runtime refuses
+  // pointer-attribute and stream-device queries, and the refusal would end the
+  // capture: take the current device, which the capturing caller has made the
+  // stream's (that is what CUDA requires of a launch into a capture anyway).
+  if (reinterpret_cast<uintptr_t>(stream) > 2) {
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(static_cast<cudaStream_t>(stream), &cs) != cudaSuccess) {
+      cudaGetLastError();
+      return VLS_ERR_DEVICE;
+    }
+    if (cs != cudaStreamCaptureStatusNone) {
+      int cur = -1;
+      if (cudaGetDevice(&cur) != cudaSuccess) {
+        cudaGetLastError();
+        return VLS_ERR_DEVICE;
+      }
+      *dev_out = cur;
+      return VLS_OK;
+    }
+  }
   int dev = -1;
   for (const void* p : ptrs) {
     if (!p) continue;

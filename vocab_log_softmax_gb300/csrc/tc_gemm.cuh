@@ -34,6 +34,8 @@ constexpr uint32_t kTmemCols = 2 * kBN;       // two fp32 accumulators of 256 co
 constexpr int kNumBars = 2 * kStages + 4 + 1; // full, empty, acc_full x2, acc_empty x2, done
 constexpr size_t kSmem = 1024 /* alignment slack */ + kStages * (kStageA + kStageB) + kNumBars * 8 + 16;
 
+constexpr int kMaxDev = 64;   // devices the per-device launch caches cover
+
 struct Sched {
   int64_t M;          // valid rows of the output
   int64_t Ncols;      // valid columns of the output
@@ -462,8 +464,11 @@ cudaError_t launch_gemm2(const void* A, int64_t lda, int64_t M, const void* Bm, 
   sc.n_units = sc.n_row_tiles * sc.n_chunks;
   sc.cols_fastest = cols_fastest ? 1 : 0;
   auto kern = gemm2_kernel<BF16, Epi>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(kSmem2));
-  if (e != cudaSuccess) return e;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) return cudaErrorInvalidDevice;
+  // per device and kernel, once: the shared-memory opt-in and the number of
+  // resident pairs (runtime queries are kept out of stream capture)
+  static int resident_on[kMaxDev] = {0};
   cudaLaunchConfig_t cfg = {};
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = kSmem2;
@@ -477,13 +482,18 @@ cudaError_t launch_gemm2(const void* A, int64_t lda, int64_t M, const void* Bm, 
   cfg.numAttrs = 1;
   // a persistent grid: only as many pairs as can be resident at once (a GPC
   // with an odd number of free SMs leaves one idle)
-  cfg.gridDim = dim3(static_cast<unsigned>(sms & ~1));
-  int resident = 0;
-  if (cudaOccupancyMaxActiveClusters(&resident, kern, &cfg) != cudaSuccess || resident < 1) {
-    cudaGetLastError();
-    resident = sms / 2;
+  if (resident_on[dev] == 0) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(kSmem2));
+    if (e != cudaSuccess) return e;
+    cfg.gridDim = dim3(static_cast<unsigned>(sms & ~1));
+    int resident = 0;
+    if (cudaOccupancyMaxActiveClusters(&resident, kern, &cfg) != cudaSuccess || resident < 1) {
+      cudaGetLastError();
+      resident = sms / 2;
+    }
+    resident_on[dev] = resident;
   }
-  const int pairs = sc.n_units < resident ? sc.n_units : resident;
+  const int pairs = sc.n_units < resident_on[dev] ? sc.n_units : resident_on[dev];
   cfg.gridDim = dim3(static_cast<unsigned>(2 * pairs));
   return cudaLaunchKernelEx(&cfg, kern, tm_a, tm_b, sc, epi);
 }
@@ -500,8 +510,14 @@ cudaError_t launch_gemm(const void* A, int64_t lda, int64_t M, const void* Bm, i
   Sched sc = make_sched(M, Ncols, K, chunk_tiles, status);
   sc.cols_fastest = cols_fastest ? 1 : 0;
   auto kern = gemm_kernel<BF16, Epi>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(kSmem));
-  if (e != cudaSuccess) return e;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) return cudaErrorInvalidDevice;
+  static bool opted_in[kMaxDev] = {false};   // per device and kernel, once
+  if (!opted_in[dev]) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(kSmem));
+    if (e != cudaSuccess) return e;
+    opted_in[dev] = true;
+  }
   const int grid = sc.n_units < sms ? sc.n_units : sms;
   kern<<<grid, kThreads, kSmem, s>>>(tm_a, tm_b, sc, epi);
   return cudaGetLastError();
