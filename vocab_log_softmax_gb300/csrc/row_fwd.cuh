@@ -62,7 +62,7 @@ struct LogpAcc {
       fp2 d;
       if (CAP) {
         fp2 e2, r2;
-        d = fma2(cap_t2(v, i, K, e2, r2), splat(K.c), nm2);
+        d = fma2((i & 1) ? cap_t2<T, true>(v, i, K, e2, r2) : cap_t2<T, false>(v, i, K, e2, r2), splat(K.c), nm2);
       } else {
         d = add2(v.pair(i), nm2);
       }
@@ -96,7 +96,7 @@ struct EntropyAcc {
       fp2 d;
       if (CAP) {
         fp2 e2, r2;
-        d = fma2(cap_t2(v, i, K, e2, r2), splat(K.c), nm2);
+        d = fma2((i & 1) ? cap_t2<T, true>(v, i, K, e2, r2) : cap_t2<T, false>(v, i, K, e2, r2), splat(K.c), nm2);
       } else {
         d = add2(v.pair_clamped(i), nm2);  // -inf columns: e = 0 and 0 * d = 0
       }
@@ -141,8 +141,8 @@ struct KlAcc {
         fp2 dp, dq;
         if (CAP) {
           fp2 e2, r2;
-          dp = fma2(cap_t2(v, i, K, e2, r2), splat(K.c), nmp2);
-          dq = fma2(cap_t2(q, i, K, e2, r2), splat(K.c), nmq2);
+          dp = fma2((i & 1) ? cap_t2<T, true>(v, i, K, e2, r2) : cap_t2<T, false>(v, i, K, e2, r2), splat(K.c), nmp2);
+          dq = fma2((i & 1) ? cap_t2<T, true>(q, i, K, e2, r2) : cap_t2<T, false>(q, i, K, e2, r2), splat(K.c), nmq2);
         } else {
           dp = add2(v.pair_clamped(i), nmp2);
           dq = add2(q.pair_clamped(i), nmq2);
@@ -212,8 +212,9 @@ struct FusedAcc {
         fp2 da, db = 0;
         if (CAP) {
           fp2 e2, r2;
-          da = fma2(cap_t2(v, i, K, e2, r2), splat(K.c), nma2);
-          if constexpr (kHasB) db = fma2(cap_t2(q, i, K, e2, r2), splat(K.c), nmb2);
+          da = fma2((i & 1) ? cap_t2<T, true>(v, i, K, e2, r2) : cap_t2<T, false>(v, i, K, e2, r2), splat(K.c), nma2);
+          if constexpr (kHasB)
+            db = fma2((i & 1) ? cap_t2<T, true>(q, i, K, e2, r2) : cap_t2<T, false>(q, i, K, e2, r2), splat(K.c), nmb2);
         } else {
           da = add2(v.pair_clamped(i), nma2);
           if constexpr (kHasB) db = add2(q.pair_clamped(i), nmb2);
@@ -271,14 +272,16 @@ constexpr int fwd_unroll() { return reads_two<OP, DIR>() ? 2 : 4; }
 // moved with the size of the argument struct (the bf16 entropy sweep went
 // from 32 to 38 registers, the KL sweep from 44 to 56), costing 5-8% of
 // bandwidth.  The bounds below keep the 16-bit sweeps at 32 registers (one
-// tensor), 40 (fused or softcapped one-tensor sweeps) and 48 (bf16 KL);
+// tensor), 40 (fused, or softcapped logp), 48 (softcapped entropy and fused,
+// bf16 KL);
 // fp32 vectors hold twice the registers and get 64.
 template <class T, int OP, bool CAP, int DIR>
 constexpr int fwd_ctas_at_256() {
   if (sizeof(T) == 4) return 4;
   if (reads_two<OP, DIR>())
     return (CAP || OP == kFwdFused || !std::is_same<T, __nv_bfloat16>::value) ? 4 : 5;
-  return (OP == kFwdFused || (CAP && OP != kFwdLogp)) ? 6 : 8;
+  if (CAP) return OP == kFwdLogp ? 6 : 5;
+  return OP == kFwdFused ? 6 : 8;
 }
 template <class T, int OP, bool CAP, int DIR>
 constexpr int fwd_min_blocks() {

@@ -328,11 +328,27 @@ __device__ __forceinline__ float cap_t(float x, const CapK& K) {
   return cap_t(x, K, e, r);
 }
 
-// Packed form of cap_t for pair i of a raw vector (same operations).
-template <class T>
+// 1/d for d in [1, 2] on the FMA pipe instead of the special-function unit:
+// the minimax quadratic 70/33 - (48/33) d + (32/99) d^2 (relative error at
+// most 1/99 on [1, 2], equioscillating at four points) refined by two
+// Newton-Raphson steps r <- r + r (1 - d r), each of which squares the
+// relative error (about 1e-8 after two, within about one fp32 ulp).
+__device__ __forceinline__ fp2 rcp2_fma(fp2 d) {
+  fp2 r = fma2(fma2(d, splat(32.0f / 99.0f), splat(-48.0f / 33.0f)), d, splat(70.0f / 33.0f));
+  const fp2 nd = mul2(d, splat(-1.0f));
+  r = fma2(r, fma2(nd, r, splat(1.0f)), r);
+  return fma2(r, fma2(nd, r, splat(1.0f)), r);
+}
+
+// Packed form of cap_t for pair i of a raw vector (same operations).  With
+// FMA_RCP the reciprocal 1/(1+e) is taken on the FMA pipe (rcp2_fma): the
+// softcapped forward sweeps do this for every other pair, so that the
+// special-function unit, their bound, carries 2.5 instead of 3 operations
+// per element.
+template <class T, bool FMA_RCP = false>
 __device__ __forceinline__ fp2 cap_t2(const Raw8<T>& v, int i, const CapK& K, fp2& e2, fp2& r2) {
   e2 = ex2_2(mul2(v.pair_abs(i), splat(K.k)));
-  r2 = rcp2(add2(e2, splat(1.0f)));
+  r2 = FMA_RCP ? rcp2_fma(add2(e2, splat(1.0f))) : rcp2(add2(e2, splat(1.0f)));
   float t0, t1;
   upk(mul2(sub2(splat(1.0f), e2), r2), t0, t1);
   t0 = __uint_as_float(__float_as_uint(t0) | (v.sign_lo(i) & 0x80000000u));
