@@ -29,11 +29,17 @@ using namespace dev;
 //    sort, so duplicates sit together in ascending j; for each distinct id
 //    in this CTA's columns, the sum of its upstream gradients in ascending j.
 // Shared memory: keys[P] (P = next power of two >= k), fix_id[k], g[k],
-// fix_g[k]: 8 P + 16 k bytes.
+// fix_g[k], and a bitmap of this CTA's 8-column vectors that hold a valid id
+// (used by the top-k logprob map, which writes its one-hot columns inline):
+// 8 P + 16 k + 4 ceil(vectors / 32) bytes.
 struct TopkPrep {
   float G;
   int nfix;
   bool any_valid;
+  const unsigned long long* key;   // the P sorted keys
+  const float* g;                  // the k upstream gradients, by j
+  const uint32_t* bitmap;          // vectors of this CTA that hold a valid id
+  int P;
 };
 
 constexpr int kTopkJBits = 11;  // j < 2048 > VLS_MAX_TOPK
@@ -44,9 +50,11 @@ __host__ __device__ __forceinline__ int topk_pow2(int k) {
   return p;
 }
 
-// keys[P] + fix_id[k] (8 bytes each) + g[k] + fix_g[k] (4 bytes each)
-__host__ __device__ __forceinline__ size_t topk_smem_bytes(int k) {
-  return 8 * static_cast<size_t>(topk_pow2(k)) + 16 * static_cast<size_t>(k);
+// keys[P] + fix_id[k] (8 bytes each) + g[k] + fix_g[k] (4 bytes each) + the
+// vector bitmap
+__host__ __device__ __forceinline__ size_t topk_smem_bytes(int k, int64_t vec_per_cta) {
+  return 8 * static_cast<size_t>(topk_pow2(k)) + 16 * static_cast<size_t>(k) +
+         4 * static_cast<size_t>((vec_per_cta + 31) / 32);
 }
 
 __device__ __forceinline__ TopkPrep prep_topk(const BwdArgs& a, int64_t row, int64_t col_beg, int64_t col_end,
@@ -60,9 +68,12 @@ __device__ __forceinline__ TopkPrep prep_topk(const BwdArgs& a, int64_t row, int
   fix_id = reinterpret_cast<int64_t*>(key + P);
   float* s_g = reinterpret_cast<float*>(fix_id + k);
   fix_g = s_g + k;
+  uint32_t* bitmap = reinterpret_cast<uint32_t*>(fix_g + k);
   constexpr unsigned long long kNone = ~0ull;
 
   if (threadIdx.x == 0) *s_nfix = 0;
+  const int nwords = static_cast<int>((col_end - col_beg + 255) >> 8);   // one bit per 8-column vector
+  for (int w = threadIdx.x; w < nwords; w += kRowThreads) bitmap[w] = 0u;
   float gpart = 0.0f;
   int any = 0;
   for (int j = threadIdx.x; j < P; j += kRowThreads) {
@@ -118,9 +129,55 @@ __device__ __forceinline__ TopkPrep prep_topk(const BwdArgs& a, int64_t row, int
     const int slot = atomicAdd(s_nfix, 1);
     fix_id[slot] = local;
     fix_g[slot] = gs;
+    const int64_t vi = (local - col_beg) >> 3;
+    atomicOr(&bitmap[vi >> 5], 1u << (vi & 31));
   }
   __syncthreads();
-  return TopkPrep{G, *s_nfix, any_valid};
+  return TopkPrep{G, *s_nfix, any_valid, key, s_g, bitmap, P};
+}
+
+// One-hot columns of one 8-column vector of the top-k logprob map, written
+// by the thread that has just stored the vector, from the raw values it
+// holds: column c gets (the sum of g_j over the valid ids_j = c, ascending j)
+// - G p_c with one rounding (times dz/dx with a cap), the arithmetic of the
+// k = 1 map's fix-up.  gcol0: the vector's first global column.  Rare (a
+// row has at most k such vectors), so it is not inlined into the sweep.
+template <class T, bool CAP>
+__device__ __noinline__ void onehot_vector(T* dst, const Raw8<T> x, int64_t gcol0, int nvalid,
+                                           const unsigned long long* key, int P, const float* s_g, float m,
+                                           float log_s, float G, float cap) {
+  const unsigned long long first = static_cast<unsigned long long>(gcol0) << kTopkJBits;
+  int lo = 0, hi = P;
+  while (lo < hi) {
+    const int mid = (lo + hi) >> 1;
+    if (key[mid] < first)
+      lo = mid + 1;
+    else
+      hi = mid;
+  }
+  const CapK K = cap_consts(CAP ? cap : 1.0f);
+  int t = lo;
+  while (t < P) {
+    const unsigned long long id = key[t] >> kTopkJBits;   // the invalid keys (all ones) sort last, far beyond
+    const int64_t e = static_cast<int64_t>(id) - gcol0;
+    if (e >= nvalid) break;
+    float gs = 0.0f;
+    for (; t < P && (key[t] >> kTopkJBits) == id; ++t) gs += s_g[key[t] & ((1ull << kTopkJBits) - 1)];
+    float xa, xb;
+    upk(x.pair(static_cast<int>(e) >> 1), xa, xb);
+    const float xe = (e & 1) ? xb : xa;
+    float d, chain = 1.0f;
+    if (CAP) {
+      float ee, r;
+      d = cap_d(cap_t(xe, K, ee, r), K.c, m);
+      chain = 4.0f * ee * r * r;
+    } else {
+      d = xe - m;
+    }
+    const float p = ex2(fmaf(d, kLog2e, -log_s * kLog2e));
+    const float r = fmaf(-G, p, gs);
+    Out8<T>::store1(dst + e, CAP ? r * chain : r);
+  }
 }
 
 // Row constants of a backward map.
@@ -224,8 +281,11 @@ __device__ __forceinline__ float fused_at(const T* xr, const T* yr, int64_t c, c
 // loads in flight; with a larger register budget occupancy halves and the
 // sweep slows down.  The softcapped map runs a software pipeline and gets
 // kCapMinBlocks CTAs per SM.
-template <class T, int OP, bool CAP, int DIR = kFusedNoKl>
-__global__ void __launch_bounds__(kRowThreads, CAP ? kCapMinBlocks : 6) row_bwd_kernel(const BwdArgs a) {
+// TOPK (logprob map with k > 1): the one-hot columns are written inline by
+// the thread that stores their vector (onehot_vector) instead of by a
+// post-pass that re-reads them after a barrier.
+template <class T, int OP, bool CAP, int DIR = kFusedNoKl, bool TOPK = false>
+__global__ void __launch_bounds__(kRowThreads, (CAP || TOPK) ? kCapMinBlocks : 6) row_bwd_kernel(const BwdArgs a) {
   constexpr bool KL = bwd_reads_two<OP, DIR>();
   const int64_t row = blockIdx.x / a.chunks;
   const int q = static_cast<int>(blockIdx.x - row * a.chunks);
@@ -257,6 +317,7 @@ __global__ void __launch_bounds__(kRowThreads, CAP ? kCapMinBlocks : 6) row_bwd_
   bool nan_row = false, zero_row = false;
   int64_t* fix_id = nullptr;
   float* fix_g = nullptr;
+  TopkPrep tp{};
   const bool has_logp = OP == kBwdLogp || (OP == kBwdFused && a.g != nullptr);
   if (OP == kBwdLogp || OP == kBwdFused) {
     // k = 1: one fixed slot; k > 1: sorted keys, upstream grads and the
@@ -296,7 +357,7 @@ __global__ void __launch_bounds__(kRowThreads, CAP ? kCapMinBlocks : 6) row_bwd_
           if (pv < (V >> 3) && pv < ve) prefetch_l2(xr + 8 * pv);
         }
       }
-      const TopkPrep tp = prep_topk(a, row, col_beg, col_end, topk_smem, fix_id, fix_g, s_warp, &s_nfix);
+      tp = prep_topk(a, row, col_beg, col_end, topk_smem, fix_id, fix_g, s_warp, &s_nfix);
       G = tp.G;
       nfix = tp.nfix;
       zero_row = !tp.any_valid;
@@ -366,6 +427,19 @@ __global__ void __launch_bounds__(kRowThreads, CAP ? kCapMinBlocks : 6) row_bwd_
     return;
   }
 
+  // top-k: the one-hot columns of a stored vector, when the bitmap flags it
+  const uint32_t* const bitmap = tp.bitmap;
+  const unsigned long long* const tkey = tp.key;
+  const float* const tg = tp.g;
+  const int tP = tp.P;
+  const float row_m = sx.m, row_ls = sx.log_s, row_G = G, row_cap = a.cap;
+  const int64_t voff = a.vocab_offset;
+  auto onehot_if_flagged = [=](int64_t vec, const Raw8<T>& xv, int nvalid) {
+    const int64_t vi = vec - vb;
+    if ((bitmap[vi >> 5] >> (vi & 31)) & 1u)
+      onehot_vector<T, CAP>(dr + 8 * vec, xv, 8 * vec + voff, nvalid, tkey, tP, tg, row_m, row_ls, row_G, row_cap);
+  };
+
   int64_t v = vb + threadIdx.x;
   const int64_t vfull_end = min(ve, V >> 3);
   if constexpr (CAP) {
@@ -390,6 +464,7 @@ __global__ void __launch_bounds__(kRowThreads, CAP ? kCapMinBlocks : 6) row_bwd_
 #pragma unroll
           for (int i = 0; i < 4; ++i) o[i] = grad_pair<T, OP, CAP, DIR>(x[u], KL ? y[u] : x[u], i, R, K);
           Out8<T>::store(dr + 8 * (at + u * kRowThreads), o);
+          if constexpr (TOPK) onehot_if_flagged(at + u * kRowThreads, x[u], 8);
         }
       };
       load(xa, ya, v);
@@ -423,6 +498,7 @@ __global__ void __launch_bounds__(kRowThreads, CAP ? kCapMinBlocks : 6) row_bwd_
 #pragma unroll
           for (int i = 0; i < 4; ++i) o[i] = grad_pair<T, OP, CAP, DIR>(x[u], KL ? y[u] : x[u], i, R, K);
           Out8<T>::store(dr + 8 * (v + u * kRowThreads), o);
+          if constexpr (TOPK) onehot_if_flagged(v + u * kRowThreads, x[u], 8);
         }
       }
     }
@@ -436,6 +512,7 @@ __global__ void __launch_bounds__(kRowThreads, CAP ? kCapMinBlocks : 6) row_bwd_
 #pragma unroll
     for (int i = 0; i < 4; ++i) o[i] = grad_pair<T, OP, CAP, DIR>(x, KL ? y : x, i, R, K);
     store_vec(dr, v, V, al, o);
+    if constexpr (TOPK) onehot_if_flagged(v, x, valid);
   }
 
   if constexpr (OP == kBwdFused) {
@@ -449,7 +526,7 @@ __global__ void __launch_bounds__(kRowThreads, CAP ? kCapMinBlocks : 6) row_bwd_
       }
     }
   }
-  if constexpr (OP == kBwdLogp) {
+  if constexpr (OP == kBwdLogp && !TOPK) {
     // one-hot columns: rewrite with (g_sum - G p) dz/dx, one rounding at the store
     if (nfix > 0) {
       __syncthreads();  // the streamed stores of this CTA precede the rewrites
@@ -476,8 +553,11 @@ template <class T, int OP, bool CAP, int DIR = kFusedNoKl>
 cudaError_t launch_bwd_t(const BwdArgs& a, cudaStream_t s) {
   const dim3 grid(static_cast<unsigned>(a.rows * a.chunks));
   const bool topk = (OP == kBwdLogp || (OP == kBwdFused && a.g != nullptr)) && a.k > 1;
-  const size_t smem = topk ? topk_smem_bytes(a.k) : 0;
-  row_bwd_kernel<T, OP, CAP, DIR><<<grid, kRowThreads, smem, s>>>(a);
+  const size_t smem = topk ? topk_smem_bytes(a.k, a.vec_per_cta) : 0;
+  if (OP == kBwdLogp && topk)
+    row_bwd_kernel<T, OP, CAP, DIR, true><<<grid, kRowThreads, smem, s>>>(a);
+  else
+    row_bwd_kernel<T, OP, CAP, DIR, false><<<grid, kRowThreads, smem, s>>>(a);
   return cudaGetLastError();
 }
 

@@ -271,9 +271,9 @@ constexpr int fwd_unroll() { return reads_two<OP, DIR>() ? 2 : 4; }
 // Without an explicit minimum, ptxas sized these kernels by heuristics that
 // moved with the size of the argument struct (the bf16 entropy sweep went
 // from 32 to 38 registers, the KL sweep from 44 to 56), costing 5-8% of
-// bandwidth.  The bounds below keep the 16-bit sweeps at 32 registers (one
-// tensor), 40 (fused, or softcapped logp), 48 (softcapped entropy and fused,
-// bf16 KL);
+// bandwidth.  The bounds below keep the bf16 sweeps at 32 registers (one
+// tensor), 40 (fp16 one-tensor, fused, or softcapped logp), 48 (softcapped
+// entropy and fused, bf16 KL);
 // fp32 vectors hold twice the registers and get 64.
 template <class T, int OP, bool CAP, int DIR>
 constexpr int fwd_ctas_at_256() {
@@ -281,7 +281,7 @@ constexpr int fwd_ctas_at_256() {
   if (reads_two<OP, DIR>())
     return (CAP || OP == kFwdFused || !std::is_same<T, __nv_bfloat16>::value) ? 4 : 5;
   if (CAP) return OP == kFwdLogp ? 6 : 5;
-  return OP == kFwdFused ? 6 : 8;
+  return (OP == kFwdFused || std::is_same<T, __half>::value) ? 6 : 8;
 }
 template <class T, int OP, bool CAP, int DIR>
 constexpr int fwd_min_blocks() {
@@ -343,6 +343,18 @@ __global__ void __launch_bounds__(kFwdThreads, (fwd_min_blocks<T, OP, CAP, DIR>(
   const int64_t vfull_end = min(ve, V >> 3);
   const bool al = aligned16(xr) && aligned16(yr);
   const CapK K = cap_consts(CAP ? a.cap : 1.0f);
+
+  // The row's first kFwdThreads target logits are loaded now by the CTA that
+  // finalises the row (rank 0), so their latency overlaps the sweep instead
+  // of following it (top-k rows gather up to k scattered columns).
+  float xt0 = 0.0f;
+  if constexpr (OP == kFwdLogp) {
+    if (q == 0 && static_cast<int>(threadIdx.x) < a.k) {
+      const int64_t id = a.ids[row * a.k + threadIdx.x];
+      const int64_t local = id - a.vocab_offset;
+      if (valid_id(id, a.vocab_total, a.ignore_index) && local >= 0 && local < V) xt0 = load1(xr + local);
+    }
+  }
 
   Acc acc;
   int64_t v = vb + threadIdx.x;
@@ -410,7 +422,7 @@ __global__ void __launch_bounds__(kFwdThreads, (fwd_min_blocks<T, OP, CAP, DIR>(
         const int64_t id = a.ids[row * a.k + j];
         const int64_t local = id - a.vocab_offset;
         const bool own = valid_id(id, a.vocab_total, a.ignore_index) && local >= 0 && local < V;
-        a.zt[row * a.k + j] = own ? load1(xr + local) : 0.0f;
+        a.zt[row * a.k + j] = own ? (j < kFwdThreads ? xt0 : load1(xr + local)) : 0.0f;
       }
     }
     return;
@@ -421,7 +433,8 @@ __global__ void __launch_bounds__(kFwdThreads, (fwd_min_blocks<T, OP, CAP, DIR>(
     if (threadIdx.x == 0) a.stats_x[row] = vls_rowstat{m, log_s};
     for (int j = threadIdx.x; j < a.k; j += kFwdThreads) {
       const int64_t id = a.ids[row * a.k + j];
-      a.logp[row * a.k + j] = valid_id(id, V, a.ignore_index) ? logp_of<CAP>(load1(xr + id), m, log_s, K) : 0.0f;
+      a.logp[row * a.k + j] =
+          valid_id(id, V, a.ignore_index) ? logp_of<CAP>(j < kFwdThreads ? xt0 : load1(xr + id), m, log_s, K) : 0.0f;
     }
   } else if constexpr (OP == kFwdEntropy) {
     if (threadIdx.x == 0) {
