@@ -67,18 +67,30 @@ struct LogpEpi {
 
   __device__ void cols(State& st, const float (&v)[32], int64_t, bool, int64_t cbase, int nvalid) const {
     float cmax = dev::neg_inf();
-#pragma unroll
-    for (int i = 0; i < 32; ++i) cmax = i < nvalid ? fmaxf(cmax, v[i]) : cmax;
-    if (cmax > st.m) {
-      st.s = st.m == dev::neg_inf() ? 0.0f : st.s * dev::ex2((st.m - cmax) * dev::kLog2e);
-      st.m = cmax;
-    }
     float cs = 0.0f;   // z - m is formed first, as in the row sweeps
+    if (nvalid == 32) {   // every chunk but the vocabulary's last
 #pragma unroll
-    for (int i = 0; i < 32; ++i) cs += i < nvalid ? dev::ex2((v[i] - st.m) * dev::kLog2e) : 0.0f;
+      for (int i = 0; i < 32; ++i) cmax = fmaxf(cmax, v[i]);
+      if (cmax > st.m) {
+        st.s = st.m == dev::neg_inf() ? 0.0f : st.s * dev::ex2((st.m - cmax) * dev::kLog2e);
+        st.m = cmax;
+      }
+#pragma unroll
+      for (int i = 0; i < 32; ++i) cs += dev::ex2((v[i] - st.m) * dev::kLog2e);
+    } else {
+#pragma unroll
+      for (int i = 0; i < 32; ++i) cmax = i < nvalid ? fmaxf(cmax, v[i]) : cmax;
+      if (cmax > st.m) {
+        st.s = st.m == dev::neg_inf() ? 0.0f : st.s * dev::ex2((st.m - cmax) * dev::kLog2e);
+        st.m = cmax;
+      }
+#pragma unroll
+      for (int i = 0; i < 32; ++i) cs += i < nvalid ? dev::ex2((v[i] - st.m) * dev::kLog2e) : 0.0f;
+    }
     st.s += cs;
 #pragma unroll
     for (int j = 0; j < kLinMaxTopk; ++j) {
+      if (j >= k) break;   // k is uniform: the loop stops after the row's own ids
       const int64_t loc = st.id[j] - cbase;
       if (loc >= 0 && loc < nvalid) st.zt[j] = pick32(v, static_cast<int>(loc));
     }
