@@ -38,6 +38,26 @@ __device__ __forceinline__ __nv_bfloat16 to_t<__nv_bfloat16>(float x) { return _
 template <>
 __device__ __forceinline__ __half to_t<__half>(float x) { return __float2half_rn(x); }
 
+// two values rounded to 16 bits and packed, the first in the low half
+template <class T>
+__device__ __forceinline__ uint32_t pack2(float lo, float hi);
+template <>
+__device__ __forceinline__ uint32_t pack2<__nv_bfloat16>(float lo, float hi) {
+  const __nv_bfloat162 r = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&r);
+}
+template <>
+__device__ __forceinline__ uint32_t pack2<__half>(float lo, float hi) {
+  const __half2 r = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&r);
+}
+
+// one half of a packed pair to 16-bit memory
+template <class T>
+__device__ __forceinline__ void st_half(T* p, uint32_t w, int hi) {
+  *reinterpret_cast<uint16_t*>(p) = static_cast<uint16_t>(hi ? w >> 16 : w);
+}
+
 // 32 values of one row to 16-bit memory: four 16-byte stores when the run is
 // whole and aligned, else element by element.
 template <class T>
@@ -122,23 +142,37 @@ struct DzEpi {
     for (int i = 0; i < 32; ++i) oh[i] = 0.0f;
 #pragma unroll
     for (int j = 0; j < kLinMaxTopk; ++j) {
+      if (j >= k) break;   // k is uniform: the scan stops after the row's own ids
       const int64_t loc = st.id[j] - cbase;
       if (loc >= 0 && loc < nvalid) {
 #pragma unroll
         for (int i = 0; i < 32; ++i) oh[i] += loc == i ? st.gj[j] : 0.0f;
       }
     }
-    float d[32];
+    // p = 2^((z - m) log2(e) - log2(S)) and dz = g one-hot - G p, pairwise
+    const dev::fp2 m2 = dev::splat(st.m), l2 = dev::splat(dev::kLog2e), c2 = dev::splat(-st.c),
+                   g2 = dev::splat(-st.G);
+    uint32_t w[16];   // dz as 16-bit pairs, column 2i in the low half
 #pragma unroll
-    for (int i = 0; i < 32; ++i) {
-      const float p = dev::ex2(fmaf(v[i] - st.m, dev::kLog2e, -st.c));
-      d[i] = fmaf(-st.G, p, oh[i]);
+    for (int i = 0; i < 16; ++i) {
+      const dev::fp2 p = dev::ex2_2(dev::fma2(dev::sub2(dev::pk(v[2 * i], v[2 * i + 1]), m2), l2, c2));
+      float d0, d1;
+      dev::upk(dev::fma2(g2, p, dev::pk(oh[2 * i], oh[2 * i + 1])), d0, d1);
+      w[i] = pack2<T>(d0, d1);
     }
-    store_row32(dz + row * ld_dz + cbase, d, nvalid);
+    T* dst = dz + row * ld_dz + cbase;
+    if (nvalid == 32 && dev::aligned16(dst)) {
+#pragma unroll
+      for (int q = 0; q < 4; ++q) dev::st16(dst + 8 * q, make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]));
+    } else {
+#pragma unroll
+      for (int i = 0; i < 32; ++i)
+        if (i < nvalid) st_half(dst + i, w[i >> 1], i & 1);
+    }
     T* col = dzt + cbase * ld_dzt + row;   // lanes hold consecutive rows: each column's store is coalesced
 #pragma unroll
     for (int i = 0; i < 32; ++i)
-      if (i < nvalid) col[i * ld_dzt] = to_t<T>(d[i]);
+      if (i < nvalid) st_half(col + i * ld_dzt, w[i >> 1], i & 1);
   }
 
   __device__ void end(State&, int64_t, bool, int) const {}

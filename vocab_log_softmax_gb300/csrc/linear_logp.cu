@@ -69,14 +69,20 @@ struct LogpEpi {
     float cmax = dev::neg_inf();
     float cs = 0.0f;   // z - m is formed first, as in the row sweeps
     if (nvalid == 32) {   // every chunk but the vocabulary's last
+      cmax = v[0];
 #pragma unroll
-      for (int i = 0; i < 32; ++i) cmax = fmaxf(cmax, v[i]);
+      for (int i = 1; i < 31; i += 2) cmax = dev::max3(cmax, v[i], v[i + 1]);
+      cmax = fmaxf(cmax, v[31]);
       if (cmax > st.m) {
         st.s = st.m == dev::neg_inf() ? 0.0f : st.s * dev::ex2((st.m - cmax) * dev::kLog2e);
         st.m = cmax;
       }
+      const dev::fp2 m2 = dev::splat(st.m), l2 = dev::splat(dev::kLog2e);
+      dev::fp2 acc = dev::splat(0.0f);
 #pragma unroll
-      for (int i = 0; i < 32; ++i) cs += dev::ex2((v[i] - st.m) * dev::kLog2e);
+      for (int i = 0; i < 32; i += 2)
+        acc = dev::add2(acc, dev::ex2_2(dev::mul2(dev::sub2(dev::pk(v[i], v[i + 1]), m2), l2)));
+      cs = dev::sum2(acc);
     } else {
 #pragma unroll
       for (int i = 0; i < 32; ++i) cmax = i < nvalid ? fmaxf(cmax, v[i]) : cmax;

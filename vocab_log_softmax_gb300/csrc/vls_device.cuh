@@ -89,6 +89,13 @@ __device__ __forceinline__ fp2 rcp2(fp2 y) {
   upk(y, a, b);
   return pk(rcp(a), rcp(b));
 }
+// max of three (PTX max.f32 with three sources, sm_100 and later; a NaN
+// source is dropped as by fmaxf)
+__device__ __forceinline__ float max3(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
 __device__ __forceinline__ float sum2(fp2 v) {
   float a, b;
   upk(v, a, b);
