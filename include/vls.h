@@ -316,9 +316,9 @@ int vls_linear_logp_partial(const void* h, int64_t ldh, const void* W, int64_t l
                             int64_t ignore_index, vls_partial* part, float* zt, uint32_t* status,
                             void* stream);
 
-/* Bytes of device workspace vls_linear_logp_bwd needs (h^T, W^T, dz and
- * dz^T in the operand dtype, each 256-byte aligned): about
- * 2 (D N + D V + 2 N V).  Returns -1 for sizes out of range. */
+/* Bytes of device workspace vls_linear_logp_bwd needs: dz [N, V] in the
+ * operand dtype, its rows padded to a multiple of 8 elements, rounded up to
+ * 256 bytes (about 2 N V).  Returns -1 for sizes out of range. */
 int64_t vls_linear_logp_bwd_workspace(int64_t N, int64_t D, int64_t V);
 
 /* Gradients of sum_{r,j} g[r, j] logp[r, j] with respect to h and W, where
@@ -332,7 +332,7 @@ int64_t vls_linear_logp_bwd_workspace(int64_t N, int64_t D, int64_t V);
  * contiguous, dtype dt.  workspace: at least
  * vls_linear_logp_bwd_workspace(N, D, V) bytes, 256-byte aligned, the
  * caller's; its contents on entry do not matter.  status as for
- * vls_linear_logp_partial.  Row counts N and V are at most 65535 * 64. */
+ * vls_linear_logp_partial.  N, D and V are at most 2^31 - 512. */
 int vls_linear_logp_bwd(const void* h, int64_t ldh, const void* W, int64_t ldw, vls_dtype dt, int64_t N,
                         int64_t D, int64_t V, const int64_t* ids, int32_t k, int64_t ignore_index,
                         const float* g, const vls_rowstat* stats, void* dh, void* dW, void* workspace,

@@ -96,6 +96,17 @@ def test_row_layout_errors(lib):
     assert lib.vls_entropy_partial(None, None, BF16, 4, 0, 0.0, None, None) == NULL   # part missing
 
 
+def test_linear_backward_workspace_size(lib):
+    """The backward's workspace is dz alone: N rows of V padded to 8
+    elements, 16-bit, rounded up to 256 bytes; sizes out of range give -1."""
+    ws = lib.vls_linear_logp_bwd_workspace
+    for n, d, v in ((300, 200, 3001), (1, 8, 1), (8192, 4096, 151936), (0, 64, 256)):
+        want = (n * ((v + 7) // 8 * 8) * 2 + 255) // 256 * 256
+        assert ws(n, d, v) == want, (n, d, v)
+    for n, d, v in ((-1, 8, 8), (8, 0, 8), (8, 8, 0), (2 ** 31, 8, 8), (8, 8, 2 ** 31), (8, 2 ** 31, 8)):
+        assert ws(n, d, v) == -1, (n, d, v)
+
+
 def test_rows_struct_matches_header():
     text = open(HEADER).read()
     assert re.search(r"typedef struct \{ int64_t ld; int64_t group; int64_t ld_group; \} vls_rows;", text)

@@ -710,13 +710,17 @@ int vls_kl_combine(const vls_partial* parts, int32_t R, int64_t N, vls_kl_dir di
 // fused linear head + logprobs
 // ---------------------------------------------------------------------------
 
+// TMA coordinates are 32-bit and a tile's last coordinate runs up to 511
+// past the end of its matrix
+constexpr int64_t kMaxLinear = kMaxGrid - 511;
+
 int64_t vls_linear_logp_chunks(int64_t V) { return V < 1 ? -1 : linear_chunks(V); }
 
 int vls_linear_logp_partial(const void* h, int64_t ldh, const void* W, int64_t ldw, vls_dtype dt, int64_t N,
                             int64_t D, int64_t V, const int64_t* ids, int32_t k, int64_t ignore_index,
                             vls_partial* part, float* zt, uint32_t* status, void* stream) {
   if (N < 0 || D < 1 || V < 1 || ldh < D || ldw < D || k < 1 || k > VLS_LINEAR_MAX_TOPK) return VLS_ERR_SHAPE;
-  if (N > kMaxGrid || V > kMaxGrid) return VLS_ERR_SHAPE;   // TMA row coordinates are 32-bit
+  if (N > kMaxLinear || V > kMaxLinear || D > kMaxLinear) return VLS_ERR_SHAPE;
   if (dt != VLS_BF16 && dt != VLS_F16) return VLS_ERR_DTYPE;
   if (N == 0) return VLS_OK;
   if (!h || !W || !ids || !part || !zt || !status) return VLS_ERR_NULL;
@@ -730,11 +734,8 @@ int vls_linear_logp_partial(const void* h, int64_t ldh, const void* W, int64_t l
   return launch_status(launch_linear_logp(a, sm_count(dev), static_cast<cudaStream_t>(stream)));
 }
 
-// largest row count of the transposes' 2-D grid (65535 blocks of 64 rows)
-constexpr int64_t kMaxTransposeRows = int64_t(65535) * 64;
-
 int64_t vls_linear_logp_bwd_workspace(int64_t N, int64_t D, int64_t V) {
-  if (N < 0 || D < 1 || V < 1 || N > kMaxTransposeRows || V > kMaxTransposeRows) return -1;
+  if (N < 0 || D < 1 || V < 1 || N > kMaxLinear || V > kMaxLinear || D > kMaxLinear) return -1;
   return static_cast<int64_t>(linear_bwd_workspace(N, D, V));
 }
 
@@ -743,7 +744,7 @@ int vls_linear_logp_bwd(const void* h, int64_t ldh, const void* W, int64_t ldw, 
                         const vls_rowstat* stats, void* dh, void* dW, void* workspace, int64_t workspace_bytes,
                         uint32_t* status, void* stream) {
   if (N < 0 || D < 1 || V < 1 || ldh < D || ldw < D || k < 1 || k > VLS_LINEAR_MAX_TOPK) return VLS_ERR_SHAPE;
-  if (N > kMaxTransposeRows || V > kMaxTransposeRows) return VLS_ERR_SHAPE;
+  if (N > kMaxLinear || V > kMaxLinear || D > kMaxLinear) return VLS_ERR_SHAPE;
   if (dt != VLS_BF16 && dt != VLS_F16) return VLS_ERR_DTYPE;
   if (N == 0) return VLS_OK;
   if (!h || !W || !ids || !g || !stats || !dh || !dW || !workspace || !status) return VLS_ERR_NULL;

@@ -5,18 +5,18 @@
 // where p = softmax(z) comes from the forward's saved (m, log S) and logit
 // tiles recomputed on the tensor cores (z is not stored by the forward).
 //
-// Steps, all on tcgen05 through the mainloop of tc_gemm.cuh, whose operands
-// are K-major:
-//  1. h^T [D, N] and W^T [D, V] by a shared-memory tiled transpose (64 x 64
-//     tiles, 16-byte accesses);
-//  2. the dz map: the forward's GEMM z = h @ W^T with an epilogue that forms
-//     dz in fp32, casts it once to the operand dtype and writes it both as
-//     dz [N, V] and as dz^T [V, N];
-//  3. dh = dz @ (W^T)^T: M = N, columns D, K = V;
-//  4. dW = dz^T @ (h^T)^T: M = V, columns D, K = N.
-// The workspace (h^T, W^T, dz, dz^T) is the caller's.  Leading dimensions are
-// padded to 8 elements (16 bytes, as TMA needs); the tensor maps carry the
-// true K, so padding is never read.
+// Three launches of the tcgen05 mainloop in tc_gemm.cuh, each reading its
+// operands where they already are:
+//  1. the dz map: the forward's GEMM z = h @ W^T (both K-major) with an
+//     epilogue that forms dz in fp32, rounds it once to the operand dtype and
+//     stores it as dz [N, V];
+//  2. dh = dz @ W: A = dz K-major (K = V), B = W read MN-major ([V, D] is
+//     [K, columns]);
+//  3. dW = dz^T @ h: A = dz read MN-major ([N, V] is [K, rows]), B = h read
+//     MN-major ([N, D] is [K, columns]).
+// The workspace (dz) is the caller's.  Its leading dimension is padded to 8
+// elements (16 bytes, as TMA needs); the tensor maps carry the true sizes, so
+// padding is never read.
 #include <type_traits>
 
 #include <cuda_bf16.h>
@@ -105,8 +105,6 @@ struct DzEpi {
   const vls_rowstat* stats;  // [N]
   T* dz;                     // [N, ld_dz]
   int64_t ld_dz;
-  T* dzt;                    // [V, ld_dzt]
-  int64_t ld_dzt;
 
   struct State {
     float m, c, G;             // max, log S * log2(e), sum of the valid upstream gradients
@@ -169,111 +167,35 @@ struct DzEpi {
       for (int i = 0; i < 32; ++i)
         if (i < nvalid) st_half(dst + i, w[i >> 1], i & 1);
     }
-    T* col = dzt + cbase * ld_dzt + row;   // lanes hold consecutive rows: each column's store is coalesced
-#pragma unroll
-    for (int i = 0; i < 32; ++i)
-      if (i < nvalid) st_half(col + i * ld_dzt, w[i >> 1], i & 1);
   }
 
   __device__ void end(State&, int64_t, bool, int) const {}
 };
 
-// y[c, r] = x[r, c] for a [rows, cols] 16-bit matrix with row stride ldx
-// into y with row stride ldy, through 64 x 64 shared-memory tiles: 16-byte
-// loads along x's rows, 16-byte stores along y's rows (element by element at
-// ragged edges).  x, y and both strides must be 16-byte aligned.
-__global__ void __launch_bounds__(256) transpose_kernel(const uint16_t* __restrict__ x, int64_t rows, int64_t cols,
-                                                         int64_t ldx, uint16_t* __restrict__ y, int64_t ldy) {
-  __shared__ __align__(16) uint16_t tile[64][72];   // 144-byte rows: 16-byte aligned, banks staggered
-  const int64_t r0 = static_cast<int64_t>(blockIdx.y) * 64, c0 = static_cast<int64_t>(blockIdx.x) * 64;
-#pragma unroll
-  for (int i = 0; i < 2; ++i) {
-    const int vec = threadIdx.x + 256 * i, r = vec >> 3, c8 = (vec & 7) * 8;
-    const int64_t gr = r0 + r, gc = c0 + c8;
-    if (gr < rows && gc + 8 <= cols) {
-      *reinterpret_cast<uint4*>(&tile[r][c8]) = __ldg(reinterpret_cast<const uint4*>(x + gr * ldx + gc));
-    } else {
-#pragma unroll
-      for (int e = 0; e < 8; ++e) tile[r][c8 + e] = (gr < rows && gc + e < cols) ? x[gr * ldx + gc + e] : 0;
-    }
-  }
-  __syncthreads();
-#pragma unroll
-  for (int i = 0; i < 2; ++i) {
-    const int vec = threadIdx.x + 256 * i, oc = vec >> 3, r8 = (vec & 7) * 8;
-    const int64_t gc = c0 + oc, gr = r0 + r8;
-    if (gc >= cols) continue;
-    uint16_t v[8];
-#pragma unroll
-    for (int e = 0; e < 8; ++e) v[e] = tile[r8 + e][oc];
-    if (gr + 8 <= rows) {
-      uint4 w;
-      w.x = v[0] | (static_cast<uint32_t>(v[1]) << 16);
-      w.y = v[2] | (static_cast<uint32_t>(v[3]) << 16);
-      w.z = v[4] | (static_cast<uint32_t>(v[5]) << 16);
-      w.w = v[6] | (static_cast<uint32_t>(v[7]) << 16);
-      *reinterpret_cast<uint4*>(y + gc * ldy + gr) = w;
-    } else {
-#pragma unroll
-      for (int e = 0; e < 8; ++e)
-        if (gr + e < rows) y[gc * ldy + gr + e] = v[e];
-    }
-  }
-}
-
-cudaError_t transpose(const void* x, int64_t rows, int64_t cols, int64_t ldx, void* y, int64_t ldy,
-                      cudaStream_t s) {
-  const dim3 grid(static_cast<unsigned>((cols + 63) / 64), static_cast<unsigned>((rows + 63) / 64));
-  transpose_kernel<<<grid, 256, 0, s>>>(static_cast<const uint16_t*>(x), rows, cols, ldx, static_cast<uint16_t*>(y),
-                                        ldy);
-  return cudaGetLastError();
-}
-
-struct Workspace {
-  size_t hT, WT, dz, dzt, total;   // byte offsets and size
-};
-
-Workspace layout(int64_t N, int64_t D, int64_t V) {
-  Workspace w;
-  size_t off = 0;
-  w.hT = off;
-  off = align256(off + static_cast<size_t>(D) * pad8(N) * 2);
-  w.WT = off;
-  off = align256(off + static_cast<size_t>(D) * pad8(V) * 2);
-  w.dz = off;
-  off = align256(off + static_cast<size_t>(N) * pad8(V) * 2);
-  w.dzt = off;
-  off = align256(off + static_cast<size_t>(V) * pad8(N) * 2);
-  w.total = off;
-  return w;
-}
+// the workspace: dz [N, pad8(V)] in the operand dtype
+size_t workspace_bytes(int64_t N, int64_t V) { return align256(static_cast<size_t>(N) * pad8(V) * 2); }
 
 template <bool BF16>
 cudaError_t bwd_t(const LinearBwdArgs& a, int sms, cudaStream_t s) {
   using T = typename std::conditional<BF16, __nv_bfloat16, __half>::type;
-  const Workspace w = layout(a.N, a.D, a.V);
-  unsigned char* ws = static_cast<unsigned char*>(a.workspace);
-  T* hT = reinterpret_cast<T*>(ws + w.hT);
-  T* WT = reinterpret_cast<T*>(ws + w.WT);
-  T* dz = reinterpret_cast<T*>(ws + w.dz);
-  T* dzt = reinterpret_cast<T*>(ws + w.dzt);
-  const int64_t ldn = pad8(a.N), ldv = pad8(a.V);
+  T* dz = static_cast<T*>(a.workspace);
+  const int64_t ldv = pad8(a.V);
   cudaError_t e;
-  if ((e = transpose(a.h, a.N, a.D, a.ldh, hT, ldn, s)) != cudaSuccess) return e;
-  if ((e = transpose(a.W, a.V, a.D, a.ldw, WT, ldv, s)) != cudaSuccess) return e;
-  const DzEpi<T> dze{a.ids, a.k, a.ignore_index, a.V, a.g, a.stats, dz, ldv, dzt, ldn};
+  const DzEpi<T> dze{a.ids, a.k, a.ignore_index, a.V, a.g, a.stats, dz, ldv};
   if ((e = tcg::launch_gemm<BF16>(a.h, a.ldh, a.N, a.W, a.ldw, a.V, a.D, kLinChunkTiles, false, a.status, dze, sms, s)) !=
       cudaSuccess)
     return e;
   const StoreEpi<T> dhe{static_cast<T*>(a.dh), a.D};
-  if ((e = tcg::launch_gemm<BF16>(dz, ldv, a.N, WT, ldv, a.D, a.V, 1, true, a.status, dhe, sms, s)) != cudaSuccess) return e;
+  if ((e = tcg::launch_gemm<BF16, false, true>(dz, ldv, a.N, a.W, a.ldw, a.D, a.V, 1, true, a.status, dhe, sms, s)) !=
+      cudaSuccess)
+    return e;
   const StoreEpi<T> dwe{static_cast<T*>(a.dW), a.D};
-  return tcg::launch_gemm<BF16>(dzt, ldn, a.V, hT, ldn, a.D, a.N, 1, true, a.status, dwe, sms, s);
+  return tcg::launch_gemm<BF16, true, true>(dz, ldv, a.V, a.h, a.ldh, a.D, a.N, 1, true, a.status, dwe, sms, s);
 }
 
 }  // namespace
 
-size_t linear_bwd_workspace(int64_t N, int64_t D, int64_t V) { return layout(N, D, V).total; }
+size_t linear_bwd_workspace(int64_t N, int64_t, int64_t V) { return workspace_bytes(N, V); }
 
 cudaError_t launch_linear_logp_bwd(const LinearBwdArgs& a, int sms, cudaStream_t s) {
   return a.dt == VLS_BF16 ? bwd_t<true>(a, sms, s) : bwd_t<false>(a, sms, s);

@@ -221,8 +221,12 @@ __device__ __forceinline__ void mma_commit(uint32_t bar) {
 // Instruction descriptor of kind::f16 with an fp32 accumulator, both
 // operands K-major: bits 4-5 D format (1 = f32), 7-9 A format and 10-12 B
 // format (0 = f16, 1 = bf16), 17-22 N/8, 24-28 M/16.
-__host__ __device__ constexpr uint32_t idesc_f16(bool bf16, uint32_t m, uint32_t n) {
-  return (1u << 4) | ((bf16 ? 1u : 0u) << 7) | ((bf16 ? 1u : 0u) << 10) | ((n >> 3) << 17) | ((m >> 4) << 24);
+// a_mn / b_mn set the operand's major-ness bit (15 for A, 16 for B): 0 when
+// K is the contiguous dimension, 1 when M (for A) or N (for B) is.
+__host__ __device__ constexpr uint32_t idesc_f16(bool bf16, uint32_t m, uint32_t n, bool a_mn = false,
+                                                 bool b_mn = false) {
+  return (1u << 4) | ((bf16 ? 1u : 0u) << 7) | ((bf16 ? 1u : 0u) << 10) | ((a_mn ? 1u : 0u) << 15) |
+         ((b_mn ? 1u : 0u) << 16) | ((n >> 3) << 17) | ((m >> 4) << 24);
 }
 
 // Shared-memory matrix descriptor of a K-major operand tile stored in the
@@ -235,6 +239,19 @@ __host__ __device__ constexpr uint32_t idesc_f16(bool bf16, uint32_t m, uint32_t
 __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t addr) {
   return static_cast<uint64_t>((addr & 0x3FFFFu) >> 4) | (1ull << 16) | (static_cast<uint64_t>(1024 >> 4) << 32) |
          (1ull << 46) | (2ull << 61);
+}
+
+// Descriptor of an MN-major operand tile in the 128-byte swizzled layout:
+// the tile is stored as blocks of 64 M (or N) elements, each block a run of K
+// rows of 128 bytes (as a TMA box of 64 x K elements writes it), the blocks
+// kMnBlockBytes apart.  The leading offset (bits 16-29) is the distance
+// between 64-element blocks along M or N, the stride offset (bits 32-45) the
+// distance between 8-row groups along K (1024 bytes).  Each 16-row K step
+// moves the start address by two such groups (2048 bytes, 128 in the field).
+constexpr uint32_t kMnBlockBytes = 64 * 64 * 2;   // 64 elements x 64 K rows of 16 bits
+__device__ __forceinline__ uint64_t sdesc_sw128_mn(uint32_t addr) {
+  return static_cast<uint64_t>((addr & 0x3FFFFu) >> 4) | (static_cast<uint64_t>(kMnBlockBytes >> 4) << 16) |
+         (static_cast<uint64_t>(1024 >> 4) << 32) | (1ull << 46) | (2ull << 61);
 }
 
 // 32 consecutive fp32 columns of this thread's tensor-memory lane (warp-wide;

@@ -1,7 +1,9 @@
 // A persistent tcgen05 GEMM mainloop with a pluggable epilogue:
 //     C[M, Ncols] = A[M, K] * B[Ncols, K]^T,
-// A and B 16-bit, both K-major (K contiguous), fp32 accumulation in tensor
-// memory.  The output tile is never stored by the mainloop: an epilogue
+// A and B 16-bit, fp32 accumulation in tensor memory.  Each operand is either
+// K-major (stored [rows, K], K contiguous) or MN-major (stored [K, rows], its
+// M or N index contiguous), chosen per launch, so a product whose operand
+// sits transposed in memory needs no transpose.  The output tile is never stored by the mainloop: an epilogue
 // object receives it, 32 columns of one row per thread at a time, and does
 // what its operation needs (fold a softmax, form a gradient, store).
 //
@@ -71,13 +73,46 @@ inline Sched make_sched(int64_t M, int64_t Ncols, int64_t K, int chunk_tiles, ui
   return s;
 }
 
+// One stage of an operand: `rows` rows (of A, or columns of B) starting at r0,
+// K slice k0 .. k0 + 63.  K-major: one TMA box of 64 x rows.  MN-major: rows
+// / 64 boxes of 64 (M or N) x 64 (K), kMnBlockBytes apart.  PAIR issues the
+// cta_group::2 form that completes on the pair leader's barrier.
+template <bool MN, int ROWS, bool PAIR>
+__device__ __forceinline__ void load_stage(uint32_t dst, const CUtensorMap* map, int32_t k0, int32_t r0,
+                                           uint32_t bar) {
+  if constexpr (!MN) {
+    if constexpr (PAIR)
+      tc::tma_load_2d_pair(dst, map, k0, r0, bar);
+    else
+      tc::tma_load_2d(dst, map, k0, r0, bar);
+  } else {
+#pragma unroll
+    for (int j = 0; j < ROWS / 64; ++j) {
+      if constexpr (PAIR)
+        tc::tma_load_2d_pair(dst + j * tc::kMnBlockBytes, map, r0 + 64 * j, k0, bar);
+      else
+        tc::tma_load_2d(dst + j * tc::kMnBlockBytes, map, r0 + 64 * j, k0, bar);
+    }
+  }
+}
+
+// Descriptor of a stage and the step of its address field per 16-wide K
+// slice: 32 bytes along a K-major row, two 8-row groups (2048 bytes) down an
+// MN-major block.
+template <bool MN>
+__device__ __forceinline__ uint64_t stage_desc(uint32_t addr) {
+  return MN ? tc::sdesc_sw128_mn(addr) : tc::sdesc_sw128(addr);
+}
+template <bool MN>
+constexpr uint64_t kDescStep = MN ? (2048 >> 4) : (32 >> 4);
+
 // Epilogue interface (one object per launch, copied to every thread):
 //   struct State;                                           per-thread, per-unit state
 //   State begin(int64_t row, bool row_ok, int chunk);       at each unit
 //   void  cols(State&, const float (&v)[32], int64_t row, bool row_ok, int64_t col0, int nvalid);
 //                                                           32 columns of the row (nvalid < 32 at the edge)
 //   void  end(State&, int64_t row, bool row_ok, int chunk); after the unit's last tile
-template <bool BF16, class Epi>
+template <bool BF16, bool A_MN, bool B_MN, class Epi>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
                 const Sched sc, const Epi epi) {
@@ -139,8 +174,8 @@ __global__ void __launch_bounds__(kThreads, 1)
               break;
             }
             tc::mbar_expect_tx(full(stage), kStageA + kStageB);
-            tc::tma_load_2d(sA + stage * kStageA, &tm_a, kb * kBK, rt * kBM, full(stage));
-            tc::tma_load_2d(sB + stage * kStageB, &tm_b, kb * kBK, t * kBN, full(stage));
+            load_stage<A_MN, kBM, false>(sA + stage * kStageA, &tm_a, kb * kBK, rt * kBM, full(stage));
+            load_stage<B_MN, kBN, false>(sB + stage * kStageB, &tm_b, kb * kBK, t * kBN, full(stage));
             ++issued;
             if (++stage == kStages) {
               stage = 0;
@@ -163,7 +198,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 1) {
     // ---------------- MMA issuer ----------------
     if (lane == 0) {
-      constexpr uint32_t idesc = tc::idesc_f16(BF16, kBM, kBN);
+      constexpr uint32_t idesc = tc::idesc_f16(BF16, kBM, kBN, A_MN, B_MN);
       int stage = 0;
       uint32_t phase = 0;
       uint32_t tc_count = 0;
@@ -186,13 +221,11 @@ __global__ void __launch_bounds__(kThreads, 1)
               break;
             }
             tc::fence_after_sync();
-            const uint64_t da = tc::sdesc_sw128(sA + stage * kStageA);
-            const uint64_t db = tc::sdesc_sw128(sB + stage * kStageB);
+            const uint64_t da = stage_desc<A_MN>(sA + stage * kStageA);
+            const uint64_t db = stage_desc<B_MN>(sB + stage * kStageB);
 #pragma unroll
-            for (int kk = 0; kk < kBK / kUK; ++kk) {
-              // 16 elements = 32 bytes further along the swizzled row: +2 in the address field
-              tc::mma_f16(d, da + 2ull * kk, db + 2ull * kk, idesc, (kb | kk) != 0 ? 1u : 0u);
-            }
+            for (int kk = 0; kk < kBK / kUK; ++kk)
+              tc::mma_f16(d, da + kDescStep<A_MN> * kk, db + kDescStep<B_MN> * kk, idesc, (kb | kk) != 0 ? 1u : 0u);
             tc::mma_commit(empty(stage));   // frees the stage once these MMAs have read it
             if (++stage == kStages) {
               stage = 0;
@@ -275,7 +308,7 @@ constexpr uint32_t kStageB2 = (kBN / 2) * kBK * 2;   // 16 KB: this CTA's 128 co
 constexpr int kNumBars2 = 2 * kStages2 + 4 + 1;
 constexpr size_t kSmem2 = 1024 + kStages2 * (kStageA2 + kStageB2) + kNumBars2 * 8 + 16;
 
-template <bool BF16, class Epi>
+template <bool BF16, bool A_MN, bool B_MN, class Epi>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm2_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
                  const Sched sc, const Epi epi) {
@@ -340,8 +373,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             if (leader) tc::mbar_expect_tx(full(stage), 2 * (kStageA2 + kStageB2));
             const uint32_t lead_full = tc::map_to_rank(full(stage), 0);
-            tc::tma_load_2d_pair(sA + stage * kStageA2, &tm_a, kb * kBK, rt * 2 * kBM + rank * kBM, lead_full);
-            tc::tma_load_2d_pair(sB + stage * kStageB2, &tm_b, kb * kBK, t * kBN + rank * (kBN / 2), lead_full);
+            load_stage<A_MN, kBM, true>(sA + stage * kStageA2, &tm_a, kb * kBK, rt * 2 * kBM + rank * kBM, lead_full);
+            load_stage<B_MN, kBN / 2, true>(sB + stage * kStageB2, &tm_b, kb * kBK, t * kBN + rank * (kBN / 2),
+                                            lead_full);
             if (++stage == kStages2) {
               stage = 0;
               phase ^= 1u;
@@ -353,7 +387,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 1) {
     // ---------------- MMA issuer (the leader) ----------------
     if (lane == 0 && leader) {
-      constexpr uint32_t idesc = tc::idesc_f16(BF16, 2 * kBM, kBN);
+      constexpr uint32_t idesc = tc::idesc_f16(BF16, 2 * kBM, kBN, A_MN, B_MN);
       int stage = 0;
       uint32_t phase = 0;
       uint32_t tc_count = 0;
@@ -376,11 +410,12 @@ __global__ void __launch_bounds__(kThreads, 1)
               break;
             }
             tc::fence_after_sync();
-            const uint64_t da = tc::sdesc_sw128(sA + stage * kStageA2);
-            const uint64_t db = tc::sdesc_sw128(sB + stage * kStageB2);
+            const uint64_t da = stage_desc<A_MN>(sA + stage * kStageA2);
+            const uint64_t db = stage_desc<B_MN>(sB + stage * kStageB2);
 #pragma unroll
             for (int kk = 0; kk < kBK / kUK; ++kk)
-              tc::mma_f16_pair(d, da + 2ull * kk, db + 2ull * kk, idesc, (kb | kk) != 0 ? 1u : 0u);
+              tc::mma_f16_pair(d, da + kDescStep<A_MN> * kk, db + kDescStep<B_MN> * kk, idesc,
+                               (kb | kk) != 0 ? 1u : 0u);
             tc::mma_commit_pair(empty(stage));   // frees this stage in both CTAs
             if (++stage == kStages2) {
               stage = 0;
@@ -449,21 +484,33 @@ __global__ void __launch_bounds__(kThreads, 1)
 bool encode_kmajor(CUtensorMap* map, const void* base, bool bf16, int64_t rows, int64_t K, int64_t ld,
                    int box_rows);
 
+// Tensor map of the same operand stored MN-major: a [K, rows] 16-bit
+// row-major matrix with row stride ld, boxes of 64 (rows) x 64 (K) elements,
+// 128-byte swizzle, zero fill outside the matrix.
+bool encode_mnmajor(CUtensorMap* map, const void* base, bool bf16, int64_t rows, int64_t K, int64_t ld);
+
+// Either form, as the operand is stored.
+inline bool encode_operand(CUtensorMap* map, bool mn, const void* base, bool bf16, int64_t rows, int64_t K,
+                           int64_t ld, int box_rows) {
+  return mn ? encode_mnmajor(map, base, bf16, rows, K, ld) : encode_kmajor(map, base, bf16, rows, K, ld, box_rows);
+}
+
 // 1 for the 1-SM kernel, 2 for CTA pairs (VLS_TC_CTA_GROUP; default 2).
 int cta_group();
 
-template <bool BF16, class Epi>
+template <bool BF16, bool A_MN, bool B_MN, class Epi>
 cudaError_t launch_gemm2(const void* A, int64_t lda, int64_t M, const void* Bm, int64_t ldb, int64_t Ncols,
                          int64_t K, int chunk_tiles, bool cols_fastest, uint32_t* status, const Epi& epi, int sms,
                          cudaStream_t s) {
   CUtensorMap tm_a, tm_b;
-  if (!encode_kmajor(&tm_a, A, BF16, M, K, lda, kBM) || !encode_kmajor(&tm_b, Bm, BF16, Ncols, K, ldb, kBN / 2))
+  if (!encode_operand(&tm_a, A_MN, A, BF16, M, K, lda, kBM) ||
+      !encode_operand(&tm_b, B_MN, Bm, BF16, Ncols, K, ldb, kBN / 2))
     return cudaErrorInvalidValue;
   Sched sc = make_sched(M, Ncols, K, chunk_tiles, status);
   sc.n_row_tiles = static_cast<int>((M + 2 * kBM - 1) / (2 * kBM));   // 256-row tiles
   sc.n_units = sc.n_row_tiles * sc.n_chunks;
   sc.cols_fastest = cols_fastest ? 1 : 0;
-  auto kern = gemm2_kernel<BF16, Epi>;
+  auto kern = gemm2_kernel<BF16, A_MN, B_MN, Epi>;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) return cudaErrorInvalidDevice;
   // per device and kernel, once: the shared-memory opt-in and the number of
@@ -498,18 +545,22 @@ cudaError_t launch_gemm2(const void* A, int64_t lda, int64_t M, const void* Bm, 
   return cudaLaunchKernelEx(&cfg, kern, tm_a, tm_b, sc, epi);
 }
 
-template <bool BF16, class Epi>
+// C = A B^T through the epilogue.  A_MN / B_MN: the operand is stored
+// MN-major ([K, M] for A, [K, Ncols] for B, row stride lda / ldb), else
+// K-major ([M, K], [Ncols, K]).
+template <bool BF16, bool A_MN = false, bool B_MN = false, class Epi>
 cudaError_t launch_gemm(const void* A, int64_t lda, int64_t M, const void* Bm, int64_t ldb, int64_t Ncols,
                         int64_t K, int chunk_tiles, bool cols_fastest, uint32_t* status, const Epi& epi, int sms,
                         cudaStream_t s) {
   if (cta_group() == 2 && sms >= 2)
-    return launch_gemm2<BF16>(A, lda, M, Bm, ldb, Ncols, K, chunk_tiles, cols_fastest, status, epi, sms, s);
+    return launch_gemm2<BF16, A_MN, B_MN>(A, lda, M, Bm, ldb, Ncols, K, chunk_tiles, cols_fastest, status, epi, sms,
+                                          s);
   CUtensorMap tm_a, tm_b;
-  if (!encode_kmajor(&tm_a, A, BF16, M, K, lda, kBM) || !encode_kmajor(&tm_b, Bm, BF16, Ncols, K, ldb, kBN))
+  if (!encode_operand(&tm_a, A_MN, A, BF16, M, K, lda, kBM) || !encode_operand(&tm_b, B_MN, Bm, BF16, Ncols, K, ldb, kBN))
     return cudaErrorInvalidValue;
   Sched sc = make_sched(M, Ncols, K, chunk_tiles, status);
   sc.cols_fastest = cols_fastest ? 1 : 0;
-  auto kern = gemm_kernel<BF16, Epi>;
+  auto kern = gemm_kernel<BF16, A_MN, B_MN, Epi>;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) return cudaErrorInvalidDevice;
   static bool opted_in[kMaxDev] = {false};   // per device and kernel, once
