@@ -23,7 +23,10 @@ def _all_outputs(a, b, ids, gk, gr, cap=0.0):
     dl = B.vls_logp_bwd(a, ids, gk, st, -100, cap)
     h, se = B.vls_entropy_fwd(a, cap)
     de = B.vls_entropy_bwd(a, gr, h, se, cap)
-    out = {"logp": lp, "stats": st, "dlogp": dl, "H": h, "dH": de}
+    # k = 1: at a few rows the backward cuts each row into more pieces than
+    # at many rows (the split follows N there); the bits must not move
+    dl1 = B.vls_logp_bwd(a, ids[:, :1].contiguous(), gk[:, :1].contiguous(), st, -100, cap)
+    out = {"logp": lp, "stats": st, "dlogp": dl, "dlogp_k1": dl1, "H": h, "dH": de}
     for d in ("reverse", "forward"):
         kl, sa, sb = B.vls_kl_fwd(a, b, d, cap)
         out["kl_" + d] = kl

@@ -62,6 +62,23 @@ void bwd_geometry(int64_t V, int32_t k, int* chunks, int64_t* vec_per_cta) {
   *vec_per_cta = ceil_div(nvec, c);
 }
 
+// Small batches: when the rows alone would leave SMs idle, the backward's
+// rows are cut into more pieces (of at least 256 vectors, one per thread)
+// until the grid covers every SM twice.  The backward is a map, so its split
+// changes no result.  Top-k rows keep whole-row pieces: each CTA prepares
+// the row's id list.
+void widen_bwd(BwdArgs& a, int sms) {
+  if (a.k > 1 || a.rows < 1) return;
+  const int64_t nvec = ceil_div(a.vocab, 8);
+  const int64_t want = ceil_div(2 * static_cast<int64_t>(sms), a.rows);
+  const int64_t most = ceil_div(nvec, 256);
+  const int64_t c = want < most ? want : most;
+  if (c > a.chunks) {
+    a.chunks = static_cast<int>(c);
+    a.vec_per_cta = ceil_div(nvec, c);
+  }
+}
+
 int sm_count(int dev) {
   static int cache[64] = {0};
   if (dev >= 0 && dev < 64 && cache[dev] > 0) return cache[dev];
@@ -312,6 +329,7 @@ int vls_logp_bwd(const void* logits, const vls_rows* rows, vls_dtype dt, int64_t
   if (int e = resolve_device({logits, ids, g, stats, dlogits}, stream, &dev)) return e;
   DeviceGuard guard;
   if (int e = guard.enter(dev)) return e;
+  widen_bwd(a, sm_count(dev));
   a.x = logits;
   a.rx = kernel_rows(*rows);
   a.ids = ids;
@@ -358,6 +376,7 @@ int vls_entropy_bwd(const void* logits, const vls_rows* rows, vls_dtype dt, int6
   if (int e = resolve_device({logits, g, H, stats, dlogits}, stream, &dev)) return e;
   DeviceGuard guard;
   if (int e = guard.enter(dev)) return e;
+  widen_bwd(a, sm_count(dev));
   a.x = logits;
   a.rx = kernel_rows(*rows);
   a.g = g;
@@ -415,6 +434,7 @@ int vls_kl_bwd(const void* pa, const vls_rows* rows_a, const void* pb, const vls
   if (int e = resolve_device({pa, pb, g, kl, stats_a, stats_b, da}, stream, &dev)) return e;
   DeviceGuard guard;
   if (int e = guard.enter(dev)) return e;
+  widen_bwd(a, sm_count(dev));
   a.x = pa;
   a.rx = kernel_rows(*rows_a);
   a.y = pb;
@@ -502,6 +522,7 @@ int vls_fused_bwd(const void* pa, const vls_rows* rows_a, const void* pb, const 
     return e;
   DeviceGuard guard;
   if (int e = guard.enter(dev)) return e;
+  widen_bwd(a, sm_count(dev));
   a.x = pa;
   a.rx = kernel_rows(*rows_a);
   a.y = want_kl ? pb : nullptr;
@@ -599,6 +620,7 @@ int vls_logp_bwd_shard(const void* logits, const vls_rows* rows, vls_dtype dt, i
   if (int e = resolve_device({logits, ids, g, stats, dlogits}, stream, &dev)) return e;
   DeviceGuard guard;
   if (int e = guard.enter(dev)) return e;
+  widen_bwd(a, sm_count(dev));
   a.x = logits;
   a.rx = kernel_rows(*rows);
   a.ids = ids;
