@@ -203,6 +203,53 @@ def test_side_stream_and_current_device_restored():
     assert torch.cuda.current_device() == 0
 
 
+@pytest.mark.gpu
+def test_concurrent_host_threads():
+    """Several host threads, each on its own stream, call the row sweeps and
+    the tensor-core linear head at once (when this test runs first in its
+    process, they also race on the linear head's one-time launch setup).
+    Every result equals the one-thread result bit for bit."""
+    import threading
+
+    import torch
+
+    from vocab_log_softmax_gb300 import binding as B
+    g = torch.Generator(device="cuda").manual_seed(3)
+    x = torch.randn((64, 30000), generator=g, device="cuda").to(torch.bfloat16)
+    ids = torch.randint(0, 30000, (64, 1), generator=g, device="cuda")
+    h = torch.randn((300, 512), generator=g, device="cuda").to(torch.bfloat16)
+    w = (0.1 * torch.randn((5000, 512), generator=g, device="cuda")).to(torch.bfloat16)
+    lids = torch.randint(0, 5000, (300, 1), generator=g, device="cuda")
+    torch.cuda.synchronize()
+    out = [None] * 6
+    errors = []
+
+    def work(i):
+        try:
+            s = torch.cuda.Stream()
+            with torch.cuda.stream(s):
+                lp, st = B.vls_logp_fwd(x, ids)
+                llp, lst, status = B.vls_linear_logp_fwd(h, w, lids)
+            s.synchronize()
+            out[i] = (lp, st, llp, lst, int(status.item()))
+        except Exception as e:  # reported below, on the main thread
+            errors.append(e)
+
+    threads = [threading.Thread(target=work, args=(i,)) for i in range(len(out))]
+    for t in threads:
+        t.start()
+    for t in threads:
+        t.join()
+    assert not errors, errors
+    ref = (*B.vls_logp_fwd(x, ids), *B.vls_linear_logp_fwd(h, w, lids)[:2])
+    torch.cuda.synchronize()
+    for o in out:
+        assert o[4] == 0
+        for a, b in zip(o[:4], ref):
+            assert torch.equal(a.view(torch.int32) if a.dtype == torch.float32 else a,
+                               b.view(torch.int32) if b.dtype == torch.float32 else b)
+
+
 def test_library_missing_fails_loudly(monkeypatch, tmp_path):
     monkeypatch.setattr(_lib, "_lib", None)
     monkeypatch.setattr(_lib, "LIB_PATH", str(tmp_path / "nope.so"))

@@ -4,6 +4,7 @@
 // Validation order for every call: shapes, dtypes and cap first (no CUDA
 // call), then the empty-input fast return, then NULL pointers, then the
 // device of every pointer and of the stream, then the launch.
+#include <atomic>
 #include <cmath>
 #include <cstdlib>
 #include <cstring>
@@ -80,14 +81,17 @@ void widen_bwd(BwdArgs& a, int sms) {
 }
 
 int sm_count(int dev) {
-  static int cache[64] = {0};
-  if (dev >= 0 && dev < 64 && cache[dev] > 0) return cache[dev];
+  static std::atomic<int> cache[64];   // several host threads may ask; a repeated query is harmless
+  if (dev >= 0 && dev < 64) {
+    const int c = cache[dev].load(std::memory_order_relaxed);
+    if (c > 0) return c;
+  }
   int n = 0;
   if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) {
     cudaGetLastError();
     n = 1;
   }
-  if (dev >= 0 && dev < 64) cache[dev] = n;
+  if (dev >= 0 && dev < 64) cache[dev].store(n, std::memory_order_relaxed);
   return n;
 }
 

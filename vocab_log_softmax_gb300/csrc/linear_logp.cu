@@ -18,6 +18,7 @@
 // Summary); the statistics are those of the single-read logprob forward
 // ("Add Triton kernels for vocab-parallel logprobs, entropy and KL",
 // DeepSpeed PR #8838, Changes).
+#include <atomic>
 #include <cstdlib>
 
 #include <cuda.h>
@@ -113,18 +114,21 @@ struct LogpEpi {
 };
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  if (!fn) {
+  static std::atomic<PFN_cuTensorMapEncodeTiled_v12000> fn{nullptr};   // looked up once (or again, harmlessly)
+  PFN_cuTensorMapEncodeTiled_v12000 f = fn.load(std::memory_order_acquire);
+  if (!f) {
     void* p = nullptr;
     cudaDriverEntryPointQueryResult q;
     if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
             cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-    else
+        q == cudaDriverEntryPointSuccess) {
+      f = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+      fn.store(f, std::memory_order_release);
+    } else {
       cudaGetLastError();
+    }
   }
-  return fn;
+  return f;
 }
 
 }  // namespace

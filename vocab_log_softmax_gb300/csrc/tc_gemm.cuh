@@ -18,6 +18,8 @@
 // MMAs.  Every wait is bounded (tc_device.cuh).
 #pragma once
 
+#include <atomic>
+
 #include "tc_device.cuh"
 #include "vls_device.cuh"
 
@@ -515,7 +517,8 @@ cudaError_t launch_gemm2(const void* A, int64_t lda, int64_t M, const void* Bm, 
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) return cudaErrorInvalidDevice;
   // per device and kernel, once: the shared-memory opt-in and the number of
   // resident pairs (runtime queries are kept out of stream capture)
-  static int resident_on[kMaxDev] = {0};
+  // (atomics: calls may come from several host threads; a repeated query is harmless)
+  static std::atomic<int> resident_on[kMaxDev];
   cudaLaunchConfig_t cfg = {};
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = kSmem2;
@@ -529,18 +532,18 @@ cudaError_t launch_gemm2(const void* A, int64_t lda, int64_t M, const void* Bm, 
   cfg.numAttrs = 1;
   // a persistent grid: only as many pairs as can be resident at once (a GPC
   // with an odd number of free SMs leaves one idle)
-  if (resident_on[dev] == 0) {
+  int resident = resident_on[dev].load(std::memory_order_acquire);
+  if (resident == 0) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(kSmem2));
     if (e != cudaSuccess) return e;
     cfg.gridDim = dim3(static_cast<unsigned>(sms & ~1));
-    int resident = 0;
     if (cudaOccupancyMaxActiveClusters(&resident, kern, &cfg) != cudaSuccess || resident < 1) {
       cudaGetLastError();
       resident = sms / 2;
     }
-    resident_on[dev] = resident;
+    resident_on[dev].store(resident, std::memory_order_release);
   }
-  const int pairs = sc.n_units < resident_on[dev] ? sc.n_units : resident_on[dev];
+  const int pairs = sc.n_units < resident ? sc.n_units : resident;
   cfg.gridDim = dim3(static_cast<unsigned>(2 * pairs));
   return cudaLaunchKernelEx(&cfg, kern, tm_a, tm_b, sc, epi);
 }
@@ -563,11 +566,11 @@ cudaError_t launch_gemm(const void* A, int64_t lda, int64_t M, const void* Bm, i
   auto kern = gemm_kernel<BF16, A_MN, B_MN, Epi>;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) return cudaErrorInvalidDevice;
-  static bool opted_in[kMaxDev] = {false};   // per device and kernel, once
-  if (!opted_in[dev]) {
+  static std::atomic<bool> opted_in[kMaxDev];   // per device and kernel, once (or again, harmlessly)
+  if (!opted_in[dev].load(std::memory_order_acquire)) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(kSmem));
     if (e != cudaSuccess) return e;
-    opted_in[dev] = true;
+    opted_in[dev].store(true, std::memory_order_release);
   }
   const int grid = sc.n_units < sms ? sc.n_units : sms;
   kern<<<grid, kThreads, kSmem, s>>>(tm_a, tm_b, sc, epi);
