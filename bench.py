@@ -348,7 +348,10 @@ class ConfigRun:
         from vocab_log_softmax_gb300 import binding as B
         self.name = name
         f32 = dict(dtype=torch.float32, device=device)
-        L = []                                       # (label, bytes, thunk)
+        L = []                                       # (label, bytes, thunk[, flops])
+        # launches timed only for comparison (another route to the same
+        # outputs); they stay out of the workload's totals
+        self.compare = set()
         if name == "logp_small":
             w = workloads.logp_small(device)
             x, ids, g = w["logits"], w["ids"], w["g"]
@@ -430,6 +433,7 @@ class ConfigRun:
                   ("separate logp bwd", bl["bwd"], lambda: B.vls_logp_bwd(a_, ids, gl, st1, dlogits=d)),
                   ("separate entropy bwd", be["bwd"], lambda: B.vls_entropy_bwd(a_, g, H, st1, dlogits=d)),
                   ("separate KL bwd", bk["bwd"], lambda: B.vls_kl_bwd(a_, b_, g, kl, st2, st3, da=d))]
+            self.compare |= {label for label, *_ in L if label.startswith("separate ")}
         elif name == "linear_logp":
             # fused linear head + logprobs on the tensor cores, against cuBLAS logits + the logp sweep
             w = workloads.linear_head(device)
@@ -452,12 +456,15 @@ class ConfigRun:
             g = w["g"]
             dh, dw = torch.empty_like(h), torch.empty_like(wt)
             ws = torch.empty((B.vls_linear_logp_bwd_workspace(n, dd, v),), dtype=torch.uint8, device=device)
-            L += [("fused linear logp (partials + combine)", io, fused, flops),
-                  ("fused linear logp bwd (dz map, dh, dW)", io + (n + v) * dd * 2 + 4 * n * v * 2,
+            # backward bytes: h and W read twice over the three products, dz
+            # written once and read twice, dh and dW written
+            L += [("fused linear logp fwd", io, fused, flops),
+                  ("fused linear logp bwd", 3 * io + 3 * n * v * 2,
                    lambda: B.vls_linear_logp_bwd(h, wt, ids, g, st, dh=dh, dW=dw, workspace=ws, status=status),
                    3 * flops),
                   ("cuBLAS h @ W^T to bf16 logits", io + n * v * 2, lambda: torch.mm(h, wt.t(), out=z), flops),
                   ("logp fwd over those logits", n * v * 2, lambda: B.vls_logp_fwd(z, ids, logp=lp, stats=st))]
+            self.compare |= {"cuBLAS h @ W^T to bf16 logits", "logp fwd over those logits"}
             self.status = status
         else:
             raise SystemExit(f"unknown workload {name}")
@@ -565,8 +572,10 @@ def run_config(args) -> None:
                                "frac_of_bf16_peak": round(fl[0] / med / 1e9 / tpeak, 4), "bf16_peak_kind": tkind})
     if getattr(run, "status", None) is not None and int(run.status.item()) != 0:
         raise SystemExit(f"{run.name}: a bounded wait in the kernel ran out (status {int(run.status.item())})")
-    total_b = sum(b for _, b, *_ in run.launches)
-    total_ms = sum(o["ms_median"] for o in ops.values())
+    own = [(label, b, fl) for label, b, _, *fl in run.launches if label not in run.compare]
+    total_b = sum(b for _, b, _ in own)
+    total_ms = sum(ops[label]["ms_median"] for label, _, _ in own)
+    total_fl = sum(fl[0] for _, _, fl in own if fl)
     # an op's forward and backward timed back to back (one event pair around both)
     pairs = {}
     for j in range(len(run.launches) - 1):
@@ -586,10 +595,15 @@ def run_config(args) -> None:
         if fl:
             autograd[label]["tflops"] = round(fl[0] / med / 1e9, 1)
     graph = graph_replay(run, args.steps, stream) if run.name == "logp_small" else None
-    print(json.dumps({"workload": run.name, "rows": run.rows, "vocab": run.vocab, "steps": args.steps,
-                      "fwd_bwd_ms": round(total_ms, 4), "tbs": round(total_b / total_ms / 1e9, 3),
-                      "peak_gbs": peak, "peak_kind": kind, "ops": ops, "fwd_bwd_back_to_back": pairs,
-                      "autograd": autograd, "graph_replay": graph}), flush=True)
+    line = {"workload": run.name, "rows": run.rows, "vocab": run.vocab, "steps": args.steps,
+            "fwd_bwd_ms": round(total_ms, 4), "tbs": round(total_b / total_ms / 1e9, 3),
+            "peak_gbs": peak, "peak_kind": kind}
+    if total_fl:   # a tensor-bound workload: its throughput against the bf16 peak
+        line.update({"tflops": round(total_fl / total_ms / 1e9, 1),
+                     "frac_of_bf16_peak": round(total_fl / total_ms / 1e9 / tpeak, 4), "bf16_peak_kind": tkind})
+    line.update({"comparison_ops": sorted(run.compare), "ops": ops, "fwd_bwd_back_to_back": pairs,
+                 "autograd": autograd, "graph_replay": graph})
+    print(json.dumps(line), flush=True)
 
 
 def time_thunk(f, steps: int, warmup: int, stream) -> list:
