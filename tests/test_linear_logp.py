@@ -204,21 +204,30 @@ def test_backward_ignored_rows_give_zero_dh():
     assert bool(torch.all(dh[dead] == 0))
 
 
-def test_backward_strided_operands():
+@pytest.mark.parametrize("d", [200, 100])
+def test_backward_strided_operands(d):
     """h and W read in place from wider buffers: the products take W and h
     as stored (their rows are the reduction index of dh and dW), so the row
     strides reach the tensor maps directly.  Same bits as contiguous copies,
-    and within the oracle bound."""
-    n, d, v = 300, 200, 3001
+    and within the oracle bound.  With D = 100 the rows of dh and dW are not
+    16-byte multiples, so their products store through the threads instead
+    of TMA."""
+    n, v = 300, 3001
     g = _gen(61)
-    hbuf = torch.randn((n, d + 8), generator=g, device=DEV).to(torch.bfloat16)
-    wbuf = (0.2 * torch.randn((v, d + 24), generator=g, device=DEV)).to(torch.bfloat16)
+    d8 = (d + 7) // 8 * 8
+    hbuf = torch.randn((n, d8 + 8), generator=g, device=DEV).to(torch.bfloat16)
+    wbuf = (0.2 * torch.randn((v, d8 + 24), generator=g, device=DEV)).to(torch.bfloat16)
     h, w = hbuf[:, :d], wbuf[:, :d]
     ids = _ids(n, v, 2, 62, 0.1)
     gr = torch.randn((n, 2), generator=g, device=DEV)
     dh, dw = _check_bwd(h, w, ids, gr, "strided linear bwd")
-    _, st, _ = B.vls_linear_logp_fwd(h.contiguous(), w.contiguous(), ids)
-    dhc, dwc, status = B.vls_linear_logp_bwd(h.contiguous(), w.contiguous(), ids, gr, st)
+    # the same values under other row strides (multiples of 8 elements, as TMA needs)
+    h2 = torch.zeros((n, d8 + 24), dtype=h.dtype, device=DEV)[:, :d]
+    w2 = torch.zeros((v, d8 + 8), dtype=w.dtype, device=DEV)[:, :d]
+    h2.copy_(h)
+    w2.copy_(w)
+    _, st, _ = B.vls_linear_logp_fwd(h2, w2, ids)
+    dhc, dwc, status = B.vls_linear_logp_bwd(h2, w2, ids, gr, st)
     torch.cuda.synchronize()
     assert int(status.item()) == 0
     assert bitwise_equal(dh, dhc) and bitwise_equal(dw, dwc)

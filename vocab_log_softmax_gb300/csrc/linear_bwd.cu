@@ -81,22 +81,121 @@ __device__ __forceinline__ void store_row32(T* dst, const float (&v)[32], int nv
   }
 }
 
-// Epilogue of a plain GEMM: C[row, col] = the accumulator, cast once.
+// Epilogue of a plain GEMM: C[row, col] = the accumulator, cast once, stored
+// by each thread (any C; the TMA form below is used where it applies).
 template <class T>
 struct StoreEpi {
+  static constexpr uint32_t kStageBytes = 0;
   T* C;
   int64_t ldc;
   struct State {};
   __device__ State begin(int64_t, bool, int) const { return {}; }
-  __device__ void cols(State&, const float (&v)[32], int64_t row, bool row_ok, int64_t cbase, int nvalid) const {
+  __device__ void cols(State&, const float (&v)[32], int64_t row, bool row_ok, int64_t cbase, int nvalid,
+                       tcg::EpiWarp&) const {
     if (row_ok && nvalid > 0) store_row32(C + row * ldc + cbase, v, nvalid);
   }
   __device__ void end(State&, int64_t, bool, int) const {}
+  __device__ void finish(tcg::EpiWarp&) const {}
 };
+
+// The same through TMA stores.  Each warp rounds its 32 rows x 32 columns
+// once to T and writes them into one of two 2 KB boxes of its staging area;
+// one lane then stores the box to C (cp.async.bulk.tensor, which clips the
+// parts outside C).  The boxes use the 64-byte swizzle: the 16-byte chunk q
+// of box row r sits at chunk q ^ ((r >> 1) & 3), so each of the warp's
+// 16-byte shared-memory writes spreads over all 32 banks.  A box is
+// rewritten only after the store issued from it has read it.
+template <class T>
+struct TmaStoreEpi {
+  static constexpr uint32_t kBoxBytes = 32 * 32 * 2;
+  static constexpr uint32_t kStageBytes = 2 * kBoxBytes;
+  CUtensorMap map;   // C [M, Ncols]: tcg::encode_store
+  int64_t M;
+  struct State {};
+  __device__ State begin(int64_t, bool, int) const { return {}; }
+  __device__ void cols(State&, const float (&v)[32], int64_t, bool, int64_t cbase, int nvalid,
+                       tcg::EpiWarp& w) const {
+    if (nvalid <= 0 || w.row0 >= M) return;   // no column or no row of C here (the same in every lane)
+    const uint32_t box = w.stage + (w.n & 1u) * kBoxBytes;
+    if (w.n >= 2) {
+      if (w.lane == 0) tc::bulk_wait_read<1>();   // the store from this box, two boxes ago
+      __syncwarp();
+    }
+    const uint32_t rowb = box + static_cast<uint32_t>(w.lane) * 64u;
+    const uint32_t sw = (static_cast<uint32_t>(w.lane) >> 1) & 3u;
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+      tc::st_shared16(rowb + ((static_cast<uint32_t>(q) ^ sw) << 4), pack2<T>(v[8 * q], v[8 * q + 1]),
+                      pack2<T>(v[8 * q + 2], v[8 * q + 3]), pack2<T>(v[8 * q + 4], v[8 * q + 5]),
+                      pack2<T>(v[8 * q + 6], v[8 * q + 7]));
+    tc::fence_proxy_async_shared();
+    __syncwarp();
+    if (w.lane == 0) {
+      tc::tma_store_2d(&map, box, static_cast<int32_t>(cbase), static_cast<int32_t>(w.row0));
+      tc::bulk_commit();
+    }
+    ++w.n;
+  }
+  __device__ void end(State&, int64_t, bool, int) const {}
+  // the CTA's shared memory outlives no store that reads it
+  __device__ void finish(tcg::EpiWarp& w) const {
+    if (w.lane == 0) tc::bulk_wait_all();
+    __syncwarp();
+  }
+};
+
+// Epilogue of a split-K product: the fp32 partial sums of K run ks go to
+// P[ks] ([M, ld] fp32, ld a multiple of 4); splitk_reduce adds the runs.
+struct PartialEpi {
+  static constexpr uint32_t kStageBytes = 0;
+  float* P;
+  int64_t M, ld;
+  struct State {};
+  __device__ State begin(int64_t, bool, int) const { return {}; }
+  __device__ void cols(State&, const float (&v)[32], int64_t row, bool row_ok, int64_t cbase, int nvalid,
+                       tcg::EpiWarp& w) const {
+    if (!row_ok || nvalid <= 0) return;
+    float* dst = P + (static_cast<int64_t>(w.ks) * M + row) * ld + cbase;
+    if (nvalid == 32) {
+#pragma unroll
+      for (int q = 0; q < 8; ++q)
+        dev::st16(dst + 4 * q, make_uint4(__float_as_uint(v[4 * q]), __float_as_uint(v[4 * q + 1]),
+                                          __float_as_uint(v[4 * q + 2]), __float_as_uint(v[4 * q + 3])));
+    } else {
+#pragma unroll
+      for (int i = 0; i < 32; ++i)
+        if (i < nvalid) dst[i] = v[i];
+    }
+  }
+  __device__ void end(State&, int64_t, bool, int) const {}
+  __device__ void finish(tcg::EpiWarp&) const {}
+};
+
+// out[e] = the runs' partial sums P[0][e] + P[1][e] + ... in that order,
+// rounded once to T; n (a multiple of 4) elements, P and out 16- and 8-byte
+// aligned.
+template <class T>
+__global__ void __launch_bounds__(256) splitk_reduce_kernel(const float* __restrict__ P, int runs, int64_t n,
+                                                            T* __restrict__ out) {
+  const int64_t n4 = n >> 2;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * 256 + threadIdx.x; i < n4;
+       i += static_cast<int64_t>(gridDim.x) * 256) {
+    float4 acc = __ldg(reinterpret_cast<const float4*>(P) + i);
+    for (int r = 1; r < runs; ++r) {
+      const float4 x = __ldg(reinterpret_cast<const float4*>(P + static_cast<int64_t>(r) * n) + i);
+      acc.x += x.x;
+      acc.y += x.y;
+      acc.z += x.z;
+      acc.w += x.w;
+    }
+    *reinterpret_cast<uint2*>(out + 4 * i) = make_uint2(pack2<T>(acc.x, acc.y), pack2<T>(acc.z, acc.w));
+  }
+}
 
 // Epilogue of the dz map: the logits tile becomes g one-hot - G p.
 template <class T>
 struct DzEpi {
+  static constexpr uint32_t kStageBytes = 0;
   const int64_t* ids;
   int32_t k;
   int64_t ignore_index;
@@ -133,7 +232,8 @@ struct DzEpi {
     return st;
   }
 
-  __device__ void cols(State& st, const float (&v)[32], int64_t row, bool row_ok, int64_t cbase, int nvalid) const {
+  __device__ void cols(State& st, const float (&v)[32], int64_t row, bool row_ok, int64_t cbase, int nvalid,
+                       tcg::EpiWarp&) const {
     if (!row_ok || nvalid == 0) return;
     float oh[32];
 #pragma unroll
@@ -170,6 +270,7 @@ struct DzEpi {
   }
 
   __device__ void end(State&, int64_t, bool, int) const {}
+  __device__ void finish(tcg::EpiWarp&) const {}
 };
 
 // the workspace: dz [N, pad8(V)] in the operand dtype
@@ -185,9 +286,41 @@ cudaError_t bwd_t(const LinearBwdArgs& a, int sms, cudaStream_t s) {
   if ((e = tcg::launch_gemm<BF16>(a.h, a.ldh, a.N, a.W, a.ldw, a.V, a.D, kLinChunkTiles, false, a.status, dze, sms, s)) !=
       cudaSuccess)
     return e;
+  // dh = dz W has K = V: at few rows its tiles alone leave most SMs idle.
+  // Then K is split into runs whose fp32 partial sums go to the dW buffer
+  // (written only by the last product, and large enough: runs x N x 4 bytes
+  // per column against V x 2), and a fixed-order sum of the runs gives dh.
+  const int runs = tcg::fill_ksplit(a.N, a.D, a.V, sms, 16);
+  const bool split = runs > 1 && int64_t(runs) * a.N * 2 <= a.V && (a.D % 4) == 0 &&
+                     (reinterpret_cast<uintptr_t>(a.dW) & 15u) == 0 && (reinterpret_cast<uintptr_t>(a.dh) & 7u) == 0;
+  if (split) {
+    float* P = static_cast<float*>(a.dW);
+    const PartialEpi pe{P, a.N, a.D};
+    if ((e = tcg::launch_gemm<BF16, false, true>(dz, ldv, a.N, a.W, a.ldw, a.D, a.V, 1, true, a.status, pe, sms, s,
+                                                 runs)) != cudaSuccess)
+      return e;
+    const int64_t n = a.N * a.D;
+    const int64_t blocks = (n / 4 + 255) / 256;
+    const int grid = static_cast<int>(blocks < 4 * sms ? blocks : 4 * sms);
+    splitk_reduce_kernel<T><<<grid > 0 ? grid : 1, 256, 0, s>>>(P, runs, n, static_cast<T*>(a.dh));
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  }
+  // dh and dW: TMA stores when the output allows them (16-byte aligned base
+  // and rows), else per-thread stores
+  TmaStoreEpi<T> dht, dwt;
+  dht.M = a.N;
+  dwt.M = a.V;
+  if (tcg::encode_store(&dht.map, a.dh, BF16, a.N, a.D, a.D) && tcg::encode_store(&dwt.map, a.dW, BF16, a.V, a.D, a.D)) {
+    if (!split &&
+        (e = tcg::launch_gemm<BF16, false, true>(dz, ldv, a.N, a.W, a.ldw, a.D, a.V, 1, true, a.status, dht, sms, s)) !=
+            cudaSuccess)
+      return e;
+    return tcg::launch_gemm<BF16, true, true>(dz, ldv, a.V, a.h, a.ldh, a.D, a.N, 1, true, a.status, dwt, sms, s);
+  }
   const StoreEpi<T> dhe{static_cast<T*>(a.dh), a.D};
-  if ((e = tcg::launch_gemm<BF16, false, true>(dz, ldv, a.N, a.W, a.ldw, a.D, a.V, 1, true, a.status, dhe, sms, s)) !=
-      cudaSuccess)
+  if (!split &&
+      (e = tcg::launch_gemm<BF16, false, true>(dz, ldv, a.N, a.W, a.ldw, a.D, a.V, 1, true, a.status, dhe, sms, s)) !=
+          cudaSuccess)
     return e;
   const StoreEpi<T> dwe{static_cast<T*>(a.dW), a.D};
   return tcg::launch_gemm<BF16, true, true>(dz, ldv, a.V, a.h, a.ldh, a.D, a.N, 1, true, a.status, dwe, sms, s);

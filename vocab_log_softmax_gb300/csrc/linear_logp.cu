@@ -42,6 +42,7 @@ __device__ __forceinline__ float pick32(const float (&v)[32], int loc) {
 // the unit's chunk of columns, the logits of its target ids, and at the end
 // of the unit one vls_partial and the targets' logits.
 struct LogpEpi {
+  static constexpr uint32_t kStageBytes = 0;
   const int64_t* ids;
   int32_t k;
   int64_t N;
@@ -66,7 +67,8 @@ struct LogpEpi {
     return st;
   }
 
-  __device__ void cols(State& st, const float (&v)[32], int64_t, bool, int64_t cbase, int nvalid) const {
+  __device__ void cols(State& st, const float (&v)[32], int64_t, bool, int64_t cbase, int nvalid,
+                       tcg::EpiWarp&) const {
     float cmax = dev::neg_inf();
     float cs = 0.0f;   // z - m is formed first, as in the row sweeps
     if (nvalid == 32) {   // every chunk but the vocabulary's last
@@ -102,6 +104,8 @@ struct LogpEpi {
       if (loc >= 0 && loc < nvalid) st.zt[j] = pick32(v, static_cast<int>(loc));
     }
   }
+
+  __device__ void finish(tcg::EpiWarp&) const {}
 
   __device__ void end(State& st, int64_t row, bool row_ok, int chunk) const {
     if (!row_ok) return;
@@ -167,6 +171,18 @@ bool encode_mnmajor(CUtensorMap* map, const void* base, bool bf16, int64_t rows,
   return fn(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2,
             const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool encode_store(CUtensorMap* map, void* base, bool bf16, int64_t rows, int64_t cols, int64_t ld) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * 2};
+  const cuuint32_t box[2] = {32, 32};
+  const cuuint32_t estr[2] = {1, 1};
+  return fn(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, base, dims, strides,
+            box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 

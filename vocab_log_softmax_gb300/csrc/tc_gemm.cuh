@@ -37,6 +37,8 @@ constexpr uint32_t kStageB = kBN * kBK * 2;   // 32 KB
 constexpr uint32_t kTmemCols = 2 * kBN;       // two fp32 accumulators of 256 columns
 constexpr int kNumBars = 2 * kStages + 4 + 1; // full, empty, acc_full x2, acc_empty x2, done
 constexpr size_t kSmem = 1024 /* alignment slack */ + kStages * (kStageA + kStageB) + kNumBars * 8 + 16;
+// epilogue staging (Epi::kStageBytes per epilogue warp) after the barriers, 1024-byte aligned
+constexpr size_t kEpiOff = (kStages * (kStageA + kStageB) + kNumBars * 8 + 16 + 1023) & ~size_t(1023);
 
 constexpr int kMaxDev = 64;   // devices the per-device launch caches cover
 
@@ -44,12 +46,17 @@ struct Sched {
   int64_t M;          // valid rows of the output
   int64_t Ncols;      // valid columns of the output
   int n_row_tiles, n_col_tiles, chunk_tiles, n_chunks, n_units, nk;
+  int ksplit;         // K is cut into ksplit runs of nk_split K blocks (split-K; 1 = whole K)
+  int nk_split;
+  int n_units_k;      // units per K run: n_row_tiles x n_chunks
   int cols_fastest;   // unit order: 0 = row tiles fastest (B chunk shared by the CTAs in flight),
                       // 1 = column chunks fastest (A row panel shared)
   uint32_t* status;   // device status word (tc::kStatusTimeout after a wait ran out)
 
-  // (row tile, column chunk) of unit u
-  __device__ __forceinline__ void unit(int u, int& rt, int& chunk) const {
+  // (row tile, column chunk, K run) of unit u; K runs outermost
+  __device__ __forceinline__ void unit(int u, int& rt, int& chunk, int& ks) const {
+    ks = u / n_units_k;
+    u -= ks * n_units_k;
     if (cols_fastest) {
       rt = u / n_chunks;
       chunk = u - rt * n_chunks;
@@ -58,18 +65,32 @@ struct Sched {
       rt = u - chunk * n_row_tiles;
     }
   }
+  // the K blocks [kb0, kb1) of K run ks
+  __device__ __forceinline__ void k_range(int ks, int& kb0, int& kb1) const {
+    kb0 = ks * nk_split;
+    kb1 = min(kb0 + nk_split, nk);
+  }
 };
 
-inline Sched make_sched(int64_t M, int64_t Ncols, int64_t K, int chunk_tiles, uint32_t* status) {
+// rows_per_tile: 128 (1-SM form) or 256 (CTA pairs).  ksplit > 1 cuts K into
+// that many runs of whole K blocks, one unit per (tile, chunk, run); the
+// epilogue then sees partial sums and the run index (EpiWarp::ks).
+inline Sched make_sched(int64_t M, int64_t Ncols, int64_t K, int chunk_tiles, uint32_t* status, int rows_per_tile,
+                        int ksplit) {
   Sched s;
   s.M = M;
   s.Ncols = Ncols;
-  s.n_row_tiles = static_cast<int>((M + kBM - 1) / kBM);
+  s.n_row_tiles = static_cast<int>((M + rows_per_tile - 1) / rows_per_tile);
   s.n_col_tiles = static_cast<int>((Ncols + kBN - 1) / kBN);
   s.chunk_tiles = chunk_tiles;
   s.n_chunks = (s.n_col_tiles + chunk_tiles - 1) / chunk_tiles;
-  s.n_units = s.n_row_tiles * s.n_chunks;
   s.nk = static_cast<int>((K + kBK - 1) / kBK);
+  if (ksplit < 1) ksplit = 1;
+  if (ksplit > s.nk) ksplit = s.nk;
+  s.nk_split = (s.nk + ksplit - 1) / ksplit;
+  s.ksplit = (s.nk + s.nk_split - 1) / s.nk_split;   // no empty run
+  s.n_units_k = s.n_row_tiles * s.n_chunks;
+  s.n_units = s.n_units_k * s.ksplit;
   s.cols_fastest = 0;
   s.status = status;
   return s;
@@ -108,16 +129,32 @@ __device__ __forceinline__ uint64_t stage_desc(uint32_t addr) {
 template <bool MN>
 constexpr uint64_t kDescStep = MN ? (2048 >> 4) : (32 >> 4);
 
-// Epilogue interface (one object per launch, copied to every thread):
+// What an epilogue warp owns: its shared-memory staging area (Epi::kStageBytes
+// bytes, 1024-byte aligned; none when that is 0), the first of its 32 rows in
+// the current unit, its lane, and a count the epilogue may keep (bulk stores
+// issued, say).
+struct EpiWarp {
+  uint32_t stage;
+  int64_t row0;
+  int lane;
+  uint32_t n;
+  int ks;   // the unit's K run (0 without split-K)
+};
+
+// Epilogue interface (one object per launch, a __grid_constant__ kernel
+// parameter, so a CUtensorMap member may serve TMA):
+//   static constexpr uint32_t kStageBytes;                  shared memory per epilogue warp
 //   struct State;                                           per-thread, per-unit state
 //   State begin(int64_t row, bool row_ok, int chunk);       at each unit
-//   void  cols(State&, const float (&v)[32], int64_t row, bool row_ok, int64_t col0, int nvalid);
-//                                                           32 columns of the row (nvalid < 32 at the edge)
+//   void  cols(State&, const float (&v)[32], int64_t row, bool row_ok, int64_t col0, int nvalid, EpiWarp&);
+//                                                           32 columns of the row (nvalid < 32 at the edge),
+//                                                           called by the whole warp
 //   void  end(State&, int64_t row, bool row_ok, int chunk); after the unit's last tile
+//   void  finish(EpiWarp&);                                 once per warp before the CTA exits
 template <bool BF16, bool A_MN, bool B_MN, class Epi>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
-                const Sched sc, const Epi epi) {
+                const Sched sc, const __grid_constant__ Epi epi) {
   extern __shared__ unsigned char smem_raw[];
   if (static_cast<int>(blockIdx.x) >= sc.n_units) return;  // whole CTA, before any barrier
 
@@ -166,11 +203,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t issued = 0;   // loads issued, for the drain below
       bool ok = true;
       for (int u = blockIdx.x; ok && u < sc.n_units; u += gridDim.x) {
-        int rt, chunk;
-        sc.unit(u, rt, chunk);
+        int rt, chunk, ks, kb0, kb1;
+        sc.unit(u, rt, chunk, ks);
+        sc.k_range(ks, kb0, kb1);
         const int t_end = min((chunk + 1) * sc.chunk_tiles, sc.n_col_tiles);
         for (int t = chunk * sc.chunk_tiles; ok && t < t_end; ++t) {
-          for (int kb = 0; kb < sc.nk; ++kb) {
+          for (int kb = kb0; kb < kb1; ++kb) {
             if (!tc::wait(empty(stage), phase ^ 1u, abort_flag, sc.status)) {
               ok = false;
               break;
@@ -206,8 +244,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t tc_count = 0;
       bool ok = true;
       for (int u = blockIdx.x; ok && u < sc.n_units; u += gridDim.x) {
-        int rt, chunk;
-        sc.unit(u, rt, chunk);
+        int rt, chunk, ks, kb0, kb1;
+        sc.unit(u, rt, chunk, ks);
+        sc.k_range(ks, kb0, kb1);
         const int t_end = min((chunk + 1) * sc.chunk_tiles, sc.n_col_tiles);
         for (int t = chunk * sc.chunk_tiles; ok && t < t_end; ++t, ++tc_count) {
           const uint32_t buf = tc_count & 1u, use = (tc_count >> 1) & 1u;
@@ -217,7 +256,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           tc::fence_after_sync();
           const uint32_t d = tmem + buf * kBN;
-          for (int kb = 0; kb < sc.nk; ++kb) {
+          for (int kb = kb0; kb < kb1; ++kb) {
             if (!tc::wait(full(stage), phase, abort_flag, sc.status)) {
               ok = false;
               break;
@@ -227,7 +266,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint64_t db = stage_desc<B_MN>(sB + stage * kStageB);
 #pragma unroll
             for (int kk = 0; kk < kBK / kUK; ++kk)
-              tc::mma_f16(d, da + kDescStep<A_MN> * kk, db + kDescStep<B_MN> * kk, idesc, (kb | kk) != 0 ? 1u : 0u);
+              tc::mma_f16(d, da + kDescStep<A_MN> * kk, db + kDescStep<B_MN> * kk, idesc,
+                          (kb > kb0 || kk > 0) ? 1u : 0u);
             tc::mma_commit(empty(stage));   // frees the stage once these MMAs have read it
             if (++stage == kStages) {
               stage = 0;
@@ -246,14 +286,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int quarter = warp & 3;                 // the tensor-memory lanes this warp may read
     const int r_in_tile = quarter * 32 + lane;
     const uint32_t lane_addr = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
+    EpiWarp ew{sbase + static_cast<uint32_t>(kEpiOff) + static_cast<uint32_t>(quarter) * Epi::kStageBytes, 0, lane, 0u, 0};
     uint32_t tc_count = 0;
     bool ok = true;
     for (int u = blockIdx.x; ok && u < sc.n_units; u += gridDim.x) {
-      int rt, chunk;
-      sc.unit(u, rt, chunk);
+      int rt, chunk, ks;
+      sc.unit(u, rt, chunk, ks);
+      ew.ks = ks;
       const int t_beg = chunk * sc.chunk_tiles, t_end = min(t_beg + sc.chunk_tiles, sc.n_col_tiles);
       const int64_t row = static_cast<int64_t>(rt) * kBM + r_in_tile;
       const bool row_ok = row < sc.M;
+      ew.row0 = row - lane;
       typename Epi::State st = epi.begin(row, row_ok, chunk);
       for (int t = t_beg; t < t_end; ++t, ++tc_count) {
         const uint32_t buf = tc_count & 1u, use = (tc_count >> 1) & 1u;
@@ -266,13 +309,27 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         __syncwarp();
         tc::fence_after_sync();
-        for (int c = 0; c < kBN / 32; ++c) {
+        // chunk c + 1 is read from tensor memory while chunk c is folded
+        auto fold = [&](const uint32_t (&r)[32], int c) {
           float v[32];
-          tc::tmem_ld32(lane_addr + buf * kBN + c * 32, v);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
           const int64_t cbase = static_cast<int64_t>(t) * kBN + c * 32;
           const int64_t left = sc.Ncols - cbase;
           const int nvalid = left <= 0 ? 0 : (left >= 32 ? 32 : static_cast<int>(left));
-          epi.cols(st, v, row, row_ok, cbase, nvalid);
+          epi.cols(st, v, row, row_ok, cbase, nvalid, ew);
+        };
+        const uint32_t acc = lane_addr + buf * kBN;
+        uint32_t ra[32], rb[32];
+        tc::tmem_ld32_issue(acc, ra);
+        tc::tmem_ld32_wait(ra);
+        for (int c = 0; c < kBN / 32; c += 2) {
+          tc::tmem_ld32_issue(acc + (c + 1) * 32, rb);
+          fold(ra, c);
+          tc::tmem_ld32_wait(rb);
+          if (c + 2 < kBN / 32) tc::tmem_ld32_issue(acc + (c + 2) * 32, ra);
+          fold(rb, c + 1);
+          if (c + 2 < kBN / 32) tc::tmem_ld32_wait(ra);
         }
         tc::fence_before_sync();
         __syncwarp();
@@ -280,6 +337,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (ok) epi.end(st, row, row_ok, chunk);
     }
+    epi.finish(ew);
   }
 
   tc::fence_before_sync();
@@ -309,11 +367,12 @@ constexpr uint32_t kStageA2 = kBM * kBK * 2;         // 16 KB: this CTA's 128 ro
 constexpr uint32_t kStageB2 = (kBN / 2) * kBK * 2;   // 16 KB: this CTA's 128 columns of B
 constexpr int kNumBars2 = 2 * kStages2 + 4 + 1;
 constexpr size_t kSmem2 = 1024 + kStages2 * (kStageA2 + kStageB2) + kNumBars2 * 8 + 16;
+constexpr size_t kEpiOff2 = (kStages2 * (kStageA2 + kStageB2) + kNumBars2 * 8 + 16 + 1023) & ~size_t(1023);
 
 template <bool BF16, bool A_MN, bool B_MN, class Epi>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm2_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
-                 const Sched sc, const Epi epi) {
+                 const Sched sc, const __grid_constant__ Epi epi) {
   extern __shared__ unsigned char smem_raw[];
   const int pair = static_cast<int>(blockIdx.x >> 1), n_pairs = static_cast<int>(gridDim.x >> 1);
   if (pair >= sc.n_units) return;   // both CTAs of the pair, before any barrier
@@ -364,11 +423,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t phase = 0;
       bool ok = true;
       for (int u = pair; ok && u < sc.n_units; u += n_pairs) {
-        int rt, chunk;
-        sc.unit(u, rt, chunk);
+        int rt, chunk, ks, kb0, kb1;
+        sc.unit(u, rt, chunk, ks);
+        sc.k_range(ks, kb0, kb1);
         const int t_end = min((chunk + 1) * sc.chunk_tiles, sc.n_col_tiles);
         for (int t = chunk * sc.chunk_tiles; ok && t < t_end; ++t) {
-          for (int kb = 0; kb < sc.nk; ++kb) {
+          for (int kb = kb0; kb < kb1; ++kb) {
             if (!tc::wait(empty(stage), phase ^ 1u, abort_flag, sc.status)) {
               ok = false;
               break;
@@ -395,8 +455,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t tc_count = 0;
       bool ok = true;
       for (int u = pair; ok && u < sc.n_units; u += n_pairs) {
-        int rt, chunk;
-        sc.unit(u, rt, chunk);
+        int rt, chunk, ks, kb0, kb1;
+        sc.unit(u, rt, chunk, ks);
+        sc.k_range(ks, kb0, kb1);
         const int t_end = min((chunk + 1) * sc.chunk_tiles, sc.n_col_tiles);
         for (int t = chunk * sc.chunk_tiles; ok && t < t_end; ++t, ++tc_count) {
           const uint32_t buf = tc_count & 1u, use = (tc_count >> 1) & 1u;
@@ -406,7 +467,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           tc::fence_after_sync();
           const uint32_t d = tmem + buf * kBN;
-          for (int kb = 0; kb < sc.nk; ++kb) {
+          for (int kb = kb0; kb < kb1; ++kb) {
             if (!tc::wait(full(stage), phase, abort_flag, sc.status)) {
               ok = false;
               break;
@@ -417,7 +478,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int kk = 0; kk < kBK / kUK; ++kk)
               tc::mma_f16_pair(d, da + kDescStep<A_MN> * kk, db + kDescStep<B_MN> * kk, idesc,
-                               (kb | kk) != 0 ? 1u : 0u);
+                               (kb > kb0 || kk > 0) ? 1u : 0u);
             tc::mma_commit_pair(empty(stage));   // frees this stage in both CTAs
             if (++stage == kStages2) {
               stage = 0;
@@ -436,14 +497,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int quarter = warp & 3;
     const int r_in_tile = quarter * 32 + lane;
     const uint32_t lane_addr = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
+    EpiWarp ew{sbase + static_cast<uint32_t>(kEpiOff2) + static_cast<uint32_t>(quarter) * Epi::kStageBytes, 0, lane, 0u, 0};
     uint32_t tc_count = 0;
     bool ok = true;
     for (int u = pair; ok && u < sc.n_units; u += n_pairs) {
-      int rt, chunk;
-      sc.unit(u, rt, chunk);
+      int rt, chunk, ks;
+      sc.unit(u, rt, chunk, ks);
+      ew.ks = ks;
       const int t_beg = chunk * sc.chunk_tiles, t_end = min(t_beg + sc.chunk_tiles, sc.n_col_tiles);
       const int64_t row = static_cast<int64_t>(rt) * 2 * kBM + rank * kBM + r_in_tile;
       const bool row_ok = row < sc.M;
+      ew.row0 = row - lane;
       typename Epi::State st = epi.begin(row, row_ok, chunk);
       for (int t = t_beg; t < t_end; ++t, ++tc_count) {
         const uint32_t buf = tc_count & 1u, use = (tc_count >> 1) & 1u;
@@ -454,13 +518,27 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         __syncwarp();
         tc::fence_after_sync();
-        for (int c = 0; c < kBN / 32; ++c) {
+        // chunk c + 1 is read from tensor memory while chunk c is folded
+        auto fold = [&](const uint32_t (&r)[32], int c) {
           float v[32];
-          tc::tmem_ld32(lane_addr + buf * kBN + c * 32, v);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
           const int64_t cbase = static_cast<int64_t>(t) * kBN + c * 32;
           const int64_t left = sc.Ncols - cbase;
           const int nvalid = left <= 0 ? 0 : (left >= 32 ? 32 : static_cast<int>(left));
-          epi.cols(st, v, row, row_ok, cbase, nvalid);
+          epi.cols(st, v, row, row_ok, cbase, nvalid, ew);
+        };
+        const uint32_t acc = lane_addr + buf * kBN;
+        uint32_t ra[32], rb[32];
+        tc::tmem_ld32_issue(acc, ra);
+        tc::tmem_ld32_wait(ra);
+        for (int c = 0; c < kBN / 32; c += 2) {
+          tc::tmem_ld32_issue(acc + (c + 1) * 32, rb);
+          fold(ra, c);
+          tc::tmem_ld32_wait(rb);
+          if (c + 2 < kBN / 32) tc::tmem_ld32_issue(acc + (c + 2) * 32, ra);
+          fold(rb, c + 1);
+          if (c + 2 < kBN / 32) tc::tmem_ld32_wait(ra);
         }
         tc::fence_before_sync();
         __syncwarp();
@@ -468,6 +546,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (ok) epi.end(st, row, row_ok, chunk);
     }
+    epi.finish(ew);
   }
 
   tc::fence_before_sync();
@@ -491,6 +570,11 @@ bool encode_kmajor(CUtensorMap* map, const void* base, bool bf16, int64_t rows, 
 // 128-byte swizzle, zero fill outside the matrix.
 bool encode_mnmajor(CUtensorMap* map, const void* base, bool bf16, int64_t rows, int64_t K, int64_t ld);
 
+// Tensor map of a [rows, cols] 16-bit row-major output with row stride ld for
+// TMA stores of 32 x 32 boxes with 64-byte swizzle.  False when the base or
+// the stride is not 16-byte aligned.
+bool encode_store(CUtensorMap* map, void* base, bool bf16, int64_t rows, int64_t cols, int64_t ld);
+
 // Either form, as the operand is stored.
 inline bool encode_operand(CUtensorMap* map, bool mn, const void* base, bool bf16, int64_t rows, int64_t K,
                            int64_t ld, int box_rows) {
@@ -503,14 +587,12 @@ int cta_group();
 template <bool BF16, bool A_MN, bool B_MN, class Epi>
 cudaError_t launch_gemm2(const void* A, int64_t lda, int64_t M, const void* Bm, int64_t ldb, int64_t Ncols,
                          int64_t K, int chunk_tiles, bool cols_fastest, uint32_t* status, const Epi& epi, int sms,
-                         cudaStream_t s) {
+                         cudaStream_t s, int ksplit) {
   CUtensorMap tm_a, tm_b;
   if (!encode_operand(&tm_a, A_MN, A, BF16, M, K, lda, kBM) ||
       !encode_operand(&tm_b, B_MN, Bm, BF16, Ncols, K, ldb, kBN / 2))
     return cudaErrorInvalidValue;
-  Sched sc = make_sched(M, Ncols, K, chunk_tiles, status);
-  sc.n_row_tiles = static_cast<int>((M + 2 * kBM - 1) / (2 * kBM));   // 256-row tiles
-  sc.n_units = sc.n_row_tiles * sc.n_chunks;
+  Sched sc = make_sched(M, Ncols, K, chunk_tiles, status, 2 * kBM, ksplit);   // 256-row tiles
   sc.cols_fastest = cols_fastest ? 1 : 0;
   auto kern = gemm2_kernel<BF16, A_MN, B_MN, Epi>;
   int dev = 0;
@@ -521,7 +603,9 @@ cudaError_t launch_gemm2(const void* A, int64_t lda, int64_t M, const void* Bm, 
   static std::atomic<int> resident_on[kMaxDev];
   cudaLaunchConfig_t cfg = {};
   cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = kSmem2;
+  constexpr size_t smem = 1024 + kEpiOff2 + 4 * static_cast<size_t>(Epi::kStageBytes);
+  static_assert(smem <= 227 * 1024, "shared memory per CTA");
+  cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -534,7 +618,7 @@ cudaError_t launch_gemm2(const void* A, int64_t lda, int64_t M, const void* Bm, 
   // with an odd number of free SMs leaves one idle)
   int resident = resident_on[dev].load(std::memory_order_acquire);
   if (resident == 0) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(kSmem2));
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     if (e != cudaSuccess) return e;
     cfg.gridDim = dim3(static_cast<unsigned>(sms & ~1));
     if (cudaOccupancyMaxActiveClusters(&resident, kern, &cfg) != cudaSuccess || resident < 1) {
@@ -548,32 +632,49 @@ cudaError_t launch_gemm2(const void* A, int64_t lda, int64_t M, const void* Bm, 
   return cudaLaunchKernelEx(&cfg, kern, tm_a, tm_b, sc, epi);
 }
 
+// Split-K factor that fills the GPU once with the units of an M x Ncols
+// output (chunk_tiles 1): as many K runs as the resident CTAs (pairs) can take
+// beside the tiles, each run at least min_k_blocks long; 1 when the tiles
+// alone fill the GPU.
+inline int fill_ksplit(int64_t M, int64_t Ncols, int64_t K, int sms, int min_k_blocks) {
+  const int64_t rows = cta_group() == 2 && sms >= 2 ? 2 * kBM : kBM;
+  const int64_t slots = cta_group() == 2 && sms >= 2 ? sms / 2 : sms;
+  const int64_t tiles = ((M + rows - 1) / rows) * ((Ncols + kBN - 1) / kBN);
+  const int64_t nk = (K + kBK - 1) / kBK;
+  int64_t k = tiles > 0 ? slots / tiles : 1;
+  const int64_t kmax = nk / (min_k_blocks > 0 ? min_k_blocks : 1);
+  if (k > kmax) k = kmax;
+  return static_cast<int>(k < 1 ? 1 : k);
+}
+
 // C = A B^T through the epilogue.  A_MN / B_MN: the operand is stored
 // MN-major ([K, M] for A, [K, Ncols] for B, row stride lda / ldb), else
-// K-major ([M, K], [Ncols, K]).
+// K-major ([M, K], [Ncols, K]).  ksplit > 1: split-K (see make_sched).
 template <bool BF16, bool A_MN = false, bool B_MN = false, class Epi>
 cudaError_t launch_gemm(const void* A, int64_t lda, int64_t M, const void* Bm, int64_t ldb, int64_t Ncols,
                         int64_t K, int chunk_tiles, bool cols_fastest, uint32_t* status, const Epi& epi, int sms,
-                        cudaStream_t s) {
+                        cudaStream_t s, int ksplit = 1) {
   if (cta_group() == 2 && sms >= 2)
     return launch_gemm2<BF16, A_MN, B_MN>(A, lda, M, Bm, ldb, Ncols, K, chunk_tiles, cols_fastest, status, epi, sms,
-                                          s);
+                                          s, ksplit);
   CUtensorMap tm_a, tm_b;
   if (!encode_operand(&tm_a, A_MN, A, BF16, M, K, lda, kBM) || !encode_operand(&tm_b, B_MN, Bm, BF16, Ncols, K, ldb, kBN))
     return cudaErrorInvalidValue;
-  Sched sc = make_sched(M, Ncols, K, chunk_tiles, status);
+  Sched sc = make_sched(M, Ncols, K, chunk_tiles, status, kBM, ksplit);
   sc.cols_fastest = cols_fastest ? 1 : 0;
   auto kern = gemm_kernel<BF16, A_MN, B_MN, Epi>;
+  constexpr size_t smem = 1024 + kEpiOff + 4 * static_cast<size_t>(Epi::kStageBytes);
+  static_assert(smem <= 227 * 1024, "shared memory per CTA");
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) return cudaErrorInvalidDevice;
   static std::atomic<bool> opted_in[kMaxDev];   // per device and kernel, once (or again, harmlessly)
   if (!opted_in[dev].load(std::memory_order_acquire)) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(kSmem));
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     if (e != cudaSuccess) return e;
     opted_in[dev].store(true, std::memory_order_release);
   }
   const int grid = sc.n_units < sms ? sc.n_units : sms;
-  kern<<<grid, kThreads, kSmem, s>>>(tm_a, tm_b, sc, epi);
+  kern<<<grid, kThreads, smem, s>>>(tm_a, tm_b, sc, epi);
   return cudaGetLastError();
 }
 
