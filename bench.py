@@ -341,7 +341,7 @@ class ConfigRun:
     """One of the five workloads, fwd+bwd of its ops, for per-config numbers
     (``--workload``).  Not the headline step; the same kernels and geometry."""
 
-    def __init__(self, name: str, device):
+    def __init__(self, name: str, device, rows: int | None = None):
         import torch
 
         import workloads
@@ -436,7 +436,8 @@ class ConfigRun:
             self.compare |= {label for label, *_ in L if label.startswith("separate ")}
         elif name == "linear_logp":
             # fused linear head + logprobs on the tensor cores, against cuBLAS logits + the logp sweep
-            w = workloads.linear_head(device)
+            # rows: the batch (8192 by default; --rows sets it for this workload)
+            w = workloads.linear_head(device) if rows is None else workloads.linear_head(device, n=rows)
             h, wt, ids = w["h"], w["w"], w["ids"]
             n, dd = h.shape
             v = wt.shape[0]
@@ -545,7 +546,7 @@ def run_config(args) -> None:
     """Per-config fwd / bwd times (median over steps) and TB/s for every op."""
     import torch
     device = torch.device("cuda", 0)
-    run = ConfigRun(args.workload, device)
+    run = ConfigRun(args.workload, device, args.rows if args.workload == "linear_logp" and args.rows != N_ROWS else None)
     for _ in range(args.warmup):
         for _, _, f, *_ in run.launches:
             f()
