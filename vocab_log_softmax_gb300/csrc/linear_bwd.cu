@@ -98,17 +98,49 @@ struct StoreEpi {
   __device__ void finish(tcg::EpiWarp&) const {}
 };
 
-// The same through TMA stores.  Each warp rounds its 32 rows x 32 columns
-// once to T and writes them into one of two 2 KB boxes of its staging area;
-// one lane then stores the box to C (cp.async.bulk.tensor, which clips the
-// parts outside C).  The boxes use the 64-byte swizzle: the 16-byte chunk q
-// of box row r sits at chunk q ^ ((r >> 1) & 3), so each of the warp's
-// 16-byte shared-memory writes spreads over all 32 banks.  A box is
-// rewritten only after the store issued from it has read it.
+// TMA stores from an epilogue warp.  The warp's 32 rows x 32 columns,
+// already rounded to 16 bits (pk: lane = row, 16 packed pairs), go into one
+// of two 2 KB boxes of its staging area; one lane then stores the box
+// (cp.async.bulk.tensor, which clips the parts outside the tensor).  The
+// boxes use the 64-byte swizzle: the 16-byte chunk q of box row r sits at
+// chunk q ^ ((r >> 1) & 3), so each of the warp's 16-byte shared-memory
+// writes spreads over all 32 banks.  A box is rewritten only after the store
+// issued from it has read it.  Called by the whole warp.
+constexpr uint32_t kBoxBytes = 32 * 32 * 2;
+constexpr uint32_t kBoxStageBytes = 2 * kBoxBytes;
+
+__device__ __forceinline__ void store_box(const CUtensorMap* map, tcg::EpiWarp& w, const uint32_t (&pk)[16],
+                                          int64_t cbase) {
+  const uint32_t box = w.stage + (w.n & 1u) * kBoxBytes;
+  if (w.n >= 2) {
+    if (w.lane == 0) tc::bulk_wait_read<1>();   // the store from this box, two boxes ago
+    __syncwarp();
+  }
+  const uint32_t rowb = box + static_cast<uint32_t>(w.lane) * 64u;
+  const uint32_t sw = (static_cast<uint32_t>(w.lane) >> 1) & 3u;
+#pragma unroll
+  for (int q = 0; q < 4; ++q)
+    tc::st_shared16(rowb + ((static_cast<uint32_t>(q) ^ sw) << 4), pk[4 * q], pk[4 * q + 1], pk[4 * q + 2],
+                    pk[4 * q + 3]);
+  tc::fence_proxy_async_shared();
+  __syncwarp();
+  if (w.lane == 0) {
+    tc::tma_store_2d(map, box, static_cast<int32_t>(cbase), static_cast<int32_t>(w.row0));
+    tc::bulk_commit();
+  }
+  ++w.n;
+}
+
+// the CTA's shared memory outlives no store that reads it
+__device__ __forceinline__ void finish_boxes(tcg::EpiWarp& w) {
+  if (w.lane == 0) tc::bulk_wait_all();
+  __syncwarp();
+}
+
+// The plain GEMM epilogue through TMA stores (store_box).
 template <class T>
 struct TmaStoreEpi {
-  static constexpr uint32_t kBoxBytes = 32 * 32 * 2;
-  static constexpr uint32_t kStageBytes = 2 * kBoxBytes;
+  static constexpr uint32_t kStageBytes = kBoxStageBytes;
   CUtensorMap map;   // C [M, Ncols]: tcg::encode_store
   int64_t M;
   struct State {};
@@ -116,32 +148,13 @@ struct TmaStoreEpi {
   __device__ void cols(State&, const float (&v)[32], int64_t, bool, int64_t cbase, int nvalid,
                        tcg::EpiWarp& w) const {
     if (nvalid <= 0 || w.row0 >= M) return;   // no column or no row of C here (the same in every lane)
-    const uint32_t box = w.stage + (w.n & 1u) * kBoxBytes;
-    if (w.n >= 2) {
-      if (w.lane == 0) tc::bulk_wait_read<1>();   // the store from this box, two boxes ago
-      __syncwarp();
-    }
-    const uint32_t rowb = box + static_cast<uint32_t>(w.lane) * 64u;
-    const uint32_t sw = (static_cast<uint32_t>(w.lane) >> 1) & 3u;
+    uint32_t pk[16];
 #pragma unroll
-    for (int q = 0; q < 4; ++q)
-      tc::st_shared16(rowb + ((static_cast<uint32_t>(q) ^ sw) << 4), pack2<T>(v[8 * q], v[8 * q + 1]),
-                      pack2<T>(v[8 * q + 2], v[8 * q + 3]), pack2<T>(v[8 * q + 4], v[8 * q + 5]),
-                      pack2<T>(v[8 * q + 6], v[8 * q + 7]));
-    tc::fence_proxy_async_shared();
-    __syncwarp();
-    if (w.lane == 0) {
-      tc::tma_store_2d(&map, box, static_cast<int32_t>(cbase), static_cast<int32_t>(w.row0));
-      tc::bulk_commit();
-    }
-    ++w.n;
+    for (int i = 0; i < 16; ++i) pk[i] = pack2<T>(v[2 * i], v[2 * i + 1]);
+    store_box(&map, w, pk, cbase);
   }
   __device__ void end(State&, int64_t, bool, int) const {}
-  // the CTA's shared memory outlives no store that reads it
-  __device__ void finish(tcg::EpiWarp& w) const {
-    if (w.lane == 0) tc::bulk_wait_all();
-    __syncwarp();
-  }
+  __device__ void finish(tcg::EpiWarp& w) const { finish_boxes(w); }
 };
 
 // Epilogue of a split-K product: the fp32 partial sums of K run ks go to
@@ -193,9 +206,9 @@ __global__ void __launch_bounds__(256) splitk_reduce_kernel(const float* __restr
 }
 
 // Epilogue of the dz map: the logits tile becomes g one-hot - G p.
-template <class T>
+template <class T, bool TMA>
 struct DzEpi {
-  static constexpr uint32_t kStageBytes = 0;
+  static constexpr uint32_t kStageBytes = TMA ? kBoxStageBytes : 0;
   const int64_t* ids;
   int32_t k;
   int64_t ignore_index;
@@ -204,6 +217,8 @@ struct DzEpi {
   const vls_rowstat* stats;  // [N]
   T* dz;                     // [N, ld_dz]
   int64_t ld_dz;
+  int64_t N;
+  CUtensorMap map;           // dz for TMA stores (TMA only): tcg::encode_store
 
   struct State {
     float m, c, G;             // max, log S * log2(e), sum of the valid upstream gradients
@@ -233,8 +248,10 @@ struct DzEpi {
   }
 
   __device__ void cols(State& st, const float (&v)[32], int64_t row, bool row_ok, int64_t cbase, int nvalid,
-                       tcg::EpiWarp&) const {
-    if (!row_ok || nvalid == 0) return;
+                       tcg::EpiWarp& ew) const {
+    // with TMA stores every lane takes part: a row past N holds zeros (its
+    // state is 0 and its logits the zero fill) and the store clips it
+    if (nvalid == 0 || (!TMA && !row_ok)) return;
     float oh[32];
 #pragma unroll
     for (int i = 0; i < 32; ++i) oh[i] = 0.0f;
@@ -258,19 +275,26 @@ struct DzEpi {
       dev::upk(dev::fma2(g2, p, dev::pk(oh[2 * i], oh[2 * i + 1])), d0, d1);
       w[i] = pack2<T>(d0, d1);
     }
-    T* dst = dz + row * ld_dz + cbase;
-    if (nvalid == 32 && dev::aligned16(dst)) {
-#pragma unroll
-      for (int q = 0; q < 4; ++q) dev::st16(dst + 8 * q, make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]));
+    if constexpr (TMA) {
+      if (ew.row0 < N) store_box(&map, ew, w, cbase);   // the same in every lane
     } else {
+      T* dst = dz + row * ld_dz + cbase;
+      if (nvalid == 32 && dev::aligned16(dst)) {
 #pragma unroll
-      for (int i = 0; i < 32; ++i)
-        if (i < nvalid) st_half(dst + i, w[i >> 1], i & 1);
+        for (int q = 0; q < 4; ++q)
+          dev::st16(dst + 8 * q, make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]));
+      } else {
+#pragma unroll
+        for (int i = 0; i < 32; ++i)
+          if (i < nvalid) st_half(dst + i, w[i >> 1], i & 1);
+      }
     }
   }
 
   __device__ void end(State&, int64_t, bool, int) const {}
-  __device__ void finish(tcg::EpiWarp&) const {}
+  __device__ void finish(tcg::EpiWarp& ew) const {
+    if constexpr (TMA) finish_boxes(ew);
+  }
 };
 
 // the workspace: dz [N, pad8(V)] in the operand dtype
@@ -282,10 +306,28 @@ cudaError_t bwd_t(const LinearBwdArgs& a, int sms, cudaStream_t s) {
   T* dz = static_cast<T*>(a.workspace);
   const int64_t ldv = pad8(a.V);
   cudaError_t e;
-  const DzEpi<T> dze{a.ids, a.k, a.ignore_index, a.V, a.g, a.stats, dz, ldv};
-  if ((e = tcg::launch_gemm<BF16>(a.h, a.ldh, a.N, a.W, a.ldw, a.V, a.D, kLinChunkTiles, false, a.status, dze, sms, s)) !=
-      cudaSuccess)
-    return e;
+  // the dz map: dz through TMA stores (the workspace always allows them)
+  auto dz_epi = [&](auto& ep) {
+    ep.ids = a.ids;
+    ep.k = a.k;
+    ep.ignore_index = a.ignore_index;
+    ep.V = a.V;
+    ep.g = a.g;
+    ep.stats = a.stats;
+    ep.dz = dz;
+    ep.ld_dz = ldv;
+    ep.N = a.N;
+  };
+  DzEpi<T, true> dzt;
+  dz_epi(dzt);
+  if (tcg::encode_store(&dzt.map, dz, BF16, a.N, a.V, ldv)) {
+    e = tcg::launch_gemm<BF16>(a.h, a.ldh, a.N, a.W, a.ldw, a.V, a.D, kLinChunkTiles, false, a.status, dzt, sms, s);
+  } else {
+    DzEpi<T, false> dze;
+    dz_epi(dze);
+    e = tcg::launch_gemm<BF16>(a.h, a.ldh, a.N, a.W, a.ldw, a.V, a.D, kLinChunkTiles, false, a.status, dze, sms, s);
+  }
+  if (e != cudaSuccess) return e;
   // dh = dz W has K = V: at few rows its tiles alone leave most SMs idle.
   // Then K is split into runs whose fp32 partial sums go to the dW buffer
   // (written only by the last product, and large enough: runs x N x 4 bytes
