@@ -263,24 +263,26 @@ template <int OP, int DIR>
 constexpr bool reads_two() { return OP == kFwdKl || (OP == kFwdFused && DIR != kFusedNoKl); }
 
 // 16-byte loads in flight per thread before any is used: 4 vectors of one
-// tensor, or 2 vectors of each of the two KL tensors.
-template <int OP, int DIR>
-constexpr int fwd_unroll() { return reads_two<OP, DIR>() ? 2 : 4; }
+// tensor, or 2 vectors of each of the two KL tensors.  The softcapped logp
+// sweep, bound by its arithmetic's latency rather than by memory, takes 6
+// (measured: 3.7% faster than 4 at 6 resident CTAs; 8 spills).
+template <int OP, int DIR, bool CAP>
+constexpr int fwd_unroll() { return reads_two<OP, DIR>() ? 2 : ((CAP && OP == kFwdLogp) ? 6 : 4); }
 
 // Resident CTAs per SM the forward sweep is compiled for, at 256 threads.
 // Without an explicit minimum, ptxas sized these kernels by heuristics that
 // moved with the size of the argument struct (the bf16 entropy sweep went
 // from 32 to 38 registers, the KL sweep from 44 to 56), costing 5-8% of
 // bandwidth.  The bounds below keep the bf16 sweeps at 32 registers (one
-// tensor), 40 (fp16 one-tensor, fused, or softcapped logp), 48 (softcapped
-// entropy and fused, bf16 KL);
+// tensor), 40 (fp16 one-tensor or fused), 48 (softcapped logp with its
+// 6-vector batches, softcapped entropy and fused, bf16 KL);
 // fp32 vectors hold twice the registers and get 64.
 template <class T, int OP, bool CAP, int DIR>
 constexpr int fwd_ctas_at_256() {
   if (sizeof(T) == 4) return 4;
   if (reads_two<OP, DIR>())
     return (CAP || OP == kFwdFused || !std::is_same<T, __nv_bfloat16>::value) ? 4 : 5;
-  if (CAP) return OP == kFwdLogp ? 6 : 5;
+  if (CAP) return 5;
   return (OP == kFwdFused || std::is_same<T, __half>::value) ? 6 : 8;
 }
 template <class T, int OP, bool CAP, int DIR>
@@ -323,7 +325,7 @@ template <class T, int OP, bool CAP, int DIR = kFusedNoKl>
 __global__ void __launch_bounds__(kFwdThreads, (fwd_min_blocks<T, OP, CAP, DIR>())) row_fwd_kernel(const FwdArgs a) {
   using Acc = typename FwdAccOf<OP, T, CAP, DIR>::type;
   using S = typename Acc::State;
-  constexpr int U = fwd_unroll<OP, DIR>();
+  constexpr int U = fwd_unroll<OP, DIR, CAP>();
   constexpr bool KL = reads_two<OP, DIR>();
   __shared__ S warp_part[kFwdWarps];
   __shared__ S cta_part[kMaxCluster];
