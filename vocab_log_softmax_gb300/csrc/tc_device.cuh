@@ -280,28 +280,10 @@ __device__ __forceinline__ uint64_t sdesc_sw128_mn(uint32_t addr) {
          (static_cast<uint64_t>(1024 >> 4) << 32) | (1ull << 46) | (2ull << 61);
 }
 
-// 32 consecutive fp32 columns of this thread's tensor-memory lane (warp-wide;
-// the warp reads its own 32-lane quarter).  The load and its wait sit in one
-// asm statement, so no use of the registers can be scheduled before the wait.
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
-  uint32_t r[32];
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
-      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
-      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];\n\t"
-      "tcgen05.wait::ld.sync.aligned;"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
-        "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
-        "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
-      : "r"(taddr)
-      : "memory");
-#pragma unroll
-  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
-}
-
-// The same load split in two, so one chunk can be in flight while the
-// previous one is used: tmem_ld32_issue starts the load, tmem_ld32_wait waits
+// 32 consecutive fp32 columns (as raw bits) of this thread's tensor-memory
+// lane, warp-wide: the warp reads its own 32-lane quarter.  The load is split
+// in two, so one chunk can be in flight while the previous one is used:
+// tmem_ld32_issue starts the load, tmem_ld32_wait waits
 // for every load this thread issued.  The wait names the registers as
 // operands it reads and writes, so no use of them moves above it.
 __device__ __forceinline__ void tmem_ld32_issue(uint32_t taddr, uint32_t (&r)[32]) {

@@ -3,19 +3,22 @@
 // A and B 16-bit, fp32 accumulation in tensor memory.  Each operand is either
 // K-major (stored [rows, K], K contiguous) or MN-major (stored [K, rows], its
 // M or N index contiguous), chosen per launch, so a product whose operand
-// sits transposed in memory needs no transpose.  The output tile is never stored by the mainloop: an epilogue
-// object receives it, 32 columns of one row per thread at a time, and does
-// what its operation needs (fold a softmax, form a gradient, store).
+// sits transposed in memory needs no transpose.  The output tile is never
+// stored by the mainloop: an epilogue object receives it, 32 columns of one
+// row per thread at a time, and does what its operation needs (fold a
+// softmax, form a gradient, store through TMA).
 //
-// Work is cut into units of (128 rows) x (a chunk of `chunk_tiles` column
-// tiles of 256), rows fastest, walked by a grid of at most one CTA per SM.
-// Roles (192 threads): warp 0 issues TMA loads of 64-wide K slices of A
-// (128 x 64) and B (256 x 64) into a 4-stage shared-memory ring (128-byte
-// swizzle); warp 1 owns 512 tensor-memory columns and one of its threads
-// issues 128x256x16 kind::f16 MMAs into one of two accumulators; warps 2-5
-// read a finished accumulator (one row per thread) and hand it to the
-// epilogue, then free it, so one tile's epilogue overlaps the next tile's
-// MMAs.  Every wait is bounded (tc_device.cuh).
+// Work is cut into units of (a row tile) x (a chunk of `chunk_tiles` column
+// tiles of 256) x (a run of K blocks, with split-K), walked by a persistent
+// grid.  Roles (192 threads): warp 0 issues TMA loads of 64-wide K slices of
+// A and B into a shared-memory ring (128-byte swizzle); warp 1 owns 512
+// tensor-memory columns and one of its threads issues kind::f16 MMAs into
+// one of two accumulators; warps 2-5 read a finished accumulator (one row
+// per thread) and hand it to the epilogue, then free it, so one tile's
+// epilogue overlaps the next tile's MMAs.  Two forms: 128-row tiles on one
+// SM (4 stages of 48 KB), and 256-row tiles on a CTA pair (cta_group::2, 6
+// stages of 32 KB per CTA), the default.  Every wait is bounded
+// (tc_device.cuh).
 #pragma once
 
 #include <atomic>
@@ -36,7 +39,6 @@ constexpr uint32_t kStageA = kBM * kBK * 2;   // 16 KB
 constexpr uint32_t kStageB = kBN * kBK * 2;   // 32 KB
 constexpr uint32_t kTmemCols = 2 * kBN;       // two fp32 accumulators of 256 columns
 constexpr int kNumBars = 2 * kStages + 4 + 1; // full, empty, acc_full x2, acc_empty x2, done
-constexpr size_t kSmem = 1024 /* alignment slack */ + kStages * (kStageA + kStageB) + kNumBars * 8 + 16;
 // epilogue staging (Epi::kStageBytes per epilogue warp) after the barriers, 1024-byte aligned
 constexpr size_t kEpiOff = (kStages * (kStageA + kStageB) + kNumBars * 8 + 16 + 1023) & ~size_t(1023);
 
@@ -366,7 +368,6 @@ constexpr int kStages2 = 6;
 constexpr uint32_t kStageA2 = kBM * kBK * 2;         // 16 KB: this CTA's 128 rows of A
 constexpr uint32_t kStageB2 = (kBN / 2) * kBK * 2;   // 16 KB: this CTA's 128 columns of B
 constexpr int kNumBars2 = 2 * kStages2 + 4 + 1;
-constexpr size_t kSmem2 = 1024 + kStages2 * (kStageA2 + kStageB2) + kNumBars2 * 8 + 16;
 constexpr size_t kEpiOff2 = (kStages2 * (kStageA2 + kStageB2) + kNumBars2 * 8 + 16 + 1023) & ~size_t(1023);
 
 template <bool BF16, bool A_MN, bool B_MN, class Epi>
