@@ -331,7 +331,10 @@ int64_t vls_linear_logp_bwd_workspace(int64_t N, int64_t D, int64_t V);
  * in fp32 and round once to dt at the store.  g: fp32 [N, k]; dh, dW:
  * contiguous, dtype dt.  workspace: at least
  * vls_linear_logp_bwd_workspace(N, D, V) bytes, 256-byte aligned, the
- * caller's; its contents on entry do not matter.  status as for
+ * caller's; its contents on entry do not matter.  When the rows are too few
+ * to fill the GPU, dh is summed in K runs (split-K) whose fp32 partial sums
+ * are kept in dW's memory before dW is computed; dh's rounding then depends
+ * on N and on the GPU's SM count, within the same fp32 bound.  status as for
  * vls_linear_logp_partial.  N, D and V are at most 2^31 - 512. */
 int vls_linear_logp_bwd(const void* h, int64_t ldh, const void* W, int64_t ldw, vls_dtype dt, int64_t N,
                         int64_t D, int64_t V, const int64_t* ids, int32_t k, int64_t ignore_index,
