@@ -328,12 +328,13 @@ cudaError_t bwd_t(const LinearBwdArgs& a, int sms, cudaStream_t s) {
     e = tcg::launch_gemm<BF16>(a.h, a.ldh, a.N, a.W, a.ldw, a.V, a.D, kLinChunkTiles, false, a.status, dze, sms, s);
   }
   if (e != cudaSuccess) return e;
-  // dh = dz W has K = V: at few rows its tiles alone leave most SMs idle.
-  // Then K is split into runs whose fp32 partial sums go to the dW buffer
-  // (written only by the last product, and large enough: runs x N x 4 bytes
-  // per column against V x 2), and a fixed-order sum of the runs gives dh.
-  const int runs = tcg::fill_ksplit(a.N, a.D, a.V, sms, 16);
-  const bool split = runs > 1 && int64_t(runs) * a.N * 2 <= a.V && (a.D % 4) == 0 &&
+  // dh = dz W has K = V: at few rows its tiles leave SMs idle, and at some
+  // row counts their last wave runs part full.  Then K is split into runs
+  // (tcg::fill_ksplit) whose fp32 partial sums go to the dW buffer (written
+  // only by the last product, and large enough: runs x N x 4 bytes per
+  // column against V x 2), and a fixed-order sum of the runs gives dh.
+  const int runs = (a.D % 4) == 0 ? tcg::fill_ksplit(a.N, a.D, a.V, sms, 16, a.V / (2 * a.N)) : 1;
+  const bool split = runs > 1 && int64_t(runs) * a.N * 2 <= a.V &&
                      (reinterpret_cast<uintptr_t>(a.dW) & 15u) == 0 && (reinterpret_cast<uintptr_t>(a.dh) & 7u) == 0;
   if (split) {
     float* P = static_cast<float*>(a.dW);
