@@ -190,6 +190,18 @@ def test_backward(n, d, v, k, dtype):
     _check_bwd(h, w, ids, gr, f"linear bwd N={n} D={d} V={v} k={k}")
 
 
+def test_backward_many_k_runs():
+    """Few rows over a long vocabulary: dh is summed in dozens of K runs
+    (32 here) whose partial sums sit in dW's memory before dW is written."""
+    n, d, v = 64, 512, 32768
+    g = _gen(71)
+    h = torch.randn((n, d), generator=g, device=DEV).to(torch.bfloat16)
+    w = (3.0 / d ** 0.5 * torch.randn((v, d), generator=g, device=DEV)).to(torch.bfloat16)
+    ids = _ids(n, v, 2, 72, 0.1)
+    gr = torch.randn((n, 2), generator=g, device=DEV)
+    _check_bwd(h, w, ids, gr, "linear bwd, many K runs")
+
+
 def test_backward_ignored_rows_give_zero_dh():
     n, d, v = 200, 128, 3000
     g = _gen(41)
