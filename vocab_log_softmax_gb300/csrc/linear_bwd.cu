@@ -52,12 +52,6 @@ __device__ __forceinline__ uint32_t pack2<__half>(float lo, float hi) {
   return *reinterpret_cast<const uint32_t*>(&r);
 }
 
-// one half of a packed pair to 16-bit memory
-template <class T>
-__device__ __forceinline__ void st_half(T* p, uint32_t w, int hi) {
-  *reinterpret_cast<uint16_t*>(p) = static_cast<uint16_t>(hi ? w >> 16 : w);
-}
-
 // 32 values of one row to 16-bit memory: four 16-byte stores when the run is
 // whole and aligned, else element by element.
 template <class T>
@@ -205,20 +199,19 @@ __global__ void __launch_bounds__(256) splitk_reduce_kernel(const float* __restr
   }
 }
 
-// Epilogue of the dz map: the logits tile becomes g one-hot - G p.
-template <class T, bool TMA>
+// Epilogue of the dz map: the logits tile becomes g one-hot - G p, stored
+// to dz through TMA boxes (store_box).
+template <class T>
 struct DzEpi {
-  static constexpr uint32_t kStageBytes = TMA ? kBoxStageBytes : 0;
+  static constexpr uint32_t kStageBytes = kBoxStageBytes;
   const int64_t* ids;
   int32_t k;
   int64_t ignore_index;
   int64_t V;
   const float* g;            // [N, k]
   const vls_rowstat* stats;  // [N]
-  T* dz;                     // [N, ld_dz]
-  int64_t ld_dz;
   int64_t N;
-  CUtensorMap map;           // dz for TMA stores (TMA only): tcg::encode_store
+  CUtensorMap map;           // dz [N, ld_dz]: tcg::encode_store
 
   struct State {
     float m, c, G;             // max, log S * log2(e), sum of the valid upstream gradients
@@ -249,9 +242,9 @@ struct DzEpi {
 
   __device__ void cols(State& st, const float (&v)[32], int64_t row, bool row_ok, int64_t cbase, int nvalid,
                        tcg::EpiWarp& ew) const {
-    // with TMA stores every lane takes part: a row past N holds zeros (its
-    // state is 0 and its logits the zero fill) and the store clips it
-    if (nvalid == 0 || (!TMA && !row_ok)) return;
+    // every lane takes part: a row past N holds zeros (its state is 0 and
+    // its logits the zero fill) and the store clips it
+    if (nvalid == 0) return;
     float oh[32];
 #pragma unroll
     for (int i = 0; i < 32; ++i) oh[i] = 0.0f;
@@ -275,26 +268,11 @@ struct DzEpi {
       dev::upk(dev::fma2(g2, p, dev::pk(oh[2 * i], oh[2 * i + 1])), d0, d1);
       w[i] = pack2<T>(d0, d1);
     }
-    if constexpr (TMA) {
-      if (ew.row0 < N) store_box(&map, ew, w, cbase);   // the same in every lane
-    } else {
-      T* dst = dz + row * ld_dz + cbase;
-      if (nvalid == 32 && dev::aligned16(dst)) {
-#pragma unroll
-        for (int q = 0; q < 4; ++q)
-          dev::st16(dst + 8 * q, make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]));
-      } else {
-#pragma unroll
-        for (int i = 0; i < 32; ++i)
-          if (i < nvalid) st_half(dst + i, w[i >> 1], i & 1);
-      }
-    }
+    if (ew.row0 < N) store_box(&map, ew, w, cbase);   // the same in every lane
   }
 
   __device__ void end(State&, int64_t, bool, int) const {}
-  __device__ void finish(tcg::EpiWarp& ew) const {
-    if constexpr (TMA) finish_boxes(ew);
-  }
+  __device__ void finish(tcg::EpiWarp& ew) const { finish_boxes(ew); }
 };
 
 // the workspace: dz [N, pad8(V)] in the operand dtype
@@ -306,28 +284,20 @@ cudaError_t bwd_t(const LinearBwdArgs& a, int sms, cudaStream_t s) {
   T* dz = static_cast<T*>(a.workspace);
   const int64_t ldv = pad8(a.V);
   cudaError_t e;
-  // the dz map: dz through TMA stores (the workspace always allows them)
-  auto dz_epi = [&](auto& ep) {
-    ep.ids = a.ids;
-    ep.k = a.k;
-    ep.ignore_index = a.ignore_index;
-    ep.V = a.V;
-    ep.g = a.g;
-    ep.stats = a.stats;
-    ep.dz = dz;
-    ep.ld_dz = ldv;
-    ep.N = a.N;
-  };
-  DzEpi<T, true> dzt;
-  dz_epi(dzt);
-  if (tcg::encode_store(&dzt.map, dz, BF16, a.N, a.V, ldv)) {
-    e = tcg::launch_gemm<BF16>(a.h, a.ldh, a.N, a.W, a.ldw, a.V, a.D, kLinChunkTiles, false, a.status, dzt, sms, s);
-  } else {
-    DzEpi<T, false> dze;
-    dz_epi(dze);
-    e = tcg::launch_gemm<BF16>(a.h, a.ldh, a.N, a.W, a.ldw, a.V, a.D, kLinChunkTiles, false, a.status, dze, sms, s);
-  }
-  if (e != cudaSuccess) return e;
+  // the dz map, dz through TMA stores (the workspace is 256-byte aligned and
+  // its rows are padded to 16-byte multiples, so the map always encodes)
+  DzEpi<T> dze;
+  dze.ids = a.ids;
+  dze.k = a.k;
+  dze.ignore_index = a.ignore_index;
+  dze.V = a.V;
+  dze.g = a.g;
+  dze.stats = a.stats;
+  dze.N = a.N;
+  if (!tcg::encode_store(&dze.map, dz, BF16, a.N, a.V, ldv)) return cudaErrorInvalidValue;
+  if ((e = tcg::launch_gemm<BF16>(a.h, a.ldh, a.N, a.W, a.ldw, a.V, a.D, kLinChunkTiles, false, a.status, dze, sms, s)) !=
+      cudaSuccess)
+    return e;
   // dh = dz W has K = V: at few rows its tiles leave SMs idle, and at some
   // row counts their last wave runs part full.  Then K is split into runs
   // (tcg::fill_ksplit) whose fp32 partial sums go to the dW buffer (written
