@@ -43,6 +43,21 @@ def test_vocab_sizes(v, dtype):
     check_logp(a, ids, gk, cap=5.0, what=f"V={v} logp cap")
 
 
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16], ids=["f32", "bf16"])
+@pytest.mark.parametrize("v", [262144, 600001, 2000003])
+def test_cluster_rows(v, dtype):
+    """Rows wider than one CTA's share of 24576 vectors: the forward sweep runs
+    on a cluster of 2, 4 and 8 CTAs (the last with more than 24576 vectors
+    each), whose states combine through distributed shared memory in rank
+    order; the backward cuts the row into many pieces."""
+    a, b, ids, gk, gr = _data(2, v, dtype, seed=v % 1009)
+    check_logp(a, ids, gk, what=f"V={v} logp")
+    check_entropy(a, gr, what=f"V={v} entropy")
+    for d in ("reverse", "forward"):
+        check_kl(a, b, gr, d, what=f"V={v} kl {d}")
+    check_logp(a, ids, gk, cap=20.0, what=f"V={v} logp cap")
+
+
 @pytest.mark.parametrize("dtype", DTYPES)
 @pytest.mark.parametrize("v,pad,shift", [(1031, 3, 0), (1031, 5, 1), (4096, 1, 1), (37, 11, 3), (151936, 8, 1)])
 def test_strided_and_misaligned_rows(v, pad, shift, dtype):
