@@ -279,13 +279,22 @@ __device__ __forceinline__ float fused_at(const T* xr, const T* yr, int64_t c, c
 
 // Six resident CTAs per SM (at most 40 registers a thread) keep enough
 // loads in flight; with a larger register budget occupancy halves and the
-// sweep slows down.  The softcapped map runs a software pipeline and gets
-// kCapMinBlocks CTAs per SM.
+// sweep slows down.  The 16-bit softcapped logprob map keeps six too: its
+// software pipeline spills a little at 40 registers, and is still 3% faster
+// than at 5 CTAs and 48 registers (and 8% faster than at 32).  The other
+// softcapped maps and the top-k map get kCapMinBlocks CTAs per SM.
 // TOPK (logprob map with k > 1): the one-hot columns are written inline by
 // the thread that stores their vector (onehot_vector) instead of by a
 // post-pass that re-reads them after a barrier.
+template <class T, int OP, bool CAP, bool TOPK>
+constexpr int bwd_min_blocks() {
+  if (TOPK) return kCapMinBlocks;
+  if (!CAP) return 6;
+  return (OP == kBwdLogp && sizeof(T) == 2) ? 6 : kCapMinBlocks;
+}
+
 template <class T, int OP, bool CAP, int DIR = kFusedNoKl, bool TOPK = false>
-__global__ void __launch_bounds__(kRowThreads, (CAP || TOPK) ? kCapMinBlocks : 6) row_bwd_kernel(const BwdArgs a) {
+__global__ void __launch_bounds__(kRowThreads, (bwd_min_blocks<T, OP, CAP, TOPK>())) row_bwd_kernel(const BwdArgs a) {
   constexpr bool KL = bwd_reads_two<OP, DIR>();
   const int64_t row = blockIdx.x / a.chunks;
   const int q = static_cast<int>(blockIdx.x - row * a.chunks);
