@@ -491,8 +491,10 @@ __global__ void __launch_bounds__(kRowThreads, (bwd_min_blocks<T, OP, CAP, TOPK>
       }
     }
   } else {
-    // light arithmetic: plain batches of U loads in flight per thread
-    constexpr int U = KL ? 2 : 4;
+    // light arithmetic: plain batches of U vectors in flight per thread; the
+    // 16-bit KL maps take 3 of each tensor (1-3% faster than 2 at the same 40
+    // registers), the fused and fp32 two-tensor maps 2 (3 spills there)
+    constexpr int U = KL ? (((OP == kBwdKlReverse || OP == kBwdKlForward) && sizeof(T) == 2) ? 3 : 2) : 4;
     if (al) {
       for (; v + (U - 1) * kRowThreads < vfull_end; v += U * kRowThreads) {
         Raw8<T> x[U], y[U];
