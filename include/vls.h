@@ -329,7 +329,9 @@ int64_t vls_linear_logp_bwd_workspace(int64_t N, int64_t D, int64_t V);
  * with the logits recomputed on the tensor cores from h and W.  dz is formed
  * in fp32 and rounded once to dt before the two products, which accumulate
  * in fp32 and round once to dt at the store.  g: fp32 [N, k]; dh, dW:
- * contiguous, dtype dt.  workspace: at least
+ * contiguous, dtype dt, overlapping neither each other, the inputs nor the
+ * workspace (rows that are 16-byte multiples on 16-byte aligned bases are
+ * stored through TMA, others by the threads).  workspace: at least
  * vls_linear_logp_bwd_workspace(N, D, V) bytes, 256-byte aligned, the
  * caller's; its contents on entry do not matter.  When the rows are too few
  * to fill the GPU, dh is summed in K runs (split-K) whose fp32 partial sums
