@@ -16,7 +16,6 @@ from .vocab_stats import (  # noqa: F401
     linear_logp_fwd,
     logp_bwd,
     logp_fwd,
-    round_to_bf16_bits,
     row_log_softmax,
     row_stats,
     softcap,

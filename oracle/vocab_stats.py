@@ -53,7 +53,10 @@ Readings where the pages are silent (each also listed in the design notes):
   ``z = h @ W^T`` (h: [N, D] hidden states, W: [V, D] head weights), with
   the gradient flowing to both h and W.
 
-Parity pins for every function here live in ``tests/test_oracle.py``.
+Parity pins for every function here are the checks in ``tests/oracle_pins.py``
+(closed forms, library routines, invariants, finite differences), run by
+``tests/test_oracle.py``; ``tests/test_oracle_mutations.py`` plants mistakes in
+a copy of this module and checks that a pin catches each.
 """
 
 from __future__ import annotations
@@ -76,20 +79,6 @@ def decode_bf16_bits(bits: np.ndarray) -> np.ndarray:
     u16 = np.asarray(bits).view(np.uint16).astype(np.uint32)
     with np.errstate(invalid="ignore"):
         return (u16 << np.uint32(16)).view(np.float32).astype(np.float64)
-
-
-def round_to_bf16_bits(x: np.ndarray) -> np.ndarray:
-    """float64 -> bfloat16 bit patterns, round to nearest even (via float32).
-
-    Used only by the oracle's own tests to build inputs; the double rounding
-    (fp64 -> fp32 -> bf16) is immaterial there.
-    """
-    f = np.asarray(x, dtype=np.float32).view(np.uint32).astype(np.uint64)
-    lsb = (f >> np.uint64(16)) & np.uint64(1)
-    is_nan = np.isnan(np.asarray(x, dtype=np.float32))
-    r = ((f + np.uint64(0x7FFF) + lsb) >> np.uint64(16)).astype(np.uint16)
-    r[is_nan] = np.uint16(0x7FC0)
-    return r
 
 
 # ----------------------------------------------------------------------------
