@@ -44,34 +44,31 @@ template <class T, bool CAP>
 struct LogpAcc {
   using State = LogpState;
   float m_raw = neg_inf(), m = neg_inf();
+  // nm2: -m, or with a cap b2 = (c - m) log2(e) (cap_d2_pair)
   fp2 nm2 = 0, s2 = 0;
 
   template <bool PARTIAL>
   __device__ __forceinline__ void update(const Raw8<T>& v, const Raw8<T>&, int valid, const CapK& K) {
     const float vm = v.max();
     if (grows<CAP>(vm, m_raw, m)) {
-      const float mn = CAP ? cap_z(vm, K) : vm;
+      const float mn = CAP ? cap_zr(vm, K) : vm;
       s2 = mul2(s2, splat(rescale(m, mn)));
       m_raw = vm;
       m = mn;
-      nm2 = splat(-mn);
+      nm2 = splat(CAP ? cap_b2(mn, K) : -mn);
     }
     if (!CAP && m == neg_inf()) return;
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-      fp2 d;
-      if (CAP) {
-        fp2 e2, r2;
-        d = fma2((i & 1) ? cap_t2<T, true>(v, i, K, e2, r2) : cap_t2<T, false>(v, i, K, e2, r2), splat(K.c), nm2);
-      } else {
-        d = add2(v.pair(i), nm2);
-      }
-      s2 = add2(s2, keep<PARTIAL>(ex2_2(mul2(d, splat(kLog2e))), i, valid));
+      const fp2 d2 = CAP ? cap_d2_pair<T>(v, i, K, nm2) : mul2(add2(v.pair(i), nm2), splat(kLog2e));
+      s2 = add2(s2, keep<PARTIAL>(ex2_2(d2), i, valid));
     }
   }
   __device__ State state() const { return {m, sum2(s2)}; }
 };
 
+// With a cap, W is accumulated in log2 units (the weights' exponents come out
+// of cap_d2_pair that way) and turned into natural units once, in state().
 template <class T, bool CAP>
 struct EntropyAcc {
   using State = EntropyState;
@@ -82,33 +79,35 @@ struct EntropyAcc {
   __device__ __forceinline__ void update(const Raw8<T>& v, const Raw8<T>&, int valid, const CapK& K) {
     const float vm = v.max();
     if (grows<CAP>(vm, m_raw, m)) {
-      const float mn = CAP ? cap_z(vm, K) : vm;
+      const float mn = CAP ? cap_zr(vm, K) : vm;
       const float f = rescale(m, mn);
-      w2 = m != neg_inf() ? mul2(fma2(s2, splat(m - mn), w2), splat(f)) : 0;
+      const float shift = CAP ? (m - mn) * kLog2e : m - mn;
+      w2 = m != neg_inf() ? mul2(fma2(s2, splat(shift), w2), splat(f)) : 0;
       s2 = mul2(s2, splat(f));
       m_raw = vm;
       m = mn;
-      nm2 = splat(-mn);
+      nm2 = splat(CAP ? cap_b2(mn, K) : -mn);
     }
     if (!CAP && m == neg_inf()) return;
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-      fp2 d;
+      fp2 d, e;
       if (CAP) {
-        fp2 e2, r2;
-        d = fma2((i & 1) ? cap_t2<T, true>(v, i, K, e2, r2) : cap_t2<T, false>(v, i, K, e2, r2), splat(K.c), nm2);
+        d = cap_d2_pair<T>(v, i, K, nm2);
+        e = keep<PARTIAL>(ex2_2(d), i, valid);
       } else {
         d = add2(v.pair_clamped(i), nm2);  // -inf columns: e = 0 and 0 * d = 0
+        e = keep<PARTIAL>(ex2_2(mul2(d, splat(kLog2e))), i, valid);
       }
-      const fp2 e = keep<PARTIAL>(ex2_2(mul2(d, splat(kLog2e))), i, valid);
       s2 = add2(s2, e);
       w2 = fma2(e, d, w2);
     }
   }
-  __device__ State state() const { return {m, sum2(s2), sum2(w2)}; }
+  __device__ State state() const { return {m, sum2(s2), CAP ? sum2(w2) * kLn2 : sum2(w2)}; }
 };
 
 // KL(P||Q): `v` is a vector of P (first argument), `q` the same columns of Q.
+// With a cap, W is accumulated in log2 units as in EntropyAcc.
 template <class T, bool CAP>
 struct KlAcc {
   using State = KlState;
@@ -121,14 +120,15 @@ struct KlAcc {
     const float vmp = v.max(), vmq = q.max();
     const bool up = grows<CAP>(vmp, mp_raw, mp), uq = grows<CAP>(vmq, mq_raw, mq);
     if (up || uq) {
-      const float Mp = up ? (CAP ? cap_z(vmp, K) : vmp) : mp;
-      const float Mq = uq ? (CAP ? cap_z(vmq, K) : vmq) : mq;
+      const float Mp = up ? (CAP ? cap_zr(vmp, K) : vmp) : mp;
+      const float Mq = uq ? (CAP ? cap_zr(vmq, K) : vmq) : mq;
       const float fp = rescale(mp, Mp), fq = rescale(mq, Mq);
-      w2 = mp != neg_inf() ? mul2(fma2(sp2, splat((mp - Mp) - (mq - Mq)), w2), splat(fp)) : 0;
+      const float shift = CAP ? ((mp - Mp) - (mq - Mq)) * kLog2e : (mp - Mp) - (mq - Mq);
+      w2 = mp != neg_inf() ? mul2(fma2(sp2, splat(shift), w2), splat(fp)) : 0;
       sp2 = mul2(sp2, splat(fp));
       sq2 = mul2(sq2, splat(fq));
-      if (up) { mp_raw = vmp; mp = Mp; nmp2 = splat(-Mp); }
-      if (uq) { mq_raw = vmq; mq = Mq; nmq2 = splat(-Mq); }
+      if (up) { mp_raw = vmp; mp = Mp; nmp2 = splat(CAP ? cap_b2(Mp, K) : -Mp); }
+      if (uq) { mq_raw = vmq; mq = Mq; nmq2 = splat(CAP ? cap_b2(Mq, K) : -Mq); }
     }
     if (!CAP) {
 #pragma unroll
@@ -138,24 +138,26 @@ struct KlAcc {
     if (p_ok && q_ok) {
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
-        fp2 dp, dq;
+        fp2 dp, dq, ep, eq;
         if (CAP) {
-          fp2 e2, r2;
-          dp = fma2((i & 1) ? cap_t2<T, true>(v, i, K, e2, r2) : cap_t2<T, false>(v, i, K, e2, r2), splat(K.c), nmp2);
-          dq = fma2((i & 1) ? cap_t2<T, true>(q, i, K, e2, r2) : cap_t2<T, false>(q, i, K, e2, r2), splat(K.c), nmq2);
+          dp = cap_d2_pair<T>(v, i, K, nmp2);
+          dq = cap_d2_pair<T>(q, i, K, nmq2);
+          ep = keep<PARTIAL>(ex2_2(dp), i, valid);
+          eq = keep<PARTIAL>(ex2_2(dq), i, valid);
         } else {
           dp = add2(v.pair_clamped(i), nmp2);
           dq = add2(q.pair_clamped(i), nmq2);
+          ep = keep<PARTIAL>(ex2_2(mul2(dp, splat(kLog2e))), i, valid);
+          eq = keep<PARTIAL>(ex2_2(mul2(dq, splat(kLog2e))), i, valid);
         }
-        const fp2 ep = keep<PARTIAL>(ex2_2(mul2(dp, splat(kLog2e))), i, valid);
-        const fp2 eq = keep<PARTIAL>(ex2_2(mul2(dq, splat(kLog2e))), i, valid);
         sp2 = add2(sp2, ep);
         sq2 = add2(sq2, eq);
         w2 = fma2(ep, sub2(dp, dq), w2);
       }
     } else if (p_ok || q_ok) {
       // one side has seen only -inf so far (no W term: a finite P column
-      // against an all -inf Q run is a mismatch, already flagged)
+      // against an all -inf Q run is a mismatch, already flagged); never
+      // with a cap, where no logit stays -inf
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         if (p_ok) sp2 = add2(sp2, keep<PARTIAL>(ex2_2(mul2(add2(v.pair_clamped(i), nmp2), splat(kLog2e))), i, valid));
@@ -163,7 +165,7 @@ struct KlAcc {
       }
     }
   }
-  __device__ State state() const { return {mp, sum2(sp2), mq, sum2(sq2), sum2(w2), flag}; }
+  __device__ State state() const { return {mp, sum2(sp2), mq, sum2(sq2), CAP ? sum2(w2) * kLn2 : sum2(w2), flag}; }
 };
 
 // Fused sweep over the policy a (`v`) and, with a KL term, the reference b
@@ -188,18 +190,19 @@ struct FusedAcc {
       ub = grows<CAP>(vmb, mb_raw, mb);
     }
     if (ua || ub) {
-      const float Ma = ua ? (CAP ? cap_z(vma, K) : vma) : ma;
-      const float Mb = ub ? (CAP ? cap_z(vmb, K) : vmb) : mb;
+      const float Ma = ua ? (CAP ? cap_zr(vma, K) : vma) : ma;
+      const float Mb = ub ? (CAP ? cap_zr(vmb, K) : vmb) : mb;
       const float fa = rescale(ma, Ma), fb = rescale(mb, Mb);
-      wh2 = ma != neg_inf() ? mul2(fma2(sa2, splat(ma - Ma), wh2), splat(fa)) : 0;
+      const float u = CAP ? kLog2e : 1.0f;   // units of W: log2 with a cap
+      wh2 = ma != neg_inf() ? mul2(fma2(sa2, splat(CAP ? (ma - Ma) * kLog2e : ma - Ma), wh2), splat(fa)) : 0;
       if constexpr (DIR == kFusedKlReverse)
-        wk2 = ma != neg_inf() ? mul2(fma2(sa2, splat((ma - Ma) - (mb - Mb)), wk2), splat(fa)) : 0;
+        wk2 = ma != neg_inf() ? mul2(fma2(sa2, splat(((ma - Ma) - (mb - Mb)) * u), wk2), splat(fa)) : 0;
       if constexpr (DIR == kFusedKlForward)
-        wk2 = mb != neg_inf() ? mul2(fma2(sb2, splat((mb - Mb) - (ma - Ma)), wk2), splat(fb)) : 0;
+        wk2 = mb != neg_inf() ? mul2(fma2(sb2, splat(((mb - Mb) - (ma - Ma)) * u), wk2), splat(fb)) : 0;
       sa2 = mul2(sa2, splat(fa));
       sb2 = mul2(sb2, splat(fb));
-      if (ua) { ma_raw = vma; ma = Ma; nma2 = splat(-Ma); }
-      if (ub) { mb_raw = vmb; mb = Mb; nmb2 = splat(-Mb); }
+      if (ua) { ma_raw = vma; ma = Ma; nma2 = splat(CAP ? cap_b2(Ma, K) : -Ma); }
+      if (ub) { mb_raw = vmb; mb = Mb; nmb2 = splat(CAP ? cap_b2(Mb, K) : -Mb); }
     }
     if constexpr (kHasB && !CAP) {
 #pragma unroll
@@ -209,21 +212,25 @@ struct FusedAcc {
     if (a_ok && (!kHasB || b_ok)) {
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
-        fp2 da, db = 0;
+        fp2 da, db = 0, ea, eb = 0;
         if (CAP) {
-          fp2 e2, r2;
-          da = fma2((i & 1) ? cap_t2<T, true>(v, i, K, e2, r2) : cap_t2<T, false>(v, i, K, e2, r2), splat(K.c), nma2);
-          if constexpr (kHasB)
-            db = fma2((i & 1) ? cap_t2<T, true>(q, i, K, e2, r2) : cap_t2<T, false>(q, i, K, e2, r2), splat(K.c), nmb2);
+          da = cap_d2_pair<T>(v, i, K, nma2);
+          ea = keep<PARTIAL>(ex2_2(da), i, valid);
+          if constexpr (kHasB) {
+            db = cap_d2_pair<T>(q, i, K, nmb2);
+            eb = keep<PARTIAL>(ex2_2(db), i, valid);
+          }
         } else {
           da = add2(v.pair_clamped(i), nma2);
-          if constexpr (kHasB) db = add2(q.pair_clamped(i), nmb2);
+          ea = keep<PARTIAL>(ex2_2(mul2(da, splat(kLog2e))), i, valid);
+          if constexpr (kHasB) {
+            db = add2(q.pair_clamped(i), nmb2);
+            eb = keep<PARTIAL>(ex2_2(mul2(db, splat(kLog2e))), i, valid);
+          }
         }
-        const fp2 ea = keep<PARTIAL>(ex2_2(mul2(da, splat(kLog2e))), i, valid);
         sa2 = add2(sa2, ea);
         wh2 = fma2(ea, da, wh2);
         if constexpr (kHasB) {
-          const fp2 eb = keep<PARTIAL>(ex2_2(mul2(db, splat(kLog2e))), i, valid);
           sb2 = add2(sb2, eb);
           if constexpr (DIR == kFusedKlReverse) wk2 = fma2(ea, sub2(da, db), wk2);
           else wk2 = fma2(eb, sub2(db, da), wk2);
@@ -231,7 +238,8 @@ struct FusedAcc {
       }
     } else if (a_ok || b_ok) {
       // one side has seen only -inf so far: no cross term (a finite column
-      // of the KL's first argument against an all -inf run is flagged)
+      // of the KL's first argument against an all -inf run is flagged);
+      // never with a cap
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         if (a_ok) {
@@ -244,7 +252,10 @@ struct FusedAcc {
       }
     }
   }
-  __device__ State state() const { return {ma, sum2(sa2), sum2(wh2), mb, sum2(sb2), sum2(wk2), flag}; }
+  __device__ State state() const {
+    const float u = CAP ? kLn2 : 1.0f;
+    return {ma, sum2(sa2), sum2(wh2) * u, mb, sum2(sb2), sum2(wk2) * u, flag};
+  }
 };
 
 template <int OP, class T, bool CAP, int DIR>
@@ -267,7 +278,13 @@ constexpr bool reads_two() { return OP == kFwdKl || (OP == kFwdFused && DIR != k
 // sweep, bound by its arithmetic's latency rather than by memory, takes 6
 // (measured: 3.7% faster than 4 at 6 resident CTAs; 8 spills).
 template <int OP, int DIR, bool CAP>
-constexpr int fwd_unroll() { return reads_two<OP, DIR>() ? 2 : ((CAP && OP == kFwdLogp) ? 6 : 4); }
+#ifndef VLS_CAP_LOGP_UNROLL
+#define VLS_CAP_LOGP_UNROLL 6
+#endif
+#ifndef VLS_CAP_LOGP_CTAS
+#define VLS_CAP_LOGP_CTAS 5
+#endif
+constexpr int fwd_unroll() { return reads_two<OP, DIR>() ? 2 : ((CAP && OP == kFwdLogp) ? VLS_CAP_LOGP_UNROLL : 4); }
 
 // Resident CTAs per SM the forward sweep is compiled for, at 256 threads.
 // Without an explicit minimum, ptxas sized these kernels by heuristics that
@@ -282,7 +299,7 @@ constexpr int fwd_ctas_at_256() {
   if (sizeof(T) == 4) return 4;
   if (reads_two<OP, DIR>())
     return (CAP || OP == kFwdFused || !std::is_same<T, __nv_bfloat16>::value) ? 4 : 5;
-  if (CAP) return 5;
+  if (CAP) return OP == kFwdLogp ? VLS_CAP_LOGP_CTAS : 5;
   return (OP == kFwdFused || std::is_same<T, __half>::value) ? 6 : 8;
 }
 template <class T, int OP, bool CAP, int DIR>
@@ -295,9 +312,11 @@ constexpr int fwd_min_blocks() {
 
 // log p of a target from its raw logit x and the row's (m, log S); NaN for
 // a row without a distribution.
+// With a cap, z - m takes the sweeps' own form (cap_d2 times ln 2), so that
+// the target's offset and the weights summed into S share their rounding.
 template <bool CAP>
 __device__ __forceinline__ float logp_of(float x, float m, float log_s, const CapK& K) {
-  const float d = CAP ? cap_d(cap_t(x, K), K.c, m) : x - m;
+  const float d = CAP ? cap_d2(x, K, cap_b2(m, K)) * kLn2 : x - m;
   return m == neg_inf() ? qnan() : d - log_s;
 }
 // H = log S - W/S

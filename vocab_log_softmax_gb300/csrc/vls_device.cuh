@@ -319,9 +319,13 @@ __device__ __forceinline__ void load_raw(Raw8<T>& r, const T* row, int64_t vec, 
 struct CapK {
   float c;     // cap
   float k;     // -2 log2(e) / c: exp(-2|x|/c) = 2^(|x| k)
+  float k2;    // 2 log2(e) / c: exp(2x/c) = 2^(x k2)
+  float a2;    // -2 c log2(e)
 };
 
-__device__ __forceinline__ CapK cap_consts(float cap) { return {cap, -2.0f * kLog2e / cap}; }
+__device__ __forceinline__ CapK cap_consts(float cap) {
+  return {cap, -2.0f * kLog2e / cap, 2.0f * kLog2e / cap, -2.0f * cap * kLog2e};
+}
 
 // tanh(x/c) and e = exp(-2|x|/c), r = 1/(1+e) for the slope.
 __device__ __forceinline__ float cap_t(float x, const CapK& K, float& e, float& r) {
@@ -365,6 +369,72 @@ __device__ __forceinline__ fp2 cap_t2(const Raw8<T>& v, int i, const CapK& K, fp
 
 // z - m for the softcapped logit: c t - m, one rounding.
 __device__ __forceinline__ float cap_d(float t, float c, float m) { return fmaf(t, c, -m); }
+
+// --------------------------------------------------------------------------
+// The softcapped logit inside the forward sweeps, where only the softmax
+// weights exp(z - m) and the target's z - m depend on it.  With
+//   z = c tanh(x/c) = c - 2c r,   r = 1/(1 + E),   E = exp(2x/c) = 2^(x k2),
+// the log2 weight is one FMA after the two special-function operations:
+//   (z - m) log2(e) = a2 r + b2,   a2 = -2c log2(e),   b2 = (c - m) log2(e).
+// The sign of x needs no handling: x = -inf gives E = 0 and r = 1 (z = -c),
+// a large x gives E = +inf and r = 0 (z = c).  The absolute error of z is
+// 2c r times the relative error of r, a few 1e-7 c, the same order as
+// cap_t's; unlike cap_t it is not small relative to z near x = 0, which the
+// standalone softcap output needs but a softmax weight does not.
+// --------------------------------------------------------------------------
+constexpr float kLn2 = 0.69314718055994531f;
+
+// Pairs (of the four in an 8-column vector) whose reciprocal 1/(1 + E) runs
+// on the FMA pipe (rcp2_fma_wide) instead of the special-function unit,
+// which bounds the softcapped sweeps: bit i set for pair i.  A function of
+// the column alone, so every sweep gets the same bits for the same column.
+#ifndef VLS_CAP_FMA_PAIRS
+#define VLS_CAP_FMA_PAIRS 0xA
+#endif
+constexpr uint32_t kCapFmaPairs = VLS_CAP_FMA_PAIRS;
+
+// 1/d for d >= 1 (or +inf) on the FMA pipe: d = 2^e f with f in [1, 2) taken
+// from the exponent field, 1/f from rcp2_fma's quadratic seed and two
+// Newton-Raphson steps (written in -f), and 2^-e put back by subtracting e
+// from the result's exponent field.  d is first limited to 2^64 by an
+// integer min on the bit pattern (which orders positive floats), so that
+// field never underflows; a reciprocal below 2^-64 then reads as 2^-64,
+// which only ever adds a term far below one ulp of c.
+__device__ __forceinline__ fp2 rcp2_fma_wide(fp2 d) {
+  float d0, d1;
+  upk(d, d0, d1);
+  const uint32_t b0 = min(__float_as_uint(d0), 0x5f800000u), b1 = min(__float_as_uint(d1), 0x5f800000u);
+  const fp2 nf = pk(__uint_as_float((b0 & 0x007fffffu) | 0xbf800000u), __uint_as_float((b1 & 0x007fffffu) | 0xbf800000u));
+  fp2 r = fma2(fma2(nf, splat(32.0f / 99.0f), splat(48.0f / 33.0f)), nf, splat(70.0f / 33.0f));
+  r = fma2(r, fma2(nf, r, splat(1.0f)), r);
+  r = fma2(r, fma2(nf, r, splat(1.0f)), r);
+  float r0, r1;
+  upk(r, r0, r1);
+  r0 = __uint_as_float(__float_as_uint(r0) - (b0 & 0x7f800000u) + 0x3f800000u);
+  r1 = __uint_as_float(__float_as_uint(r1) - (b1 & 0x7f800000u) + 0x3f800000u);
+  return pk(r0, r1);
+}
+
+// r = 1/(1 + exp(2x/c)) of one logit.
+__device__ __forceinline__ float cap_r(float x, const CapK& K) { return rcp(1.0f + ex2(x * K.k2)); }
+// The softcapped value c - 2c r of one logit (the row max of a sweep).
+__device__ __forceinline__ float cap_zr(float x, const CapK& K) { return fmaf(cap_r(x, K), -2.0f * K.c, K.c); }
+// b2 = (c - m) log2(e) for the running max m.
+__device__ __forceinline__ float cap_b2(float m, const CapK& K) { return (K.c - m) * kLog2e; }
+// (z - m) log2(e) of one logit, given b2 of m.
+__device__ __forceinline__ float cap_d2(float x, const CapK& K, float b2) { return fmaf(cap_r(x, K), K.a2, b2); }
+
+// (z - m) log2(e) for pair i of a raw vector, given b2 of m in both halves.
+template <class T, bool FMA_RCP>
+__device__ __forceinline__ fp2 cap_d2_pair(const Raw8<T>& v, int i, const CapK& K, fp2 b2) {
+  const fp2 den = add2(ex2_2(mul2(v.pair(i), splat(K.k2))), splat(1.0f));
+  const fp2 r = FMA_RCP ? rcp2_fma_wide(den) : rcp2(den);
+  return fma2(r, splat(K.a2), b2);
+}
+template <class T>
+__device__ __forceinline__ fp2 cap_d2_pair(const Raw8<T>& v, int i, const CapK& K, fp2 b2) {
+  return ((kCapFmaPairs >> i) & 1u) ? cap_d2_pair<T, true>(v, i, K, b2) : cap_d2_pair<T, false>(v, i, K, b2);
+}
 
 // The softcapped value of the row max (tanh is increasing, so the max of z
 // is the cap of the max of x).
