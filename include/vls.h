@@ -96,8 +96,10 @@ enum {
                            sit on different devices                               */
   VLS_ERR_LAUNCH = 6,   /* the CUDA launch failed (cudaGetLastError after launch) */
   VLS_ERR_ARG = 7,      /* another bad argument (e.g. an unknown KL direction)    */
-  VLS_ERR_TOO_LARGE = 8 /* the call needs more than the fixed scratch of
+  VLS_ERR_TOO_LARGE = 8, /* the call needs more than the fixed scratch of
                            vls_linear_logp_fwd_noalloc                            */
+  VLS_ERR_TIMEOUT = 9   /* vls_check_device_error: a bounded wait in a tensor-core
+                           kernel ran out (its outputs are invalid)               */
 };
 
 /* Largest top-k the logprob calls accept. */
@@ -349,17 +351,21 @@ int vls_linear_logp_bwd(const void* h, int64_t ldh, const void* W, int64_t ldw, 
  * allocate device memory, such as a serving engine that has given all of it
  * to its own pool and forbids further cudaMalloc calls, or a program held to
  * a fixed device-memory budget.  The intermediate partials live in one fixed
- * array of the library (32 MiB, held on every GPU that loads the library
- * until the process exits), which bounds a call: N * S <= 2^20 and
+ * array of the library (32 MiB), which bounds a call: N * S <= 2^20 and
  * N * S * k <= 2^21 with S = vls_linear_logp_chunks(V) (for V = 151936,
  * S = 75: up to 13981 rows at k = 1); larger calls return VLS_ERR_TOO_LARGE
  * before touching the GPU.  Arguments, outputs and status are those of
  * vls_linear_logp_partial and vls_logp_combine: logp [N, k] and stats [N].
+ * The array is held until the process exits on every GPU where it is
+ * loaded: with CUDA's lazy module loading (the default) each GPU where this
+ * call has been made, with eager loading (CUDA_MODULE_LOADING=EAGER) every
+ * GPU the process uses, from the moment the library loads.  It is the
+ * library's own memory, not counted as the call's peak extra memory.
  * The first call on a device looks up the array's address there (a runtime
  * query, no allocation), so make that first call before any stream capture.
- * Every call uses the same array: calls whose work overlaps on the GPU (on
- * different streams or from different threads) race and must be ordered by
- * the caller. */
+ * The launch device is chosen as for the other calls.  Every call uses the
+ * same array: calls whose work overlaps on the GPU (on different streams or
+ * from different threads) race and must be ordered by the caller. */
 int vls_linear_logp_fwd_noalloc(const void* h, int64_t ldh, const void* W, int64_t ldw, vls_dtype dt,
                                 int64_t N, int64_t D, int64_t V, const int64_t* ids, int32_t k,
                                 int64_t ignore_index, float* logp, vls_rowstat* stats, uint32_t* status,
@@ -371,6 +377,27 @@ int vls_linear_logp_fwd_noalloc(const void* h, int64_t ldh, const void* W, int64
 
 /* Static, NUL-terminated name of a status code ("VLS_OK", ...); never NULL. */
 const char* vls_status_string(int status);
+
+/* Reports failures of work already enqueued on the CURRENT device, which the
+ * calls themselves cannot return because they only enqueue it.  Synchronises
+ * the device (cudaDeviceSynchronize), then reads the library's status word
+ * on it.  Every wait of the tensor-core kernels (the vls_linear_logp_* calls)
+ * is bounded in time; one that runs out makes the kernel drain the copies
+ * and products it has in flight and return early, and sets bit 0 both of
+ * the call's own status word and of this library word.  A failed kernel is
+ * reported, never replaced by another path ("Final Logit Softcap", section
+ * Backends: a failed launch is not retried with another backend, fallback
+ * happens only when a backend cannot be loaded).  Returns VLS_ERR_TIMEOUT
+ * when that happened since the last call that returned it (the word is then
+ * cleared),
+ * VLS_ERR_LAUNCH when the synchronisation reports a CUDA error of earlier
+ * work, else VLS_OK.  It synchronises, so it must not be called while a
+ * stream of the device is being captured into a graph; call it when no
+ * tensor-core call is in flight from another thread (a bit set between the
+ * read and the clear would be lost).  The row kernels have no waits of
+ * their own: their only cross-CTA synchronisation is the hardware cluster
+ * barrier, which every CTA of a cluster reaches. */
+int vls_check_device_error(void);
 
 /* Library version, major*10000 + minor*100 + patch. */
 int vls_version(void);

@@ -13,6 +13,7 @@ from vocab_log_softmax_gb300 import _lib, build
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 HEADER = os.path.join(ROOT, "include", "vls.h")
+TEST_HEADER = os.path.join(ROOT, "include", "vls_test.h")
 
 OK, NULL, SHAPE, DTYPE, CAP, DEVICE, LAUNCH, ARG = range(8)
 F32, BF16 = 0, 1
@@ -26,8 +27,8 @@ def lib():
     return _lib.load()
 
 
-def declared_functions():
-    text = open(HEADER).read()
+def declared_functions(header=HEADER):
+    text = open(header).read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
     return sorted(set(re.findall(r"\b(vls_[a-z_0-9]+)\s*\(", text)))
 
@@ -43,6 +44,16 @@ def test_every_declared_symbol_is_exported(lib):
     for name in declared_functions():
         assert hasattr(lib, name), name
         assert name in _lib.SIGNATURES, f"binding lacks {name}"
+
+
+def test_test_build_exports_both_headers_and_the_product_only_its_own(lib):
+    tlib = _lib.load_test()
+    hooks = declared_functions(TEST_HEADER)
+    assert sorted(hooks) == sorted(_lib.TEST_SIGNATURES)
+    for name in declared_functions() + hooks:
+        assert hasattr(tlib, name), name
+    for name in hooks:
+        assert not hasattr(lib, name), name
 
 
 def test_status_strings(lib):

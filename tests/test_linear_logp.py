@@ -262,17 +262,17 @@ def test_autograd_linear_logprobs():
     assert bitwise_equal(h.grad.reshape(n, d), dh) and bitwise_equal(w.grad, dw)
 
 
-def test_one_sm_kernel_in_a_fresh_process():
-    """The 1-SM form of the tensor-core GEMM (VLS_TC_CTA_GROUP=1, read once
-    per process) passes the exact-integer and backward parity checks too."""
-    import os
-    import subprocess
-    import sys
-    here = os.path.dirname(os.path.abspath(__file__))
-    env = dict(os.environ, VLS_TC_CTA_GROUP="1")
-    r = subprocess.run([sys.executable, "-m", "pytest", "-q", "-x", "-p", "no:cacheprovider",
-                        os.path.join(here, "test_linear_logp.py"),
-                        "-k", "exact_integer or (test_backward and 300) or strided"],
-                       env=env, capture_output=True, text=True, timeout=600)
-    assert r.returncode == 0, r.stdout[-3000:] + r.stderr[-2000:]
-    assert " passed" in r.stdout and "failed" not in r.stdout
+def test_one_sm_kernel():
+    """The 1-SM form of the tensor-core GEMM (selected through the test
+    build's tuning hook; the product library always takes CTA pairs) passes
+    the exact-integer and backward parity checks too."""
+    from vocab_log_softmax_gb300 import _lib
+    tlib = _lib.load_test()
+    assert tlib.vls_test_set_tuning(0, 0, 1) == 0
+    try:
+        with _lib.using(tlib):
+            test_exact_integer_inputs(torch.bfloat16)
+            test_backward(300, 256, 5003, 2, torch.bfloat16)
+            test_backward_strided_operands(200)
+    finally:
+        tlib.vls_test_set_tuning(0, 0, 0)

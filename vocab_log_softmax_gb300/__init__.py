@@ -17,8 +17,9 @@ from __future__ import annotations
 
 import torch
 
-from ._lib import VlsArgumentError, VlsError  # noqa: F401
+from ._lib import VlsArgumentError, VlsDeviceError, VlsError  # noqa: F401
 from .binding import (  # noqa: F401
+    vls_check_device_error,
     vls_linear_logp_bwd,
     vls_linear_logp_fwd,
     vls_entropy_bwd,
@@ -35,7 +36,13 @@ from .binding import (  # noqa: F401
     vls_version,
 )
 
-__all__ = ["logprobs", "entropy", "kl", "softcap", "stats", "linear_logprobs"]
+__all__ = ["logprobs", "entropy", "kl", "softcap", "stats", "linear_logprobs", "check_device_error"]
+
+
+def check_device_error() -> None:
+    """Raises VlsDeviceError if a bounded wait of a tensor-core kernel ran out
+    on the current device since the last check (synchronises the device)."""
+    vls_check_device_error()
 
 
 def _addressable(rows: torch.Tensor) -> bool:
@@ -235,34 +242,40 @@ def softcap(x: torch.Tensor, cap: float = 30.0) -> torch.Tensor:
 
 class _LinearLogprobs(torch.autograd.Function):
     @staticmethod
-    def forward(ctx, hidden, weight, ids, ignore_index):
+    def forward(ctx, hidden, weight, ids, ignore_index, check):
         h = hidden.reshape(-1, hidden.shape[-1])
         if h.shape[-1] > 1 and h.stride(-1) != 1:
             h = h.contiguous()
         w = weight if weight.stride(-1) == 1 else weight.contiguous()
         ids2 = _ids_rows(ids, h.shape[0])
-        logp, st, _ = vls_linear_logp_fwd(h, w, ids2, ignore_index)
+        logp, st, _ = vls_linear_logp_fwd(h, w, ids2, ignore_index, check=check)
         ctx.save_for_backward(h, w, ids2, st)
-        ctx.meta = (ignore_index, hidden.shape)
+        ctx.meta = (ignore_index, hidden.shape, check)
         return logp.reshape(ids.shape)
 
     @staticmethod
     def backward(ctx, grad):
         h, w, ids2, st = ctx.saved_tensors
-        ignore_index, shape = ctx.meta
+        ignore_index, shape, check = ctx.meta
         g = grad.reshape(ids2.shape).to(torch.float32).contiguous()
-        dh, dw, _ = vls_linear_logp_bwd(h, w, ids2, g, st, ignore_index)
-        return dh.reshape(shape), dw, None, None
+        dh, dw, _ = vls_linear_logp_bwd(h, w, ids2, g, st, ignore_index, check=check)
+        return dh.reshape(shape), dw, None, None, None
 
 
 def linear_logprobs(hidden: torch.Tensor, weight: torch.Tensor, ids: torch.Tensor,
-                    ignore_index: int = -100) -> torch.Tensor:
+                    ignore_index: int = -100, check: bool = True) -> torch.Tensor:
     """log_softmax(hidden @ weight^T)[..., ids] without storing the logits.
 
     hidden: [..., D] and weight: [V, D], both bfloat16 or both float16; ids
     shaped like hidden's leading dims ([...] or [..., k], k <= 16).  The
-    gradient flows to hidden and weight.  The kernels' bounded waits report
-    through a status word that this API does not read (no host
-    synchronisation); ``binding.vls_linear_logp_fwd`` / ``_bwd`` return it.
+    gradient flows to hidden and weight.
+
+    Every wait inside the tensor-core kernels is bounded; one that runs out
+    makes the kernel return early with invalid outputs and sets a status
+    word.  With check=True (the default) the forward and the backward each
+    synchronise the device after their kernels, read that word and raise
+    VlsDeviceError when it is set.  check=False skips the synchronisation
+    (the calls stay asynchronous); ``check_device_error()`` then reports
+    the same failures later, for any number of calls at once.
     """
-    return _LinearLogprobs.apply(hidden, weight, ids, int(ignore_index))
+    return _LinearLogprobs.apply(hidden, weight, ids, int(ignore_index), bool(check))

@@ -70,6 +70,15 @@ def _ptr(t) -> int | None:
     return None if t is None else t.data_ptr()
 
 
+def _raise_on_status(fn: str, status: torch.Tensor) -> None:
+    """check=True of the tensor-core calls: synchronises the device, reads the
+    call's status word and raises VlsDeviceError when a bounded wait in the
+    kernel ran out (the call's outputs are then invalid)."""
+    torch.cuda.synchronize(status.device)
+    if int(status.item()) & 1:
+        raise _lib.VlsDeviceError(fn, _lib.VLS_ERR_TIMEOUT)
+
+
 def _stats(n: int, device, out=None) -> torch.Tensor:
     """vls_rowstat [N]: (m, log S) pairs as a float32 [N, 2] tensor."""
     if out is not None:
@@ -413,8 +422,12 @@ def _matrix(t: torch.Tensor, what: str) -> tuple[int, int, int]:
 
 
 def vls_linear_logp_partial(h: torch.Tensor, w: torch.Tensor, ids: torch.Tensor, ignore_index: int = -100, *,
-                            part=None, zt=None, status=None, stream=None):
-    """(part [S, N, 6], zt [S, N, k], status [1] int32) of the linear head z = h @ w^T."""
+                            part=None, zt=None, status=None, stream=None, check=False):
+    """(part [S, N, 6], zt [S, N, k], status [1] int32) of the linear head z = h @ w^T.
+
+    The call only enqueues its kernel; `status` gets bit 0 if one of the
+    kernel's bounded waits ran out.  check=True synchronises the device and
+    raises VlsDeviceError in that case."""
     lib = _lib.load()
     n, d, ldh = _matrix(h, "h")
     v, dw, ldw = _matrix(w, "W")
@@ -433,14 +446,19 @@ def vls_linear_logp_partial(h: torch.Tensor, w: torch.Tensor, ids: torch.Tensor,
     st = lib.vls_linear_logp_partial(_ptr(h), ldh, _ptr(w), ldw, _dtype(h), n, d, v, _ptr(ids), k,
                                      int(ignore_index), _ptr(part), _ptr(zt), _ptr(status), _stream(h, stream))
     _lib.check("vls_linear_logp_partial", st)
+    if check:
+        _raise_on_status("vls_linear_logp_partial", status)
     return part, zt, status
 
 
 def vls_linear_logp_fwd(h: torch.Tensor, w: torch.Tensor, ids: torch.Tensor, ignore_index: int = -100, *,
-                        stream=None) -> tuple[torch.Tensor, torch.Tensor, torch.Tensor]:
-    """(logp [N, k], stats [N, 2], status [1]): the two C calls in sequence."""
+                        stream=None, check=False) -> tuple[torch.Tensor, torch.Tensor, torch.Tensor]:
+    """(logp [N, k], stats [N, 2], status [1]): the two C calls in sequence
+    (check as for vls_linear_logp_partial)."""
     part, zt, status = vls_linear_logp_partial(h, w, ids, ignore_index, stream=stream)
     logp, stats = vls_logp_combine(part, zt, ids, w.shape[0], ignore_index, 0.0, stream=stream)
+    if check:
+        _raise_on_status("vls_linear_logp_partial", status)
     return logp, stats, status
 
 
@@ -449,9 +467,11 @@ def vls_linear_logp_bwd_workspace(n: int, d: int, v: int) -> int:
 
 
 def vls_linear_logp_bwd(h: torch.Tensor, w: torch.Tensor, ids: torch.Tensor, g: torch.Tensor, stats: torch.Tensor,
-                        ignore_index: int = -100, *, dh=None, dW=None, workspace=None, status=None, stream=None):
+                        ignore_index: int = -100, *, dh=None, dW=None, workspace=None, status=None, stream=None,
+                        check=False):
     """(dh [N, D], dW [V, D], status [1]) of sum(g * logp) for the linear head
-    z = h @ w^T; `stats` is vls_linear_logp_fwd's."""
+    z = h @ w^T; `stats` is vls_linear_logp_fwd's (check as for
+    vls_linear_logp_partial)."""
     lib = _lib.load()
     n, d, ldh = _matrix(h, "h")
     v, dw, ldw = _matrix(w, "W")
@@ -472,14 +492,17 @@ def vls_linear_logp_bwd(h: torch.Tensor, w: torch.Tensor, ids: torch.Tensor, g: 
                                  _ptr(g), _ptr(stats), _ptr(dh), _ptr(dW), _ptr(workspace),
                                  workspace.numel() * workspace.element_size(), _ptr(status), _stream(h, stream))
     _lib.check("vls_linear_logp_bwd", st)
+    if check:
+        _raise_on_status("vls_linear_logp_bwd", status)
     return dh, dW, status
 
 
 def vls_linear_logp_fwd_noalloc(h: torch.Tensor, w: torch.Tensor, ids: torch.Tensor, ignore_index: int = -100, *,
-                                logp=None, stats=None, status=None, stream=None):
+                                logp=None, stats=None, status=None, stream=None, check=False):
     """vls_linear_logp_fwd through the C entry point that needs no buffer
     beyond the inputs and outputs (its intermediates sit in a fixed array of
-    the library).  Returns (logp [N, k], stats [N, 2], status [1])."""
+    the library).  Returns (logp [N, k], stats [N, 2], status [1]) (check as
+    for vls_linear_logp_partial)."""
     lib = _lib.load()
     n, d, ldh = _matrix(h, "h")
     v, dw, ldw = _matrix(w, "W")
@@ -494,7 +517,16 @@ def vls_linear_logp_fwd_noalloc(h: torch.Tensor, w: torch.Tensor, ids: torch.Ten
                                          int(ignore_index), _ptr(logp), _ptr(stats), _ptr(status),
                                          _stream(h, stream))
     _lib.check("vls_linear_logp_fwd_noalloc", st)
+    if check:
+        _raise_on_status("vls_linear_logp_fwd_noalloc", status)
     return logp, stats, status
+
+
+def vls_check_device_error() -> None:
+    """Synchronises the current device and raises VlsDeviceError when a
+    bounded wait of a tensor-core kernel ran out there since the last check
+    (VlsError for a CUDA error of earlier work).  Clears the report."""
+    _lib.check("vls_check_device_error", _lib.load().vls_check_device_error())
 
 
 def vls_status_string(status: int) -> str:

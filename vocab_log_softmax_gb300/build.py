@@ -5,6 +5,12 @@
 Each ``csrc/*.cu`` translation unit is compiled by nvcc in parallel, then
 linked into ``vocab_log_softmax_gb300/lib/libvls.so`` with the CUDA runtime
 linked statically, so the library needs no ``libcudart`` at load time.
+
+The same objects also make ``lib/libvls_test.so``, the test build: only the
+C layer (``api.cu``) is compiled a second time, with ``VLS_TEST_HOOKS``, which
+adds the hooks of ``include/vls_test.h`` (injected host-side failures, a
+shorter wait limit for the tensor-core kernels, other launch geometries).
+The kernels are the same objects in both libraries.
 """
 
 from __future__ import annotations
@@ -23,6 +29,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB_DIR = os.path.join(PKG, "lib")
 LIB = os.path.join(LIB_DIR, "libvls.so")
+TEST_LIB = os.path.join(LIB_DIR, "libvls_test.so")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH + [
@@ -44,15 +51,15 @@ def sources() -> list[str]:
 
 def headers() -> list[str]:
     hs = [os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith((".h", ".cuh"))]
-    return hs + [os.path.join(INCLUDE, "vls.h")]
+    return hs + [os.path.join(INCLUDE, f) for f in os.listdir(INCLUDE) if f.endswith(".h")]
 
 
 def _newest(paths) -> float:
     return max(os.path.getmtime(p) for p in paths)
 
 
-def _compile(src: str, extra: list[str]) -> str:
-    obj = os.path.join(BUILD, os.path.basename(src) + ".o")
+def _compile(src: str, extra: list[str], suffix: str = "") -> str:
+    obj = os.path.join(BUILD, os.path.basename(src) + suffix + ".o")
     cmd = [nvcc()] + NVCC_FLAGS + extra + ["-c", src, "-o", obj]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
@@ -60,26 +67,36 @@ def _compile(src: str, extra: list[str]) -> str:
     return obj
 
 
-def build(force: bool = False, jobs: int | None = None, extra: list[str] | None = None,
-          verbose: bool = False) -> str:
-    """Compiles and links libvls.so if any source is newer than it; returns its path."""
-    srcs = sources()
-    if not force and os.path.exists(LIB) and os.path.getmtime(LIB) >= _newest(srcs + headers()):
-        return LIB
-    os.makedirs(BUILD, exist_ok=True)
-    os.makedirs(LIB_DIR, exist_ok=True)
-    jobs = jobs or min(len(srcs), os.cpu_count() or 4)
-    extra = list(extra or [])
-    with cf.ThreadPoolExecutor(max_workers=jobs) as ex:
-        objs = list(ex.map(lambda s: _compile(s, extra), srcs))
-    tmp = LIB + ".tmp"
+def _link(objs: list[str], out: str) -> None:
+    tmp = out + ".tmp"
     cmd = [nvcc()] + ARCH + ["-shared", "-cudart", "static", "-o", tmp] + objs
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{' '.join(cmd)}\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB)
+    os.replace(tmp, out)
+
+
+def build(force: bool = False, jobs: int | None = None, extra: list[str] | None = None,
+          verbose: bool = False) -> str:
+    """Compiles and links libvls.so and libvls_test.so if any source is newer
+    than them; returns the path of libvls.so."""
+    srcs = sources()
+    newest = _newest(srcs + headers())
+    if (not force and all(os.path.exists(p) and os.path.getmtime(p) >= newest for p in (LIB, TEST_LIB))):
+        return LIB
+    os.makedirs(BUILD, exist_ok=True)
+    os.makedirs(LIB_DIR, exist_ok=True)
+    api = os.path.join(CSRC, "api.cu")
+    jobs = jobs or min(len(srcs) + 1, os.cpu_count() or 4)
+    extra = list(extra or [])
+    units = [(s, extra, "") for s in srcs] + [(api, extra + ["-DVLS_TEST_HOOKS"], ".test")]
+    with cf.ThreadPoolExecutor(max_workers=jobs) as ex:
+        objs = list(ex.map(lambda u: _compile(*u), units))
+    product, test_api = objs[:-1], objs[-1]
+    _link(product, LIB)
+    _link([test_api if o.endswith("api.cu.o") else o for o in product], TEST_LIB)
     if verbose:
-        print(f"built {LIB}", file=sys.stderr)
+        print(f"built {LIB} and {TEST_LIB}", file=sys.stderr)
     return LIB
 
 

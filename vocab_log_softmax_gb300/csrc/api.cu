@@ -11,6 +11,7 @@
 #include <initializer_list>
 
 #include "vls_internal.h"
+#include "vls_test.h"
 
 namespace vls {
 namespace {
@@ -27,21 +28,42 @@ int check_softcap_cap(float cap) { return (std::isfinite(cap) && cap > 0.0f) ? V
 
 int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
-// Optional tuning overrides (read once); they change the reduction tree, so
-// results are reproducible for a fixed setting only.
-int64_t env_int(const char* name, int64_t fallback) {
-  const char* s = std::getenv(name);
-  if (!s || !*s) return fallback;
-  const long long v = std::atoll(s);
-  return v > 0 ? v : fallback;
+// ---------------------------------------------------------------------------
+// Tuning and fault injection.  The product library has fixed values.  The
+// test build (VLS_TEST_HOOKS, lib/libvls_test.so, hooks in include/vls_test.h)
+// lets a test choose other launch geometries, the 1-SM tensor-core form and
+// a shorter wait limit, and make a call fail on purpose on the host, so that
+// error paths can be exercised without a GPU fault.
+// ---------------------------------------------------------------------------
+constexpr int64_t kFwdVecPerCta = 24576;
+constexpr int64_t kBwdVecPerCta = 4096;
+
+#ifdef VLS_TEST_HOOKS
+std::atomic<int> g_fault{VLS_TEST_FAULT_NONE};
+std::atomic<uint64_t> g_wait_ns{0};
+std::atomic<int64_t> g_fwd_vec{0}, g_bwd_vec{0};
+std::atomic<int> g_cta_group{0};
+int64_t fwd_vec_target() {
+  const int64_t v = g_fwd_vec.load(std::memory_order_relaxed);
+  return v > 0 ? v : kFwdVecPerCta;
 }
+int64_t bwd_vec_target() {
+  const int64_t v = g_bwd_vec.load(std::memory_order_relaxed);
+  return v > 0 ? v : kBwdVecPerCta;
+}
+bool fault_is(int mode) { return g_fault.load(std::memory_order_relaxed) == mode; }
+#else
+constexpr int64_t fwd_vec_target() { return kFwdVecPerCta; }
+constexpr int64_t bwd_vec_target() { return kBwdVecPerCta; }
+constexpr bool fault_is(int) { return false; }
+#endif
 
 // Forward geometry: a function of V only.  One CTA per row up to 24576
 // vectors (196608 columns), then a cluster of up to 8 CTAs.  Fewer, longer
 // CTAs win at the row counts this path serves (thousands of rows): every CTA
 // of a cluster waits at the cluster barrier for its slowest sibling.
 void fwd_geometry(int64_t V, int* cluster, int64_t* vec_per_cta) {
-  static const int64_t target = env_int("VLS_FWD_VEC_PER_CTA", 24576);
+  const int64_t target = fwd_vec_target();
   const int64_t nvec = ceil_div(V, 8);
   int64_t c = ceil_div(nvec, target);
   if (c < 1) c = 1;
@@ -54,7 +76,7 @@ void fwd_geometry(int64_t V, int* cluster, int64_t* vec_per_cta) {
 // prepare their id list once per CTA, so they take whole rows up to 262144
 // columns.
 void bwd_geometry(int64_t V, int32_t k, int* chunks, int64_t* vec_per_cta) {
-  static const int64_t target = env_int("VLS_BWD_VEC_PER_CTA", 4096);
+  const int64_t target = bwd_vec_target();
   const int64_t nvec = ceil_div(V, 8);
   const int64_t t = k > 1 ? 8 * target : target;
   int64_t c = ceil_div(nvec, t);
@@ -97,6 +119,9 @@ int sm_count(int dev) {
 
 // Finds the one device that holds every non-NULL pointer and owns the stream.
 int resolve_device(std::initializer_list<const void*> ptrs, void* stream, int* dev_out) {
+  // test build: the device check fails before any CUDA call
+  if (fault_is(VLS_TEST_FAULT_VALIDATE)) return VLS_ERR_ARG;
+  if (fault_is(VLS_TEST_FAULT_DEVICE)) return VLS_ERR_DEVICE;
   // While a stream is being captured into a CUDA graph the runtime refuses
   // pointer-attribute and stream-device queries, and the refusal would end the
   // capture: take the current device, which the capturing caller has made the
@@ -176,6 +201,10 @@ int launch_status(cudaError_t e) {
   return e == cudaSuccess ? VLS_OK : VLS_ERR_LAUNCH;
 }
 
+// The launch of a call and its status.  In the test build a launch fault
+// skips the launch (outputs are left as they were) and reports VLS_ERR_LAUNCH.
+#define VLS_LAUNCH(call) (fault_is(VLS_TEST_FAULT_LAUNCH) ? VLS_ERR_LAUNCH : launch_status(call))
+
 int check_rows(int64_t N, int64_t V) {
   if (N < 0 || V < 1) return VLS_ERR_SHAPE;
   return VLS_OK;
@@ -233,14 +262,99 @@ int check_shard(int64_t N, int64_t V_shard, int64_t offset, int64_t V_total) {
   return VLS_OK;
 }
 
+// Bit 0 (tc::kStatusTimeout): a bounded wait in a tensor-core kernel ran
+// out on this device since the last vls_check_device_error.  A __device__
+// variable exists once on every device that loads this module.
+__device__ uint32_t g_device_status;
+
+std::atomic<uint32_t*> g_status_addr[64];   // its address per device, once looked up
+
 }  // namespace
+
+int launch_device(const void* p, void* stream, int* dev) { return resolve_device({p}, stream, dev); }
+
+uint32_t* tc_sticky_status() {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+    cudaGetLastError();
+    return nullptr;
+  }
+  uint32_t* p = g_status_addr[dev].load(std::memory_order_acquire);
+  if (!p) {
+    // in host code the variable's name only stands for the symbol: its
+    // device address is asked of the runtime, with the device current
+    void* a = nullptr;
+    if (cudaGetSymbolAddress(&a, g_device_status) != cudaSuccess) {
+      cudaGetLastError();
+      return nullptr;
+    }
+    p = static_cast<uint32_t*>(a);
+    g_status_addr[dev].store(p, std::memory_order_release);
+  }
+  return p;
+}
+
+uint64_t tc_wait_ns() {
+#ifdef VLS_TEST_HOOKS
+  const uint64_t v = g_wait_ns.load(std::memory_order_relaxed);
+  if (v > 0) return v;
+#endif
+  return kTcWaitNs;
+}
+
+namespace tcg {
+int cta_group() {
+#ifdef VLS_TEST_HOOKS
+  if (g_cta_group.load(std::memory_order_relaxed) == 1) return 1;
+#endif
+  return 2;
+}
+}  // namespace tcg
+
 }  // namespace vls
 
 using namespace vls;
 
 extern "C" {
 
-int vls_version(void) { return 100; }
+int vls_version(void) { return 101; }
+
+int vls_check_device_error(void) {
+  if (cudaDeviceSynchronize() != cudaSuccess) {
+    cudaGetLastError();
+    return VLS_ERR_LAUNCH;
+  }
+  uint32_t v = 0;
+  if (cudaMemcpyFromSymbol(&v, g_device_status, sizeof(v)) != cudaSuccess) {
+    cudaGetLastError();
+    return VLS_ERR_LAUNCH;
+  }
+  if (v == 0) return VLS_OK;
+  const uint32_t zero = 0;
+  if (cudaMemcpyToSymbol(g_device_status, &zero, sizeof(zero)) != cudaSuccess) cudaGetLastError();
+  return VLS_ERR_TIMEOUT;
+}
+
+#ifdef VLS_TEST_HOOKS
+int vls_test_set_fault(int mode) {
+  if (mode < VLS_TEST_FAULT_NONE || mode > VLS_TEST_FAULT_DEVICE) return VLS_ERR_ARG;
+  g_fault.store(mode, std::memory_order_relaxed);
+  return VLS_OK;
+}
+
+int vls_test_set_wait_ns(uint64_t ns) {
+  g_wait_ns.store(ns, std::memory_order_relaxed);
+  return VLS_OK;
+}
+
+int vls_test_set_tuning(int64_t fwd_vec_per_cta, int64_t bwd_vec_per_cta, int tc_cta_group) {
+  if (fwd_vec_per_cta < 0 || bwd_vec_per_cta < 0 || tc_cta_group < 0 || tc_cta_group > 2) return VLS_ERR_ARG;
+  g_fwd_vec.store(fwd_vec_per_cta, std::memory_order_relaxed);
+  g_bwd_vec.store(bwd_vec_per_cta, std::memory_order_relaxed);
+  g_cta_group.store(tc_cta_group, std::memory_order_relaxed);
+  return VLS_OK;
+}
+#endif
 
 const char* vls_status_string(int status) {
   switch (status) {
@@ -254,6 +368,7 @@ const char* vls_status_string(int status) {
     case VLS_ERR_LAUNCH: return "VLS_ERR_LAUNCH: CUDA launch failed";
     case VLS_ERR_ARG: return "VLS_ERR_ARG: bad argument";
     case VLS_ERR_TOO_LARGE: return "VLS_ERR_TOO_LARGE: the call needs more than the no-alloc call's fixed scratch";
+    case VLS_ERR_TIMEOUT: return "VLS_ERR_TIMEOUT: a bounded wait in a tensor-core kernel ran out";
     default: return "VLS_ERR_UNKNOWN";
   }
 }
@@ -270,7 +385,7 @@ int vls_softcap_fwd(const void* x, void* y, int64_t n, vls_dtype dt, float cap, 
   if (int e = guard.enter(dev)) return e;
   CapArgs a{x, nullptr, 0, y, n, cap, 1.0f / cap, 0};
   a.grid = sm_count(dev);
-  return launch_status(launch_softcap_fwd(dt, a, static_cast<cudaStream_t>(stream)));
+  return VLS_LAUNCH(launch_softcap_fwd(dt, a, static_cast<cudaStream_t>(stream)));
 }
 
 int vls_softcap_bwd(const void* x, const void* gy, vls_dtype gy_dt, void* gx, int64_t n, vls_dtype dt,
@@ -286,7 +401,7 @@ int vls_softcap_bwd(const void* x, const void* gy, vls_dtype gy_dt, void* gx, in
   if (int e = guard.enter(dev)) return e;
   CapArgs a{x, gy, gy_dt == VLS_F32 ? 1 : 0, gx, n, cap, 1.0f / cap, 0};
   a.grid = sm_count(dev);
-  return launch_status(launch_softcap_bwd(dt, a, static_cast<cudaStream_t>(stream)));
+  return VLS_LAUNCH(launch_softcap_bwd(dt, a, static_cast<cudaStream_t>(stream)));
 }
 
 int vls_logp_fwd(const void* logits, const vls_rows* rows, vls_dtype dt, int64_t N, int64_t V,
@@ -313,7 +428,7 @@ int vls_logp_fwd(const void* logits, const vls_rows* rows, vls_dtype dt, int64_t
   a.ignore_index = ignore_index;
   a.logp = logp;
   a.stats_x = stats;
-  return launch_status(launch_fwd_logp(dt, cap > 0.0f, a, static_cast<cudaStream_t>(stream)));
+  return VLS_LAUNCH(launch_fwd_logp(dt, cap > 0.0f, a, static_cast<cudaStream_t>(stream)));
 }
 
 int vls_logp_bwd(const void* logits, const vls_rows* rows, vls_dtype dt, int64_t N, int64_t V,
@@ -341,7 +456,7 @@ int vls_logp_bwd(const void* logits, const vls_rows* rows, vls_dtype dt, int64_t
   a.g = g;
   a.stats_x = stats;
   a.dx = dlogits;
-  return launch_status(launch_bwd_logp(dt, cap > 0.0f, a, static_cast<cudaStream_t>(stream)));
+  return VLS_LAUNCH(launch_bwd_logp(dt, cap > 0.0f, a, static_cast<cudaStream_t>(stream)));
 }
 
 int vls_entropy_fwd(const void* logits, const vls_rows* rows, vls_dtype dt, int64_t N, int64_t V, float cap,
@@ -362,7 +477,7 @@ int vls_entropy_fwd(const void* logits, const vls_rows* rows, vls_dtype dt, int6
   a.rx = kernel_rows(*rows);
   a.out = H;
   a.stats_x = stats;
-  return launch_status(launch_fwd_entropy(dt, cap > 0.0f, a, static_cast<cudaStream_t>(stream)));
+  return VLS_LAUNCH(launch_fwd_entropy(dt, cap > 0.0f, a, static_cast<cudaStream_t>(stream)));
 }
 
 int vls_entropy_bwd(const void* logits, const vls_rows* rows, vls_dtype dt, int64_t N, int64_t V, float cap,
@@ -387,7 +502,7 @@ int vls_entropy_bwd(const void* logits, const vls_rows* rows, vls_dtype dt, int6
   a.fout = H;
   a.stats_x = stats;
   a.dx = dlogits;
-  return launch_status(launch_bwd_entropy(dt, cap > 0.0f, a, static_cast<cudaStream_t>(stream)));
+  return VLS_LAUNCH(launch_bwd_entropy(dt, cap > 0.0f, a, static_cast<cudaStream_t>(stream)));
 }
 
 int vls_kl_fwd(const void* pa, const vls_rows* rows_a, const void* pb, const vls_rows* rows_b,
@@ -417,7 +532,7 @@ int vls_kl_fwd(const void* pa, const vls_rows* rows_a, const void* pb, const vls
   a.stats_x = rev ? stats_a : stats_b;
   a.stats_y = rev ? stats_b : stats_a;
   a.out = kl;
-  return launch_status(launch_fwd_kl(dt, cap > 0.0f, a, static_cast<cudaStream_t>(stream)));
+  return VLS_LAUNCH(launch_fwd_kl(dt, cap > 0.0f, a, static_cast<cudaStream_t>(stream)));
 }
 
 int vls_kl_bwd(const void* pa, const vls_rows* rows_a, const void* pb, const vls_rows* rows_b,
@@ -448,7 +563,7 @@ int vls_kl_bwd(const void* pa, const vls_rows* rows_a, const void* pb, const vls
   a.stats_x = stats_a;
   a.stats_y = stats_b;
   a.dx = da;
-  return launch_status(
+  return VLS_LAUNCH(
       launch_bwd_kl(dir == VLS_KL_REVERSE, dt, cap > 0.0f, a, static_cast<cudaStream_t>(stream)));
 }
 
@@ -495,7 +610,7 @@ int vls_fused_fwd(const void* pa, const vls_rows* rows_a, const void* pb, const 
   a.stats_x = stats_a;
   a.stats_y = stats_b;
   const FusedKl fk = !want_kl ? kFusedNoKl : (dir == VLS_KL_REVERSE ? kFusedKlReverse : kFusedKlForward);
-  return launch_status(launch_fwd_fused(fk, dt, cap > 0.0f, a, static_cast<cudaStream_t>(stream)));
+  return VLS_LAUNCH(launch_fwd_fused(fk, dt, cap > 0.0f, a, static_cast<cudaStream_t>(stream)));
 }
 
 int vls_fused_bwd(const void* pa, const vls_rows* rows_a, const void* pb, const vls_rows* rows_b,
@@ -543,7 +658,7 @@ int vls_fused_bwd(const void* pa, const vls_rows* rows_a, const void* pb, const 
   a.stats_y = stats_b;
   a.dx = da;
   const FusedKl fk = !want_kl ? kFusedNoKl : (dir == VLS_KL_REVERSE ? kFusedKlReverse : kFusedKlForward);
-  return launch_status(launch_bwd_fused(fk, dt, cap > 0.0f, a, static_cast<cudaStream_t>(stream)));
+  return VLS_LAUNCH(launch_bwd_fused(fk, dt, cap > 0.0f, a, static_cast<cudaStream_t>(stream)));
 }
 
 // ---------------------------------------------------------------------------
@@ -577,7 +692,7 @@ int vls_logp_partial(const void* logits, const vls_rows* rows, vls_dtype dt, int
   a.vocab_total = V_total;
   a.part = part;
   a.zt = zt;
-  return launch_status(launch_fwd_logp(dt, cap > 0.0f, a, static_cast<cudaStream_t>(stream)));
+  return VLS_LAUNCH(launch_fwd_logp(dt, cap > 0.0f, a, static_cast<cudaStream_t>(stream)));
 }
 
 int vls_logp_combine(const vls_partial* parts, const float* zt, int32_t R, int64_t N, const int64_t* ids,
@@ -604,7 +719,7 @@ int vls_logp_combine(const vls_partial* parts, const float* zt, int32_t R, int64
   a.cap = cap;
   a.logp = logp;
   a.stats_x = stats;
-  return launch_status(launch_combine(kFwdLogp, a, static_cast<cudaStream_t>(stream)));
+  return VLS_LAUNCH(launch_combine(kFwdLogp, a, static_cast<cudaStream_t>(stream)));
 }
 
 int vls_logp_bwd_shard(const void* logits, const vls_rows* rows, vls_dtype dt, int64_t N, int64_t V_shard,
@@ -634,7 +749,7 @@ int vls_logp_bwd_shard(const void* logits, const vls_rows* rows, vls_dtype dt, i
   a.dx = dlogits;
   a.vocab_offset = vocab_offset;
   a.vocab_total = V_total;
-  return launch_status(launch_bwd_logp(dt, cap > 0.0f, a, static_cast<cudaStream_t>(stream)));
+  return VLS_LAUNCH(launch_bwd_logp(dt, cap > 0.0f, a, static_cast<cudaStream_t>(stream)));
 }
 
 int vls_entropy_partial(const void* logits, const vls_rows* rows, vls_dtype dt, int64_t N, int64_t V_shard,
@@ -657,7 +772,7 @@ int vls_entropy_partial(const void* logits, const vls_rows* rows, vls_dtype dt, 
   a.x = logits;
   if (V_shard > 0) a.rx = kernel_rows(*rows);
   a.part = part;
-  return launch_status(launch_fwd_entropy(dt, cap > 0.0f, a, static_cast<cudaStream_t>(stream)));
+  return VLS_LAUNCH(launch_fwd_entropy(dt, cap > 0.0f, a, static_cast<cudaStream_t>(stream)));
 }
 
 int vls_entropy_combine(const vls_partial* parts, int32_t R, int64_t N, float* H, vls_rowstat* stats,
@@ -676,7 +791,7 @@ int vls_entropy_combine(const vls_partial* parts, int32_t R, int64_t N, float* H
   a.rows = N;
   a.out = H;
   a.stats_x = stats;
-  return launch_status(launch_combine(kFwdEntropy, a, static_cast<cudaStream_t>(stream)));
+  return VLS_LAUNCH(launch_combine(kFwdEntropy, a, static_cast<cudaStream_t>(stream)));
 }
 
 int vls_kl_partial(const void* pa, const vls_rows* rows_a, const void* pb, const vls_rows* rows_b,
@@ -707,7 +822,7 @@ int vls_kl_partial(const void* pa, const vls_rows* rows_a, const void* pb, const
     a.ry = kernel_rows(rev ? *rows_b : *rows_a);
   }
   a.part = part;
-  return launch_status(launch_fwd_kl(dt, cap > 0.0f, a, static_cast<cudaStream_t>(stream)));
+  return VLS_LAUNCH(launch_fwd_kl(dt, cap > 0.0f, a, static_cast<cudaStream_t>(stream)));
 }
 
 int vls_kl_combine(const vls_partial* parts, int32_t R, int64_t N, vls_kl_dir dir, float* kl,
@@ -729,7 +844,7 @@ int vls_kl_combine(const vls_partial* parts, int32_t R, int64_t N, vls_kl_dir di
   const bool rev = dir == VLS_KL_REVERSE;
   a.stats_x = rev ? stats_a : stats_b;
   a.stats_y = rev ? stats_b : stats_a;
-  return launch_status(launch_combine(kFwdKl, a, static_cast<cudaStream_t>(stream)));
+  return VLS_LAUNCH(launch_combine(kFwdKl, a, static_cast<cudaStream_t>(stream)));
 }
 
 // ---------------------------------------------------------------------------
@@ -756,8 +871,8 @@ int vls_linear_logp_partial(const void* h, int64_t ldh, const void* W, int64_t l
   if (int e = resolve_device({h, W, ids, part, zt, status}, stream, &dev)) return e;
   DeviceGuard guard;
   if (int e = guard.enter(dev)) return e;
-  LinearArgs a{h, ldh, W, ldw, dt, N, D, V, ids, k, ignore_index, part, zt, status};
-  return launch_status(launch_linear_logp(a, sm_count(dev), static_cast<cudaStream_t>(stream)));
+  LinearArgs a{h, ldh, W, ldw, dt, N, D, V, ids, k, ignore_index, part, zt, status, tc_sticky_status(), tc_wait_ns()};
+  return VLS_LAUNCH(launch_linear_logp(a, sm_count(dev), static_cast<cudaStream_t>(stream)));
 }
 
 int64_t vls_linear_logp_bwd_workspace(int64_t N, int64_t D, int64_t V) {
@@ -782,8 +897,9 @@ int vls_linear_logp_bwd(const void* h, int64_t ldh, const void* W, int64_t ldw, 
   if (int e = resolve_device({h, W, ids, g, stats, dh, dW, workspace, status}, stream, &dev)) return e;
   DeviceGuard guard;
   if (int e = guard.enter(dev)) return e;
-  LinearBwdArgs a{h, ldh, W, ldw, dt, N, D, V, ids, k, ignore_index, g, stats, dh, dW, workspace, status};
-  return launch_status(launch_linear_logp_bwd(a, sm_count(dev), static_cast<cudaStream_t>(stream)));
+  LinearBwdArgs a{h, ldh, W, ldw, dt, N, D, V, ids, k, ignore_index, g, stats, dh, dW, workspace, status,
+                  tc_sticky_status(), tc_wait_ns()};
+  return VLS_LAUNCH(launch_linear_logp_bwd(a, sm_count(dev), static_cast<cudaStream_t>(stream)));
 }
 
 }  // extern "C"

@@ -283,6 +283,7 @@ cudaError_t bwd_t(const LinearBwdArgs& a, int sms, cudaStream_t s) {
   using T = typename std::conditional<BF16, __nv_bfloat16, __half>::type;
   T* dz = static_cast<T*>(a.workspace);
   const int64_t ldv = pad8(a.V);
+  const tc::WaitCtl wc{a.status, a.sticky, a.wait_ns};
   cudaError_t e;
   // the dz map, dz through TMA stores (the workspace is 256-byte aligned and
   // its rows are padded to 16-byte multiples, so the map always encodes)
@@ -295,7 +296,7 @@ cudaError_t bwd_t(const LinearBwdArgs& a, int sms, cudaStream_t s) {
   dze.stats = a.stats;
   dze.N = a.N;
   if (!tcg::encode_store(&dze.map, dz, BF16, a.N, a.V, ldv)) return cudaErrorInvalidValue;
-  if ((e = tcg::launch_gemm<BF16>(a.h, a.ldh, a.N, a.W, a.ldw, a.V, a.D, kLinChunkTiles, false, a.status, dze, sms, s)) !=
+  if ((e = tcg::launch_gemm<BF16>(a.h, a.ldh, a.N, a.W, a.ldw, a.V, a.D, kLinChunkTiles, false, wc, dze, sms, s)) !=
       cudaSuccess)
     return e;
   // dh = dz W has K = V: at few rows its tiles leave SMs idle, and at some
@@ -309,7 +310,7 @@ cudaError_t bwd_t(const LinearBwdArgs& a, int sms, cudaStream_t s) {
   if (split) {
     float* P = static_cast<float*>(a.dW);
     const PartialEpi pe{P, a.N, a.D};
-    if ((e = tcg::launch_gemm<BF16, false, true>(dz, ldv, a.N, a.W, a.ldw, a.D, a.V, 1, true, a.status, pe, sms, s,
+    if ((e = tcg::launch_gemm<BF16, false, true>(dz, ldv, a.N, a.W, a.ldw, a.D, a.V, 1, true, wc, pe, sms, s,
                                                  runs)) != cudaSuccess)
       return e;
     const int64_t n = a.N * a.D;
@@ -325,18 +326,18 @@ cudaError_t bwd_t(const LinearBwdArgs& a, int sms, cudaStream_t s) {
   dwt.M = a.V;
   if (tcg::encode_store(&dht.map, a.dh, BF16, a.N, a.D, a.D) && tcg::encode_store(&dwt.map, a.dW, BF16, a.V, a.D, a.D)) {
     if (!split &&
-        (e = tcg::launch_gemm<BF16, false, true>(dz, ldv, a.N, a.W, a.ldw, a.D, a.V, 1, true, a.status, dht, sms, s)) !=
+        (e = tcg::launch_gemm<BF16, false, true>(dz, ldv, a.N, a.W, a.ldw, a.D, a.V, 1, true, wc, dht, sms, s)) !=
             cudaSuccess)
       return e;
-    return tcg::launch_gemm<BF16, true, true>(dz, ldv, a.V, a.h, a.ldh, a.D, a.N, 1, true, a.status, dwt, sms, s);
+    return tcg::launch_gemm<BF16, true, true>(dz, ldv, a.V, a.h, a.ldh, a.D, a.N, 1, true, wc, dwt, sms, s);
   }
   const StoreEpi<T> dhe{static_cast<T*>(a.dh), a.D};
   if (!split &&
-      (e = tcg::launch_gemm<BF16, false, true>(dz, ldv, a.N, a.W, a.ldw, a.D, a.V, 1, true, a.status, dhe, sms, s)) !=
+      (e = tcg::launch_gemm<BF16, false, true>(dz, ldv, a.N, a.W, a.ldw, a.D, a.V, 1, true, wc, dhe, sms, s)) !=
           cudaSuccess)
     return e;
   const StoreEpi<T> dwe{static_cast<T*>(a.dW), a.D};
-  return tcg::launch_gemm<BF16, true, true>(dz, ldv, a.V, a.h, a.ldh, a.D, a.N, 1, true, a.status, dwe, sms, s);
+  return tcg::launch_gemm<BF16, true, true>(dz, ldv, a.V, a.h, a.ldh, a.D, a.N, 1, true, wc, dwe, sms, s);
 }
 
 }  // namespace

@@ -19,7 +19,6 @@
 // ("Add Triton kernels for vocab-parallel logprobs, entropy and KL",
 // DeepSpeed PR #8838, Changes).
 #include <atomic>
-#include <cstdlib>
 
 #include <cuda.h>
 #include <cudaTypedefs.h>
@@ -139,14 +138,6 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 
 namespace tcg {
 
-int cta_group() {
-  static const int g = [] {
-    const char* v = std::getenv("VLS_TC_CTA_GROUP");
-    return (v && v[0] == '1') ? 1 : 2;
-  }();
-  return g;
-}
-
 bool encode_kmajor(CUtensorMap* map, const void* base, bool bf16, int64_t rows, int64_t K, int64_t ld,
                    int box_rows) {
   auto fn = encode_fn();
@@ -195,11 +186,10 @@ int64_t linear_chunks(int64_t V) {
 
 cudaError_t launch_linear_logp(const LinearArgs& la, int sms, cudaStream_t s) {
   const LogpEpi epi{la.ids, la.k, la.N, la.part, la.zt};
+  const tc::WaitCtl wc{la.status, la.sticky, la.wait_ns};
   return la.dt == VLS_BF16
-             ? tcg::launch_gemm<true>(la.h, la.ldh, la.N, la.W, la.ldw, la.V, la.D, kLinChunkTiles, false, la.status, epi,
-                                      sms, s)
-             : tcg::launch_gemm<false>(la.h, la.ldh, la.N, la.W, la.ldw, la.V, la.D, kLinChunkTiles, false, la.status, epi,
-                                       sms, s);
+             ? tcg::launch_gemm<true>(la.h, la.ldh, la.N, la.W, la.ldw, la.V, la.D, kLinChunkTiles, false, wc, epi, sms, s)
+             : tcg::launch_gemm<false>(la.h, la.ldh, la.N, la.W, la.ldw, la.V, la.D, kLinChunkTiles, false, wc, epi, sms, s);
 }
 
 }  // namespace vls

@@ -11,10 +11,13 @@
 // in one fixed array in the library's own device memory, so a call needs
 // only the inputs and the outputs.
 //
-// The array lives for as long as the library is loaded, on every GPU that
-// loads it (kScratchBytes = 32 MiB).  Every call shares it, so two calls
-// whose kernels overlap on the GPU (on different streams, or from different
-// host threads) race on it and may return each other's results.
+// The array (kScratchBytes = 32 MiB) lives for as long as the library is
+// loaded, on every GPU where this file's module is loaded: with CUDA's lazy
+// module loading (the default) that is each GPU where this entry point has
+// been called, with eager loading every GPU of the process.  Every call
+// shares it, so two calls whose kernels overlap on the GPU (on different
+// streams, or from different host threads) race on it and may return each
+// other's results.
 #include <mutex>
 
 #include "vls_internal.h"
@@ -73,14 +76,11 @@ extern "C" int vls_linear_logp_fwd_noalloc(const void* h, int64_t ldh, const voi
   if (N > kNoAllocPartials / chunks || N * chunks * k > kNoAllocTargets) return VLS_ERR_TOO_LARGE;
   if (N == 0) return VLS_OK;
   if (!h) return VLS_ERR_NULL;
-  cudaPointerAttributes at;
-  if (cudaPointerGetAttributes(&at, h) != cudaSuccess) {
-    cudaGetLastError();
-    return VLS_ERR_DEVICE;
-  }
-  if (at.type != cudaMemoryTypeDevice && at.type != cudaMemoryTypeManaged) return VLS_ERR_DEVICE;
+  // the device the launch goes to, chosen as for every other call
+  int dev = -1;
+  if (int e = vls::launch_device(h, stream, &dev)) return e;
   void* base = nullptr;
-  if (int e = scratch_on(at.device, &base)) return e;
+  if (int e = scratch_on(dev, &base)) return e;
   vls_partial* part = static_cast<vls_partial*>(base);
   float* zt = reinterpret_cast<float*>(static_cast<unsigned char*>(base) + kPartBytes);
   // every partial and target entry of [chunks, N(, k)] is written by the first

@@ -10,14 +10,23 @@
 
 #include <cuda.h>
 
+#include "vls_internal.h"
+
 namespace vls {
 namespace tc {
 
 // Nanoseconds a wait may take before the kernel gives up.  A legitimate wait
 // here lasts microseconds (one tile of MMAs or one TMA load).
-constexpr uint64_t kWaitNs = 4000000000ull;
+constexpr uint64_t kWaitNs = kTcWaitNs;
 // Status bits written to the caller's device status word.
 constexpr uint32_t kStatusTimeout = 1u;
+
+// Where a wait that runs out reports, and how long a wait may take.
+struct WaitCtl {
+  uint32_t* status;   // the caller's status word (may be null)
+  uint32_t* sticky;   // the library's per-device word that vls_check_device_error reads (may be null)
+  uint64_t limit_ns;  // how long a protocol wait may take (kWaitNs unless a test build shortens it)
+};
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -27,6 +36,11 @@ __device__ __forceinline__ uint64_t global_ns() {
   uint64_t t;
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
   return t;
+}
+
+__device__ __forceinline__ void report_timeout(const WaitCtl& w) {
+  if (w.status) atomicOr(w.status, kStatusTimeout);
+  if (w.sticky) atomicOr(w.sticky, kStatusTimeout);
 }
 
 // ---- mbarrier ----
@@ -48,6 +62,12 @@ __device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
   asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
 }
 
+// Counts `bytes` of the current phase's transactions as done without a copy
+// (the drain of an aborted CTA pair stands in for a copy that was never issued).
+__device__ __forceinline__ void mbar_complete_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.complete_tx.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
@@ -61,30 +81,32 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 }
 
 // Waits for the phase of parity `parity` of `bar` to complete.  Returns false
-// when another role of the CTA has aborted or when kWaitNs ran out (then it
-// raises the abort flag and the status word itself).
+// when another role of the CTA has aborted or when w.limit_ns ran out (then
+// it raises the abort flag and reports through w itself).
 __device__ __forceinline__ bool wait(uint32_t bar, uint32_t parity, volatile uint32_t* abort_flag,
-                                     uint32_t* status) {
+                                     const WaitCtl& w) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_ns();
   while (true) {
     if (mbar_try_wait(bar, parity)) return true;
     if (*abort_flag) return false;
-    if (global_ns() - t0 > kWaitNs) {
+    if (global_ns() - t0 > w.limit_ns) {
       *abort_flag = 1u;
-      if (status) atomicOr(status, kStatusTimeout);
+      report_timeout(w);
       return false;
     }
   }
 }
 
 // The same wait without the abort flag, for draining work already issued
-// when the CTA shuts down after an abort.
-__device__ __forceinline__ bool wait_drain(uint32_t bar, uint32_t parity, uint32_t* status) {
+// when the CTA shuts down (after an abort, or at the end).  It always allows
+// the full kWaitNs, whatever the protocol waits' limit, so that a CTA never
+// releases shared or tensor memory that a copy or an MMA still uses.
+__device__ __forceinline__ bool wait_drain(uint32_t bar, uint32_t parity, const WaitCtl& w) {
   const uint64_t t0 = global_ns();
   while (!mbar_try_wait(bar, parity)) {
     if (global_ns() - t0 > kWaitNs) {
-      if (status) atomicOr(status, kStatusTimeout);
+      report_timeout(w);
       return false;
     }
   }
@@ -146,6 +168,11 @@ __device__ __forceinline__ uint32_t map_to_rank(uint32_t addr, uint32_t rank) {
   uint32_t r;
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
   return r;
+}
+
+// 32-bit store into the shared memory of any CTA of the cluster (address from map_to_rank).
+__device__ __forceinline__ void st_cluster_u32(uint32_t cluster_addr, uint32_t v) {
+  asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(cluster_addr), "r"(v) : "memory");
 }
 
 // Arrival on an mbarrier of any CTA of the cluster (address from map_to_rank).

@@ -53,7 +53,7 @@ struct Sched {
   int n_units_k;      // units per K run: n_row_tiles x n_chunks
   int cols_fastest;   // unit order: 0 = row tiles fastest (B chunk shared by the CTAs in flight),
                       // 1 = column chunks fastest (A row panel shared)
-  uint32_t* status;   // device status word (tc::kStatusTimeout after a wait ran out)
+  tc::WaitCtl wc;     // where a wait that runs out reports (tc::kStatusTimeout), and the wait limit
 
   // (row tile, column chunk, K run) of unit u; K runs outermost
   __device__ __forceinline__ void unit(int u, int& rt, int& chunk, int& ks) const {
@@ -77,8 +77,8 @@ struct Sched {
 // rows_per_tile: 128 (1-SM form) or 256 (CTA pairs).  ksplit > 1 cuts K into
 // that many runs of whole K blocks, one unit per (tile, chunk, run); the
 // epilogue then sees partial sums and the run index (EpiWarp::ks).
-inline Sched make_sched(int64_t M, int64_t Ncols, int64_t K, int chunk_tiles, uint32_t* status, int rows_per_tile,
-                        int ksplit) {
+inline Sched make_sched(int64_t M, int64_t Ncols, int64_t K, int chunk_tiles, const tc::WaitCtl& wc,
+                        int rows_per_tile, int ksplit) {
   Sched s;
   s.M = M;
   s.Ncols = Ncols;
@@ -94,7 +94,7 @@ inline Sched make_sched(int64_t M, int64_t Ncols, int64_t K, int chunk_tiles, ui
   s.n_units_k = s.n_row_tiles * s.n_chunks;
   s.n_units = s.n_units_k * s.ksplit;
   s.cols_fastest = 0;
-  s.status = status;
+  s.wc = wc;
   return s;
 }
 
@@ -211,7 +211,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int t_end = min((chunk + 1) * sc.chunk_tiles, sc.n_col_tiles);
         for (int t = chunk * sc.chunk_tiles; ok && t < t_end; ++t) {
           for (int kb = kb0; kb < kb1; ++kb) {
-            if (!tc::wait(empty(stage), phase ^ 1u, abort_flag, sc.status)) {
+            if (!tc::wait(empty(stage), phase ^ 1u, abort_flag, sc.wc)) {
               ok = false;
               break;
             }
@@ -226,14 +226,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
-      // After an abort, wait for the loads still in flight before the CTA
-      // releases its shared memory: the last load issued into each stage.
-      if (!ok) {
-        for (int s = 0; s < kStages; ++s) {
-          if (issued > static_cast<uint32_t>(s)) {
-            const uint32_t last = (issued - 1 - s) / kStages;   // index of the last load into stage s
-            tc::wait_drain(full(s), last & 1u, sc.status);
-          }
+      // Before the CTA releases its shared memory, every load issued has
+      // landed: the last one into each stage.  After a normal run the MMA
+      // thread has waited for all of them and these waits return at once;
+      // after an abort (this role's or another's) some may still be in flight.
+      for (int s = 0; s < kStages; ++s) {
+        if (issued > static_cast<uint32_t>(s)) {
+          const uint32_t last = (issued - 1 - s) / kStages;   // index of the last load into stage s
+          tc::wait_drain(full(s), last & 1u, sc.wc);
         }
       }
     }
@@ -252,14 +252,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int t_end = min((chunk + 1) * sc.chunk_tiles, sc.n_col_tiles);
         for (int t = chunk * sc.chunk_tiles; ok && t < t_end; ++t, ++tc_count) {
           const uint32_t buf = tc_count & 1u, use = (tc_count >> 1) & 1u;
-          if (!tc::wait(acc_empty(buf), use ^ 1u, abort_flag, sc.status)) {
+          if (!tc::wait(acc_empty(buf), use ^ 1u, abort_flag, sc.wc)) {
             ok = false;
             break;
           }
           tc::fence_after_sync();
           const uint32_t d = tmem + buf * kBN;
           for (int kb = kb0; kb < kb1; ++kb) {
-            if (!tc::wait(full(stage), phase, abort_flag, sc.status)) {
+            if (!tc::wait(full(stage), phase, abort_flag, sc.wc)) {
               ok = false;
               break;
             }
@@ -281,7 +281,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       // every MMA this thread issued has completed before tensor memory is freed
       tc::mma_commit(done_bar);
-      tc::wait_drain(done_bar, 0u, sc.status);
+      tc::wait_drain(done_bar, 0u, sc.wc);
     }
   } else {
     // ---------------- epilogue: warps 2-5 ----------------
@@ -304,7 +304,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t buf = tc_count & 1u, use = (tc_count >> 1) & 1u;
         // one lane waits and the warp follows it, so the warp-wide tensor-memory
         // loads below are never reached by part of a warp
-        const bool got = lane == 0 ? tc::wait(acc_full(buf), use, abort_flag, sc.status) : true;
+        const bool got = lane == 0 ? tc::wait(acc_full(buf), use, abort_flag, sc.wc) : true;
         if (!__shfl_sync(0xffffffffu, got ? 1 : 0, 0)) {
           ok = false;
           break;
@@ -394,6 +394,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t done_bar = bar0 + 8u * (2 * kStages2 + 4);
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + kNumBars2);
   volatile uint32_t* abort_flag = tmem_holder + 1;
+  // written by the other CTA of the pair at the end: its abort flag and its
+  // count of issued loads
+  volatile uint32_t* peer_state = tmem_holder + 2;
+  uint32_t issued = 0;   // loads this CTA's producer issued (thread 0)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
@@ -430,7 +434,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int t_end = min((chunk + 1) * sc.chunk_tiles, sc.n_col_tiles);
         for (int t = chunk * sc.chunk_tiles; ok && t < t_end; ++t) {
           for (int kb = kb0; kb < kb1; ++kb) {
-            if (!tc::wait(empty(stage), phase ^ 1u, abort_flag, sc.status)) {
+            if (!tc::wait(empty(stage), phase ^ 1u, abort_flag, sc.wc)) {
               ok = false;
               break;
             }
@@ -439,6 +443,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             load_stage<A_MN, kBM, true>(sA + stage * kStageA2, &tm_a, kb * kBK, rt * 2 * kBM + rank * kBM, lead_full);
             load_stage<B_MN, kBN / 2, true>(sB + stage * kStageB2, &tm_b, kb * kBK, t * kBN + rank * (kBN / 2),
                                             lead_full);
+            ++issued;
             if (++stage == kStages2) {
               stage = 0;
               phase ^= 1u;
@@ -462,14 +467,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int t_end = min((chunk + 1) * sc.chunk_tiles, sc.n_col_tiles);
         for (int t = chunk * sc.chunk_tiles; ok && t < t_end; ++t, ++tc_count) {
           const uint32_t buf = tc_count & 1u, use = (tc_count >> 1) & 1u;
-          if (!tc::wait(acc_empty(buf), use ^ 1u, abort_flag, sc.status)) {
+          if (!tc::wait(acc_empty(buf), use ^ 1u, abort_flag, sc.wc)) {
             ok = false;
             break;
           }
           tc::fence_after_sync();
           const uint32_t d = tmem + buf * kBN;
           for (int kb = kb0; kb < kb1; ++kb) {
-            if (!tc::wait(full(stage), phase, abort_flag, sc.status)) {
+            if (!tc::wait(full(stage), phase, abort_flag, sc.wc)) {
               ok = false;
               break;
             }
@@ -491,7 +496,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       // every pair MMA has completed before either CTA frees its memory
       tc::mma_commit_pair(done_bar);
-      tc::wait_drain(done_bar, 0u, sc.status);
+      tc::wait_drain(done_bar, 0u, sc.wc);
     }
   } else {
     // ---------------- epilogue: warps 2-5 of both CTAs ----------------
@@ -512,7 +517,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       typename Epi::State st = epi.begin(row, row_ok, chunk);
       for (int t = t_beg; t < t_end; ++t, ++tc_count) {
         const uint32_t buf = tc_count & 1u, use = (tc_count >> 1) & 1u;
-        const bool got = lane == 0 ? tc::wait(acc_full(buf), use, abort_flag, sc.status) : true;
+        const bool got = lane == 0 ? tc::wait(acc_full(buf), use, abort_flag, sc.wc) : true;
         if (!__shfl_sync(0xffffffffu, got ? 1 : 0, 0)) {
           ok = false;
           break;
@@ -552,7 +557,40 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   tc::fence_before_sync();
   __syncthreads();
-  tc::cluster_sync_all();   // no CTA leaves while its pair may still read its memory
+  // Every role of this CTA is done.  Both CTAs' loads complete on the
+  // leader's `full` barriers, so after an abort only the leader can tell when
+  // a load still in flight has landed.  Each CTA tells the other its abort
+  // flag and how many loads it issued, then the pair meets; no CTA leaves
+  // while its pair may still read its memory.
+  if (threadIdx.x == 0) {
+    const uint32_t peer = rank ^ 1u;
+    tc::st_cluster_u32(tc::map_to_rank(tc::smem_u32(const_cast<uint32_t*>(peer_state)), peer), *abort_flag);
+    tc::st_cluster_u32(tc::map_to_rank(tc::smem_u32(const_cast<uint32_t*>(peer_state + 1)), peer), issued);
+  }
+  tc::cluster_sync_all();
+  if (*abort_flag || peer_state[0]) {   // the same decision in both CTAs
+    // After a normal run the MMA thread has waited for every load.  After an
+    // abort the leader waits for the last load of each stage, both CTAs'
+    // halves.  Per stage the two producers differ by at most one load (a
+    // stage is refilled only after both halves of its previous load were
+    // consumed), and a load only one of them issued is made whole: the
+    // leader counts the missing half as done (complete_tx) or makes the
+    // arrival its own producer never made (expect_tx of the peer's half).
+    if (leader && threadIdx.x == 0) {
+      const uint32_t peer_issued = peer_state[1];
+      for (int s = 0; s < kStages2; ++s) {
+        const uint32_t us = static_cast<uint32_t>(s);
+        const uint32_t mine = issued > us ? (issued - 1 - us) / kStages2 + 1 : 0;
+        const uint32_t theirs = peer_issued > us ? (peer_issued - 1 - us) / kStages2 + 1 : 0;
+        if (mine == 0 && theirs == 0) continue;
+        if (mine > theirs) tc::mbar_complete_tx(full(s), kStageA2 + kStageB2);
+        else if (theirs > mine) tc::mbar_expect_tx(full(s), kStageA2 + kStageB2);
+        const uint32_t last = (mine > theirs ? mine : theirs) - 1;
+        tc::wait_drain(full(s), last & 1u, sc.wc);
+      }
+    }
+    tc::cluster_sync_all();
+  }
   if (warp == 1) {
     __syncwarp();
     tc::fence_after_sync();
@@ -582,18 +620,19 @@ inline bool encode_operand(CUtensorMap* map, bool mn, const void* base, bool bf1
   return mn ? encode_mnmajor(map, base, bf16, rows, K, ld) : encode_kmajor(map, base, bf16, rows, K, ld, box_rows);
 }
 
-// 1 for the 1-SM kernel, 2 for CTA pairs (VLS_TC_CTA_GROUP; default 2).
+// 1 for the 1-SM kernel, 2 for CTA pairs (the default; a test build of the
+// library can select the 1-SM form).  Defined by the C layer.
 int cta_group();
 
 template <bool BF16, bool A_MN, bool B_MN, class Epi>
 cudaError_t launch_gemm2(const void* A, int64_t lda, int64_t M, const void* Bm, int64_t ldb, int64_t Ncols,
-                         int64_t K, int chunk_tiles, bool cols_fastest, uint32_t* status, const Epi& epi, int sms,
+                         int64_t K, int chunk_tiles, bool cols_fastest, const tc::WaitCtl& wc, const Epi& epi, int sms,
                          cudaStream_t s, int ksplit) {
   CUtensorMap tm_a, tm_b;
   if (!encode_operand(&tm_a, A_MN, A, BF16, M, K, lda, kBM) ||
       !encode_operand(&tm_b, B_MN, Bm, BF16, Ncols, K, ldb, kBN / 2))
     return cudaErrorInvalidValue;
-  Sched sc = make_sched(M, Ncols, K, chunk_tiles, status, 2 * kBM, ksplit);   // 256-row tiles
+  Sched sc = make_sched(M, Ncols, K, chunk_tiles, wc, 2 * kBM, ksplit);   // 256-row tiles
   sc.cols_fastest = cols_fastest ? 1 : 0;
   auto kern = gemm2_kernel<BF16, A_MN, B_MN, Epi>;
   int dev = 0;
@@ -676,15 +715,15 @@ inline int fill_ksplit(int64_t M, int64_t Ncols, int64_t K, int sms, int min_k_b
 // K-major ([M, K], [Ncols, K]).  ksplit > 1: split-K (see make_sched).
 template <bool BF16, bool A_MN = false, bool B_MN = false, class Epi>
 cudaError_t launch_gemm(const void* A, int64_t lda, int64_t M, const void* Bm, int64_t ldb, int64_t Ncols,
-                        int64_t K, int chunk_tiles, bool cols_fastest, uint32_t* status, const Epi& epi, int sms,
+                        int64_t K, int chunk_tiles, bool cols_fastest, const tc::WaitCtl& wc, const Epi& epi, int sms,
                         cudaStream_t s, int ksplit = 1) {
   if (cta_group() == 2 && sms >= 2)
-    return launch_gemm2<BF16, A_MN, B_MN>(A, lda, M, Bm, ldb, Ncols, K, chunk_tiles, cols_fastest, status, epi, sms,
+    return launch_gemm2<BF16, A_MN, B_MN>(A, lda, M, Bm, ldb, Ncols, K, chunk_tiles, cols_fastest, wc, epi, sms,
                                           s, ksplit);
   CUtensorMap tm_a, tm_b;
   if (!encode_operand(&tm_a, A_MN, A, BF16, M, K, lda, kBM) || !encode_operand(&tm_b, B_MN, Bm, BF16, Ncols, K, ldb, kBN))
     return cudaErrorInvalidValue;
-  Sched sc = make_sched(M, Ncols, K, chunk_tiles, status, kBM, ksplit);
+  Sched sc = make_sched(M, Ncols, K, chunk_tiles, wc, kBM, ksplit);
   sc.cols_fastest = cols_fastest ? 1 : 0;
   auto kern = gemm_kernel<BF16, A_MN, B_MN, Epi>;
   constexpr size_t smem = 1024 + kEpiOff + 4 * static_cast<size_t>(Epi::kStageBytes);

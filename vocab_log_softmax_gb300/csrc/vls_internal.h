@@ -42,6 +42,9 @@ constexpr int kCapMinBlocks = VLS_CAP_MIN_BLOCKS;
 // visits its vectors in increasing order.
 constexpr int kUnroll = 4;
 constexpr int kMaxCluster = 8;
+// Nanoseconds one protocol wait of a tensor-core kernel may take before the
+// kernel gives up (a legitimate wait lasts microseconds).
+constexpr uint64_t kTcWaitNs = 4000000000ull;
 
 struct FwdArgs {
   // logits (logp / entropy), or the first KL argument: the distribution the
@@ -156,7 +159,9 @@ struct LinearArgs {
   int64_t ignore_index;
   vls_partial* part;   // [S, N]
   float* zt;           // [S, N, k]
-  uint32_t* status;
+  uint32_t* status;    // the caller's status word
+  uint32_t* sticky;    // the library's status word on this device (tc_sticky_status)
+  uint64_t wait_ns;    // limit of one protocol wait (tc_wait_ns)
 };
 
 int64_t linear_chunks(int64_t V);
@@ -177,9 +182,24 @@ struct LinearBwdArgs {
   void* dW;                  // [V, D] contiguous, dtype dt
   void* workspace;           // linear_bwd_workspace(N, D, V) bytes, 256-byte aligned
   uint32_t* status;
+  uint32_t* sticky;
+  uint64_t wait_ns;
 };
 
 size_t linear_bwd_workspace(int64_t N, int64_t D, int64_t V);
+
+// Defined by the C layer (api.cu): the address of the library's device
+// status word on the current device (null if it cannot be had), the limit of
+// one protocol wait in the tensor-core kernels, and their CTA-group form.
+uint32_t* tc_sticky_status();
+// The device a call whose first input pointer is p launches on: p's device,
+// or the current device while `stream` is being captured (as every call of
+// the C layer chooses it); VLS_ERR_DEVICE when p is not device memory.
+int launch_device(const void* p, void* stream, int* dev);
+uint64_t tc_wait_ns();
+namespace tcg {
+int cta_group();
+}
 
 // Launchers: one per kernel family, dispatching on dtype and softcap.  They
 // return a cudaError_t of the launch.
