@@ -406,6 +406,42 @@ class ConfigRun:
                   ("k=256 logp bwd", bk["bwd"], lambda: B.vls_logp_bwd(x, w["idsk"], w["gk"], st, dlogits=d)),
                   ("entropy fwd", be["fwd"], lambda: B.vls_entropy_fwd(x, H=H, stats=st)),
                   ("entropy bwd", be["bwd"], lambda: B.vls_entropy_bwd(x, w["g_row"], H, st, dlogits=d))]
+
+            def peak_extra():
+                """Device memory the calls need beyond their inputs, the returned
+                gradient and the forward outputs: the saved per-row stats
+                (8 B per row) plus whatever the calls allocate, measured
+                through torch's allocator and through the device's free memory
+                (2 MiB granularity).  Also through the autograd API, where
+                the stats are saved by the function and the gradient and
+                outputs are allocated by it."""
+                import vocab_log_softmax_gb300 as Vl
+                launches = [f for _, _, f in L]
+                torch.cuda.synchronize()
+                torch.cuda.reset_peak_memory_stats()
+                base, free0 = torch.cuda.memory_allocated(), torch.cuda.mem_get_info()[0]
+                for f in launches:
+                    f()
+                torch.cuda.synchronize()
+                by_calls = torch.cuda.max_memory_allocated() - base
+                free_delta = max(0, free0 - torch.cuda.mem_get_info()[0])
+                leaf = x.detach().requires_grad_(True)
+                g1 = w["g1"].reshape(w["ids1"].shape)
+                torch.cuda.synchronize()
+                torch.cuda.reset_peak_memory_stats()
+                base = torch.cuda.memory_allocated()
+                out = Vl.logprobs(leaf, w["ids1"])
+                out.backward(g1)
+                torch.cuda.synchronize()
+                autograd_extra = (torch.cuda.max_memory_allocated() - base - leaf.grad.numel() * leaf.grad.element_size()
+                                  - out.numel() * out.element_size())
+                del out, leaf
+                stats_bytes = n * 8
+                return {"saved_stats_bytes": stats_bytes, "allocated_by_calls_bytes": by_calls,
+                        "device_free_delta_bytes": free_delta,
+                        "peak_extra_bytes": stats_bytes + max(by_calls, free_delta),
+                        "autograd_k1_peak_extra_bytes": autograd_extra, "limit_bytes": 1 << 20}
+            self.peak_extra = peak_extra
         elif name == "fused":
             # logprobs + entropy + reverse KL of one policy: fused calls vs the six separate calls
             w = workloads.kl_masked(device, n=N_ROWS, v=VOCAB)
@@ -471,6 +507,7 @@ class ConfigRun:
             raise SystemExit(f"unknown workload {name}")
         self.launches = L
         self.rows, self.vocab = n, v
+        self.small = name == "logp_small"   # 8 MB of inputs: inside L2
         if name == "fused":
             w = {"a": w["a"], "b": w["b"], "g": w["g"], "ids": wl["ids"], "gl": wl["g"]}
         self.autograd = self._autograd_thunks(name, w, device)
@@ -546,14 +583,35 @@ def run_config(args) -> None:
     """Per-config fwd / bwd times (median over steps) and TB/s for every op."""
     import torch
     device = torch.device("cuda", 0)
-    run = ConfigRun(args.workload, device, args.rows if args.workload == "linear_logp" and args.rows != N_ROWS else None)
-    for _ in range(args.warmup):
+    rows = args.rows if args.workload == "linear_logp" and args.rows != N_ROWS else None
+    print(json.dumps(measure_workload(args.workload, device, args.steps, args.warmup, rows)), flush=True)
+
+
+def l2_flusher(device):
+    """Writes a buffer twice the size of L2 (129 MB) between timed steps of a
+    workload small enough to stay in L2, so that each step starts cold."""
+    import torch
+    buf = torch.empty((64 << 20,), dtype=torch.float32, device=device)   # 256 MB
+    return lambda: buf.zero_()
+
+
+def measure_workload(name: str, device, steps: int, warmup: int, rows: int | None = None) -> dict:
+    """One workload's launches timed with CUDA events: per-op median ms,
+    TB/s and fraction of the measured copy bandwidth, fwd+bwd back to back,
+    the autograd API, and (C1) CUDA-graph replay.  Workloads smaller than L2
+    (C1) flush it between timed steps, outside the timed launches."""
+    import torch
+    run = ConfigRun(name, device, rows)
+    flush = l2_flusher(device) if run.small else None
+    for _ in range(warmup):
         for _, _, f, *_ in run.launches:
             f()
     torch.cuda.synchronize()
     stream = torch.cuda.current_stream(device)
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(run.launches) + 1)] for _ in range(args.steps)]
-    for s in range(args.steps):
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(run.launches) + 1)] for _ in range(steps)]
+    for s in range(steps):
+        if flush:
+            flush()
         for j, (_, _, f, *_) in enumerate(run.launches):
             ev[s][j].record(stream)
             f()
@@ -563,7 +621,7 @@ def run_config(args) -> None:
     tpeak, tkind = tensor_peak()
     ops = {}
     for j, (label, nbytes, _, *fl) in enumerate(run.launches):
-        ts = sorted(ev[s][j].elapsed_time(ev[s][j + 1]) for s in range(args.steps))
+        ts = sorted(ev[s][j].elapsed_time(ev[s][j + 1]) for s in range(steps))
         med = ts[len(ts) // 2]
         ops[label] = {"ms_median": round(med, 4), "ms_p10": round(ts[len(ts) // 10], 4),
                       "ms_p90": round(ts[(9 * len(ts)) // 10], 4), "tbs": round(nbytes / med / 1e9, 3),
@@ -582,39 +640,45 @@ def run_config(args) -> None:
     for j in range(len(run.launches) - 1):
         lf, lb = run.launches[j][0], run.launches[j + 1][0]
         if lf.endswith(" fwd") and lb == lf[:-4] + " bwd":
-            ts = sorted(ev[s][j].elapsed_time(ev[s][j + 2]) for s in range(args.steps))
+            ts = sorted(ev[s][j].elapsed_time(ev[s][j + 2]) for s in range(steps))
             nb = run.launches[j][1] + run.launches[j + 1][1]
             pairs[lf[:-4] + " fwd+bwd"] = {"ms_median": round(ts[len(ts) // 2], 4), "ms_p10": round(ts[len(ts) // 10], 4),
                                            "ms_p90": round(ts[(9 * len(ts)) // 10], 4),
                                            "tbs": round(nb / ts[len(ts) // 2] / 1e9, 3)}
     autograd = {}
     for label, nbytes, f, *fl in run.autograd:
-        ts = time_thunk(f, args.steps, args.warmup, stream)
+        ts = time_thunk(f, steps, warmup, stream, flush)
         med = ts[len(ts) // 2]
         autograd[label] = {"ms_median": round(med, 4), "ms_p10": round(ts[len(ts) // 10], 4),
                            "ms_p90": round(ts[(9 * len(ts)) // 10], 4), "tbs": round(nbytes / med / 1e9, 3)}
         if fl:
             autograd[label]["tflops"] = round(fl[0] / med / 1e9, 1)
-    graph = graph_replay(run, args.steps, stream) if run.name == "logp_small" else None
-    line = {"workload": run.name, "rows": run.rows, "vocab": run.vocab, "steps": args.steps,
+    graph = graph_replay(run, steps, stream, flush) if run.name == "logp_small" else None
+    line = {"workload": run.name, "rows": run.rows, "vocab": run.vocab, "steps": steps,
             "fwd_bwd_ms": round(total_ms, 4), "tbs": round(total_b / total_ms / 1e9, 3),
-            "peak_gbs": peak, "peak_kind": kind}
+            "peak_gbs": peak, "peak_kind": kind,
+            "l2": "flushed between timed steps (inputs fit in L2)" if flush else "inputs larger than L2; no flush"}
     if total_fl:   # a tensor-bound workload: its throughput against the bf16 peak
         line.update({"tflops": round(total_fl / total_ms / 1e9, 1),
                      "frac_of_bf16_peak": round(total_fl / total_ms / 1e9 / tpeak, 4), "bf16_peak_kind": tkind})
     line.update({"comparison_ops": sorted(run.compare), "ops": ops, "fwd_bwd_back_to_back": pairs,
                  "autograd": autograd, "graph_replay": graph})
-    print(json.dumps(line), flush=True)
+    if getattr(run, "peak_extra", None) is not None:
+        line["peak_extra_memory"] = run.peak_extra()
+    return line
 
 
-def time_thunk(f, steps: int, warmup: int, stream) -> list:
-    """Sorted CUDA-event times (ms) of f() over `steps` calls after `warmup`."""
+def time_thunk(f, steps: int, warmup: int, stream, flush=None) -> list:
+    """Sorted CUDA-event times (ms) of f() over `steps` calls after `warmup`
+    (flush(), if given, runs before each timed call, outside its events)."""
     import torch
     for _ in range(warmup):
         f()
     torch.cuda.synchronize()
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
     for a, b in ev:
+        if flush:
+            flush()
         a.record(stream)
         f()
         b.record(stream)
@@ -622,7 +686,7 @@ def time_thunk(f, steps: int, warmup: int, stream) -> list:
     return sorted(a.elapsed_time(b) for a, b in ev)
 
 
-def graph_replay(run, steps: int, stream) -> dict:
+def graph_replay(run, steps: int, stream, flush=None) -> dict:
     """The workload's launches captured once in a CUDA graph and replayed: the
     per-replay time without host launch overhead (for launch-bound sizes)."""
     import torch
@@ -641,7 +705,7 @@ def graph_replay(run, steps: int, stream) -> dict:
                 f()
     except RuntimeError as e:
         return {"unavailable": str(e).splitlines()[0][:200]}
-    ts = time_thunk(graph.replay, steps, 3, torch.cuda.current_stream())
+    ts = time_thunk(graph.replay, steps, 3, torch.cuda.current_stream(), flush)
     nb = sum(b for _, b, *_ in run.launches)
     med = ts[len(ts) // 2]
     return {"launches_per_replay": len(run.launches), "ms_median": round(med, 4), "ms_p10": round(ts[len(ts) // 10], 4),
@@ -730,6 +794,60 @@ def time_e2e(step: Step, steps: int, device, chunks: int = E2E_CHUNKS, copy_stre
 
 
 # ----------------------------------------------------------------------------
+# the five configurations, each on its own (reported beside the headline step)
+# ----------------------------------------------------------------------------
+
+CONFIGS = [
+    ("C1", "logp_small", "logprobs k=1, 64 x 32000 fp32 (launch-bound: CUDA-graph replay reported too)"),
+    ("C2", "logp_offset", "logprobs k=1, 8192 x 151936 bf16, offset rows, ignored and out-of-range targets"),
+    ("C3", "kl_masked", "entropy, forward KL and reverse KL, 8192 x 75968 bf16, masked columns, mismatch rows"),
+    ("C4", "softcap_wide", "softcap-fused logprobs at caps 30 and 20, and the standalone softcap, 4096 x 262144 bf16"),
+    ("C5", "long_seq", "logprobs k=1 and k=256, entropy, 32768 x 151936 bf16; peak extra device memory"),
+]
+
+
+def config_summary(line: dict) -> dict:
+    """The compact per-config record of the bench line: per op its forward
+    and backward median ms, TB/s and fraction of the measured copy
+    bandwidth, and the config's fwd+bwd totals."""
+    peak = line["peak_gbs"]
+    ops = {}
+    for label, v in line["ops"].items():
+        if label in line["comparison_ops"]:
+            continue
+        op, ps = label.rsplit(" ", 1)
+        e = ops.setdefault(op, {})
+        e[f"{ps}_ms"] = v["ms_median"]
+        e[f"{ps}_tbs"] = v["tbs"]
+        e[f"{ps}_frac"] = v["frac_of_measured"]
+    for op, e in ops.items():
+        if "fwd_ms" in e and "bwd_ms" in e:
+            b = line["ops"][op + " fwd"]["bytes"] + line["ops"][op + " bwd"]["bytes"]
+            ms = e["fwd_ms"] + e["bwd_ms"]
+            e.update({"fwd_bwd_ms": round(ms, 4), "fwd_bwd_tbs": round(b / ms / 1e9, 3),
+                      "fwd_bwd_frac": round(b / ms / 1e6 / peak, 4)})
+    out = {"workload": line["workload"], "rows": line["rows"], "vocab": line["vocab"], "steps": line["steps"],
+           "fwd_bwd_ms": line["fwd_bwd_ms"], "tbs": line["tbs"], "frac_of_measured": round(line["tbs"] * 1e3 / peak, 4),
+           "l2": line["l2"], "ops": ops}
+    if line.get("graph_replay"):
+        out["graph_replay"] = {k: line["graph_replay"][k] for k in ("ms_median", "tbs") if k in line["graph_replay"]}
+    if line.get("peak_extra_memory"):
+        out["peak_extra_memory"] = line["peak_extra_memory"]
+    return out
+
+
+def measure_configs(device, steps: int, warmup: int) -> dict:
+    import torch
+    res = {}
+    for key, name, what in CONFIGS:
+        line = measure_workload(name, device, steps, warmup)
+        res[key] = {"what": what, **config_summary(line)}
+        torch.cuda.synchronize()
+        torch.cuda.empty_cache()
+    return res
+
+
+# ----------------------------------------------------------------------------
 # CPU oracle (baseline arm)
 # ----------------------------------------------------------------------------
 
@@ -768,19 +886,74 @@ def host_rows(inp: dict, lo: int, hi: int) -> dict:
     return out
 
 
-def cpu_baseline(inp: dict, n: int, v: int, budget_s: float = 15.0) -> dict:
-    """The oracle, as it stands, on a bounded sample of rows of the workload."""
-    probe = host_rows(inp, 0, 2)
+def host_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:  # pragma: no cover
+        return os.cpu_count() or 1
+
+
+_BARRIER = None
+
+
+def _oracle_init(barrier) -> None:
+    global _BARRIER
+    _BARRIER = barrier
+    for var in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+        os.environ[var] = "1"
+
+
+def _oracle_worker(job: tuple) -> tuple:
+    """One process of the oracle pool: builds its own block of rows of the
+    workload on the CPU (same recipe, its own seed), waits for the others,
+    then runs the whole path on it `warmup + steps` times; returns the
+    start and end of the timed steps on the system-wide monotonic clock."""
+    rows, v, worker, steps, warmup = job
+    import workloads
+    inp = host_rows(_cpu_inputs(workloads, rows, v, seed_offset=100 * (worker + 1)), 0, rows)
+    _BARRIER.wait()
+    for _ in range(warmup):
+        oracle_step(inp)
+    _BARRIER.wait()
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        oracle_step(inp)
+    return t0, time.perf_counter()
+
+
+def oracle_pool(rows_per_worker: int, v: int, steps: int, warmup: int, workers: int) -> float:
+    """Seconds per step of the oracle over `workers` processes, each on its
+    own block of rows: the wall time from the first worker's start to the
+    last worker's end.  Processes are spawned (never forked after CUDA)."""
+    import multiprocessing as mp
+    ctx = mp.get_context("spawn")
+    barrier = ctx.Barrier(workers)
+    with ctx.Pool(workers, initializer=_oracle_init, initargs=(barrier,)) as pool:
+        spans = pool.map(_oracle_worker, [(rows_per_worker, v, w, steps, warmup) for w in range(workers)])
+    return (max(t1 for _, t1 in spans) - min(t0 for t0, _ in spans)) / steps
+
+
+def _oracle_row_seconds(v: int) -> float:
+    """Seconds of one row of the whole path on the oracle, on this core."""
+    import workloads
+    probe = host_rows(_cpu_inputs(workloads, 2, v), 0, 2)
+    oracle_step(probe)
     t0 = time.perf_counter()
     oracle_step(probe)
-    per_row = (time.perf_counter() - t0) / 2
-    s = int(max(2, min(n, budget_s / max(per_row, 1e-6))))
-    rows = host_rows(inp, 0, s)
-    t0 = time.perf_counter()
-    oracle_step(rows)
-    dt = time.perf_counter() - t0
-    return {"value": round(step_bytes(s, v) / dt / 1e12, 6), "unit": "TB/s", "cores": 1, "kind": "oracle",
-            "sample": f"first {s} of {n} rows of every input tensor, full V={v}; one numpy process",
+    return (time.perf_counter() - t0) / 2
+
+
+def cpu_baseline(n: int, v: int, budget_s: float = 8.0) -> dict:
+    """The oracle, as it stands, on every host core: one process per core,
+    each on its own block of rows of the workload (about budget_s seconds of
+    work each)."""
+    cores = host_cores()
+    rows = int(max(2, min(n, budget_s / max(_oracle_row_seconds(v), 1e-6))))
+    dt = oracle_pool(rows, v, 1, 0, cores)
+    total = rows * cores
+    return {"value": round(step_bytes(total, v) / dt / 1e12, 6), "unit": "TB/s", "cores": cores, "kind": "oracle",
+            "sample": f"{cores} processes x {rows} rows of the workload's recipe (each its own seeded block), "
+                      f"full V={v}; the whole path once; numpy fp64",
             "seconds": round(dt, 2)}
 
 
@@ -788,40 +961,31 @@ def run_reference(args) -> None:
     rank, world, _ = dist_env()
     if rank != 0:
         return
-    import workloads
     n, v = args.rows, VOCAB
-    budget = 150.0
-    probe_inp = _cpu_inputs(workloads, 2, v)
-    rows = host_rows(probe_inp, 0, 2)
-    t0 = time.perf_counter()
-    oracle_step(rows)
-    per_row = (time.perf_counter() - t0) / 2
-    s = int(max(1, min(n, budget / (args.steps + args.warmup) / max(per_row, 1e-6))))
-    rows = host_rows(_cpu_inputs(workloads, s, v), 0, s)
-    for _ in range(args.warmup):
-        oracle_step(rows)
-    t0 = time.perf_counter()
-    for _ in range(args.steps):
-        oracle_step(rows)
-    dt = (time.perf_counter() - t0) / args.steps
+    cores = host_cores()
+    budget = 150.0           # seconds of the whole run, all steps
+    per_row = _oracle_row_seconds(v)
+    rows = int(max(1, min(n, budget / (args.steps + args.warmup) / max(per_row, 1e-6))))
+    dt = oracle_pool(rows, v, args.steps, args.warmup, cores)
+    s = rows * cores
     value = step_bytes(s, v) / dt / 1e12
     line = {
         "impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": "TB/s", "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt * 1e3, 3),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": WORKLOAD, "rows_per_step": s, "rows_in_workload": n, "vocab": v,
-                   "sample": f"{s} rows per step (bounded sample of the {n}-row batch)"},
-        "cpu_baseline": {"value": round(value, 6), "unit": "TB/s", "cores": 1, "kind": "oracle",
-                         "sample": f"{s} of {n} rows per step, full V={v}"},
+                   "sample": f"{cores} processes x {rows} rows per step (bounded sample of the {n}-row batch)"},
+        "cpu_baseline": {"value": round(value, 6), "unit": "TB/s", "cores": cores, "kind": "oracle",
+                         "sample": f"{cores} processes x {rows} of {n} rows per step, full V={v}"},
         "e2e": {"value": round(value, 6), "unit": "TB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
 
 
-def _cpu_inputs(workloads, n: int, v: int) -> dict:
-    c2 = workloads.logp_offset("cpu", n=n, v=v)
-    c3 = workloads.kl_masked("cpu", n=max(n, 2), v=v)
-    c4 = workloads.softcap_wide("cpu", n=n, v=v)
+def _cpu_inputs(workloads, n: int, v: int, seed_offset: int = 0) -> dict:
+    c2 = workloads.logp_offset("cpu", n=n, v=v, seed=1 + seed_offset)
+    c3 = workloads.kl_masked("cpu", n=max(n, 2), v=v, seed=2 + seed_offset)
+    c4 = workloads.softcap_wide("cpu", n=n, v=v, seed=3 + seed_offset)
     return {"x": c2["logits"], "ids": c2["ids"], "g": c2["g"], "a": c3["a"][:n], "b": c3["b"][:n],
             "g_row": c3["g"][:n], "xc": c4["logits"], "ids_c": c4["ids"], "g_c": c4["g"], "gy": c4["gy_bf16"]}
 
@@ -842,6 +1006,9 @@ def main() -> None:
     ap.add_argument("--e2e-copy-streams", type=int, default=E2E_COPY_STREAMS,
                     help="copy streams per direction in the host-buffer pipeline")
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timing leg")
+    ap.add_argument("--no-configs", action="store_true", help="skip the per-config block (C1-C5)")
+    ap.add_argument("--config-steps", type=int, default=20, help="timed steps per config in the per-config block")
+    ap.add_argument("--config-warmup", type=int, default=3, help="warm-up steps per config (at least 3)")
     ap.add_argument("--workload", default="step",
                     choices=["step", "logp_small", "logp_offset", "kl_masked", "softcap_wide", "long_seq", "fused",
                              "linear_logp"],
@@ -870,6 +1037,7 @@ def main() -> None:
     step = Step(device, n, v, seed_offset=rank * 10)
     torch.cuda.synchronize()
 
+    launches_per_step = len(step.launches())
     total_ms, per, clk = time_device(step, args.steps, args.warmup, device)
     total_ms = max_over_ranks(total_ms, device)
     ms = total_ms / args.steps
@@ -907,7 +1075,14 @@ def main() -> None:
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        cpu = cpu_baseline(step.inp, n, v)
+        cpu = cpu_baseline(n, v)
+
+    configs = None
+    if not args.no_configs:
+        del step
+        torch.cuda.synchronize()
+        torch.cuda.empty_cache()
+        configs = measure_configs(device, args.config_steps, max(3, args.config_warmup))
 
     if rank == 0:
         line = {
@@ -921,8 +1096,9 @@ def main() -> None:
             "roofline": roofline,
             "cpu_baseline": cpu,
             "e2e": e2e,
-            "gpu_launches": len(step.launches()) * args.steps,
+            "gpu_launches": launches_per_step * args.steps,
             "clocks": clk,
+            "configs": configs,
         }
         print(json.dumps(line), flush=True)
     if world > 1:

@@ -60,3 +60,23 @@ def test_max_over_ranks_gloo():
 def test_single_process_helpers():
     assert bench.max_over_ranks(3.5) == 3.5
     assert bench.dist_env()[1] >= 1
+
+
+def test_config_summary_groups_forward_and_backward():
+    """The per-config block: each op's forward and backward, its fwd+bwd
+    throughput from the two launches' bytes, comparison launches left out."""
+    peak = 6000.0
+    line = {"workload": "x", "rows": 8, "vocab": 10, "steps": 3, "fwd_bwd_ms": 3.0, "tbs": 2.0, "peak_gbs": peak,
+            "l2": "no flush", "comparison_ops": ["other fwd"],
+            "ops": {"a fwd": {"ms_median": 1.0, "tbs": 1.0, "frac_of_measured": 1.0 / 6, "bytes": 1e9},
+                    "a bwd": {"ms_median": 2.0, "tbs": 1.5, "frac_of_measured": 0.25, "bytes": 3e9},
+                    "other fwd": {"ms_median": 9.0, "tbs": 0.1, "frac_of_measured": 0.0, "bytes": 1e9}},
+            "fwd_bwd_back_to_back": {}, "autograd": {}, "graph_replay": {"ms_median": 0.5, "tbs": 8.0}}
+    out = bench.config_summary(line)
+    assert set(out["ops"]) == {"a"}
+    a = out["ops"]["a"]
+    assert a["fwd_ms"] == 1.0 and a["bwd_ms"] == 2.0 and a["fwd_bwd_ms"] == 3.0
+    assert abs(a["fwd_bwd_tbs"] - 4e9 / 3.0 / 1e9) < 1e-3 and abs(a["fwd_bwd_frac"] - 4e9 / 3.0 / 1e6 / peak) < 1e-3
+    assert out["graph_replay"] == {"ms_median": 0.5, "tbs": 8.0}
+    assert abs(out["frac_of_measured"] - 2.0 * 1e3 / peak) < 1e-4
+    assert [k for k, *_ in bench.CONFIGS] == ["C1", "C2", "C3", "C4", "C5"]
