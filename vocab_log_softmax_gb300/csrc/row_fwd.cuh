@@ -47,17 +47,28 @@ struct LogpAcc {
   // nm2: -m, or with a cap b2 = (c - m) log2(e) (cap_d2_pair)
   fp2 nm2 = 0, s2 = 0;
 
+  // wa: with a cap, the warp's raw max over this vector's group (warp_max)
   template <bool PARTIAL>
-  __device__ __forceinline__ void update(const Raw8<T>& v, const Raw8<T>&, int valid, const CapK& K) {
-    const float vm = v.max();
-    if (grows<CAP>(vm, m_raw, m)) {
-      const float mn = CAP ? cap_zr(vm, K) : vm;
-      s2 = mul2(s2, splat(rescale(m, mn)));
-      m_raw = vm;
-      m = mn;
-      nm2 = splat(CAP ? cap_b2(mn, K) : -mn);
+  __device__ __forceinline__ void update(const Raw8<T>& v, const Raw8<T>&, int valid, const CapK& K, float wa = 0.0f,
+                                         float = 0.0f) {
+    if constexpr (CAP) {
+      if (grows<CAP>(wa, m_raw, m)) {   // the same decision in every lane of the warp
+        const float mn = cap_zr_rare(wa, K);
+        s2 = mul2(s2, splat(rescale_rare(m, mn)));
+        m_raw = wa;
+        m = mn;
+        nm2 = splat(cap_b2(mn, K));
+      }
+    } else {
+      const float vm = v.max();
+      if (grows<CAP>(vm, m_raw, m)) {
+        s2 = mul2(s2, splat(rescale(m, vm)));
+        m_raw = vm;
+        m = vm;
+        nm2 = splat(-vm);
+      }
+      if (m == neg_inf()) return;
     }
-    if (!CAP && m == neg_inf()) return;
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       const fp2 d2 = CAP ? cap_d2_pair<T>(v, i, K, nm2) : mul2(add2(v.pair(i), nm2), splat(kLog2e));
@@ -76,11 +87,12 @@ struct EntropyAcc {
   fp2 nm2 = 0, s2 = 0, w2 = 0;
 
   template <bool PARTIAL>
-  __device__ __forceinline__ void update(const Raw8<T>& v, const Raw8<T>&, int valid, const CapK& K) {
-    const float vm = v.max();
+  __device__ __forceinline__ void update(const Raw8<T>& v, const Raw8<T>&, int valid, const CapK& K, float wa = 0.0f,
+                                         float = 0.0f) {
+    const float vm = CAP ? wa : v.max();   // with a cap, the warp's max: the same decision in every lane
     if (grows<CAP>(vm, m_raw, m)) {
-      const float mn = CAP ? cap_zr(vm, K) : vm;
-      const float f = rescale(m, mn);
+      const float mn = CAP ? cap_zr_rare(vm, K) : vm;
+      const float f = CAP ? rescale_rare(m, mn) : rescale(m, mn);
       const float shift = CAP ? (m - mn) * kLog2e : m - mn;
       w2 = m != neg_inf() ? mul2(fma2(s2, splat(shift), w2), splat(f)) : 0;
       s2 = mul2(s2, splat(f));
@@ -115,14 +127,17 @@ struct KlAcc {
   fp2 nmp2 = 0, nmq2 = 0, sp2 = 0, sq2 = 0, w2 = 0;
   uint32_t flag = 0;
 
+  // wp, wq: with a cap, the warp's raw maxima over this vector's group of P and of Q
   template <bool PARTIAL>
-  __device__ __forceinline__ void update(const Raw8<T>& v, const Raw8<T>& q, int valid, const CapK& K) {
-    const float vmp = v.max(), vmq = q.max();
+  __device__ __forceinline__ void update(const Raw8<T>& v, const Raw8<T>& q, int valid, const CapK& K,
+                                         float wp = 0.0f, float wq = 0.0f) {
+    // with a cap, the warp's maxima: the same decisions in every lane
+    const float vmp = CAP ? wp : v.max(), vmq = CAP ? wq : q.max();
     const bool up = grows<CAP>(vmp, mp_raw, mp), uq = grows<CAP>(vmq, mq_raw, mq);
     if (up || uq) {
-      const float Mp = up ? (CAP ? cap_zr(vmp, K) : vmp) : mp;
-      const float Mq = uq ? (CAP ? cap_zr(vmq, K) : vmq) : mq;
-      const float fp = rescale(mp, Mp), fq = rescale(mq, Mq);
+      const float Mp = up ? (CAP ? cap_zr_rare(vmp, K) : vmp) : mp;
+      const float Mq = uq ? (CAP ? cap_zr_rare(vmq, K) : vmq) : mq;
+      const float fp = CAP ? rescale_rare(mp, Mp) : rescale(mp, Mp), fq = CAP ? rescale_rare(mq, Mq) : rescale(mq, Mq);
       const float shift = CAP ? ((mp - Mp) - (mq - Mq)) * kLog2e : (mp - Mp) - (mq - Mq);
       w2 = mp != neg_inf() ? mul2(fma2(sp2, splat(shift), w2), splat(fp)) : 0;
       sp2 = mul2(sp2, splat(fp));
@@ -179,20 +194,22 @@ struct FusedAcc {
   fp2 nma2 = 0, nmb2 = 0, sa2 = 0, wh2 = 0, sb2 = 0, wk2 = 0;
   uint32_t flag = 0;
 
+  // wa, wb: with a cap, the warp's raw maxima over this vector's group of a and of b
   template <bool PARTIAL>
-  __device__ __forceinline__ void update(const Raw8<T>& v, const Raw8<T>& q, int valid, const CapK& K) {
-    const float vma = v.max();
+  __device__ __forceinline__ void update(const Raw8<T>& v, const Raw8<T>& q, int valid, const CapK& K,
+                                         float wa = 0.0f, float wb = 0.0f) {
+    const float vma = CAP ? wa : v.max();   // with a cap, the warp's max: the same decisions in every lane
     const bool ua = grows<CAP>(vma, ma_raw, ma);
     float vmb = neg_inf();
     bool ub = false;
     if constexpr (kHasB) {
-      vmb = q.max();
+      vmb = CAP ? wb : q.max();
       ub = grows<CAP>(vmb, mb_raw, mb);
     }
     if (ua || ub) {
-      const float Ma = ua ? (CAP ? cap_zr(vma, K) : vma) : ma;
-      const float Mb = ub ? (CAP ? cap_zr(vmb, K) : vmb) : mb;
-      const float fa = rescale(ma, Ma), fb = rescale(mb, Mb);
+      const float Ma = ua ? (CAP ? cap_zr_rare(vma, K) : vma) : ma;
+      const float Mb = ub ? (CAP ? cap_zr_rare(vmb, K) : vmb) : mb;
+      const float fa = CAP ? rescale_rare(ma, Ma) : rescale(ma, Ma), fb = CAP ? rescale_rare(mb, Mb) : rescale(mb, Mb);
       const float u = CAP ? kLog2e : 1.0f;   // units of W: log2 with a cap
       wh2 = ma != neg_inf() ? mul2(fma2(sa2, splat(CAP ? (ma - Ma) * kLog2e : ma - Ma), wh2), splat(fa)) : 0;
       if constexpr (DIR == kFusedKlReverse)
@@ -285,6 +302,12 @@ template <int OP, int DIR, bool CAP>
 #define VLS_CAP_LOGP_CTAS 5
 #endif
 constexpr int fwd_unroll() { return reads_two<OP, DIR>() ? 2 : ((CAP && OP == kFwdLogp) ? VLS_CAP_LOGP_UNROLL : 4); }
+
+// Vectors per lane over which the softcapped sweeps take one warp max.
+#ifndef VLS_CAP_MAX_GROUP
+#define VLS_CAP_MAX_GROUP 2
+#endif
+constexpr int kCapMaxGroup = VLS_CAP_MAX_GROUP;
 
 // Resident CTAs per SM the forward sweep is compiled for, at 256 threads.
 // Without an explicit minimum, ptxas sized these kernels by heuristics that
@@ -379,29 +402,85 @@ __global__ void __launch_bounds__(kFwdThreads, (fwd_min_blocks<T, OP, CAP, DIR>(
 
   Acc acc;
   int64_t v = vb + threadIdx.x;
-  if (al) {
-    for (; v + (U - 1) * kFwdThreads < vfull_end; v += U * kFwdThreads) {
-      Raw8<T> rx[U], ry[U];
+  if constexpr (!CAP) {
+    if (al) {
+      for (; v + (U - 1) * kFwdThreads < vfull_end; v += U * kFwdThreads) {
+        Raw8<T> rx[U], ry[U];
 #pragma unroll
-      for (int u = 0; u < U; ++u) {
-        rx[u].load(xr + 8 * (v + u * kFwdThreads));
-        if constexpr (KL) ry[u].load(yr + 8 * (v + u * kFwdThreads));
+        for (int u = 0; u < U; ++u) {
+          rx[u].load(xr + 8 * (v + u * kFwdThreads));
+          if constexpr (KL) ry[u].load(yr + 8 * (v + u * kFwdThreads));
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) acc.template update<false>(rx[u], KL ? ry[u] : rx[u], 8, K);
       }
-#pragma unroll
-      for (int u = 0; u < U; ++u) acc.template update<false>(rx[u], KL ? ry[u] : rx[u], 8, K);
     }
-  }
-  // remaining vectors, the partial last vector and unaligned rows: same
-  // vectors, same order, same arithmetic
-  for (; v < ve; v += kFwdThreads) {
-    Raw8<T> rx, ry;
-    int valid;
-    load_raw(rx, xr, v, V, al, valid);
-    if constexpr (KL) load_raw(ry, yr, v, V, al, valid);
-    if (valid == 8)
-      acc.template update<false>(rx, KL ? ry : rx, 8, K);
-    else
-      acc.template update<true>(rx, KL ? ry : rx, valid, K);
+    // remaining vectors, the partial last vector and unaligned rows: same
+    // vectors, same order, same arithmetic
+    for (; v < ve; v += kFwdThreads) {
+      Raw8<T> rx, ry;
+      int valid;
+      load_raw(rx, xr, v, V, al, valid);
+      if constexpr (KL) load_raw(ry, yr, v, V, al, valid);
+      if (valid == 8)
+        acc.template update<false>(rx, KL ? ry : rx, 8, K);
+      else
+        acc.template update<true>(rx, KL ? ry : rx, valid, K);
+    }
+  } else {
+    // With a cap every lane of a warp runs the same iterations: the running
+    // max is taken over the warp (warp_max), once per group of
+    // kCapMaxGroup vectors of each lane (v, v + T, ...).  A lane past the end
+    // of its run sees vectors of -inf with no valid column, which leave its
+    // sums unchanged.  Batches (U a multiple of the group) and the tail
+    // loop form the same groups, so aligned and unaligned rows get the same
+    // bits.
+    constexpr int G = kCapMaxGroup;
+    static_assert(U % G == 0, "batches hold whole groups");
+    const int lane = threadIdx.x & 31;
+    if (al) {
+      // whole batches for every lane of the warp (its last lane decides)
+      for (; v - lane + 31 + (U - 1) * kFwdThreads < vfull_end; v += U * kFwdThreads) {
+        Raw8<T> rx[U], ry[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+          rx[u].load(xr + 8 * (v + u * kFwdThreads));
+          if constexpr (KL) ry[u].load(yr + 8 * (v + u * kFwdThreads));
+        }
+#pragma unroll
+        for (int g = 0; g < U; g += G) {
+          const float wa = warp_max(group_max<T, G>(rx + g));
+          const float wb = KL ? warp_max(group_max<T, G>(ry + g)) : 0.0f;
+#pragma unroll
+          for (int u = 0; u < G; ++u) acc.template update<false>(rx[g + u], KL ? ry[g + u] : rx[g + u], 8, K, wa, wb);
+        }
+      }
+    }
+    for (; v - lane < ve; v += G * kFwdThreads) {
+      Raw8<T> rx[G], ry[G];
+      int valid[G];
+#pragma unroll
+      for (int u = 0; u < G; ++u) {
+        const int64_t vu = v + u * kFwdThreads;
+        valid[u] = 0;
+        if (vu < ve) {
+          load_raw(rx[u], xr, vu, V, al, valid[u]);
+          if constexpr (KL) load_raw(ry[u], yr, vu, V, al, valid[u]);
+        } else {   // no vector here: -inf, which adds nothing
+          rx[u].load_scalar(xr, 0);
+          if constexpr (KL) ry[u].load_scalar(yr, 0);
+        }
+      }
+      const float wa = warp_max(group_max<T, G>(rx));
+      const float wb = KL ? warp_max(group_max<T, G>(ry)) : 0.0f;
+#pragma unroll
+      for (int u = 0; u < G; ++u) {
+        if (valid[u] == 8)
+          acc.template update<false>(rx[u], KL ? ry[u] : rx[u], 8, K, wa, wb);
+        else
+          acc.template update<true>(rx[u], KL ? ry[u] : rx[u], valid[u], K, wa, wb);
+      }
+    }
   }
 
   // ---- fixed-tree reduction: lanes, warps, cluster ranks ----

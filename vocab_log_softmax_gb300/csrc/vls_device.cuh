@@ -4,6 +4,7 @@
 #pragma once
 
 #include <cstdint>
+#include <type_traits>
 
 #include <cooperative_groups.h>
 #include <cuda_bf16.h>
@@ -321,10 +322,18 @@ struct CapK {
   float k;     // -2 log2(e) / c: exp(-2|x|/c) = 2^(|x| k)
   float k2;    // 2 log2(e) / c: exp(2x/c) = 2^(x k2)
   float a2;    // -2 c log2(e)
+  // the largest x with x k2 <= 64 (so that exp(2x/c) <= 2^64), rounded down
+  // to each input type: fp32, and packed pairs of bfloat16 and of float16
+  float xmax;
+  uint32_t xmax_bf16x2, xmax_f16x2;
 };
 
 __device__ __forceinline__ CapK cap_consts(float cap) {
-  return {cap, -2.0f * kLog2e / cap, 2.0f * kLog2e / cap, -2.0f * cap * kLog2e};
+  const float k2 = 2.0f * kLog2e / cap;
+  const float xm = __fdiv_rd(64.0f, k2);
+  const uint32_t b = __float_as_uint(xm) >> 16;                       // positive: truncation rounds down
+  const uint32_t h = __half_as_ushort(__float2half_rd(xm));           // saturates at the largest finite half
+  return {cap, -2.0f * kLog2e / cap, k2, -2.0f * cap * kLog2e, xm, b | (b << 16), h | (h << 16)};
 }
 
 // tanh(x/c) and e = exp(-2|x|/c), r = 1/(1+e) for the slope.
@@ -339,27 +348,11 @@ __device__ __forceinline__ float cap_t(float x, const CapK& K) {
   return cap_t(x, K, e, r);
 }
 
-// 1/d for d in [1, 2] on the FMA pipe instead of the special-function unit:
-// the minimax quadratic 70/33 - (48/33) d + (32/99) d^2 (relative error at
-// most 1/99 on [1, 2], equioscillating at four points) refined by two
-// Newton-Raphson steps r <- r + r (1 - d r), each of which squares the
-// relative error (about 1e-8 after two, within about one fp32 ulp).
-__device__ __forceinline__ fp2 rcp2_fma(fp2 d) {
-  fp2 r = fma2(fma2(d, splat(32.0f / 99.0f), splat(-48.0f / 33.0f)), d, splat(70.0f / 33.0f));
-  const fp2 nd = mul2(d, splat(-1.0f));
-  r = fma2(r, fma2(nd, r, splat(1.0f)), r);
-  return fma2(r, fma2(nd, r, splat(1.0f)), r);
-}
-
-// Packed form of cap_t for pair i of a raw vector (same operations).  With
-// FMA_RCP the reciprocal 1/(1+e) is taken on the FMA pipe (rcp2_fma): the
-// softcapped forward sweeps do this for every other pair, so that the
-// special-function unit, their bound, carries 2.5 instead of 3 operations
-// per element.
-template <class T, bool FMA_RCP = false>
+// Packed form of cap_t for pair i of a raw vector (same operations).
+template <class T>
 __device__ __forceinline__ fp2 cap_t2(const Raw8<T>& v, int i, const CapK& K, fp2& e2, fp2& r2) {
   e2 = ex2_2(mul2(v.pair_abs(i), splat(K.k)));
-  r2 = FMA_RCP ? rcp2_fma(add2(e2, splat(1.0f))) : rcp2(add2(e2, splat(1.0f)));
+  r2 = rcp2(add2(e2, splat(1.0f)));
   float t0, t1;
   upk(mul2(sub2(splat(1.0f), e2), r2), t0, t1);
   t0 = __uint_as_float(__float_as_uint(t0) | (v.sign_lo(i) & 0x80000000u));
@@ -385,38 +378,85 @@ __device__ __forceinline__ float cap_d(float t, float c, float m) { return fmaf(
 constexpr float kLn2 = 0.69314718055994531f;
 
 // Pairs (of the four in an 8-column vector) whose reciprocal 1/(1 + E) runs
-// on the FMA pipe (rcp2_fma_wide) instead of the special-function unit,
+// on the FMA pipe (rcp2_fma_neg) instead of the special-function unit,
 // which bounds the softcapped sweeps: bit i set for pair i.  A function of
 // the column alone, so every sweep gets the same bits for the same column.
 #ifndef VLS_CAP_FMA_PAIRS
-#define VLS_CAP_FMA_PAIRS 0xA
+#define VLS_CAP_FMA_PAIRS 0xB
 #endif
 constexpr uint32_t kCapFmaPairs = VLS_CAP_FMA_PAIRS;
 
-// 1/d for d >= 1 (or +inf) on the FMA pipe: d = 2^e f with f in [1, 2) taken
-// from the exponent field, 1/f from rcp2_fma's quadratic seed and two
-// Newton-Raphson steps (written in -f), and 2^-e put back by subtracting e
-// from the result's exponent field.  d is first limited to 2^64 by an
-// integer min on the bit pattern (which orders positive floats), so that
-// field never underflows; a reciprocal below 2^-64 then reads as 2^-64,
-// which only ever adds a term far below one ulp of c.
-__device__ __forceinline__ fp2 rcp2_fma_wide(fp2 d) {
-  float d0, d1;
-  upk(d, d0, d1);
-  const uint32_t b0 = min(__float_as_uint(d0), 0x5f800000u), b1 = min(__float_as_uint(d1), 0x5f800000u);
-  const fp2 nf = pk(__uint_as_float((b0 & 0x007fffffu) | 0xbf800000u), __uint_as_float((b1 & 0x007fffffu) | 0xbf800000u));
-  fp2 r = fma2(fma2(nf, splat(32.0f / 99.0f), splat(48.0f / 33.0f)), nf, splat(70.0f / 33.0f));
-  r = fma2(r, fma2(nf, r, splat(1.0f)), r);
-  r = fma2(r, fma2(nf, r, splat(1.0f)), r);
-  float r0, r1;
-  upk(r, r0, r1);
-  r0 = __uint_as_float(__float_as_uint(r0) - (b0 & 0x7f800000u) + 0x3f800000u);
-  r1 = __uint_as_float(__float_as_uint(r1) - (b1 & 0x7f800000u) + 0x3f800000u);
-  return pk(r0, r1);
+// -1/(-nd) = 1/d for d in [1, 2^70] on the FMA pipe, from nd = -d: a seed
+// from the bit pattern (0x7EF311C2 - bits(d), written 0xFEF311C2 - bits(nd);
+// the constant fitted here to a relative error of at most 5.1% on that
+// range), one third-order step r (1 + e + e^2) and one Newton-Raphson step
+// r (1 + e), e = 1 - d r: each step multiplies the error's order, to within
+// one fp32 ulp (0.77 ulp at most, checked on [1, 2^70]).
+__device__ __forceinline__ fp2 rcp2_fma_neg(fp2 nd) {
+  float a, b;
+  upk(nd, a, b);
+  fp2 r = pk(__uint_as_float(0xFEF311C2u - __float_as_uint(a)), __uint_as_float(0xFEF311C2u - __float_as_uint(b)));
+  fp2 e = fma2(nd, r, splat(1.0f));
+  r = fma2(r, fma2(e, e, e), r);
+  e = fma2(nd, r, splat(1.0f));
+  return fma2(r, e, r);
+}
+
+// Max over G vectors: one packed max tree over their words and one unpack
+// for 16-bit types (the same value as the max of the vectors' maxima).
+template <class T, int G>
+__device__ __forceinline__ float group_max(const Raw8<T>* v) {
+  if constexpr (sizeof(T) == 4) {
+    float m = v[0].max();
+#pragma unroll
+    for (int u = 1; u < G; ++u) m = fmaxf(m, v[u].max());
+    return m;
+  } else {
+    constexpr bool kBf16 = std::is_same<T, __nv_bfloat16>::value;
+    auto mx2 = [](uint32_t a, uint32_t b) { return kBf16 ? bmax2(a, b) : hmax2(a, b); };
+    uint32_t m = mx2(mx2(v[0].w[0], v[0].w[1]), mx2(v[0].w[2], v[0].w[3]));
+#pragma unroll
+    for (int u = 1; u < G; ++u) m = mx2(m, mx2(mx2(v[u].w[0], v[u].w[1]), mx2(v[u].w[2], v[u].w[3])));
+    if constexpr (kBf16) return fmaxf(__uint_as_float(m << 16), __uint_as_float(m & 0xffff0000u));
+    else return fmaxf(h2f(m & 0xffffu), h2f(m >> 16));
+  }
+}
+
+// The running max of the softcapped sweeps is taken over the 32 lanes of a
+// warp (redux.sync.max.f32, sm_100 family), so that every lane sees the same
+// running max.  Its growth, which costs three special-function operations
+// (the cap of the new max and the rescale of the sums), is then a
+// warp-uniform event, rare after the first vectors, instead of one that some
+// lane of the warp meets at almost every vector.  A lane without a vector
+// contributes -inf.
+__device__ __forceinline__ float warp_max(float x) {
+  float r;
+  asm volatile("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(r) : "f"(x));
+  return r;
 }
 
 // r = 1/(1 + exp(2x/c)) of one logit.
 __device__ __forceinline__ float cap_r(float x, const CapK& K) { return rcp(1.0f + ex2(x * K.k2)); }
+
+// The same special-function operations as volatile asm, for the rare growth
+// step of a warp's running max: the compiler may not evaluate them
+// speculatively ahead of the (warp-uniform) branch, where they would occupy
+// the special-function unit at every group of vectors instead of only when
+// the max grows.
+__device__ __forceinline__ float ex2_rare(float x) {
+  float y;
+  asm volatile("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+__device__ __forceinline__ float rcp_rare(float x) {
+  float y;
+  asm volatile("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+// cap_zr and rescale for that step (same operations, same bits)
+__device__ __forceinline__ float cap_zr_rare(float x, const CapK& K) {
+  return fmaf(rcp_rare(1.0f + ex2_rare(x * K.k2)), -2.0f * K.c, K.c);
+}
 // The softcapped value c - 2c r of one logit (the row max of a sweep).
 __device__ __forceinline__ float cap_zr(float x, const CapK& K) { return fmaf(cap_r(x, K), -2.0f * K.c, K.c); }
 // b2 = (c - m) log2(e) for the running max m.
@@ -424,11 +464,35 @@ __device__ __forceinline__ float cap_b2(float m, const CapK& K) { return (K.c - 
 // (z - m) log2(e) of one logit, given b2 of m.
 __device__ __forceinline__ float cap_d2(float x, const CapK& K, float b2) { return fmaf(cap_r(x, K), K.a2, b2); }
 
+// Pair i of a raw vector with both values limited to K.xmax (one packed min
+// for 16-bit types); -inf stays -inf.
+__device__ __forceinline__ fp2 pair_min(const Raw8<__nv_bfloat16>& v, int i, const CapK& K) {
+  uint32_t w;
+  asm("min.bf16x2 %0, %1, %2;" : "=r"(w) : "r"(v.w[i]), "r"(K.xmax_bf16x2));
+  return pk(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
+}
+__device__ __forceinline__ fp2 pair_min(const Raw8<__half>& v, int i, const CapK& K) {
+  uint32_t w;
+  asm("min.f16x2 %0, %1, %2;" : "=r"(w) : "r"(v.w[i]), "r"(K.xmax_f16x2));
+  return pk(h2f(w & 0xffffu), h2f(w >> 16));
+}
+__device__ __forceinline__ fp2 pair_min(const Raw8<float>& v, int i, const CapK& K) {
+  return pk(fminf(v.v[2 * i], K.xmax), fminf(v.v[2 * i + 1], K.xmax));
+}
+
 // (z - m) log2(e) for pair i of a raw vector, given b2 of m in both halves.
+// With FMA_RCP the reciprocal runs on the FMA pipe (rcp2_fma_neg), on x
+// limited to K.xmax so that 1 + E stays within its range; the reciprocal
+// below 2^-64 it then gives in place of a smaller one only ever adds a term
+// far below one ulp of c.
 template <class T, bool FMA_RCP>
 __device__ __forceinline__ fp2 cap_d2_pair(const Raw8<T>& v, int i, const CapK& K, fp2 b2) {
-  const fp2 den = add2(ex2_2(mul2(v.pair(i), splat(K.k2))), splat(1.0f));
-  const fp2 r = FMA_RCP ? rcp2_fma_wide(den) : rcp2(den);
+  fp2 r;
+  if constexpr (FMA_RCP) {
+    r = rcp2_fma_neg(sub2(splat(-1.0f), ex2_2(mul2(pair_min(v, i, K), splat(K.k2)))));
+  } else {
+    r = rcp2(add2(ex2_2(mul2(v.pair(i), splat(K.k2))), splat(1.0f)));
+  }
   return fma2(r, splat(K.a2), b2);
 }
 template <class T>
@@ -455,6 +519,9 @@ __device__ __forceinline__ float cap_z(float x, const CapK& K) { return K.c * ca
 // 0 when m_old = -inf.
 __device__ __forceinline__ float rescale(float m_old, float m_new) {
   return ex2((m_old - m_new) * kLog2e);
+}
+__device__ __forceinline__ float rescale_rare(float m_old, float m_new) {
+  return ex2_rare((m_old - m_new) * kLog2e);
 }
 
 struct LogpState {
