@@ -48,7 +48,7 @@ struct LogpAcc {
   fp2 nm2 = 0, s2 = 0;
 
   // wa: with a cap, the warp's raw max over this vector's group (warp_max)
-  template <bool PARTIAL>
+  template <bool PARTIAL, bool CLAMP = true>
   __device__ __forceinline__ void update(const Raw8<T>& v, const Raw8<T>&, int valid, const CapK& K, float wa = 0.0f,
                                          float = 0.0f) {
     if constexpr (CAP) {
@@ -71,7 +71,7 @@ struct LogpAcc {
     }
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-      const fp2 d2 = CAP ? cap_d2_pair<T>(v, i, K, nm2) : mul2(add2(v.pair(i), nm2), splat(kLog2e));
+      const fp2 d2 = CAP ? cap_d2_pair<T, CLAMP>(v, i, K, nm2) : mul2(add2(v.pair(i), nm2), splat(kLog2e));
       s2 = add2(s2, keep<PARTIAL>(ex2_2(d2), i, valid));
     }
   }
@@ -86,7 +86,7 @@ struct EntropyAcc {
   float m_raw = neg_inf(), m = neg_inf();
   fp2 nm2 = 0, s2 = 0, w2 = 0;
 
-  template <bool PARTIAL>
+  template <bool PARTIAL, bool CLAMP = true>
   __device__ __forceinline__ void update(const Raw8<T>& v, const Raw8<T>&, int valid, const CapK& K, float wa = 0.0f,
                                          float = 0.0f) {
     const float vm = CAP ? wa : v.max();   // with a cap, the warp's max: the same decision in every lane
@@ -105,7 +105,7 @@ struct EntropyAcc {
     for (int i = 0; i < 4; ++i) {
       fp2 d, e;
       if (CAP) {
-        d = cap_d2_pair<T>(v, i, K, nm2);
+        d = cap_d2_pair<T, CLAMP>(v, i, K, nm2);
         e = keep<PARTIAL>(ex2_2(d), i, valid);
       } else {
         d = add2(v.pair_clamped(i), nm2);  // -inf columns: e = 0 and 0 * d = 0
@@ -128,7 +128,7 @@ struct KlAcc {
   uint32_t flag = 0;
 
   // wp, wq: with a cap, the warp's raw maxima over this vector's group of P and of Q
-  template <bool PARTIAL>
+  template <bool PARTIAL, bool CLAMP = true>
   __device__ __forceinline__ void update(const Raw8<T>& v, const Raw8<T>& q, int valid, const CapK& K,
                                          float wp = 0.0f, float wq = 0.0f) {
     // with a cap, the warp's maxima: the same decisions in every lane
@@ -155,8 +155,8 @@ struct KlAcc {
       for (int i = 0; i < 4; ++i) {
         fp2 dp, dq, ep, eq;
         if (CAP) {
-          dp = cap_d2_pair<T>(v, i, K, nmp2);
-          dq = cap_d2_pair<T>(q, i, K, nmq2);
+          dp = cap_d2_pair<T, CLAMP>(v, i, K, nmp2);
+          dq = cap_d2_pair<T, CLAMP>(q, i, K, nmq2);
           ep = keep<PARTIAL>(ex2_2(dp), i, valid);
           eq = keep<PARTIAL>(ex2_2(dq), i, valid);
         } else {
@@ -195,7 +195,7 @@ struct FusedAcc {
   uint32_t flag = 0;
 
   // wa, wb: with a cap, the warp's raw maxima over this vector's group of a and of b
-  template <bool PARTIAL>
+  template <bool PARTIAL, bool CLAMP = true>
   __device__ __forceinline__ void update(const Raw8<T>& v, const Raw8<T>& q, int valid, const CapK& K,
                                          float wa = 0.0f, float wb = 0.0f) {
     const float vma = CAP ? wa : v.max();   // with a cap, the warp's max: the same decisions in every lane
@@ -231,10 +231,10 @@ struct FusedAcc {
       for (int i = 0; i < 4; ++i) {
         fp2 da, db = 0, ea, eb = 0;
         if (CAP) {
-          da = cap_d2_pair<T>(v, i, K, nma2);
+          da = cap_d2_pair<T, CLAMP>(v, i, K, nma2);
           ea = keep<PARTIAL>(ex2_2(da), i, valid);
           if constexpr (kHasB) {
-            db = cap_d2_pair<T>(q, i, K, nmb2);
+            db = cap_d2_pair<T, CLAMP>(q, i, K, nmb2);
             eb = keep<PARTIAL>(ex2_2(db), i, valid);
           }
         } else {
@@ -451,8 +451,15 @@ __global__ void __launch_bounds__(kFwdThreads, (fwd_min_blocks<T, OP, CAP, DIR>(
         for (int g = 0; g < U; g += G) {
           const float wa = warp_max(group_max<T, G>(rx + g));
           const float wb = KL ? warp_max(group_max<T, G>(ry + g)) : 0.0f;
+          if ((KL ? fmaxf(wa, wb) : wa) > K.xmax) {   // the same in every lane: rare
 #pragma unroll
-          for (int u = 0; u < G; ++u) acc.template update<false>(rx[g + u], KL ? ry[g + u] : rx[g + u], 8, K, wa, wb);
+            for (int u = 0; u < G; ++u)
+              acc.template update<false, true>(rx[g + u], KL ? ry[g + u] : rx[g + u], 8, K, wa, wb);
+          } else {
+#pragma unroll
+            for (int u = 0; u < G; ++u)
+              acc.template update<false, false>(rx[g + u], KL ? ry[g + u] : rx[g + u], 8, K, wa, wb);
+          }
         }
       }
     }
@@ -476,9 +483,9 @@ __global__ void __launch_bounds__(kFwdThreads, (fwd_min_blocks<T, OP, CAP, DIR>(
 #pragma unroll
       for (int u = 0; u < G; ++u) {
         if (valid[u] == 8)
-          acc.template update<false>(rx[u], KL ? ry[u] : rx[u], 8, K, wa, wb);
+          acc.template update<false, true>(rx[u], KL ? ry[u] : rx[u], 8, K, wa, wb);
         else
-          acc.template update<true>(rx[u], KL ? ry[u] : rx[u], valid[u], K, wa, wb);
+          acc.template update<true, true>(rx[u], KL ? ry[u] : rx[u], valid[u], K, wa, wb);
       }
     }
   }

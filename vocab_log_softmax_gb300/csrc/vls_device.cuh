@@ -485,19 +485,22 @@ __device__ __forceinline__ fp2 pair_min(const Raw8<float>& v, int i, const CapK&
 // limited to K.xmax so that 1 + E stays within its range; the reciprocal
 // below 2^-64 it then gives in place of a smaller one only ever adds a term
 // far below one ulp of c.
-template <class T, bool FMA_RCP>
+// CLAMP = false is for vectors known to hold nothing above K.xmax (the sweep
+// checks the warp's max of the group): the limit is then skipped, with the
+// same results.
+template <class T, bool FMA_RCP, bool CLAMP>
 __device__ __forceinline__ fp2 cap_d2_pair(const Raw8<T>& v, int i, const CapK& K, fp2 b2) {
   fp2 r;
   if constexpr (FMA_RCP) {
-    r = rcp2_fma_neg(sub2(splat(-1.0f), ex2_2(mul2(pair_min(v, i, K), splat(K.k2)))));
+    r = rcp2_fma_neg(sub2(splat(-1.0f), ex2_2(mul2(CLAMP ? pair_min(v, i, K) : v.pair(i), splat(K.k2)))));
   } else {
     r = rcp2(add2(ex2_2(mul2(v.pair(i), splat(K.k2))), splat(1.0f)));
   }
   return fma2(r, splat(K.a2), b2);
 }
-template <class T>
+template <class T, bool CLAMP = true>
 __device__ __forceinline__ fp2 cap_d2_pair(const Raw8<T>& v, int i, const CapK& K, fp2 b2) {
-  return ((kCapFmaPairs >> i) & 1u) ? cap_d2_pair<T, true>(v, i, K, b2) : cap_d2_pair<T, false>(v, i, K, b2);
+  return ((kCapFmaPairs >> i) & 1u) ? cap_d2_pair<T, true, CLAMP>(v, i, K, b2) : cap_d2_pair<T, false, CLAMP>(v, i, K, b2);
 }
 
 // The softcapped value of the row max (tanh is increasing, so the max of z
