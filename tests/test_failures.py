@@ -169,3 +169,11 @@ def _expire_and_recover(tlib, form):
 @pytest.mark.gpu
 def test_expired_wait_one_sm_form(tlib):
     _expire_and_recover(tlib, 1)
+
+
+@pytest.mark.gpu
+def test_expired_wait_cta_pairs(tlib):
+    """The same on the default form, where both CTAs' loads complete on the
+    leader's barriers: after the abort the pair exchanges its issue counts
+    and the leader waits for every load of both CTAs before the pair leaves."""
+    _expire_and_recover(tlib, 2)
