@@ -29,7 +29,8 @@
  *  - N == 0 (or n == 0) returns VLS_OK without touching any pointer and
  *    without a launch.
  *  - Logits are finite or -inf (a mask).  A row whose logits are all -inf
- *    has no distribution: its statistics and gradient row are NaN.
+ *    has no distribution: its statistics and gradient row are NaN.  A NaN
+ *    logit makes every statistic and gradient of its row NaN.
  *  - cap: 0 means no softcap.  cap > 0 applies y = cap*tanh(x/cap) to every
  *    logit before the softmax, in registers ("Final Logit Softcap",
  *    section Summary); -inf logits then become -cap.

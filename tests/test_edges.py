@@ -117,6 +117,29 @@ def test_masks_and_ignores(dtype):
         check_kl(a, b, gr, d, cap=4.0, what="masked kl cap")
 
 
+@pytest.mark.parametrize("dtype", DTYPES)
+@pytest.mark.parametrize("cap", [0.0, 30.0])
+def test_nan_logit_makes_its_row_nan(cap, dtype):
+    """A NaN logit makes every statistic of its row NaN, and every gradient
+    of that row, as in the oracle; the other rows are untouched.  With a cap,
+    logits above about 22 c are limited before the exponential: a NaN beside
+    such a value (in the same pair, the same vector, or the ragged tail) must
+    stay NaN through that limit."""
+    v = 4099
+    a, b, ids, gk, gr = _data(6, v, dtype, seed=31)
+    nan = float("nan")
+    a[0, 0], a[0, 1] = nan, 1e4            # same pair as a limited value
+    a[1, 2000], a[1, 2003] = nan, 1e4      # same vector
+    a[2, v - 1] = nan                      # ragged tail
+    a[3, 10] = 1e4                         # limited value, finite row
+    b[4, 77] = nan                         # reference only (KL)
+    check_logp(a, ids, gk, cap=cap, what="nan logp")
+    check_logp(a, ids[:, :1].contiguous(), gk[:, :1].contiguous(), cap=cap, what="nan logp k=1")
+    check_entropy(a, gr, cap=cap, what="nan entropy")
+    for d in ("reverse", "forward"):
+        check_kl(a, b, gr, d, cap=cap, what="nan kl")
+
+
 def test_zero_rows_are_exact():
     a, _, ids, gk, _ = _data(4, 777, torch.bfloat16, seed=9)
     ids[:] = -100

@@ -166,15 +166,15 @@ __device__ __noinline__ void onehot_vector(T* dst, const Raw8<T> x, int64_t gcol
     float xa, xb;
     upk(x.pair(static_cast<int>(e) >> 1), xa, xb);
     const float xe = (e & 1) ? xb : xa;
-    float d, chain = 1.0f;
+    float p, chain = 1.0f;
     if (CAP) {
-      float ee, r;
-      d = cap_d(cap_t(xe, K, ee, r), K.c, m);
-      chain = 4.0f * ee * r * r;
+      float E;
+      const float r = cap_r_lim(xe, K, E);
+      p = ex2(fmaf(r, K.a2, cap_b2_ls(m, log_s, K)));
+      chain = 4.0f * E * r * r;
     } else {
-      d = xe - m;
+      p = ex2(fmaf(xe - m, kLog2e, -log_s * kLog2e));
     }
-    const float p = ex2(fmaf(d, kLog2e, -log_s * kLog2e));
     const float r = fmaf(-G, p, gs);
     Out8<T>::store1(dst + e, CAP ? r * chain : r);
   }
@@ -183,7 +183,7 @@ __device__ __noinline__ void onehot_vector(T* dst, const Raw8<T> x, int64_t gcol
 // Row constants of a backward map.
 struct BwdRow {
   fp2 nm2;      // -m (of x)
-  fp2 nls2;     // -log S * log2 e (of x)
+  fp2 nls2;     // -log S * log2 e (of x); the softcapped logp map: (c - m - log S) log2 e
   fp2 coef2;    // logp: -G (times 4 with a cap); entropy: -g; KL: g
   fp2 k2;       // entropy: log S - H;  reverse KL: log S_a - log S_b + KL
   fp2 nmq2;     // KL: -m_b
@@ -200,6 +200,13 @@ constexpr bool bwd_reads_two() { return OP == kBwdKlReverse || OP == kBwdKlForwa
 template <class T, int OP, bool CAP, int DIR = kFusedNoKl>
 __device__ __forceinline__ fp2 grad_pair(const Raw8<T>& x, const Raw8<T>& y, int i, const BwdRow& R,
                                          const CapK& K) {
+  if constexpr (CAP && OP == kBwdLogp) {
+    // -4 G p E r r; nls2 holds (c - m - log S) log2(e) here
+    fp2 E;
+    const fp2 r = cap_r_pair(x, i, K, E);
+    const fp2 p = ex2_2(fma2(r, splat(K.a2), R.nls2));
+    return mul2(mul2(p, R.coef2), mul2(mul2(E, r), r));
+  }
   fp2 d, e2 = 0, r2 = 0;
   if (CAP) {
     d = fma2(cap_t2(x, i, K, e2, r2), splat(K.c), R.nm2);
@@ -264,13 +271,13 @@ __device__ __forceinline__ float fused_at(const T* xr, const T* yr, int64_t c, c
     d = cap_d(cap_t(x, K, e, r), K.c, sx.m);
     chain = 4.0f * e * r * r;
   } else {
-    d = fmaxf(x, kLowest) - sx.m;
+    d = max_nan(x, kLowest) - sx.m;
   }
   const float p = ex2(fmaf(d, kLog2e, -sx.log_s * kLog2e));
   float r = fmaf(p * d, c1, fmaf(p, c0, gsum));
   if constexpr (DIR != kFusedNoKl) {
     const float y = load1(yr + c);
-    const float db = CAP ? cap_d(cap_t(y, K), K.c, mq) : fmaxf(y, kLowest) - mq;
+    const float db = CAP ? cap_d(cap_t(y, K), K.c, mq) : max_nan(y, kLowest) - mq;
     if constexpr (DIR == kFusedKlReverse) r = fmaf(p * db, c2, r);
     else r = fmaf(ex2(fmaf(db, kLog2e, -log_sq * kLog2e)), ngk, r);
   }
@@ -286,11 +293,18 @@ __device__ __forceinline__ float fused_at(const T* xr, const T* yr, int64_t c, c
 // TOPK (logprob map with k > 1): the one-hot columns are written inline by
 // the thread that stores their vector (onehot_vector) instead of by a
 // post-pass that re-reads them after a barrier.
+#ifndef VLS_CAP_LOGP_BWD_CTAS
+#define VLS_CAP_LOGP_BWD_CTAS 6
+#endif
+// vectors per buffer of the softcapped maps' two-buffer pipeline (16-bit, one tensor)
+#ifndef VLS_CAP_BWD_VECS
+#define VLS_CAP_BWD_VECS 2
+#endif
 template <class T, int OP, bool CAP, bool TOPK>
 constexpr int bwd_min_blocks() {
   if (TOPK) return kCapMinBlocks;
   if (!CAP) return 6;
-  return (OP == kBwdLogp && sizeof(T) == 2) ? 6 : kCapMinBlocks;
+  return (OP == kBwdLogp && sizeof(T) == 2) ? VLS_CAP_LOGP_BWD_CTAS : kCapMinBlocks;
 }
 
 template <class T, int OP, bool CAP, int DIR = kFusedNoKl, bool TOPK = false>
@@ -311,7 +325,7 @@ __global__ void __launch_bounds__(kRowThreads, (bwd_min_blocks<T, OP, CAP, TOPK>
   const vls_rowstat sx = a.stats_x[row];
   BwdRow R;
   R.nm2 = splat(-sx.m);
-  R.nls2 = splat(-sx.log_s * kLog2e);
+  R.nls2 = splat((CAP && OP == kBwdLogp) ? cap_b2_ls(sx.m, sx.log_s, K) : -sx.log_s * kLog2e);
   R.k2 = 0;
   R.nmq2 = 0;
   R.nlsq2 = 0;
@@ -455,7 +469,7 @@ __global__ void __launch_bounds__(kRowThreads, (bwd_min_blocks<T, OP, CAP, TOPK>
     // Heavy per-element arithmetic (two exponentials and a reciprocal):
     // software-pipelined, the next batch's loads issued before the current
     // batch is computed, alternating between two register buffers.
-    constexpr int U = (KL || sizeof(T) == 4) ? 1 : 2;
+    constexpr int U = (KL || sizeof(T) == 4) ? 1 : VLS_CAP_BWD_VECS;
     constexpr int64_t kStep = U * kRowThreads;
     if (al && v + (U - 1) * kRowThreads < vfull_end) {
       Raw8<T> xa[U], ya[U], xb[U], yb[U];
@@ -544,15 +558,15 @@ __global__ void __launch_bounds__(kRowThreads, (bwd_min_blocks<T, OP, CAP, TOPK>
       for (int f = threadIdx.x; f < nfix; f += kRowThreads) {
         const int64_t c = fix_id[f];
         const float x = load1(xr + c);
-        float d, chain = 1.0f;
+        float p, chain = 1.0f;
         if (CAP) {
-          float e, r;
-          d = cap_d(cap_t(x, K, e, r), K.c, sx.m);
-          chain = 4.0f * e * r * r;
+          float E;
+          const float r = cap_r_lim(x, K, E);
+          p = ex2(fmaf(r, K.a2, cap_b2_ls(sx.m, sx.log_s, K)));
+          chain = 4.0f * E * r * r;
         } else {
-          d = x - sx.m;
+          p = ex2(fmaf(x - sx.m, kLog2e, -sx.log_s * kLog2e));
         }
-        const float p = ex2(fmaf(d, kLog2e, -sx.log_s * kLog2e));
         const float r = fmaf(-G, p, fix_g[f]);
         Out8<T>::store1(dr + c, CAP ? r * chain : r);
       }

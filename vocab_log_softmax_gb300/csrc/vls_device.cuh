@@ -117,6 +117,19 @@ __device__ __forceinline__ uint32_t beq2(uint32_t a, uint32_t b) {
 }
 
 // float16x2 helpers on raw 32-bit words.
+// max that returns NaN when either operand is NaN (the plain forms, like
+// fmaxf, return the other): the clamp of -inf to the lowest finite value
+// must not hide a NaN logit, which makes its whole row NaN.
+__device__ __forceinline__ uint32_t bmax2_nan(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("max.NaN.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  return r;
+}
+__device__ __forceinline__ float max_nan(float a, float b) {
+  float r;
+  asm("max.NaN.f32 %0, %1, %2;" : "=f"(r) : "f"(a), "f"(b));
+  return r;
+}
 __device__ __forceinline__ uint32_t hmax2(uint32_t a, uint32_t b) {
   uint32_t r;
   asm("max.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
@@ -210,7 +223,7 @@ struct Raw8<__nv_bfloat16> {
     return pk(__uint_as_float(w[i] << 16), __uint_as_float(w[i] & 0xffff0000u));
   }
   __device__ __forceinline__ fp2 pair_clamped(int i) const {
-    const uint32_t c = bmax2(w[i], kLowestBf16x2);
+    const uint32_t c = bmax2_nan(w[i], kLowestBf16x2);
     return pk(__uint_as_float(c << 16), __uint_as_float(c & 0xffff0000u));
   }
   __device__ __forceinline__ fp2 pair_abs(int i) const {
@@ -251,7 +264,7 @@ struct Raw8<__half> {
   }
   __device__ __forceinline__ fp2 pair(int i) const { return pk(h2f(w[i] & 0xffffu), h2f(w[i] >> 16)); }
   __device__ __forceinline__ fp2 pair_clamped(int i) const {
-    return pk(fmaxf(h2f(w[i] & 0xffffu), kLowest), fmaxf(h2f(w[i] >> 16), kLowest));
+    return pk(max_nan(h2f(w[i] & 0xffffu), kLowest), max_nan(h2f(w[i] >> 16), kLowest));
   }
   __device__ __forceinline__ fp2 pair_abs(int i) const {
     const uint32_t a = w[i] & 0x7fff7fffu;
@@ -283,7 +296,7 @@ struct Raw8<float> {
   }
   __device__ __forceinline__ fp2 pair(int i) const { return pk(v[2 * i], v[2 * i + 1]); }
   __device__ __forceinline__ fp2 pair_clamped(int i) const {
-    return pk(fmaxf(v[2 * i], kLowest), fmaxf(v[2 * i + 1], kLowest));
+    return pk(max_nan(v[2 * i], kLowest), max_nan(v[2 * i + 1], kLowest));
   }
   __device__ __forceinline__ fp2 pair_abs(int i) const { return pk(fabsf(v[2 * i]), fabsf(v[2 * i + 1])); }
   __device__ __forceinline__ uint32_t sign_lo(int i) const { return __float_as_uint(v[2 * i]); }
@@ -464,20 +477,27 @@ __device__ __forceinline__ float cap_b2(float m, const CapK& K) { return (K.c - 
 // (z - m) log2(e) of one logit, given b2 of m.
 __device__ __forceinline__ float cap_d2(float x, const CapK& K, float b2) { return fmaf(cap_r(x, K), K.a2, b2); }
 
+// min(x, y) that returns NaN when either is NaN (fminf returns the other).
+__device__ __forceinline__ float min_nan(float x, float y) {
+  float r;
+  asm("min.NaN.f32 %0, %1, %2;" : "=f"(r) : "f"(x), "f"(y));
+  return r;
+}
+
 // Pair i of a raw vector with both values limited to K.xmax (one packed min
-// for 16-bit types); -inf stays -inf.
+// for 16-bit types); -inf stays -inf and NaN stays NaN.
 __device__ __forceinline__ fp2 pair_min(const Raw8<__nv_bfloat16>& v, int i, const CapK& K) {
   uint32_t w;
-  asm("min.bf16x2 %0, %1, %2;" : "=r"(w) : "r"(v.w[i]), "r"(K.xmax_bf16x2));
+  asm("min.NaN.bf16x2 %0, %1, %2;" : "=r"(w) : "r"(v.w[i]), "r"(K.xmax_bf16x2));
   return pk(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
 }
 __device__ __forceinline__ fp2 pair_min(const Raw8<__half>& v, int i, const CapK& K) {
   uint32_t w;
-  asm("min.f16x2 %0, %1, %2;" : "=r"(w) : "r"(v.w[i]), "r"(K.xmax_f16x2));
+  asm("min.NaN.f16x2 %0, %1, %2;" : "=r"(w) : "r"(v.w[i]), "r"(K.xmax_f16x2));
   return pk(h2f(w & 0xffffu), h2f(w >> 16));
 }
 __device__ __forceinline__ fp2 pair_min(const Raw8<float>& v, int i, const CapK& K) {
-  return pk(fminf(v.v[2 * i], K.xmax), fminf(v.v[2 * i + 1], K.xmax));
+  return pk(min_nan(v.v[2 * i], K.xmax), min_nan(v.v[2 * i + 1], K.xmax));
 }
 
 // (z - m) log2(e) for pair i of a raw vector, given b2 of m in both halves.
@@ -501,6 +521,38 @@ __device__ __forceinline__ fp2 cap_d2_pair(const Raw8<T>& v, int i, const CapK& 
 template <class T, bool CLAMP = true>
 __device__ __forceinline__ fp2 cap_d2_pair(const Raw8<T>& v, int i, const CapK& K, fp2 b2) {
   return ((kCapFmaPairs >> i) & 1u) ? cap_d2_pair<T, true, CLAMP>(v, i, K, b2) : cap_d2_pair<T, false, CLAMP>(v, i, K, b2);
+}
+
+// The logprob backward map's form.  There the logit enters through
+// p = exp(z - m - log S) and the slope dz/dx = 1 - tanh(x/c)^2 = 4 E r^2:
+//   log2 p = a2 r + (c - m - log S) log2(e),
+// one FMA after E = exp(2x/c) and r = 1/(1 + E), with x limited to K.xmax
+// so that E <= 2^64 and E r r stays finite (the slope it gives beyond that,
+// below 2^-62, is as good as 0 next to any gradient; x = -inf gives E = 0,
+// r = 1 and slope 0).  No sign handling and no 1 - e: three fewer packed
+// operations a pair than cap_t2.  p carries the r-form's absolute error of z
+// (a few 1e-7 c) as a relative error, which the gradient's bf16, fp16 and
+// fp32 rounding rules all absorb.
+// Pairs whose reciprocal runs on the FMA pipe in this map: 0 and 2 (bit i
+// for pair i), 2% faster than none and than three; all four is 7% slower.
+#ifndef VLS_CAP_BWD_FMA_PAIRS
+#define VLS_CAP_BWD_FMA_PAIRS 0x5
+#endif
+constexpr uint32_t kCapBwdFmaPairs = VLS_CAP_BWD_FMA_PAIRS;
+
+template <class T>
+__device__ __forceinline__ fp2 cap_r_pair(const Raw8<T>& v, int i, const CapK& K, fp2& E) {
+  E = ex2_2(mul2(pair_min(v, i, K), splat(K.k2)));
+  return ((kCapBwdFmaPairs >> i) & 1u) ? rcp2_fma_neg(sub2(splat(-1.0f), E)) : rcp2(add2(E, splat(1.0f)));
+}
+// Scalar form (same operations as the special-function pairs).
+__device__ __forceinline__ float cap_r_lim(float x, const CapK& K, float& E) {
+  E = ex2(min_nan(x, K.xmax) * K.k2);
+  return rcp(1.0f + E);
+}
+// (c - m - log S) log2(e) of a row.
+__device__ __forceinline__ float cap_b2_ls(float m, float log_s, const CapK& K) {
+  return ((K.c - m) - log_s) * kLog2e;
 }
 
 // The softcapped value of the row max (tanh is increasing, so the max of z
