@@ -140,6 +140,21 @@ def test_nan_logit_makes_its_row_nan(cap, dtype):
         check_kl(a, b, gr, d, cap=cap, what="nan kl")
 
 
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16], ids=["f32", "bf16"])
+@pytest.mark.parametrize("cap", [50.0, 100.0])
+def test_large_caps(cap, dtype):
+    """Caps above the pages' 20 and 30 (50 is another common softcap).  The
+    capped logit carries an absolute error of a few 1e-7 * cap, so the
+    results still meet the fp32 rule at these caps, in a short row and a
+    full-width one, with logits spread enough to reach the cap's bend."""
+    for n, v, scale in ((6, 4099, 40.0), (3, 151936, 25.0)):
+        a, b, ids, gk, gr = _data(n, v, dtype, seed=int(cap) + v % 97, scale=scale)
+        check_logp(a, ids, gk, cap=cap, what=f"cap={cap} V={v} logp")
+        check_entropy(a, gr, cap=cap, what=f"cap={cap} V={v} entropy")
+        for d in ("reverse", "forward"):
+            check_kl(a, b, gr, d, cap=cap, what=f"cap={cap} V={v} kl")
+
+
 def test_zero_rows_are_exact():
     a, _, ids, gk, _ = _data(4, 777, torch.bfloat16, seed=9)
     ids[:] = -100

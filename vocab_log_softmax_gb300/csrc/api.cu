@@ -74,15 +74,22 @@ void fwd_geometry(int64_t V, int* cluster, int64_t* vec_per_cta) {
 
 // Backward geometry: results do not depend on it (pure map).  Top-k rows
 // prepare their id list once per CTA, so they take whole rows up to 262144
-// columns.
+// columns.  A piece's run of vectors is rounded up to a multiple of
+// kBwdVecRound (two batches of one vector per thread), so that the sweeps'
+// batched loops cover it whole and only a row's last piece ends in the
+// one-vector-at-a-time tail: at 151936 columns that made the maps 2-4%
+// faster (4096 + 4096 + 4096 + 4096 + 2608 vectors instead of 5 x 3799).
+constexpr int64_t kBwdVecRound = 512;
 void bwd_geometry(int64_t V, int32_t k, int* chunks, int64_t* vec_per_cta) {
   const int64_t target = bwd_vec_target();
   const int64_t nvec = ceil_div(V, 8);
   const int64_t t = k > 1 ? 8 * target : target;
   int64_t c = ceil_div(nvec, t);
   if (c < 1) c = 1;
-  *chunks = static_cast<int>(c);
-  *vec_per_cta = ceil_div(nvec, c);
+  int64_t per = ceil_div(ceil_div(nvec, c), kBwdVecRound) * kBwdVecRound;
+  if (per > nvec) per = nvec;
+  *chunks = static_cast<int>(ceil_div(nvec, per));
+  *vec_per_cta = per;
 }
 
 // Small batches: when the rows alone would leave SMs idle, the backward's

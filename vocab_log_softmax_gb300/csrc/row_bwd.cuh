@@ -287,8 +287,9 @@ __device__ __forceinline__ float fused_at(const T* xr, const T* yr, int64_t c, c
 // Six resident CTAs per SM (at most 40 registers a thread) keep enough
 // loads in flight; with a larger register budget occupancy halves and the
 // sweep slows down.  The 16-bit softcapped logprob map keeps six too: its
-// software pipeline spills a little at 40 registers, and is still 3% faster
-// than at 5 CTAs and 48 registers (and 8% faster than at 32).  The other
+// software pipeline spills a little at 40 registers, and is still 6% faster
+// than at 5 CTAs and 48 registers (and 8% faster than at 32); buffers of 3
+// or 4 vectors at 4 or 5 CTAs were 1-9% slower at 151936 columns.  The other
 // softcapped maps and the top-k map get kCapMinBlocks CTAs per SM.
 // TOPK (logprob map with k > 1): the one-hot columns are written inline by
 // the thread that stores their vector (onehot_vector) instead of by a
