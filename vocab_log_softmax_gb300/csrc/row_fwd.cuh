@@ -291,17 +291,22 @@ template <int OP, int DIR>
 constexpr bool reads_two() { return OP == kFwdKl || (OP == kFwdFused && DIR != kFusedNoKl); }
 
 // 16-byte loads in flight per thread before any is used: 4 vectors of one
-// tensor, or 2 vectors of each of the two KL tensors.  The softcapped logp
-// sweep, bound by its arithmetic's latency rather than by memory, takes 6
-// (measured: 3.7% faster than 4 at 6 resident CTAs; 8 spills).
-template <int OP, int DIR, bool CAP>
+// tensor; 3 vectors of each of the two 16-bit KL tensors (2.5-3.8% faster
+// than 2 at the same 48 registers and 5 CTAs; 4, or 6 CTAs, spill), 2 of
+// each in the other two-tensor sweeps.  The softcapped logp sweep, bound by
+// its arithmetic's latency rather than by memory, takes 6 (measured: 3.7%
+// faster than 4 at 6 resident CTAs; 8 spills).
 #ifndef VLS_CAP_LOGP_UNROLL
 #define VLS_CAP_LOGP_UNROLL 6
 #endif
 #ifndef VLS_CAP_LOGP_CTAS
 #define VLS_CAP_LOGP_CTAS 5
 #endif
-constexpr int fwd_unroll() { return reads_two<OP, DIR>() ? 2 : ((CAP && OP == kFwdLogp) ? VLS_CAP_LOGP_UNROLL : 4); }
+template <class T, int OP, int DIR, bool CAP>
+constexpr int fwd_unroll() {
+  if (reads_two<OP, DIR>()) return (OP == kFwdKl && !CAP && sizeof(T) == 2) ? 3 : 2;
+  return (CAP && OP == kFwdLogp) ? VLS_CAP_LOGP_UNROLL : 4;
+}
 
 // Vectors per lane over which the softcapped sweeps take one warp max.
 #ifndef VLS_CAP_MAX_GROUP
@@ -367,7 +372,7 @@ template <class T, int OP, bool CAP, int DIR = kFusedNoKl>
 __global__ void __launch_bounds__(kFwdThreads, (fwd_min_blocks<T, OP, CAP, DIR>())) row_fwd_kernel(const FwdArgs a) {
   using Acc = typename FwdAccOf<OP, T, CAP, DIR>::type;
   using S = typename Acc::State;
-  constexpr int U = fwd_unroll<OP, DIR, CAP>();
+  constexpr int U = fwd_unroll<T, OP, DIR, CAP>();
   constexpr bool KL = reads_two<OP, DIR>();
   __shared__ S warp_part[kFwdWarps];
   __shared__ S cta_part[kMaxCluster];
