@@ -921,40 +921,71 @@ def _oracle_worker(job: tuple) -> tuple:
     return t0, time.perf_counter()
 
 
-def oracle_pool(rows_per_worker: int, v: int, steps: int, warmup: int, workers: int) -> float:
-    """Seconds per step of the oracle over `workers` processes, each on its
-    own block of rows: the wall time from the first worker's start to the
-    last worker's end.  Processes are spawned (never forked after CUDA)."""
-    import multiprocessing as mp
-    ctx = mp.get_context("spawn")
-    barrier = ctx.Barrier(workers)
-    with ctx.Pool(workers, initializer=_oracle_init, initargs=(barrier,)) as pool:
-        spans = pool.map(_oracle_worker, [(rows_per_worker, v, w, steps, warmup) for w in range(workers)])
-    return (max(t1 for _, t1 in spans) - min(t0 for t0, _ in spans)) / steps
-
-
-def _oracle_row_seconds(v: int) -> float:
-    """Seconds of one row of the whole path on the oracle, on this core."""
+def _oracle_calibrate(v: int) -> float:
+    """Seconds of one row of the whole path on the oracle in one process of
+    the pool, timed while every other process runs the same probe (the
+    processes share the host's memory bandwidth)."""
     import workloads
     probe = host_rows(_cpu_inputs(workloads, 2, v), 0, 2)
+    _BARRIER.wait()
     oracle_step(probe)
     t0 = time.perf_counter()
     oracle_step(probe)
     return (time.perf_counter() - t0) / 2
 
 
-def cpu_baseline(n: int, v: int, budget_s: float = 8.0) -> dict:
+def host_memory_available() -> int:
+    """Bytes of host memory available now (MemAvailable), 8 GiB if unknown."""
+    try:
+        with open("/proc/meminfo") as f:
+            for line in f:
+                if line.startswith("MemAvailable:"):
+                    return int(line.split()[1]) * 1024
+    except OSError:
+        pass
+    return 8 << 30
+
+
+ORACLE_BYTES_PER_COLUMN = 96   # peak host memory of one oracle row of the whole path, per column (measured ~70)
+
+
+def oracle_pool(v: int, steps: int, warmup: int, workers: int, budget_s: float, max_rows: int) -> tuple:
+    """The oracle over `workers` processes, each on its own block of rows,
+    sized so that its warm-up and timed passes take about budget_s seconds
+    under contention and all blocks together stay within 40% of the host's
+    available memory.  Returns (rows per worker, seconds per step: the wall
+    time from the first worker's start to the last worker's end).  Processes
+    are spawned (never forked after CUDA)."""
+    import multiprocessing as mp
+    mem_rows = int(0.4 * host_memory_available() / (workers * ORACLE_BYTES_PER_COLUMN * v))
+    ctx = mp.get_context("spawn")
+    barrier = ctx.Barrier(workers)
+    with ctx.Pool(workers, initializer=_oracle_init, initargs=(barrier,)) as pool:
+        per_row = max(pool.map(_oracle_calibrate, [v] * workers))
+        rows = int(max(1, min(max_rows, mem_rows, budget_s / (steps + warmup) / max(per_row, 1e-6))))
+        spans = pool.map(_oracle_worker, [(rows, v, w, steps, warmup) for w in range(workers)])
+    return rows, (max(t1 for _, t1 in spans) - min(t0 for t0, _ in spans)) / steps
+
+
+def cpu_baseline(n: int, v: int, budget_s: float = 12.0) -> dict:
     """The oracle, as it stands, on every host core: one process per core,
     each on its own block of rows of the workload (about budget_s seconds of
     work each)."""
     cores = host_cores()
-    rows = int(max(2, min(n, budget_s / max(_oracle_row_seconds(v), 1e-6))))
-    dt = oracle_pool(rows, v, 1, 0, cores)
+    rows, dt = oracle_pool(v, 1, 0, cores, budget_s, n)
     total = rows * cores
     return {"value": round(step_bytes(total, v) / dt / 1e12, 6), "unit": "TB/s", "cores": cores, "kind": "oracle",
             "sample": f"{cores} processes x {rows} rows of the workload's recipe (each its own seeded block), "
                       f"full V={v}; the whole path once; numpy fp64",
             "seconds": round(dt, 2)}
+
+
+def step_config(n: int, v: int, world: int) -> dict:
+    """The workload the step line is quoted on; both arms print it as is."""
+    return {"workload": WORKLOAD, "rows_per_gpu": n, "vocab": v, "global_rows": n * world,
+            "parallelism": f"dp{world} (row shards, no collective)",
+            "l2": "inputs (2.5 GB per tensor) larger than L2; no flush",
+            "bytes_per_step_per_gpu": step_bytes(n, v)}
 
 
 def run_reference(args) -> None:
@@ -963,20 +994,17 @@ def run_reference(args) -> None:
         return
     n, v = args.rows, VOCAB
     cores = host_cores()
-    budget = 150.0           # seconds of the whole run, all steps
-    per_row = _oracle_row_seconds(v)
-    rows = int(max(1, min(n, budget / (args.steps + args.warmup) / max(per_row, 1e-6))))
-    dt = oracle_pool(rows, v, args.steps, args.warmup, cores)
+    rows, dt = oracle_pool(v, args.steps, args.warmup, cores, 150.0, n)   # about 150 s for the whole run
     s = rows * cores
     value = step_bytes(s, v) / dt / 1e12
     line = {
         "impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": "TB/s", "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt * 1e3, 3),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": WORKLOAD, "rows_per_step": s, "rows_in_workload": n, "vocab": v,
-                   "sample": f"{cores} processes x {rows} rows per step (bounded sample of the {n}-row batch)"},
+        "config": step_config(n, v, world),
         "cpu_baseline": {"value": round(value, 6), "unit": "TB/s", "cores": cores, "kind": "oracle",
-                         "sample": f"{cores} processes x {rows} of {n} rows per step, full V={v}"},
+                         "sample": f"{cores} processes x {rows} of the {n} rows per step ({s} rows, a bounded "
+                                   f"sample of the batch; value = their algorithmic bytes / time), full V={v}"},
         "e2e": {"value": round(value, 6), "unit": "TB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -1089,10 +1117,8 @@ def main() -> None:
             "metric": METRIC, "value": round(value, 4), "unit": "TB/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": round(ms, 4), "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-            "config": {"workload": WORKLOAD, "rows_per_gpu": n, "vocab": v, "global_rows": n * world,
-                       "parallelism": f"dp{world} (row shards, no collective)",
-                       "l2": "inputs (2.5 GB per tensor) larger than L2; no flush",
-                       "bytes_per_step": sb, "per_op": per_op},
+            "config": step_config(n, v, world),
+            "per_op": per_op,
             "roofline": roofline,
             "cpu_baseline": cpu,
             "e2e": e2e,
