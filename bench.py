@@ -926,12 +926,13 @@ def _oracle_calibrate(v: int) -> float:
     the pool, timed while every other process runs the same probe (the
     processes share the host's memory bandwidth)."""
     import workloads
-    probe = host_rows(_cpu_inputs(workloads, 2, v), 0, 2)
+    rows = 8                 # more than the host's caches hold, as in the timed passes
+    probe = host_rows(_cpu_inputs(workloads, rows, v), 0, rows)
     _BARRIER.wait()
     oracle_step(probe)
     t0 = time.perf_counter()
     oracle_step(probe)
-    return (time.perf_counter() - t0) / 2
+    return (time.perf_counter() - t0) / rows
 
 
 def host_memory_available() -> int:
@@ -994,7 +995,7 @@ def run_reference(args) -> None:
         return
     n, v = args.rows, VOCAB
     cores = host_cores()
-    rows, dt = oracle_pool(v, args.steps, args.warmup, cores, 150.0, n)   # about 150 s for the whole run
+    rows, dt = oracle_pool(v, args.steps, args.warmup, cores, 120.0, n)   # about 2-3 minutes for the whole run
     s = rows * cores
     value = step_bytes(s, v) / dt / 1e12
     line = {
