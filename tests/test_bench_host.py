@@ -80,3 +80,22 @@ def test_config_summary_groups_forward_and_backward():
     assert out["graph_replay"] == {"ms_median": 0.5, "tbs": 8.0}
     assert abs(out["frac_of_measured"] - 2.0 * 1e3 / peak) < 1e-4
     assert [k for k, *_ in bench.CONFIGS] == ["C1", "C2", "C3", "C4", "C5"]
+
+
+@pytest.mark.timeout(300)
+def test_oracle_pool_sizes_its_sample(monkeypatch):
+    """The CPU legs time the oracle over a spawned pool: rows sized from a
+    probe timed in every process at once, within the time budget, the row
+    limit and the host-memory cap (here forced to two rows)."""
+    v = 2048
+    rows, dt = bench.oracle_pool(v, 1, 0, 2, budget_s=0.5, max_rows=64)
+    assert 1 <= rows <= 64 and dt > 0
+    monkeypatch.setattr(bench, "host_memory_available", lambda: int(2 * 2 * bench.ORACLE_BYTES_PER_COLUMN * v / 0.4) + 1)
+    rows, dt = bench.oracle_pool(v, 1, 0, 2, budget_s=60.0, max_rows=64)
+    assert rows == 2 and dt > 0
+
+
+def test_both_arms_share_the_workload_config():
+    c = bench.step_config(8192, 151936, 1)
+    assert c == bench.step_config(8192, 151936, 1) and c["rows_per_gpu"] == 8192 and c["global_rows"] == 8192
+    assert "per_op" not in c and c["bytes_per_step_per_gpu"] == bench.step_bytes(8192, 151936)
