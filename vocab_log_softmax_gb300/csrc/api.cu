@@ -124,6 +124,27 @@ int sm_count(int dev) {
   return n;
 }
 
+// Few rows (the small-batch workloads): a launch with at most one CTA per
+// SM (forward) or two (backward, after widen_bwd) leaves most of the GPU
+// idle, and each CTA waits on DRAM latency batch after batch.  Then every
+// CTA first asks L2 for its whole run, when the launch's inputs take at most
+// a quarter of L2.  A prefetch changes no result.
+#ifndef VLS_PREFETCH_MAX_BYTES
+#define VLS_PREFETCH_MAX_BYTES (32ll << 20)
+#endif
+constexpr int64_t kPrefetchMaxBytes = VLS_PREFETCH_MAX_BYTES;
+int64_t input_bytes(int64_t N, int64_t V, vls_dtype dt, bool two) {
+  return N * V * (dt == VLS_F32 ? 4 : 2) * (two ? 2 : 1);
+}
+void few_rows_prefetch(FwdArgs& a, vls_dtype dt, int dev) {
+  a.prefetch = a.rows * a.cluster <= sm_count(dev) &&
+               input_bytes(a.rows, a.vocab, dt, a.y != nullptr) <= kPrefetchMaxBytes;
+}
+void few_rows_prefetch(BwdArgs& a, vls_dtype dt, int dev) {
+  a.prefetch = a.rows * a.chunks <= 2 * static_cast<int64_t>(sm_count(dev)) &&
+               input_bytes(a.rows, a.vocab, dt, a.y != nullptr) <= kPrefetchMaxBytes;
+}
+
 // Finds the one device that holds every non-NULL pointer and owns the stream.
 int resolve_device(std::initializer_list<const void*> ptrs, void* stream, int* dev_out) {
   // test build: the device check fails before any CUDA call
@@ -435,6 +456,7 @@ int vls_logp_fwd(const void* logits, const vls_rows* rows, vls_dtype dt, int64_t
   a.ignore_index = ignore_index;
   a.logp = logp;
   a.stats_x = stats;
+  few_rows_prefetch(a, dt, dev);
   return VLS_LAUNCH(launch_fwd_logp(dt, cap > 0.0f, a, static_cast<cudaStream_t>(stream)));
 }
 
@@ -463,6 +485,7 @@ int vls_logp_bwd(const void* logits, const vls_rows* rows, vls_dtype dt, int64_t
   a.g = g;
   a.stats_x = stats;
   a.dx = dlogits;
+  few_rows_prefetch(a, dt, dev);
   return VLS_LAUNCH(launch_bwd_logp(dt, cap > 0.0f, a, static_cast<cudaStream_t>(stream)));
 }
 
@@ -484,6 +507,7 @@ int vls_entropy_fwd(const void* logits, const vls_rows* rows, vls_dtype dt, int6
   a.rx = kernel_rows(*rows);
   a.out = H;
   a.stats_x = stats;
+  few_rows_prefetch(a, dt, dev);
   return VLS_LAUNCH(launch_fwd_entropy(dt, cap > 0.0f, a, static_cast<cudaStream_t>(stream)));
 }
 
@@ -509,6 +533,7 @@ int vls_entropy_bwd(const void* logits, const vls_rows* rows, vls_dtype dt, int6
   a.fout = H;
   a.stats_x = stats;
   a.dx = dlogits;
+  few_rows_prefetch(a, dt, dev);
   return VLS_LAUNCH(launch_bwd_entropy(dt, cap > 0.0f, a, static_cast<cudaStream_t>(stream)));
 }
 
@@ -539,6 +564,7 @@ int vls_kl_fwd(const void* pa, const vls_rows* rows_a, const void* pb, const vls
   a.stats_x = rev ? stats_a : stats_b;
   a.stats_y = rev ? stats_b : stats_a;
   a.out = kl;
+  few_rows_prefetch(a, dt, dev);
   return VLS_LAUNCH(launch_fwd_kl(dt, cap > 0.0f, a, static_cast<cudaStream_t>(stream)));
 }
 
@@ -570,6 +596,7 @@ int vls_kl_bwd(const void* pa, const vls_rows* rows_a, const void* pb, const vls
   a.stats_x = stats_a;
   a.stats_y = stats_b;
   a.dx = da;
+  few_rows_prefetch(a, dt, dev);
   return VLS_LAUNCH(
       launch_bwd_kl(dir == VLS_KL_REVERSE, dt, cap > 0.0f, a, static_cast<cudaStream_t>(stream)));
 }
@@ -617,6 +644,7 @@ int vls_fused_fwd(const void* pa, const vls_rows* rows_a, const void* pb, const 
   a.stats_x = stats_a;
   a.stats_y = stats_b;
   const FusedKl fk = !want_kl ? kFusedNoKl : (dir == VLS_KL_REVERSE ? kFusedKlReverse : kFusedKlForward);
+  few_rows_prefetch(a, dt, dev);
   return VLS_LAUNCH(launch_fwd_fused(fk, dt, cap > 0.0f, a, static_cast<cudaStream_t>(stream)));
 }
 
@@ -665,6 +693,7 @@ int vls_fused_bwd(const void* pa, const vls_rows* rows_a, const void* pb, const 
   a.stats_y = stats_b;
   a.dx = da;
   const FusedKl fk = !want_kl ? kFusedNoKl : (dir == VLS_KL_REVERSE ? kFusedKlReverse : kFusedKlForward);
+  few_rows_prefetch(a, dt, dev);
   return VLS_LAUNCH(launch_bwd_fused(fk, dt, cap > 0.0f, a, static_cast<cudaStream_t>(stream)));
 }
 
@@ -699,6 +728,7 @@ int vls_logp_partial(const void* logits, const vls_rows* rows, vls_dtype dt, int
   a.vocab_total = V_total;
   a.part = part;
   a.zt = zt;
+  few_rows_prefetch(a, dt, dev);
   return VLS_LAUNCH(launch_fwd_logp(dt, cap > 0.0f, a, static_cast<cudaStream_t>(stream)));
 }
 
@@ -756,6 +786,7 @@ int vls_logp_bwd_shard(const void* logits, const vls_rows* rows, vls_dtype dt, i
   a.dx = dlogits;
   a.vocab_offset = vocab_offset;
   a.vocab_total = V_total;
+  few_rows_prefetch(a, dt, dev);
   return VLS_LAUNCH(launch_bwd_logp(dt, cap > 0.0f, a, static_cast<cudaStream_t>(stream)));
 }
 
@@ -779,6 +810,7 @@ int vls_entropy_partial(const void* logits, const vls_rows* rows, vls_dtype dt, 
   a.x = logits;
   if (V_shard > 0) a.rx = kernel_rows(*rows);
   a.part = part;
+  few_rows_prefetch(a, dt, dev);
   return VLS_LAUNCH(launch_fwd_entropy(dt, cap > 0.0f, a, static_cast<cudaStream_t>(stream)));
 }
 
@@ -829,6 +861,7 @@ int vls_kl_partial(const void* pa, const vls_rows* rows_a, const void* pb, const
     a.ry = kernel_rows(rev ? *rows_b : *rows_a);
   }
   a.part = part;
+  few_rows_prefetch(a, dt, dev);
   return VLS_LAUNCH(launch_fwd_kl(dt, cap > 0.0f, a, static_cast<cudaStream_t>(stream)));
 }
 

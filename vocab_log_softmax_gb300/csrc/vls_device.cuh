@@ -162,6 +162,20 @@ __device__ __forceinline__ void prefetch_l2(const void* p) {
   asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
 }
 
+// Starts pulling [p, p + bytes) into L2 with one bulk prefetch per 16 KiB,
+// issued by the CTA's first threads (p 16-byte aligned, bytes a multiple of
+// 16; no register, no wait).
+__device__ __forceinline__ void prefetch_l2_range(const void* p, int64_t bytes) {
+  constexpr int64_t kChunk = 16384;
+  for (int64_t off = static_cast<int64_t>(threadIdx.x) * kChunk; off < bytes;
+       off += static_cast<int64_t>(blockDim.x) * kChunk) {
+    const int64_t n = bytes - off < kChunk ? bytes - off : kChunk;
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(static_cast<const char*>(p) + off),
+                 "r"(static_cast<uint32_t>(n))
+                 : "memory");
+  }
+}
+
 __device__ __forceinline__ void st16(void* p, uint4 v) {
   asm volatile("st.global.v4.u32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z),
                "r"(v.w)

@@ -82,6 +82,8 @@ struct FwdArgs {
   // fused sweep: entropy and KL outputs (either may be null)
   float* h;
   float* kl;
+  // few rows: every CTA first asks L2 for its whole run (changes no result)
+  int prefetch;
 };
 
 struct BwdArgs {
@@ -113,6 +115,8 @@ struct BwdArgs {
   const float* g_kl;
   const float* h;
   const float* kl;
+  // few rows: every CTA first asks L2 for its whole piece (changes no result)
+  int prefetch;
 };
 
 struct CombineArgs {
