@@ -124,11 +124,12 @@ int sm_count(int dev) {
   return n;
 }
 
-// Few rows (the small-batch workloads): a launch with at most one CTA per
-// SM (forward) or two (backward, after widen_bwd) leaves most of the GPU
-// idle, and each CTA waits on DRAM latency batch after batch.  Then every
-// CTA first asks L2 for its whole run, when the launch's inputs take at most
-// a quarter of L2.  A prefetch changes no result.
+// Few rows (the small-batch workloads): a forward launch with at most one
+// CTA per SM leaves most of the GPU idle, and each CTA waits on DRAM latency
+// batch after batch.  Then every CTA first asks L2 for its whole run, when
+// the launch's inputs take at most a quarter of L2.  A prefetch changes no
+// result.  (The backward maps are already cut into small pieces at few rows,
+// see widen_bwd, and gained nothing from it.)
 #ifndef VLS_PREFETCH_MAX_BYTES
 #define VLS_PREFETCH_MAX_BYTES (32ll << 20)
 #endif
@@ -138,10 +139,6 @@ int64_t input_bytes(int64_t N, int64_t V, vls_dtype dt, bool two) {
 }
 void few_rows_prefetch(FwdArgs& a, vls_dtype dt, int dev) {
   a.prefetch = a.rows * a.cluster <= sm_count(dev) &&
-               input_bytes(a.rows, a.vocab, dt, a.y != nullptr) <= kPrefetchMaxBytes;
-}
-void few_rows_prefetch(BwdArgs& a, vls_dtype dt, int dev) {
-  a.prefetch = a.rows * a.chunks <= 2 * static_cast<int64_t>(sm_count(dev)) &&
                input_bytes(a.rows, a.vocab, dt, a.y != nullptr) <= kPrefetchMaxBytes;
 }
 
@@ -485,7 +482,6 @@ int vls_logp_bwd(const void* logits, const vls_rows* rows, vls_dtype dt, int64_t
   a.g = g;
   a.stats_x = stats;
   a.dx = dlogits;
-  few_rows_prefetch(a, dt, dev);
   return VLS_LAUNCH(launch_bwd_logp(dt, cap > 0.0f, a, static_cast<cudaStream_t>(stream)));
 }
 
@@ -533,7 +529,6 @@ int vls_entropy_bwd(const void* logits, const vls_rows* rows, vls_dtype dt, int6
   a.fout = H;
   a.stats_x = stats;
   a.dx = dlogits;
-  few_rows_prefetch(a, dt, dev);
   return VLS_LAUNCH(launch_bwd_entropy(dt, cap > 0.0f, a, static_cast<cudaStream_t>(stream)));
 }
 
@@ -596,7 +591,6 @@ int vls_kl_bwd(const void* pa, const vls_rows* rows_a, const void* pb, const vls
   a.stats_x = stats_a;
   a.stats_y = stats_b;
   a.dx = da;
-  few_rows_prefetch(a, dt, dev);
   return VLS_LAUNCH(
       launch_bwd_kl(dir == VLS_KL_REVERSE, dt, cap > 0.0f, a, static_cast<cudaStream_t>(stream)));
 }
@@ -693,7 +687,6 @@ int vls_fused_bwd(const void* pa, const vls_rows* rows_a, const void* pb, const 
   a.stats_y = stats_b;
   a.dx = da;
   const FusedKl fk = !want_kl ? kFusedNoKl : (dir == VLS_KL_REVERSE ? kFusedKlReverse : kFusedKlForward);
-  few_rows_prefetch(a, dt, dev);
   return VLS_LAUNCH(launch_bwd_fused(fk, dt, cap > 0.0f, a, static_cast<cudaStream_t>(stream)));
 }
 
@@ -786,7 +779,6 @@ int vls_logp_bwd_shard(const void* logits, const vls_rows* rows, vls_dtype dt, i
   a.dx = dlogits;
   a.vocab_offset = vocab_offset;
   a.vocab_total = V_total;
-  few_rows_prefetch(a, dt, dev);
   return VLS_LAUNCH(launch_bwd_logp(dt, cap > 0.0f, a, static_cast<cudaStream_t>(stream)));
 }
 

@@ -322,11 +322,6 @@ __global__ void __launch_bounds__(kRowThreads, (bwd_min_blocks<T, OP, CAP, TOPK>
   T* dr = static_cast<T*>(a.dx) + row * V;
   const bool al = aligned16(xr) && aligned16(dr) && aligned16(yr);
   const CapK K = cap_consts(CAP ? a.cap : 1.0f);
-  if (a.prefetch && al) {
-    const int64_t full = min(ve, V >> 3) - vb;
-    prefetch_l2_range(xr + 8 * vb, full * 8 * static_cast<int64_t>(sizeof(T)));
-    if constexpr (KL) prefetch_l2_range(yr + 8 * vb, full * 8 * static_cast<int64_t>(sizeof(T)));
-  }
 
   const vls_rowstat sx = a.stats_x[row];
   BwdRow R;

@@ -115,8 +115,6 @@ struct BwdArgs {
   const float* g_kl;
   const float* h;
   const float* kl;
-  // few rows: every CTA first asks L2 for its whole piece (changes no result)
-  int prefetch;
 };
 
 struct CombineArgs {
