@@ -294,13 +294,14 @@ constexpr bool reads_two() { return OP == kFwdKl || (OP == kFwdFused && DIR != k
 // tensor; 3 vectors of each of the two 16-bit KL tensors (2.5-3.8% faster
 // than 2 at the same 48 registers and 5 CTAs; 4, or 6 CTAs, spill), 2 of
 // each in the other two-tensor sweeps.  The softcapped logp sweep, bound by
-// its arithmetic's latency rather than by memory, takes 6 (measured: 3.7%
-// faster than 4 at 6 resident CTAs; 8 spills).
+// its arithmetic rather than by memory, takes 4 at 6 resident CTAs (with the
+// reciprocal of pairs 0, 2 and 3 on the FMA pipe: 1.0% faster than 6 vectors
+// at 5 CTAs at 151936 columns, 2.8% at 262144; 8 at 4 CTAs was slower).
 #ifndef VLS_CAP_LOGP_UNROLL
-#define VLS_CAP_LOGP_UNROLL 6
+#define VLS_CAP_LOGP_UNROLL 4
 #endif
 #ifndef VLS_CAP_LOGP_CTAS
-#define VLS_CAP_LOGP_CTAS 5
+#define VLS_CAP_LOGP_CTAS 6
 #endif
 template <class T, int OP, int DIR, bool CAP>
 constexpr int fwd_unroll() {

@@ -409,7 +409,7 @@ constexpr float kLn2 = 0.69314718055994531f;
 // which bounds the softcapped sweeps: bit i set for pair i.  A function of
 // the column alone, so every sweep gets the same bits for the same column.
 #ifndef VLS_CAP_FMA_PAIRS
-#define VLS_CAP_FMA_PAIRS 0xB
+#define VLS_CAP_FMA_PAIRS 0xD
 #endif
 constexpr uint32_t kCapFmaPairs = VLS_CAP_FMA_PAIRS;
 
