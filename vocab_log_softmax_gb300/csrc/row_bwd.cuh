@@ -301,15 +301,19 @@ __device__ __forceinline__ float fused_at(const T* xr, const T* yr, int64_t c, c
 #ifndef VLS_CAP_BWD_VECS
 #define VLS_CAP_BWD_VECS 2
 #endif
-template <class T, int OP, bool CAP, bool TOPK>
+// The fused map with a KL term (two tensors, 16-bit) takes batches of 3
+// vectors of each at 5 CTAs: 6.3% (reverse) and 2.5% (forward KL) faster
+// than 2 at 6 CTAs; either change alone was slower, and without a KL term
+// 5 CTAs were 3.9% slower.
+template <class T, int OP, bool CAP, int DIR, bool TOPK>
 constexpr int bwd_min_blocks() {
   if (TOPK) return kCapMinBlocks;
-  if (!CAP) return 6;
+  if (!CAP) return (OP == kBwdFused && DIR != kFusedNoKl && sizeof(T) == 2) ? 5 : 6;
   return (OP == kBwdLogp && sizeof(T) == 2) ? VLS_CAP_LOGP_BWD_CTAS : kCapMinBlocks;
 }
 
 template <class T, int OP, bool CAP, int DIR = kFusedNoKl, bool TOPK = false>
-__global__ void __launch_bounds__(kRowThreads, (bwd_min_blocks<T, OP, CAP, TOPK>())) row_bwd_kernel(const BwdArgs a) {
+__global__ void __launch_bounds__(kRowThreads, (bwd_min_blocks<T, OP, CAP, DIR, TOPK>())) row_bwd_kernel(const BwdArgs a) {
   constexpr bool KL = bwd_reads_two<OP, DIR>();
   const int64_t row = blockIdx.x / a.chunks;
   const int q = static_cast<int>(blockIdx.x - row * a.chunks);
@@ -508,8 +512,9 @@ __global__ void __launch_bounds__(kRowThreads, (bwd_min_blocks<T, OP, CAP, TOPK>
   } else {
     // light arithmetic: plain batches of U vectors in flight per thread; the
     // 16-bit KL maps take 3 of each tensor (1-3% faster than 2 at the same 40
-    // registers), the fused and fp32 two-tensor maps 2 (3 spills there)
-    constexpr int U = KL ? (((OP == kBwdKlReverse || OP == kBwdKlForward) && sizeof(T) == 2) ? 3 : 2) : 4;
+    // registers), and so does the 16-bit fused map with a KL term (at 5 CTAs,
+    // see bwd_min_blocks); fp32 two-tensor maps 2
+    constexpr int U = KL ? (sizeof(T) == 2 ? 3 : 2) : 4;
     if (al) {
       for (; v + (U - 1) * kRowThreads < vfull_end; v += U * kRowThreads) {
         Raw8<T> x[U], y[U];

@@ -320,14 +320,16 @@ constexpr int kCapMaxGroup = VLS_CAP_MAX_GROUP;
 // moved with the size of the argument struct (the bf16 entropy sweep went
 // from 32 to 38 registers, the KL sweep from 44 to 56), costing 5-8% of
 // bandwidth.  The bounds below keep the bf16 sweeps at 32 registers (one
-// tensor), 40 (fp16 one-tensor or fused), 48 (softcapped logp with its
-// 6-vector batches, softcapped entropy and fused, bf16 KL);
-// fp32 vectors hold twice the registers and get 64.
+// tensor), 40 (fp16 one-tensor, fused without a KL term, softcapped logp),
+// 48 (softcapped entropy and fused, KL, and fused with a KL term: 4.7% and
+// 2.5% faster there than at 64 registers and 4 CTAs for reverse and forward
+// KL); fp16 two-tensor sweeps and fp32 vectors, which hold twice the
+// registers, get 64.
 template <class T, int OP, bool CAP, int DIR>
 constexpr int fwd_ctas_at_256() {
   if (sizeof(T) == 4) return 4;
   if (reads_two<OP, DIR>())
-    return (CAP || OP == kFwdFused || !std::is_same<T, __nv_bfloat16>::value) ? 4 : 5;
+    return (CAP || !std::is_same<T, __nv_bfloat16>::value) ? 4 : 5;
   if (CAP) return OP == kFwdLogp ? VLS_CAP_LOGP_CTAS : 5;
   return (OP == kFwdFused || std::is_same<T, __half>::value) ? 6 : 8;
 }
