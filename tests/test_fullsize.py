@@ -2,8 +2,8 @@
 checked on sampled rows (the oracle computes them one by one) and on
 properties that hold at any size; plus the zero-workspace check: the calls
 allocate no device memory beyond their outputs (the long-sequence case,
-"perf(logp): fused zero-workspace backward ...", RL-Kernel PR #495, Tests:
-"fused: zero bytes beyond the output")."""
+"perf(logp): fused zero-workspace backward ...", RL-Kernel PR #495, Tests: the
+fused path's memory check)."""
 
 import gc
 
